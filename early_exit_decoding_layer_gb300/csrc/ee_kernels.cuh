@@ -1,0 +1,188 @@
+// Launch parameters and host-side launchers of the decode-step kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ee.h"
+
+namespace ee {
+
+// ------------------------------------------------------------------ lists
+// A sequence list in device memory: [0] = count, [1 + i] = sequence id.
+constexpr int kListLen = 1 + EE_MAX_BATCH;
+
+// Per-step device state that the kernels read and update.
+struct StepLists {
+  int32_t part[kListLen];   // sequences taking part in this step
+  int32_t full[kListLen];   // still on the bf16 backbone (ascending ids)
+  int32_t exitl[kListLen];  // exited, running the int4 copies (ascending ids)
+  int32_t fin[kListLen];    // rows of the final LM head
+};
+
+// Host -> device step descriptor (copied each step from pinned staging).
+struct StepDesc {
+  int32_t n_part;
+  int32_t part[EE_MAX_BATCH];
+  int32_t n_fin;
+  int32_t fin[EE_MAX_BATCH];
+  int32_t tokens[EE_MAX_BATCH];     // by sequence id
+  int32_t pos[EE_MAX_BATCH];        // position of this step's token, by sequence id
+  int32_t new_block[EE_MAX_BATCH];  // block to map at pos/16, or -1, by sequence id
+  int32_t debug;                    // keep per-layer hidden states
+};
+
+// Device -> host step outputs (one copy per step).
+struct StepOut {
+  int32_t next_token[EE_MAX_BATCH];
+  int32_t exit_layer[EE_MAX_BATCH];
+  int32_t err;                      // first device error code, 0 if none
+  int32_t pad[3];
+  float conf[EE_MAX_BATCH * EE_MAX_CHECKPOINTS];  // [seq][checkpoint], NaN = not evaluated
+};
+
+// ------------------------------------------------------------------ GEMV
+enum Epi : int32_t {
+  EPI_F32 = 0,     // out_f32[seq * out_stride + n] = y
+  EPI_QKV = 1,     // RoPE on q/k row pairs, q -> q_out, k/v -> paged cache
+  EPI_RESID = 2,   // h[seq, n] += y (+ debug copy)
+  EPI_SWIGLU = 3,  // rows (2i, 2i+1) = (gate_i, up_i) -> x_out[seq, i] = silu(g) u
+  EPI_X = 4,       // x_out[seq, n] = y (bf16 and fp16 copies)
+  EPI_HEAD = 5,    // vocabulary head: per-row softmax statistics and argmax
+};
+
+enum HeadMode : int32_t { HEAD_CONF_ARGMAX = 0, HEAD_CHECKPOINT = 1, HEAD_FINAL = 2 };
+
+struct LinearParams {
+  int32_t N, K;
+  // weights: bf16 [N, K]; int4 packed [N, K/2] with bf16 scales [N, sstride]
+  const uint16_t* w;
+  const uint8_t* wq;
+  const uint16_t* ws;
+  int32_t sstride;
+  // rows: either lists (count + ids) or a direct count with ids 0..m_direct-1
+  const int32_t* list_full;  // rows on the bf16 weights (may be null)
+  const int32_t* list_exit;  // rows on the int4 weights (may be null)
+  int32_t m_direct_full;     // used when list_full == null
+  int32_t m_direct_exit;     // used when list_exit == null
+  // activations by sequence id: bf16 for bf16 weights, fp16 (permuted runs of 8) for int4
+  const uint16_t* xb;
+  const uint16_t* xh;
+  int32_t x_stride;
+  int32_t epi;
+  // EPI_F32
+  float* out_f32;
+  int32_t out_stride;
+  // EPI_QKV
+  float* q_out;              // [seq][Hq*hd]
+  uint16_t* kc;              // this layer's K cache [blocks][Hkv][16][hd]
+  uint16_t* vc;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  const int32_t* pos;        // by sequence id
+  const float2* rope;        // [max_seq_len][hd/2] (cos, sin)
+  int32_t n_heads, n_kv_heads, head_dim;
+  // EPI_RESID
+  float* h;
+  int32_t h_stride;
+  float* hdbg;               // [seq][h_stride] copy when *dbg_flag != 0
+  const int32_t* dbg_flag;
+  // EPI_SWIGLU / EPI_X
+  uint16_t* xb_out;
+  uint16_t* xh_out;
+  int32_t xo_stride;
+  // EPI_HEAD
+  int32_t head_mode;
+  float* head_part;          // [grid][EE_MAX_BATCH][4] partial (max, sum, argmax, -)
+  int32_t* head_counter;     // zero between launches
+  float* conf_out;           // HEAD_CONF_ARGMAX: [m]; HEAD_CHECKPOINT: StepOut.conf
+  int32_t* argmax_out;       // HEAD_CONF_ARGMAX: [m]; HEAD_FINAL: StepOut.next_token
+  StepLists* lists;          // HEAD_CHECKPOINT: lists to compact
+  int32_t* exit_layer;       // HEAD_CHECKPOINT: StepOut.exit_layer
+  const float* gamma;        // thresholds [n_checkpoints]
+  int32_t ckpt_index, ckpt_layer;
+  int32_t* err;
+};
+
+// Bytes of dynamic shared memory the GEMV kernel uses.
+size_t linear_smem_bytes();
+// Sets the kernels' shared-memory attributes on the current device (call once
+// per device before the first launch, outside stream capture).
+cudaError_t linear_prepare();
+// Launches the GEMV on `grid` CTAs (grid <= number of SMs).  pdl: launch
+// with programmatic stream serialisation.
+cudaError_t launch_linear(const LinearParams& p, int grid, bool pdl, cudaStream_t st);
+int linear_grid(int N, int num_sms);
+
+// ------------------------------------------------------------------ attention
+struct AttnParams {
+  const int32_t* list;       // sequences (count + ids) or null -> ids 0..m_direct-1
+  int32_t m_direct;
+  int32_t n_heads, n_kv_heads, head_dim;
+  const float* q;            // [seq][Hq*hd]
+  int32_t q_stride;
+  const uint16_t* kc;
+  const uint16_t* vc;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  const int32_t* pos;        // query position by sequence id (ctx = pos + 1)
+  int32_t nsplit;
+  float* part;               // scratch partials
+  int32_t* counters;         // [batch_slots][Hkv], zero between launches
+  float* o_f32;              // [seq][Hq*hd] (op) or null
+  uint16_t* ob;              // bf16 [seq][xo_stride] or null
+  uint16_t* oh;              // fp16, permuted runs of 8, or null
+  int32_t o_stride;
+  int32_t* err;
+};
+size_t attention_part_floats(int batch_slots, int n_heads, int n_kv_heads, int head_dim, int nsplit);
+cudaError_t launch_attention(const AttnParams& p, int batch_slots, bool pdl, cudaStream_t st);
+int attention_nsplit(int batch, int n_kv_heads, int num_sms);
+
+// ------------------------------------------------------------------ small kernels
+struct NormParams {
+  const int32_t* list;
+  const float* h;
+  int32_t h_stride;
+  const uint16_t* g;
+  int32_t d;
+  float eps;
+  uint16_t* xb;
+  uint16_t* xh;               // may be null
+  int32_t x_stride;
+};
+cudaError_t launch_rmsnorm(const NormParams& p, int batch_slots, bool pdl, cudaStream_t st);
+
+struct BeginParams {
+  const StepDesc* desc;
+  StepLists* lists;
+  StepOut* out;
+  const uint16_t* embed;
+  int32_t d;
+  float* h;
+  int32_t h_stride;
+  int32_t* pos;
+  int32_t* block_table;
+  int32_t bt_stride;
+  int32_t n_layers;
+  int32_t n_ckpt;
+  int32_t* dbg_flag;
+};
+cudaError_t launch_step_begin(const BeginParams& p, int batch_slots, cudaStream_t st);
+
+cudaError_t launch_quantize_int4(const uint16_t* w, int rows, int cols, uint8_t* packed,
+                                 uint16_t* scales, int sstride, cudaStream_t st);
+
+// Row copy with an optional row permutation (load-time re-layout).
+enum RowMap : int32_t {
+  MAP_IDENTITY = 0,     // dst row = r
+  MAP_ROPE_PAIRS = 1,   // within heads of `param` rows: i < hd/2 -> 2i, else 2(i-hd/2)+1
+  MAP_INTERLEAVE = 2,   // dst row = 2r + param
+};
+cudaError_t launch_copy_rows(void* dst, int64_t dst_stride_bytes, int64_t dst_row0,
+                             const void* src, int64_t src_stride_bytes, int64_t row_bytes,
+                             int64_t nrows, int map, int param, cudaStream_t st);
+cudaError_t launch_transpose_bf16(uint16_t* dst, const uint16_t* src, int n, cudaStream_t st);
+cudaError_t launch_fill_u16(uint16_t* p, uint16_t v, int64_t n, cudaStream_t st);
+
+}  // namespace ee

@@ -1,0 +1,1163 @@
+// Runtime of the early-exit decode library: context, arena layout, weight
+// loading and re-layout, host-side paged-KV allocator, the decode-step
+// orchestrator (kernels chained with programmatic dependent launch and
+// replayed from CUDA graphs), and the C ABI declared in include/ee.h.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <map>
+#include <string>
+#include <vector>
+
+#include "../../include/ee.h"
+#include "ee_kernels.cuh"
+
+using namespace ee;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kHeadGridMax = 256;       // CTAs of a vocabulary-head launch (<= SMs)
+constexpr int kAttnSplitSlots = 1024;   // batch x splits capacity of the attention scratch
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int sstride_of(int K) { return (int)align_up((size_t)ceil_div(K, EE_QUANT_GROUP), 8); }
+
+struct Carver {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carver(uint8_t* b) : base(b) {}
+  template <class T>
+  T* take(size_t count) {
+    off = align_up(off, kAlign);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+struct Mat4 {  // int4 copy of one fused matrix
+  uint8_t* q;
+  uint16_t* s;
+};
+
+struct LayerBufs {
+  uint16_t *wqkv, *wo, *wgu, *wd, *g_attn, *g_ffn;
+  Mat4 qkv, o, gu, d;
+};
+
+struct Dims {
+  int L, d, hq, hkv, hd, F, V, nck, maxb, maxs;
+  int dq, dk, nqkv, bps, nblocks;
+  size_t kv_layer_elems;
+};
+
+Dims dims_of(const ee_config& c) {
+  Dims m;
+  m.L = c.n_layers;
+  m.d = c.d_model;
+  m.hq = c.n_heads;
+  m.hkv = c.n_kv_heads;
+  m.hd = c.head_dim;
+  m.F = c.ffn_dim;
+  m.V = c.vocab;
+  m.nck = c.n_checkpoints;
+  m.maxb = c.max_batch;
+  m.maxs = c.max_seq_len;
+  m.dq = m.hq * m.hd;
+  m.dk = m.hkv * m.hd;
+  m.nqkv = m.dq + 2 * m.dk;
+  m.bps = (int)ceil_div(m.maxs, EE_KV_BLOCK);
+  m.nblocks = m.maxb * m.bps;
+  m.kv_layer_elems = (size_t)m.nblocks * m.hkv * EE_KV_BLOCK * m.hd;
+  return m;
+}
+
+}  // namespace
+
+struct ee_ctx {
+  ee_config cfg;
+  std::vector<int32_t> ckpts;
+  Dims m;
+  int dev = 0, num_sms = 0;
+  cudaStream_t user_stream = nullptr;
+  cudaStream_t st = nullptr;
+  cudaEvent_t ev = nullptr;
+  uint8_t* arena = nullptr;
+  size_t arena_bytes = 0;
+
+  std::vector<LayerBufs> layers;
+  uint16_t *E = nullptr, *g_final = nullptr;
+  std::vector<uint16_t*> Tt;
+  uint16_t *kcache = nullptr, *vcache = nullptr;
+  int32_t* block_table = nullptr;
+  int32_t* pos = nullptr;
+  float2* rope = nullptr;
+  float* h = nullptr;
+  uint16_t *xb = nullptr, *xh = nullptr, *ab = nullptr, *ah = nullptr, *actb = nullptr,
+           *acth = nullptr, *ub = nullptr;
+  float* q = nullptr;
+  float* attn_part = nullptr;
+  int32_t* attn_cnt = nullptr;
+  float* head_part = nullptr;
+  int32_t* head_cnt = nullptr;
+  float* hdbg = nullptr;
+  StepLists* lists = nullptr;
+  StepDesc* desc_dev = nullptr;
+  StepOut* out_dev = nullptr;
+  int32_t* dbg_flag = nullptr;
+  float* gamma_dev = nullptr;
+  uint8_t* staging = nullptr;
+  size_t staging_bytes = 0;
+  size_t zero_begin = 0, zero_end = 0;  // arena range cleared at create (counters)
+
+  StepDesc* desc_host = nullptr;
+  StepOut* out_host = nullptr;
+
+  // host bookkeeping
+  std::vector<int32_t> free_blocks;  // descending; back() is the lowest free id
+  std::vector<std::vector<int32_t>> seq_blocks;
+  std::vector<int32_t> seq_pos;
+  int batch = 0;
+  std::vector<char> layer_loaded;
+  bool shared_loaded = false;
+  std::vector<float> gamma;
+  int exit_enabled = 1, use_graph = 1, debug = 0;
+  bool cuda_broken = false;
+  std::map<std::pair<int, int>, cudaGraphExec_t> graphs;
+  std::string err;
+};
+
+namespace {
+
+ee_status fail(ee_ctx* c, ee_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (c) {
+    c->err = buf;
+    if (s == EE_ERR_CUDA) c->cuda_broken = true;
+  }
+  return s;
+}
+
+#define EE_CUDA(ctx, call)                                                                       \
+  do {                                                                                           \
+    cudaError_t e_ = (call);                                                                     \
+    if (e_ != cudaSuccess)                                                                       \
+      return fail((ctx), EE_ERR_CUDA, "%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_),   \
+                  __FILE__, __LINE__);                                                           \
+  } while (0)
+
+const char* validate_config(const ee_config* c) {
+  if (!c) return "config is NULL";
+  if (c->n_layers < 1 || c->d_model < 32 || c->n_heads < 1 || c->n_kv_heads < 1 ||
+      c->head_dim < 2 || c->ffn_dim < 32 || c->vocab < 2)
+    return "shape fields must be positive (d_model, ffn_dim >= 32, vocab >= 2)";
+  if (c->d_model % 32 || c->ffn_dim % 32 || (c->n_heads * c->head_dim) % 32)
+    return "d_model, ffn_dim and n_heads*head_dim must be multiples of 32";
+  if (c->n_heads % c->n_kv_heads) return "n_heads must be a multiple of n_kv_heads";
+  if (c->head_dim != 64 && c->head_dim != 128) return "head_dim must be 64 or 128";
+  const int G = c->n_heads / c->n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return "n_heads / n_kv_heads must be 1, 2, 4 or 8";
+  if (c->vocab % 2) return "vocab must be even";
+  if (c->quant_group != EE_QUANT_GROUP) return "quant_group must be 128";
+  if (c->kv_block != EE_KV_BLOCK) return "kv_block must be 16";
+  if (c->max_batch < 1 || c->max_batch > EE_MAX_BATCH) return "max_batch must be in [1, 64]";
+  if (c->max_seq_len < 2) return "max_seq_len must be >= 2";
+  if (!(c->rms_eps > 0.0f) || !(c->rope_theta > 0.0f)) return "rms_eps and rope_theta must be > 0";
+  if (c->n_checkpoints < 0 || c->n_checkpoints > EE_MAX_CHECKPOINTS) return "n_checkpoints out of range";
+  if (c->n_checkpoints > 0 && !c->checkpoint_layers) return "checkpoint_layers is NULL";
+  for (int i = 0; i < c->n_checkpoints; ++i) {
+    const int l = c->checkpoint_layers[i];
+    if (l < 0 || l > c->n_layers - 2) return "checkpoint layer out of [0, n_layers-2]";
+    if (i > 0 && l <= c->checkpoint_layers[i - 1]) return "checkpoint layers must be strictly ascending";
+  }
+  return nullptr;
+}
+
+// Lays the arena out (base == null: sizing only).
+size_t carve(ee_ctx* c, const ee_config& cfg, uint8_t* base) {
+  const Dims m = dims_of(cfg);
+  Carver cv(base);
+  std::vector<LayerBufs> layers(m.L);
+  for (int j = 0; j < m.L; ++j) {
+    LayerBufs& b = layers[j];
+    b.wqkv = cv.take<uint16_t>((size_t)m.nqkv * m.d);
+    b.wo = cv.take<uint16_t>((size_t)m.d * m.dq);
+    b.wgu = cv.take<uint16_t>((size_t)2 * m.F * m.d);
+    b.wd = cv.take<uint16_t>((size_t)m.d * m.F);
+    b.g_attn = cv.take<uint16_t>(m.d);
+    b.g_ffn = cv.take<uint16_t>(m.d);
+    b.qkv.q = cv.take<uint8_t>((size_t)m.nqkv * m.d / 2);
+    b.qkv.s = cv.take<uint16_t>((size_t)m.nqkv * sstride_of(m.d));
+    b.o.q = cv.take<uint8_t>((size_t)m.d * m.dq / 2);
+    b.o.s = cv.take<uint16_t>((size_t)m.d * sstride_of(m.dq));
+    b.gu.q = cv.take<uint8_t>((size_t)2 * m.F * m.d / 2);
+    b.gu.s = cv.take<uint16_t>((size_t)2 * m.F * sstride_of(m.d));
+    b.d.q = cv.take<uint8_t>((size_t)m.d * m.F / 2);
+    b.d.s = cv.take<uint16_t>((size_t)m.d * sstride_of(m.F));
+  }
+  uint16_t* E = cv.take<uint16_t>((size_t)m.V * m.d);
+  uint16_t* gf = cv.take<uint16_t>(m.d);
+  std::vector<uint16_t*> Tt(m.nck);
+  for (int i = 0; i < m.nck; ++i) Tt[i] = cv.take<uint16_t>((size_t)m.d * m.d);
+  uint16_t* kc = cv.take<uint16_t>(m.kv_layer_elems * m.L);
+  uint16_t* vc = cv.take<uint16_t>(m.kv_layer_elems * m.L);
+  int32_t* bt = cv.take<int32_t>((size_t)m.maxb * m.bps);
+  int32_t* pos = cv.take<int32_t>(EE_MAX_BATCH);
+  float2* rope = cv.take<float2>((size_t)m.maxs * (m.hd / 2));
+  float* h = cv.take<float>((size_t)EE_MAX_BATCH * m.d);
+  uint16_t* xb = cv.take<uint16_t>((size_t)EE_MAX_BATCH * m.d);
+  uint16_t* xh = cv.take<uint16_t>((size_t)EE_MAX_BATCH * m.d);
+  uint16_t* ab = cv.take<uint16_t>((size_t)EE_MAX_BATCH * m.dq);
+  uint16_t* ah = cv.take<uint16_t>((size_t)EE_MAX_BATCH * m.dq);
+  uint16_t* actb = cv.take<uint16_t>((size_t)EE_MAX_BATCH * m.F);
+  uint16_t* acth = cv.take<uint16_t>((size_t)EE_MAX_BATCH * m.F);
+  uint16_t* ub = cv.take<uint16_t>((size_t)EE_MAX_BATCH * m.d);
+  float* q = cv.take<float>((size_t)EE_MAX_BATCH * m.dq);
+  float* apart = cv.take<float>((size_t)kAttnSplitSlots * m.hkv * (m.hq / m.hkv) * (m.hd + 2));
+  float* hpart = cv.take<float>((size_t)kHeadGridMax * EE_MAX_BATCH * 4);
+  float* hdbg = cv.take<float>((size_t)m.L * EE_MAX_BATCH * m.d);
+  StepDesc* desc = cv.take<StepDesc>(1);
+  StepOut* out = cv.take<StepOut>(1);
+  float* gam = cv.take<float>(EE_MAX_CHECKPOINTS);
+  const size_t zb = align_up(cv.off, kAlign);
+  StepLists* lists = cv.take<StepLists>(1);
+  int32_t* acnt = cv.take<int32_t>((size_t)EE_MAX_BATCH * m.hkv);
+  int32_t* hcnt = cv.take<int32_t>(64);
+  int32_t* dflag = cv.take<int32_t>(1);
+  const size_t ze = align_up(cv.off, kAlign);
+  const size_t stg = 2 * (size_t)std::max({(size_t)m.F * m.d, (size_t)m.dq * m.d, (size_t)m.d * m.d,
+                                          (size_t)m.dk * m.d});
+  uint8_t* staging = cv.take<uint8_t>(stg);
+  const size_t total = align_up(cv.off, kAlign);
+  if (c) {
+    c->layers = layers;
+    c->E = E;
+    c->g_final = gf;
+    c->Tt = Tt;
+    c->kcache = kc;
+    c->vcache = vc;
+    c->block_table = bt;
+    c->pos = pos;
+    c->rope = rope;
+    c->h = h;
+    c->xb = xb;
+    c->xh = xh;
+    c->ab = ab;
+    c->ah = ah;
+    c->actb = actb;
+    c->acth = acth;
+    c->ub = ub;
+    c->q = q;
+    c->attn_part = apart;
+    c->head_part = hpart;
+    c->hdbg = hdbg;
+    c->desc_dev = desc;
+    c->out_dev = out;
+    c->gamma_dev = gam;
+    c->lists = lists;
+    c->attn_cnt = acnt;
+    c->head_cnt = hcnt;
+    c->dbg_flag = dflag;
+    c->staging = staging;
+    c->staging_bytes = stg;
+    c->zero_begin = zb;
+    c->zero_end = ze;
+  }
+  return total;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    cudaGetDevice(&prev);
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+// Orders our stream after everything already queued on the caller's stream.
+ee_status join_user_stream(ee_ctx* c) {
+  EE_CUDA(c, cudaEventRecord(c->ev, c->user_stream));
+  EE_CUDA(c, cudaStreamWaitEvent(c->st, c->ev, 0));
+  return EE_OK;
+}
+
+// ---------------------------------------------------------------- step enqueue
+ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
+  const Dims& m = c->m;
+  cudaStream_t st = c->st;
+  EE_CUDA(c, cudaMemcpyAsync(c->desc_dev, c->desc_host, sizeof(StepDesc), cudaMemcpyHostToDevice, st));
+
+  BeginParams bp = {};
+  bp.desc = c->desc_dev;
+  bp.lists = c->lists;
+  bp.out = c->out_dev;
+  bp.embed = c->E;
+  bp.d = m.d;
+  bp.h = c->h;
+  bp.h_stride = m.d;
+  bp.pos = c->pos;
+  bp.block_table = c->block_table;
+  bp.bt_stride = m.bps;
+  bp.n_layers = m.L;
+  bp.n_ckpt = m.nck;
+  bp.dbg_flag = c->dbg_flag;
+  EE_CUDA(c, launch_step_begin(bp, B, st));
+
+  int32_t* err = &c->out_dev->err;
+  const int nsplit = attention_nsplit(B, m.hkv, c->num_sms);
+
+  NormParams np = {};
+  np.h = c->h;
+  np.h_stride = m.d;
+  np.d = m.d;
+  np.eps = c->cfg.rms_eps;
+  np.x_stride = m.d;
+
+  LinearParams base = {};
+  base.err = err;
+  base.block_table = c->block_table;
+  base.bt_stride = m.bps;
+  base.pos = c->pos;
+  base.rope = c->rope;
+  base.n_heads = m.hq;
+  base.n_kv_heads = m.hkv;
+  base.head_dim = m.hd;
+  base.h = c->h;
+  base.h_stride = m.d;
+  base.dbg_flag = c->dbg_flag;
+  base.head_part = c->head_part;
+  base.gamma = c->gamma_dev;
+
+  for (int j = 0; j < m.L; ++j) {
+    const LayerBufs& w = c->layers[j];
+    // attention RMSNorm of every participating sequence
+    np.list = c->lists->part;
+    np.g = w.g_attn;
+    np.xb = c->xb;
+    np.xh = c->xh;
+    EE_CUDA(c, launch_rmsnorm(np, B, true, st));
+    // QKV projection + RoPE + K/V write into the shared paged cache
+    LinearParams p = base;
+    p.N = m.nqkv;
+    p.K = m.d;
+    p.w = w.wqkv;
+    p.wq = w.qkv.q;
+    p.ws = w.qkv.s;
+    p.sstride = sstride_of(m.d);
+    p.list_full = c->lists->full;
+    p.list_exit = c->lists->exitl;
+    p.xb = c->xb;
+    p.xh = c->xh;
+    p.x_stride = m.d;
+    p.epi = EPI_QKV;
+    p.q_out = c->q;
+    p.kc = c->kcache + (size_t)j * m.kv_layer_elems;
+    p.vc = c->vcache + (size_t)j * m.kv_layer_elems;
+    EE_CUDA(c, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
+    // decode attention
+    AttnParams ap = {};
+    ap.list = c->lists->part;
+    ap.n_heads = m.hq;
+    ap.n_kv_heads = m.hkv;
+    ap.head_dim = m.hd;
+    ap.q = c->q;
+    ap.q_stride = m.dq;
+    ap.kc = p.kc;
+    ap.vc = p.vc;
+    ap.block_table = c->block_table;
+    ap.bt_stride = m.bps;
+    ap.pos = c->pos;
+    ap.nsplit = nsplit;
+    ap.part = c->attn_part;
+    ap.counters = c->attn_cnt;
+    ap.ob = c->ab;
+    ap.oh = c->ah;
+    ap.o_stride = m.dq;
+    ap.err = err;
+    EE_CUDA(c, launch_attention(ap, B, true, st));
+    // O projection + residual
+    p = base;
+    p.N = m.d;
+    p.K = m.dq;
+    p.w = w.wo;
+    p.wq = w.o.q;
+    p.ws = w.o.s;
+    p.sstride = sstride_of(m.dq);
+    p.list_full = c->lists->full;
+    p.list_exit = c->lists->exitl;
+    p.xb = c->ab;
+    p.xh = c->ah;
+    p.x_stride = m.dq;
+    p.epi = EPI_RESID;
+    EE_CUDA(c, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
+    // FFN RMSNorm
+    np.g = w.g_ffn;
+    EE_CUDA(c, launch_rmsnorm(np, B, true, st));
+    // gate/up + SwiGLU
+    p = base;
+    p.N = 2 * m.F;
+    p.K = m.d;
+    p.w = w.wgu;
+    p.wq = w.gu.q;
+    p.ws = w.gu.s;
+    p.sstride = sstride_of(m.d);
+    p.list_full = c->lists->full;
+    p.list_exit = c->lists->exitl;
+    p.xb = c->xb;
+    p.xh = c->xh;
+    p.x_stride = m.d;
+    p.epi = EPI_SWIGLU;
+    p.xb_out = c->actb;
+    p.xh_out = c->acth;
+    p.xo_stride = m.F;
+    EE_CUDA(c, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
+    // down projection + residual (+ per-layer copy in debug mode)
+    p = base;
+    p.N = m.d;
+    p.K = m.F;
+    p.w = w.wd;
+    p.wq = w.d.q;
+    p.ws = w.d.s;
+    p.sstride = sstride_of(m.F);
+    p.list_full = c->lists->full;
+    p.list_exit = c->lists->exitl;
+    p.xb = c->actb;
+    p.xh = c->acth;
+    p.x_stride = m.F;
+    p.epi = EPI_RESID;
+    p.hdbg = c->hdbg + (size_t)j * EE_MAX_BATCH * m.d;
+    EE_CUDA(c, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
+
+    const auto ck = std::find(c->ckpts.begin(), c->ckpts.end(), j);
+    if (heads && ck != c->ckpts.end()) {
+      const int ci = (int)(ck - c->ckpts.begin());
+      // u = RMSNorm_final(h) T_c for the sequences still on the backbone
+      NormParams fp = np;
+      fp.list = c->lists->full;
+      fp.g = c->g_final;
+      fp.xh = nullptr;
+      EE_CUDA(c, launch_rmsnorm(fp, B, true, st));
+      p = base;
+      p.N = m.d;
+      p.K = m.d;
+      p.w = c->Tt[ci];
+      p.list_full = c->lists->full;
+      p.list_exit = nullptr;
+      p.xb = c->xb;
+      p.x_stride = m.d;
+      p.epi = EPI_X;
+      p.xb_out = c->ub;
+      p.xo_stride = m.d;
+      EE_CUDA(c, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
+      // z = u E^T, conf = max softmax, exit if conf > gamma_c, compact the lists
+      p = base;
+      p.N = m.V;
+      p.K = m.d;
+      p.w = c->E;
+      p.list_full = c->lists->full;
+      p.list_exit = nullptr;
+      p.xb = c->ub;
+      p.x_stride = m.d;
+      p.epi = EPI_HEAD;
+      p.head_mode = HEAD_CHECKPOINT;
+      p.head_counter = c->head_cnt + 1 + ci;
+      p.conf_out = c->out_dev->conf;
+      p.lists = c->lists;
+      p.exit_layer = c->out_dev->exit_layer;
+      p.ckpt_index = ci;
+      p.ckpt_layer = j;
+      EE_CUDA(c, launch_linear(p, std::min(linear_grid(p.N, c->num_sms), kHeadGridMax), true, st));
+    }
+  }
+  // final LM head: argmax of RMSNorm_final(h) E^T
+  NormParams fp = np;
+  fp.list = c->lists->fin;
+  fp.g = c->g_final;
+  fp.xh = nullptr;
+  EE_CUDA(c, launch_rmsnorm(fp, B, true, st));
+  LinearParams p = base;
+  p.N = m.V;
+  p.K = m.d;
+  p.w = c->E;
+  p.list_full = c->lists->fin;
+  p.list_exit = nullptr;
+  p.xb = c->xb;
+  p.x_stride = m.d;
+  p.epi = EPI_HEAD;
+  p.head_mode = HEAD_FINAL;
+  p.head_counter = c->head_cnt;
+  p.argmax_out = c->out_dev->next_token;
+  EE_CUDA(c, launch_linear(p, std::min(linear_grid(p.N, c->num_sms), kHeadGridMax), true, st));
+  EE_CUDA(c, cudaMemcpyAsync(c->out_host, c->out_dev, sizeof(StepOut), cudaMemcpyDeviceToHost, st));
+  return EE_OK;
+}
+
+ee_status run_step(ee_ctx* c, int B, bool heads) {
+  if (c->use_graph) {
+    const auto key = std::make_pair(B, heads ? 1 : 0);
+    auto it = c->graphs.find(key);
+    if (it == c->graphs.end()) {
+      cudaGraph_t g = nullptr;
+      EE_CUDA(c, cudaStreamBeginCapture(c->st, cudaStreamCaptureModeThreadLocal));
+      const ee_status s = enqueue_step(c, B, heads);
+      const cudaError_t e = cudaStreamEndCapture(c->st, &g);
+      if (s != EE_OK) {
+        if (g) cudaGraphDestroy(g);
+        return s;
+      }
+      if (e != cudaSuccess) return fail(c, EE_ERR_CUDA, "graph capture failed: %s", cudaGetErrorString(e));
+      cudaGraphExec_t ex = nullptr;
+      const cudaError_t ei = cudaGraphInstantiate(&ex, g, 0);
+      cudaGraphDestroy(g);
+      if (ei != cudaSuccess)
+        return fail(c, EE_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(ei));
+      it = c->graphs.emplace(key, ex).first;
+    }
+    EE_CUDA(c, cudaGraphLaunch(it->second, c->st));
+  } else {
+    const ee_status s = enqueue_step(c, B, heads);
+    if (s != EE_OK) return s;
+  }
+  EE_CUDA(c, cudaStreamSynchronize(c->st));
+  if (c->out_host->err != 0)
+    return fail(c, EE_ERR_DEVICE_TIMEOUT,
+                "a bounded device wait gave up (code %d: 1 = stage fill, 2 = stage drain, 3 = exit drain)",
+                c->out_host->err);
+  return EE_OK;
+}
+
+void reset_blocks(ee_ctx* c) {
+  c->free_blocks.resize(c->m.nblocks);
+  for (int i = 0; i < c->m.nblocks; ++i) c->free_blocks[i] = c->m.nblocks - 1 - i;
+  c->seq_blocks.assign(c->m.maxb, {});
+  c->seq_pos.assign(c->m.maxb, 0);
+  c->batch = 0;
+}
+
+int32_t alloc_block(ee_ctx* c) {
+  if (c->free_blocks.empty()) return -1;
+  const int32_t b = c->free_blocks.back();
+  c->free_blocks.pop_back();
+  return b;
+}
+
+ee_status fill_sentinel(ee_ctx* c) {
+  const size_t n = c->m.kv_layer_elems * c->m.L;
+  EE_CUDA(c, launch_fill_u16(c->kcache, 0xFFFF, (int64_t)n, c->st));
+  EE_CUDA(c, launch_fill_u16(c->vcache, 0xFFFF, (int64_t)n, c->st));
+  return EE_OK;
+}
+
+ee_status check_ready(ee_ctx* c) {
+  if (c->cuda_broken) return fail(c, EE_ERR_CUDA, "context unusable after an earlier CUDA error");
+  for (int j = 0; j < c->m.L; ++j)
+    if (!c->layer_loaded[j]) return fail(c, EE_ERR_STATE, "layer %d weights not loaded", j);
+  if (!c->shared_loaded) return fail(c, EE_ERR_STATE, "shared weights (E, g_final, T) not loaded");
+  return EE_OK;
+}
+
+// copy a host/device matrix [rows, cols] bf16 into its place in a fused block
+ee_status place_bf16(ee_ctx* c, const uint16_t* src, int rows, int cols, uint16_t* dst, int row0,
+                     int map, int param) {
+  const size_t bytes = (size_t)rows * cols * 2;
+  if (bytes > c->staging_bytes) return fail(c, EE_ERR_INVALID_ARG, "matrix larger than staging");
+  EE_CUDA(c, cudaMemcpyAsync(c->staging, src, bytes, cudaMemcpyDefault, c->st));
+  EE_CUDA(c, launch_copy_rows(dst, (int64_t)cols * 2, row0, c->staging, (int64_t)cols * 2,
+                              (int64_t)cols * 2, rows, map, param, c->st));
+  return EE_OK;
+}
+
+ee_status place_int4(ee_ctx* c, const uint8_t* q, const uint16_t* s, int rows, int cols, Mat4 dst,
+                     int row0, int map, int param) {
+  const int ng = (int)ceil_div(cols, EE_QUANT_GROUP), ss = sstride_of(cols);
+  size_t bytes = (size_t)rows * cols / 2;
+  EE_CUDA(c, cudaMemcpyAsync(c->staging, q, bytes, cudaMemcpyDefault, c->st));
+  EE_CUDA(c, launch_copy_rows(dst.q, cols / 2, row0, c->staging, cols / 2, cols / 2, rows, map, param, c->st));
+  bytes = (size_t)rows * ng * 2;
+  EE_CUDA(c, cudaMemcpyAsync(c->staging, s, bytes, cudaMemcpyDefault, c->st));
+  EE_CUDA(c, launch_copy_rows(dst.s, (int64_t)ss * 2, row0, c->staging, (int64_t)ng * 2, (int64_t)ng * 2,
+                              rows, map, param, c->st));
+  return EE_OK;
+}
+
+struct MatPlace {
+  int block;  // 0 qkv, 1 o, 2 gu, 3 d
+  int row0, rows, cols, map, param;
+};
+
+MatPlace placement(const Dims& m, int mat) {
+  switch (mat) {
+    case EE_WQ: return {0, 0, m.dq, m.d, MAP_ROPE_PAIRS, m.hd};
+    case EE_WK: return {0, m.dq, m.dk, m.d, MAP_ROPE_PAIRS, m.hd};
+    case EE_WV: return {0, m.dq + m.dk, m.dk, m.d, MAP_IDENTITY, 0};
+    case EE_WO: return {1, 0, m.d, m.dq, MAP_IDENTITY, 0};
+    case EE_WG: return {2, 0, m.F, m.d, MAP_INTERLEAVE, 0};
+    case EE_WU: return {2, 0, m.F, m.d, MAP_INTERLEAVE, 1};
+    default: return {3, 0, m.d, m.F, MAP_IDENTITY, 0};
+  }
+}
+
+int64_t device_row(const MatPlace& pl, int64_t r) {
+  if (pl.map == MAP_ROPE_PAIRS) {
+    const int64_t head = r / pl.param, i = r % pl.param, half = pl.param / 2;
+    return pl.row0 + head * pl.param + (i < half ? 2 * i : 2 * (i - half) + 1);
+  }
+  if (pl.map == MAP_INTERLEAVE) return pl.row0 + 2 * r + pl.param;
+  return pl.row0 + r;
+}
+
+}  // namespace
+
+// ======================================================================= C ABI
+extern "C" {
+
+size_t ee_arena_bytes(const ee_config* cfg) {
+  if (validate_config(cfg)) return 0;
+  return carve(nullptr, *cfg, nullptr);
+}
+
+ee_status ee_create(const ee_config* cfg, void* dev_arena, size_t arena_bytes, void* stream,
+                    ee_ctx** out) {
+  if (!out) return EE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (const char* why = validate_config(cfg)) {
+    (void)why;
+    return EE_ERR_INVALID_ARG;
+  }
+  if (!dev_arena || (uintptr_t)dev_arena % kAlign) return EE_ERR_INVALID_ARG;
+  const size_t need = carve(nullptr, *cfg, nullptr);
+  if (arena_bytes < need) return EE_ERR_OOM_ARENA;
+
+  ee_ctx* c = new ee_ctx();
+  c->cfg = *cfg;
+  c->ckpts.assign(cfg->checkpoint_layers, cfg->checkpoint_layers + cfg->n_checkpoints);
+  c->cfg.checkpoint_layers = c->ckpts.data();
+  c->m = dims_of(*cfg);
+  c->arena = (uint8_t*)dev_arena;
+  c->arena_bytes = arena_bytes;
+  c->user_stream = (cudaStream_t)stream;
+  c->layer_loaded.assign(c->m.L, 0);
+  c->gamma.assign(c->m.nck, INFINITY);
+  carve(c, *cfg, c->arena);
+  auto bail = [&](ee_status s) {
+    ee_destroy(c);
+    return s;
+  };
+  if (cudaGetDevice(&c->dev) != cudaSuccess) return bail(EE_ERR_CUDA);
+  if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->dev) != cudaSuccess)
+    return bail(EE_ERR_CUDA);
+  if (c->num_sms > kHeadGridMax) c->num_sms = kHeadGridMax;
+  if (linear_prepare() != cudaSuccess) return bail(EE_ERR_CUDA);
+  if (cudaStreamCreateWithFlags(&c->st, cudaStreamNonBlocking) != cudaSuccess) return bail(EE_ERR_CUDA);
+  if (cudaEventCreateWithFlags(&c->ev, cudaEventDisableTiming) != cudaSuccess) return bail(EE_ERR_CUDA);
+  if (cudaHostAlloc((void**)&c->desc_host, sizeof(StepDesc), cudaHostAllocDefault) != cudaSuccess ||
+      cudaHostAlloc((void**)&c->out_host, sizeof(StepOut), cudaHostAllocDefault) != cudaSuccess)
+    return bail(EE_ERR_CUDA);
+  memset(c->desc_host, 0, sizeof(StepDesc));
+  memset(c->out_host, 0, sizeof(StepOut));
+  if (join_user_stream(c) != EE_OK) return bail(EE_ERR_CUDA);
+  // counters and lists start at zero
+  if (cudaMemsetAsync(c->arena + c->zero_begin, 0, c->zero_end - c->zero_begin, c->st) != cudaSuccess)
+    return bail(EE_ERR_CUDA);
+  // RoPE table: angle = pos * theta^(-2i/hd), in double, stored as float (cos, sin)
+  {
+    const int half = c->m.hd / 2;
+    std::vector<float2> tab((size_t)c->m.maxs * half);
+    for (int p = 0; p < c->m.maxs; ++p)
+      for (int i = 0; i < half; ++i) {
+        const double inv = pow((double)cfg->rope_theta, -2.0 * i / (double)c->m.hd);
+        const double a = (double)p * inv;
+        tab[(size_t)p * half + i] = make_float2((float)cos(a), (float)sin(a));
+      }
+    if (cudaMemcpyAsync(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice, c->st) !=
+        cudaSuccess)
+      return bail(EE_ERR_CUDA);
+    std::vector<float> g(EE_MAX_CHECKPOINTS, INFINITY);
+    if (cudaMemcpyAsync(c->gamma_dev, g.data(), g.size() * sizeof(float), cudaMemcpyHostToDevice, c->st) !=
+        cudaSuccess)
+      return bail(EE_ERR_CUDA);
+    if (fill_sentinel(c) != EE_OK) return bail(EE_ERR_CUDA);
+    if (cudaStreamSynchronize(c->st) != cudaSuccess) return bail(EE_ERR_CUDA);
+  }
+  reset_blocks(c);
+  *out = c;
+  return EE_OK;
+}
+
+void ee_destroy(ee_ctx* c) {
+  if (!c) return;
+  for (auto& kv : c->graphs) cudaGraphExecDestroy(kv.second);
+  if (c->st) cudaStreamSynchronize(c->st);
+  if (c->desc_host) cudaFreeHost(c->desc_host);
+  if (c->out_host) cudaFreeHost(c->out_host);
+  if (c->ev) cudaEventDestroy(c->ev);
+  if (c->st) cudaStreamDestroy(c->st);
+  delete c;
+}
+
+const char* ee_last_error(const ee_ctx* c) { return c ? c->err.c_str() : "null context"; }
+
+ee_status ee_load_layer(ee_ctx* c, int32_t layer, const ee_layer_weights* lw) {
+  if (!c) return EE_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= c->m.L) return fail(c, EE_ERR_INVALID_ARG, "layer %d out of range", layer);
+  if (!lw || !lw->g_attn || !lw->g_ffn || !lw->wq || !lw->wk || !lw->wv || !lw->wo || !lw->wg ||
+      !lw->wu || !lw->wd)
+    return fail(c, EE_ERR_INVALID_ARG, "layer %d: a bf16 weight pointer is NULL", layer);
+  int given = 0;
+  for (int k = 0; k < EE_N_MATS; ++k) {
+    if ((lw->q4[k] == nullptr) != (lw->s4[k] == nullptr))
+      return fail(c, EE_ERR_INVALID_ARG, "layer %d: q4[%d] and s4[%d] must both be set or both NULL", layer, k, k);
+    given += lw->q4[k] != nullptr;
+  }
+  if (given != 0 && given != EE_N_MATS)
+    return fail(c, EE_ERR_INVALID_ARG, "layer %d: give all seven int4 copies or none", layer);
+  if (c->cuda_broken) return fail(c, EE_ERR_CUDA, "context unusable after an earlier CUDA error");
+  DeviceGuard dg(c->dev);
+  if (join_user_stream(c) != EE_OK) return EE_ERR_CUDA;
+  const Dims& m = c->m;
+  LayerBufs& b = c->layers[layer];
+  uint16_t* blocks_bf[4] = {b.wqkv, b.wo, b.wgu, b.wd};
+  Mat4 blocks_q[4] = {b.qkv, b.o, b.gu, b.d};
+  const uint16_t* srcs[EE_N_MATS] = {lw->wq, lw->wk, lw->wv, lw->wo, lw->wg, lw->wu, lw->wd};
+  for (int k = 0; k < EE_N_MATS; ++k) {
+    const MatPlace pl = placement(m, k);
+    ee_status s = place_bf16(c, srcs[k], pl.rows, pl.cols, blocks_bf[pl.block], pl.row0, pl.map, pl.param);
+    if (s != EE_OK) return s;
+    if (given) {
+      s = place_int4(c, lw->q4[k], lw->s4[k], pl.rows, pl.cols, blocks_q[pl.block], pl.row0, pl.map, pl.param);
+      if (s != EE_OK) return s;
+    }
+  }
+  if (!given) {
+    // the exit copy: quantise each fused block in its kernel row order
+    const int rows[4] = {m.nqkv, m.d, 2 * m.F, m.d};
+    const int cols[4] = {m.d, m.dq, m.d, m.F};
+    for (int k = 0; k < 4; ++k)
+      EE_CUDA(c, launch_quantize_int4(blocks_bf[k], rows[k], cols[k], blocks_q[k].q, blocks_q[k].s,
+                                      sstride_of(cols[k]), c->st));
+  }
+  EE_CUDA(c, cudaMemcpyAsync(b.g_attn, lw->g_attn, (size_t)m.d * 2, cudaMemcpyDefault, c->st));
+  EE_CUDA(c, cudaMemcpyAsync(b.g_ffn, lw->g_ffn, (size_t)m.d * 2, cudaMemcpyDefault, c->st));
+  EE_CUDA(c, cudaStreamSynchronize(c->st));
+  c->layer_loaded[layer] = 1;
+  return EE_OK;
+}
+
+ee_status ee_load_shared(ee_ctx* c, const ee_shared_weights* sw) {
+  if (!c) return EE_ERR_INVALID_ARG;
+  if (!sw || !sw->embed || !sw->g_final || (c->m.nck > 0 && !sw->exit_T))
+    return fail(c, EE_ERR_INVALID_ARG, "shared weights: NULL pointer");
+  for (int i = 0; i < c->m.nck; ++i)
+    if (!sw->exit_T[i]) return fail(c, EE_ERR_INVALID_ARG, "exit_T[%d] is NULL", i);
+  if (c->cuda_broken) return fail(c, EE_ERR_CUDA, "context unusable after an earlier CUDA error");
+  DeviceGuard dg(c->dev);
+  if (join_user_stream(c) != EE_OK) return EE_ERR_CUDA;
+  const Dims& m = c->m;
+  EE_CUDA(c, cudaMemcpyAsync(c->E, sw->embed, (size_t)m.V * m.d * 2, cudaMemcpyDefault, c->st));
+  EE_CUDA(c, cudaMemcpyAsync(c->g_final, sw->g_final, (size_t)m.d * 2, cudaMemcpyDefault, c->st));
+  for (int i = 0; i < m.nck; ++i) {
+    EE_CUDA(c, cudaMemcpyAsync(c->staging, sw->exit_T[i], (size_t)m.d * m.d * 2, cudaMemcpyDefault, c->st));
+    EE_CUDA(c, launch_transpose_bf16(c->Tt[i], (const uint16_t*)c->staging, m.d, c->st));
+  }
+  EE_CUDA(c, cudaStreamSynchronize(c->st));
+  c->shared_loaded = true;
+  return EE_OK;
+}
+
+ee_status ee_load_weights(ee_ctx* c, const ee_weights* w) {
+  if (!c) return EE_ERR_INVALID_ARG;
+  if (!w || !w->layers) return fail(c, EE_ERR_INVALID_ARG, "weights: NULL pointer");
+  for (int j = 0; j < c->m.L; ++j) {
+    const ee_status s = ee_load_layer(c, j, &w->layers[j]);
+    if (s != EE_OK) return s;
+  }
+  return ee_load_shared(c, &w->shared);
+}
+
+ee_status ee_set_thresholds(ee_ctx* c, const float* gamma) {
+  if (!c) return EE_ERR_INVALID_ARG;
+  if (c->m.nck > 0 && !gamma) return fail(c, EE_ERR_INVALID_ARG, "gamma is NULL");
+  for (int i = 0; i < c->m.nck; ++i)
+    if (isnan(gamma[i])) return fail(c, EE_ERR_INVALID_ARG, "gamma[%d] is NaN", i);
+  if (c->cuda_broken) return fail(c, EE_ERR_CUDA, "context unusable after an earlier CUDA error");
+  DeviceGuard dg(c->dev);
+  std::vector<float> g(EE_MAX_CHECKPOINTS, INFINITY);
+  for (int i = 0; i < c->m.nck; ++i) g[i] = gamma[i];
+  c->gamma.assign(g.begin(), g.begin() + c->m.nck);
+  if (join_user_stream(c) != EE_OK) return EE_ERR_CUDA;
+  EE_CUDA(c, cudaMemcpyAsync(c->gamma_dev, g.data(), g.size() * sizeof(float), cudaMemcpyHostToDevice, c->st));
+  EE_CUDA(c, cudaStreamSynchronize(c->st));
+  return EE_OK;
+}
+
+ee_status ee_set_exit_enabled(ee_ctx* c, int32_t enabled) {
+  if (!c) return EE_ERR_INVALID_ARG;
+  c->exit_enabled = enabled ? 1 : 0;
+  return EE_OK;
+}
+
+ee_status ee_set_use_graph(ee_ctx* c, int32_t use_graph) {
+  if (!c) return EE_ERR_INVALID_ARG;
+  c->use_graph = use_graph ? 1 : 0;
+  return EE_OK;
+}
+
+ee_status ee_set_debug(ee_ctx* c, int32_t debug) {
+  if (!c) return EE_ERR_INVALID_ARG;
+  c->debug = debug ? 1 : 0;
+  return EE_OK;
+}
+
+ee_status ee_reset(ee_ctx* c) {
+  if (!c) return EE_ERR_INVALID_ARG;
+  if (c->cuda_broken) return fail(c, EE_ERR_CUDA, "context unusable after an earlier CUDA error");
+  DeviceGuard dg(c->dev);
+  if (join_user_stream(c) != EE_OK) return EE_ERR_CUDA;
+  reset_blocks(c);
+  if (fill_sentinel(c) != EE_OK) return EE_ERR_CUDA;
+  EE_CUDA(c, cudaStreamSynchronize(c->st));
+  return EE_OK;
+}
+
+ee_status ee_prefill(ee_ctx* c, int32_t batch, const int32_t* prompt_lens, const int32_t* tokens_concat,
+                     int32_t* first_tokens_out) {
+  if (!c) return EE_ERR_INVALID_ARG;
+  const Dims& m = c->m;
+  if (batch < 1 || batch > m.maxb)
+    return fail(c, EE_ERR_CAPACITY, "batch %d outside [1, max_batch=%d]", batch, m.maxb);
+  if (!prompt_lens || !tokens_concat || !first_tokens_out)
+    return fail(c, EE_ERR_INVALID_ARG, "prefill: NULL pointer");
+  int64_t total = 0;
+  int Tmax = 0;
+  for (int s = 0; s < batch; ++s) {
+    if (prompt_lens[s] < 1) return fail(c, EE_ERR_INVALID_ARG, "prompt %d is empty", s);
+    if (prompt_lens[s] >= m.maxs)
+      return fail(c, EE_ERR_CAPACITY, "prompt %d length %d >= max_seq_len %d", s, prompt_lens[s], m.maxs);
+    total += prompt_lens[s];
+    Tmax = std::max(Tmax, prompt_lens[s]);
+  }
+  for (int64_t i = 0; i < total; ++i)
+    if (tokens_concat[i] < 0 || tokens_concat[i] >= m.V)
+      return fail(c, EE_ERR_INVALID_ARG, "prompt token %lld = %d outside [0, vocab)", (long long)i,
+                  tokens_concat[i]);
+  ee_status s = check_ready(c);
+  if (s != EE_OK) return s;
+  DeviceGuard dg(c->dev);
+  if (join_user_stream(c) != EE_OK) return EE_ERR_CUDA;
+  reset_blocks(c);
+  c->batch = batch;
+  // blocks for every prompt, sequence by sequence, lowest ids first
+  std::vector<int32_t> bt((size_t)m.maxb * m.bps, 0);
+  std::vector<int64_t> offs(batch);
+  int64_t off = 0;
+  for (int q = 0; q < batch; ++q) {
+    offs[q] = off;
+    off += prompt_lens[q];
+    const int nb = (int)ceil_div(prompt_lens[q], EE_KV_BLOCK);
+    for (int i = 0; i < nb; ++i) {
+      const int32_t b = alloc_block(c);
+      if (b < 0) return fail(c, EE_ERR_CAPACITY, "KV cache out of blocks");
+      c->seq_blocks[q].push_back(b);
+      bt[(size_t)q * m.bps + i] = b;
+    }
+  }
+  EE_CUDA(c, cudaMemcpyAsync(c->block_table, bt.data(), bt.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
+                             c->st));
+  EE_CUDA(c, cudaStreamSynchronize(c->st));
+  StepDesc* d = c->desc_host;
+  for (int t = 0; t < Tmax; ++t) {
+    d->n_part = 0;
+    d->n_fin = 0;
+    for (int q = 0; q < batch; ++q) {
+      d->new_block[q] = -1;
+      if (t < prompt_lens[q]) {
+        d->part[d->n_part++] = q;
+        d->tokens[q] = tokens_concat[offs[q] + t];
+        d->pos[q] = t;
+        if (t == prompt_lens[q] - 1) d->fin[d->n_fin++] = q;
+      }
+    }
+    d->debug = c->debug;
+    s = run_step(c, batch, false);
+    if (s != EE_OK) return s;
+    for (int i = 0; i < d->n_fin; ++i) first_tokens_out[d->fin[i]] = c->out_host->next_token[d->fin[i]];
+  }
+  for (int q = 0; q < batch; ++q) c->seq_pos[q] = prompt_lens[q];
+  return EE_OK;
+}
+
+ee_status ee_decode_step(ee_ctx* c, const int32_t* in_tokens, int32_t* next_tokens_out,
+                         int32_t* exit_layers_out) {
+  if (!c) return EE_ERR_INVALID_ARG;
+  if (c->batch < 1) return fail(c, EE_ERR_STATE, "decode before prefill");
+  if (!in_tokens || !next_tokens_out || !exit_layers_out)
+    return fail(c, EE_ERR_INVALID_ARG, "decode: NULL pointer");
+  const Dims& m = c->m;
+  const int B = c->batch;
+  for (int q = 0; q < B; ++q) {
+    if (in_tokens[q] < 0 || in_tokens[q] >= m.V)
+      return fail(c, EE_ERR_INVALID_ARG, "token %d of sequence %d outside [0, vocab)", in_tokens[q], q);
+    if (c->seq_pos[q] >= m.maxs)
+      return fail(c, EE_ERR_CAPACITY, "sequence %d reached max_seq_len %d", q, m.maxs);
+  }
+  ee_status s = check_ready(c);
+  if (s != EE_OK) return s;
+  DeviceGuard dg(c->dev);
+  if (join_user_stream(c) != EE_OK) return EE_ERR_CUDA;
+  StepDesc* d = c->desc_host;
+  d->n_part = B;
+  d->n_fin = B;
+  for (int q = 0; q < B; ++q) {
+    d->part[q] = q;
+    d->fin[q] = q;
+    d->tokens[q] = in_tokens[q];
+    d->pos[q] = c->seq_pos[q];
+    d->new_block[q] = -1;
+    if (c->seq_pos[q] % EE_KV_BLOCK == 0) {
+      const int32_t b = alloc_block(c);
+      if (b < 0) return fail(c, EE_ERR_CAPACITY, "KV cache out of blocks");
+      c->seq_blocks[q].push_back(b);
+      d->new_block[q] = b;
+    }
+  }
+  d->debug = c->debug;
+  s = run_step(c, B, c->exit_enabled && m.nck > 0);
+  if (s != EE_OK) return s;
+  for (int q = 0; q < B; ++q) {
+    next_tokens_out[q] = c->out_host->next_token[q];
+    exit_layers_out[q] = c->out_host->exit_layer[q];
+    c->seq_pos[q] += 1;
+  }
+  return EE_OK;
+}
+
+ee_status ee_seq_info(const ee_ctx* c, int32_t* batch, int32_t seq, int32_t* pos) {
+  if (!c) return EE_ERR_INVALID_ARG;
+  if (batch) *batch = c->batch;
+  if (pos) {
+    if (seq < 0 || seq >= c->batch) return EE_ERR_INVALID_ARG;
+    *pos = c->seq_pos[seq];
+  }
+  return EE_OK;
+}
+
+ee_status ee_debug_hidden(ee_ctx* c, int32_t layer, float* out) {
+  if (!c || !out) return EE_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= c->m.L) return fail(c, EE_ERR_INVALID_ARG, "layer out of range");
+  DeviceGuard dg(c->dev);
+  EE_CUDA(c, cudaMemcpy(out, c->hdbg + (size_t)layer * EE_MAX_BATCH * c->m.d,
+                        (size_t)c->batch * c->m.d * sizeof(float), cudaMemcpyDeviceToHost));
+  return EE_OK;
+}
+
+ee_status ee_debug_conf(ee_ctx* c, float* out) {
+  if (!c || !out) return EE_ERR_INVALID_ARG;
+  for (int q = 0; q < c->batch; ++q)
+    for (int k = 0; k < c->m.nck; ++k) out[q * c->m.nck + k] = c->out_host->conf[q * EE_MAX_CHECKPOINTS + k];
+  return EE_OK;
+}
+
+ee_status ee_debug_kv(ee_ctx* c, int32_t seq, int32_t layer, int32_t pos, uint16_t* k, uint16_t* v) {
+  if (!c || !k || !v) return EE_ERR_INVALID_ARG;
+  const Dims& m = c->m;
+  if (seq < 0 || seq >= c->batch || layer < 0 || layer >= m.L || pos < 0 || pos >= c->seq_pos[seq])
+    return fail(c, EE_ERR_INVALID_ARG, "debug_kv: index out of range");
+  DeviceGuard dg(c->dev);
+  const int32_t block = c->seq_blocks[seq][pos / EE_KV_BLOCK];
+  const int off = pos % EE_KV_BLOCK;
+  for (int g = 0; g < m.hkv; ++g) {
+    const size_t e = (size_t)layer * m.kv_layer_elems + (((size_t)block * m.hkv + g) * EE_KV_BLOCK + off) * m.hd;
+    EE_CUDA(c, cudaMemcpy(k + (size_t)g * m.hd, c->kcache + e, (size_t)m.hd * 2, cudaMemcpyDeviceToHost));
+    EE_CUDA(c, cudaMemcpy(v + (size_t)g * m.hd, c->vcache + e, (size_t)m.hd * 2, cudaMemcpyDeviceToHost));
+  }
+  return EE_OK;
+}
+
+ee_status ee_debug_block_table(ee_ctx* c, int32_t seq, int32_t* out, int32_t cap, int32_t* n_blocks) {
+  if (!c || !n_blocks) return EE_ERR_INVALID_ARG;
+  if (seq < 0 || seq >= c->batch) return fail(c, EE_ERR_INVALID_ARG, "seq out of range");
+  const auto& b = c->seq_blocks[seq];
+  *n_blocks = (int32_t)b.size();
+  if (out)
+    for (int i = 0; i < (int)b.size() && i < cap; ++i) out[i] = b[i];
+  // cross-check with the device copy
+  DeviceGuard dg(c->dev);
+  std::vector<int32_t> dev(c->m.bps);
+  EE_CUDA(c, cudaMemcpy(dev.data(), c->block_table + (size_t)seq * c->m.bps, dev.size() * 4,
+                        cudaMemcpyDeviceToHost));
+  for (size_t i = 0; i < b.size(); ++i)
+    if (dev[i] != b[i]) return fail(c, EE_ERR_STATE, "device block table differs at %zu", i);
+  return EE_OK;
+}
+
+ee_status ee_debug_int4(ee_ctx* c, int32_t layer, int32_t mat, uint8_t* packed, uint16_t* scales) {
+  if (!c || !packed || !scales) return EE_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= c->m.L || mat < 0 || mat >= EE_N_MATS)
+    return fail(c, EE_ERR_INVALID_ARG, "debug_int4: index out of range");
+  DeviceGuard dg(c->dev);
+  const Dims& m = c->m;
+  const MatPlace pl = placement(m, mat);
+  const LayerBufs& b = c->layers[layer];
+  const Mat4 blk[4] = {b.qkv, b.o, b.gu, b.d};
+  const int K = pl.cols, ng = (int)ceil_div(K, EE_QUANT_GROUP), ss = sstride_of(K);
+  for (int r = 0; r < pl.rows; ++r) {
+    const int64_t dr = device_row(pl, r);
+    EE_CUDA(c, cudaMemcpy(packed + (size_t)r * K / 2, blk[pl.block].q + dr * K / 2, K / 2,
+                          cudaMemcpyDeviceToHost));
+    EE_CUDA(c, cudaMemcpy(scales + (size_t)r * ng, blk[pl.block].s + dr * ss, (size_t)ng * 2,
+                          cudaMemcpyDeviceToHost));
+  }
+  return EE_OK;
+}
+
+// ------------------------------------------------------------------ single kernels
+static int device_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (linear_prepare() != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n > kHeadGridMax ? kHeadGridMax : n;
+}
+
+ee_status ee_op_quantize_int4(const uint16_t* w, int32_t rows, int32_t cols, uint8_t* packed,
+                              uint16_t* scales, int32_t scale_stride, void* stream) {
+  if (!w || !packed || !scales || rows < 0 || cols <= 0 || cols % 32 ||
+      scale_stride < ceil_div(cols, EE_QUANT_GROUP))
+    return EE_ERR_INVALID_ARG;
+  return launch_quantize_int4(w, rows, cols, packed, scales, scale_stride, (cudaStream_t)stream) ==
+                 cudaSuccess
+             ? EE_OK
+             : EE_ERR_CUDA;
+}
+
+static ee_status op_linear(int32_t M, int32_t N, int32_t K, const uint16_t* xb, const uint16_t* xh,
+                           const uint16_t* w, const uint8_t* q, const uint16_t* s, int32_t sstride, float* y,
+                           int32_t* err, void* stream) {
+  if (M < 1 || M > EE_MAX_BATCH || N < 2 || N % 2 || K < 32 || K % 32 || !y) return EE_ERR_INVALID_ARG;
+  if (q && ((uintptr_t)q % 16 || (uintptr_t)s % 16 || sstride % 8)) return EE_ERR_INVALID_ARG;
+  if (w && (uintptr_t)w % 16) return EE_ERR_INVALID_ARG;
+  const int sms = device_sms();
+  if (sms <= 0) return EE_ERR_CUDA;
+  LinearParams p = {};
+  p.N = N;
+  p.K = K;
+  p.w = w;
+  p.wq = q;
+  p.ws = s;
+  p.sstride = sstride;
+  p.m_direct_full = w ? M : 0;
+  p.m_direct_exit = q ? M : 0;
+  p.xb = xb;
+  p.xh = xh;
+  p.x_stride = K;
+  p.epi = EPI_F32;
+  p.out_f32 = y;
+  p.out_stride = N;
+  p.err = err;
+  return launch_linear(p, linear_grid(N, sms), false, (cudaStream_t)stream) == cudaSuccess ? EE_OK
+                                                                                           : EE_ERR_CUDA;
+}
+
+ee_status ee_op_linear_bf16(int32_t M, int32_t N, int32_t K, const uint16_t* x, const uint16_t* w, float* y,
+                            int32_t* err_flag, void* stream) {
+  if (!x || !w) return EE_ERR_INVALID_ARG;
+  return op_linear(M, N, K, x, nullptr, w, nullptr, nullptr, 0, y, err_flag, stream);
+}
+
+ee_status ee_op_linear_int4(int32_t M, int32_t N, int32_t K, const uint16_t* x_f16, const uint8_t* packed,
+                            const uint16_t* scales, int32_t scale_stride, float* y, int32_t* err_flag,
+                            void* stream) {
+  if (!x_f16 || !packed || !scales || scale_stride < ceil_div(K, EE_QUANT_GROUP)) return EE_ERR_INVALID_ARG;
+  return op_linear(M, N, K, nullptr, x_f16, nullptr, packed, scales, scale_stride, y, err_flag, stream);
+}
+
+size_t ee_attention_scratch_bytes(int32_t B, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim) {
+  if (B < 1 || B > EE_MAX_BATCH || n_kv_heads < 1 || n_heads % n_kv_heads) return 0;
+  const int nsplit = attention_nsplit(B, n_kv_heads, kHeadGridMax);
+  return align_up(attention_part_floats(B, n_heads, n_kv_heads, head_dim, nsplit) * 4, kAlign) +
+         (size_t)EE_MAX_BATCH * n_kv_heads * 4;
+}
+
+ee_status ee_op_attention(int32_t B, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, const float* q,
+                          const uint16_t* kcache, const uint16_t* vcache, const int32_t* block_table,
+                          int32_t bt_stride, const int32_t* pos, float* o, void* scratch, int32_t* err_flag,
+                          void* stream) {
+  if (B < 1 || B > EE_MAX_BATCH || n_kv_heads < 1 || n_heads % n_kv_heads || (head_dim != 64 && head_dim != 128))
+    return EE_ERR_INVALID_ARG;
+  const int G = n_heads / n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return EE_ERR_INVALID_ARG;
+  if (!q || !kcache || !vcache || !block_table || !pos || !o || !scratch || bt_stride < 1)
+    return EE_ERR_INVALID_ARG;
+  const int sms = device_sms();
+  if (sms <= 0) return EE_ERR_CUDA;
+  AttnParams p = {};
+  p.m_direct = B;
+  p.n_heads = n_heads;
+  p.n_kv_heads = n_kv_heads;
+  p.head_dim = head_dim;
+  p.q = q;
+  p.q_stride = n_heads * head_dim;
+  p.kc = kcache;
+  p.vc = vcache;
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.pos = pos;
+  p.nsplit = attention_nsplit(B, n_kv_heads, sms);
+  const size_t pbytes =
+      align_up(attention_part_floats(B, n_heads, n_kv_heads, head_dim,
+                                     attention_nsplit(B, n_kv_heads, kHeadGridMax)) * 4, kAlign);
+  p.part = (float*)scratch;
+  p.counters = (int32_t*)((uint8_t*)scratch + pbytes);
+  p.o_f32 = o;
+  p.o_stride = n_heads * head_dim;
+  p.err = err_flag;
+  return launch_attention(p, B, false, (cudaStream_t)stream) == cudaSuccess ? EE_OK : EE_ERR_CUDA;
+}
+
+size_t ee_head_scratch_bytes(int32_t M) {
+  if (M < 1 || M > EE_MAX_BATCH) return 0;
+  return (size_t)kHeadGridMax * EE_MAX_BATCH * 4 * 4 + kAlign;
+}
+
+ee_status ee_op_vocab_head(int32_t M, int32_t V, int32_t d, const uint16_t* u, const uint16_t* E, float* conf,
+                           int32_t* argmax, void* scratch, int32_t* err_flag, void* stream) {
+  if (M < 1 || M > EE_MAX_BATCH || V < 2 || V % 2 || d < 32 || d % 32 || !u || !E || !conf || !argmax ||
+      !scratch)
+    return EE_ERR_INVALID_ARG;
+  const int sms = device_sms();
+  if (sms <= 0) return EE_ERR_CUDA;
+  LinearParams p = {};
+  p.N = V;
+  p.K = d;
+  p.w = E;
+  p.m_direct_full = M;
+  p.xb = u;
+  p.x_stride = d;
+  p.epi = EPI_HEAD;
+  p.head_mode = HEAD_CONF_ARGMAX;
+  p.head_part = (float*)scratch;
+  p.head_counter = (int32_t*)((uint8_t*)scratch + (size_t)kHeadGridMax * EE_MAX_BATCH * 4 * 4);
+  p.conf_out = conf;
+  p.argmax_out = argmax;
+  p.err = err_flag;
+  return launch_linear(p, std::min(linear_grid(V, sms), kHeadGridMax), false, (cudaStream_t)stream) ==
+                 cudaSuccess
+             ? EE_OK
+             : EE_ERR_CUDA;
+}
+
+}  // extern "C"

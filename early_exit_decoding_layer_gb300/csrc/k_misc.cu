@@ -1,0 +1,281 @@
+// Small kernels of the decode step (RMSNorm, step start with the embedding
+// gather) and the load-time kernels (int4 quantiser, row re-layout,
+// transpose, fill).
+#include <math.h>
+
+#include "ee_common.cuh"
+#include "ee_kernels.cuh"
+
+namespace ee {
+
+namespace {
+
+// ------------------------------------------------------------------ RMSNorm
+// x = h * rsqrt(mean(h^2) + eps) * g for every listed sequence; writes the
+// bf16 copy and (if requested) the fp16 copy in the int4 kernels' pair order.
+__global__ void __launch_bounds__(256) k_rmsnorm(const NormParams p) {
+  __shared__ float red[8];
+  grid_dep_wait();
+  grid_dep_launch();
+  const int count = ld_volatile_i32(p.list);
+  const int z = blockIdx.x;
+  if (z >= count) return;
+  const int seq = p.list[1 + z];
+  const float* h = p.h + (size_t)seq * p.h_stride;
+  const int tid = threadIdx.x;
+  float ss = 0.0f;
+  for (int i = tid * 4; i < p.d; i += 256 * 4) {
+    const float4 v = *reinterpret_cast<const float4*>(h + i);
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
+  }
+  ss = warp_sum(ss);
+  if ((tid & 31) == 0) red[tid >> 5] = ss;
+  __syncthreads();
+  float tot = 0.0f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) tot += red[w];
+  const float r = rsqrtf(tot / (float)p.d + p.eps);
+  uint16_t* xb = p.xb + (size_t)seq * p.x_stride;
+  uint16_t* xh = p.xh ? p.xh + (size_t)seq * p.x_stride : nullptr;
+  for (int i = tid * 4; i < p.d; i += 256 * 4) {
+    const float4 v = *reinterpret_cast<const float4*>(h + i);
+    const uint2 gw = *reinterpret_cast<const uint2*>(p.g + i);
+    const float x0 = v.x * r * bf16_lo(gw.x), x1 = v.y * r * bf16_hi(gw.x);
+    const float x2 = v.z * r * bf16_lo(gw.y), x3 = v.w * r * bf16_hi(gw.y);
+    uint2 o;
+    o.x = uint32_t(float_to_bf16_bits(x0)) | (uint32_t(float_to_bf16_bits(x1)) << 16);
+    o.y = uint32_t(float_to_bf16_bits(x2)) | (uint32_t(float_to_bf16_bits(x3)) << 16);
+    *reinterpret_cast<uint2*>(xb + i) = o;
+    if (xh) {
+      xh[xh_slot(i)] = float_to_half_bits(x0);
+      xh[xh_slot(i + 1)] = float_to_half_bits(x1);
+      xh[xh_slot(i + 2)] = float_to_half_bits(x2);
+      xh[xh_slot(i + 3)] = float_to_half_bits(x3);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ step start
+// CTA z handles the z-th participating sequence: position, new KV block,
+// embedding gather h = E[token] (fp32), per-step outputs reset.  CTA 0 also
+// sets the lists: full = participants, exit = empty, final-head rows.
+__global__ void __launch_bounds__(256) k_step_begin(const BeginParams p) {
+  const StepDesc* d = p.desc;
+  const int z = blockIdx.x, tid = threadIdx.x;
+  const int n = min(d->n_part, EE_MAX_BATCH);
+  if (z == 0) {
+    if (tid < EE_MAX_BATCH) {
+      const int v = tid < n ? d->part[tid] : 0;
+      p.lists->part[1 + tid] = v;
+      p.lists->full[1 + tid] = v;
+      p.lists->exitl[1 + tid] = 0;
+      p.lists->fin[1 + tid] = tid < d->n_fin ? d->fin[tid] : 0;
+    }
+    if (tid == 0) {
+      p.lists->part[0] = n;
+      p.lists->full[0] = n;
+      p.lists->exitl[0] = 0;
+      p.lists->fin[0] = min(d->n_fin, EE_MAX_BATCH);
+      p.out->err = 0;
+      *p.dbg_flag = d->debug;
+    }
+  }
+  if (z >= n) return;
+  const int seq = d->part[z];
+  const int pos = d->pos[seq];
+  if (tid == 0) {
+    p.pos[seq] = pos;
+    if (d->new_block[seq] >= 0) p.block_table[(size_t)seq * p.bt_stride + (pos >> 4)] = d->new_block[seq];
+    p.out->exit_layer[seq] = p.n_layers - 1;
+    p.out->next_token[seq] = -1;
+  }
+  for (int c = tid; c < EE_MAX_CHECKPOINTS; c += 256)
+    p.out->conf[seq * EE_MAX_CHECKPOINTS + c] = __int_as_float(0x7fc00000);
+  const uint16_t* e = p.embed + (size_t)d->tokens[seq] * p.d;
+  float* h = p.h + (size_t)seq * p.h_stride;
+  for (int i = tid * 2; i < p.d; i += 512) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(e + i);
+    *reinterpret_cast<float2*>(h + i) = make_float2(bf16_lo(w), bf16_hi(w));
+  }
+}
+
+// ------------------------------------------------------------------ quantiser
+// One warp per (row, group of 128 columns): s = bf16(amax / 7) and
+// q = clamp(round_half_even(w / s), -8, 7), both divisions IEEE round to
+// nearest in fp32; amax = 0 gives s = 0, q = 0.  Lane l handles columns
+// 4l..4l+3 of the group and writes their two packed bytes (column 2j in the
+// low nibble).
+__global__ void __launch_bounds__(256) k_quantize(const uint16_t* w, int rows, int cols,
+                                                  uint8_t* packed, uint16_t* scales, int sstride) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ng = (cols + EE_QUANT_GROUP - 1) / EE_QUANT_GROUP;
+  const long long gw = (long long)blockIdx.x * 8 + warp;
+  if (gw >= (long long)rows * ng) return;
+  const int r = (int)(gw / ng), gi = (int)(gw % ng);
+  const int c0 = gi * EE_QUANT_GROUP + lane * 4;
+  const bool valid = c0 < cols;
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  if (valid) {
+    const uint2 u = *reinterpret_cast<const uint2*>(w + (size_t)r * cols + c0);
+    v[0] = bf16_lo(u.x);
+    v[1] = bf16_hi(u.x);
+    v[2] = bf16_lo(u.y);
+    v[3] = bf16_hi(u.y);
+  }
+  float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+  amax = warp_max(amax);
+  const uint16_t sb = float_to_bf16_bits(__fdiv_rn(amax, 7.0f));
+  const float s = bf16_bits_to_float(sb);
+  int q[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    int qi = 0;
+    if (s != 0.0f) {
+      qi = __float2int_rn(__fdiv_rn(v[i], s));
+      qi = qi < -8 ? -8 : (qi > 7 ? 7 : qi);
+    }
+    q[i] = qi;
+  }
+  if (valid) {
+    const uint16_t two = (uint16_t)((q[0] & 0xF) | ((q[1] & 0xF) << 4) | ((q[2] & 0xF) << 8) |
+                                    ((q[3] & 0xF) << 12));
+    *reinterpret_cast<uint16_t*>(packed + (size_t)r * (cols / 2) + c0 / 2) = two;
+  }
+  if (lane == 0) {
+    scales[(size_t)r * sstride + gi] = sb;
+    if (gi == ng - 1)
+      for (int j = ng; j < sstride; ++j) scales[(size_t)r * sstride + j] = 0;
+  }
+}
+
+// ------------------------------------------------------------------ re-layout
+__device__ __forceinline__ long long map_row(long long r, int map, int param) {
+  if (map == MAP_ROPE_PAIRS) {
+    const long long head = r / param, i = r % param, half = param / 2;
+    return head * param + (i < half ? 2 * i : 2 * (i - half) + 1);
+  }
+  if (map == MAP_INTERLEAVE) return 2 * r + param;
+  return r;
+}
+
+__global__ void k_copy_rows16(uint8_t* dst, long long dst_stride, long long dst_row0,
+                              const uint8_t* src, long long src_stride, long long row_bytes,
+                              long long nrows, int map, int param) {
+  const long long per_row = row_bytes / 16;
+  const long long total = per_row * nrows;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long r = i / per_row, c = i % per_row;
+    const long long dr = dst_row0 + map_row(r, map, param);
+    *reinterpret_cast<uint4*>(dst + dr * dst_stride + c * 16) =
+        *reinterpret_cast<const uint4*>(src + r * src_stride + c * 16);
+  }
+}
+
+__global__ void k_copy_rows2(uint8_t* dst, long long dst_stride, long long dst_row0,
+                             const uint8_t* src, long long src_stride, long long row_bytes,
+                             long long nrows, int map, int param) {
+  const long long per_row = row_bytes / 2;
+  const long long total = per_row * nrows;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long r = i / per_row, c = i % per_row;
+    const long long dr = dst_row0 + map_row(r, map, param);
+    *reinterpret_cast<uint16_t*>(dst + dr * dst_stride + c * 2) =
+        *reinterpret_cast<const uint16_t*>(src + r * src_stride + c * 2);
+  }
+}
+
+__global__ void k_transpose(uint16_t* dst, const uint16_t* src, int n) {
+  __shared__ uint16_t tile[32][33];
+  const int bx = blockIdx.x * 32, by = blockIdx.y * 32;
+  for (int j = threadIdx.y; j < 32; j += 8) {
+    const int r = by + j, c = bx + threadIdx.x;
+    if (r < n && c < n) tile[j][threadIdx.x] = src[(size_t)r * n + c];
+  }
+  __syncthreads();
+  for (int j = threadIdx.y; j < 32; j += 8) {
+    const int r = bx + j, c = by + threadIdx.x;
+    if (r < n && c < n) dst[(size_t)r * n + c] = tile[threadIdx.x][j];
+  }
+}
+
+__global__ void k_fill_u16(uint16_t* p, uint16_t v, long long n) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    p[i] = v;
+}
+
+cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, cudaStream_t st, bool pdl, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cfg;
+}
+
+}  // namespace
+
+cudaError_t launch_rmsnorm(const NormParams& p, int batch_slots, bool pdl, cudaStream_t st) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(batch_slots), dim3(256), st, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, k_rmsnorm, p);
+}
+
+cudaError_t launch_step_begin(const BeginParams& p, int batch_slots, cudaStream_t st) {
+  k_step_begin<<<batch_slots, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_int4(const uint16_t* w, int rows, int cols, uint8_t* packed,
+                                 uint16_t* scales, int sstride, cudaStream_t st) {
+  const long long warps = (long long)rows * ((cols + EE_QUANT_GROUP - 1) / EE_QUANT_GROUP);
+  const long long blocks = (warps + 7) / 8;
+  if (blocks <= 0) return cudaSuccess;
+  k_quantize<<<(unsigned)blocks, 256, 0, st>>>(w, rows, cols, packed, scales, sstride);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_rows(void* dst, int64_t dst_stride_bytes, int64_t dst_row0, const void* src,
+                             int64_t src_stride_bytes, int64_t row_bytes, int64_t nrows, int map,
+                             int param, cudaStream_t st) {
+  if (nrows <= 0 || row_bytes <= 0) return cudaSuccess;
+  const bool v16 = (row_bytes % 16 == 0) && (dst_stride_bytes % 16 == 0) &&
+                   (src_stride_bytes % 16 == 0) && ((uintptr_t)dst % 16 == 0) &&
+                   ((uintptr_t)src % 16 == 0);
+  const long long units = v16 ? row_bytes / 16 * nrows : row_bytes / 2 * nrows;
+  long long blocks = (units + 255) / 256;
+  if (blocks > 65535) blocks = 65535;
+  if (v16)
+    k_copy_rows16<<<(unsigned)blocks, 256, 0, st>>>((uint8_t*)dst, dst_stride_bytes, dst_row0,
+                                                    (const uint8_t*)src, src_stride_bytes, row_bytes,
+                                                    nrows, map, param);
+  else
+    k_copy_rows2<<<(unsigned)blocks, 256, 0, st>>>((uint8_t*)dst, dst_stride_bytes, dst_row0,
+                                                   (const uint8_t*)src, src_stride_bytes, row_bytes,
+                                                   nrows, map, param);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_bf16(uint16_t* dst, const uint16_t* src, int n, cudaStream_t st) {
+  dim3 grid((n + 31) / 32, (n + 31) / 32), block(32, 8);
+  k_transpose<<<grid, block, 0, st>>>(dst, src, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_u16(uint16_t* p, uint16_t v, int64_t n, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  long long blocks = (n + 255) / 256;
+  if (blocks > 65535) blocks = 65535;
+  k_fill_u16<<<(unsigned)blocks, 256, 0, st>>>(p, v, n);
+  return cudaGetLastError();
+}
+
+}  // namespace ee

@@ -1,0 +1,179 @@
+"""Helpers of the GPU parity tests: build a DecodeEngine and an oracle over
+the same seeded weights, and drive both step by step.
+
+Decision rule (exit decisions and greedy tokens must be identical except
+where floating point legitimately decides otherwise):
+* an exit decision may differ only where the oracle's confidence lies within
+  a window of gamma_l; two windows are counted: the absolute |conf - gamma| <
+  1e-3 of the workload definition and the relative |conf - gamma| < 1e-2 gamma
+  that the tests enforce (with random N(0, 0.02) weights confidences are
+  ~1e-3, so the absolute window would excuse every decision; the relative one
+  follows from the error budget: hidden states agree to ~1e-3 relative, logits
+  to ~1e-3 absolute, so conf to ~1e-3 relative, and 1e-2 leaves a 10x margin);
+* a token may differ only where the oracle's top-2 final-logit margin is
+  below 1e-3.
+In both cases the oracle adopts the GPU's decision / token and continues.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+import early_exit_decoding_layer_gb300 as ee
+import oracle
+import synth
+
+HIDDEN_TOL = 1e-2        # per-layer relative L2 of the residual stream
+CONF_REL_TOL = 2e-2      # GPU vs oracle confidence, relative
+REL_WINDOW = 1e-2        # decision window, relative to gamma
+ABS_WINDOW = 1e-3        # decision window of the workload definition
+MARGIN_WINDOW = 1e-3     # token window: top-2 logit margin
+
+
+def load_engine(w: synth.Workload, max_batch=None, max_seq_len=None, checkpoints=None,
+                int4_from_oracle=False, layers=None) -> ee.DecodeEngine:
+    shape = w.shape
+    ck = tuple(w.checkpoints if checkpoints is None else checkpoints)
+    eng = ee.DecodeEngine(shape, ck, max_batch or w.batch, max_seq_len or w.max_seq_len())
+    for j in range(shape.n_layers):
+        lw = synth.layer_weights(shape, w.seed, j)
+        int4 = None
+        if int4_from_oracle:
+            int4 = {}
+            for m in synth.MATS:
+                q, s = oracle.quantize_int4_group(lw[m], shape.quant_group)
+                int4[m] = (oracle.pack_int4(q), s)
+        eng.load_layer(j, lw, int4)
+    T = [synth.exit_transform(shape, w.seed, c) for c in range(len(ck))]
+    eng.load_shared(synth.embedding(shape, w.seed), synth.final_gain(shape), T)
+    return eng
+
+
+def build_oracle(w: synth.Workload, max_batch=None, max_seq_len=None, checkpoints=None,
+                 cache_bytes=4 << 30) -> oracle.Oracle:
+    o = oracle.build_oracle(w, cache_bytes=cache_bytes, max_batch=max_batch or w.batch,
+                            max_seq_len=max_seq_len or w.max_seq_len())
+    if checkpoints is not None:
+        ck = tuple(checkpoints)
+        o.cfg.checkpoints = ck
+        o.W.T = [oracle.bf16_to_f64(synth.exit_transform(w.shape, w.seed, c)) for c in range(len(ck))]
+        o.gamma = np.full(len(ck), np.inf)
+    return o
+
+
+def rel_l2(a, b) -> float:
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+@dataclass
+class Stats:
+    steps: int = 0
+    decisions: int = 0
+    exit_mismatch: int = 0
+    token_mismatch: int = 0
+    in_abs_window: int = 0
+    in_rel_window: int = 0
+    max_hidden_rel: float = 0.0
+    max_conf_rel: float = 0.0
+    gpu_exits: list = field(default_factory=list)
+    gpu_tokens: list = field(default_factory=list)
+
+
+def drive(eng: ee.DecodeEngine, orc: oracle.Oracle, prompts, gamma, steps: int,
+          check_hidden: bool = True, gamma_per_step=None, exit_enabled: bool = True) -> Stats:
+    """Prefill both sides, then decode `steps` steps, asserting parity."""
+    L = orc.cfg.n_layers
+    ck = list(orc.cfg.checkpoints)
+    st = Stats()
+    eng.set_exit_enabled(exit_enabled)
+    eng.set_debug(check_hidden)
+    g0 = np.asarray(gamma, dtype=np.float64)
+    eng.set_thresholds(g0)
+    orc.set_thresholds(g0)
+    gfirst = eng.prefill(prompts)
+    ofirst = orc.prefill(prompts)
+    for s in range(len(prompts)):
+        if gfirst[s] != ofirst[s]:
+            hs, logits = oracle.forward_full(orc.cfg, orc.W, list(prompts[s]))
+            assert oracle.top2_margin(logits) < MARGIN_WINDOW, (s, gfirst[s], ofirst[s])
+            st.token_mismatch += 1
+    tok = gfirst.copy()
+    for k in range(steps):
+        if gamma_per_step is not None:
+            g = np.asarray(gamma_per_step[k], dtype=np.float64)
+            eng.set_thresholds(g)
+            orc.set_thresholds(g)
+        else:
+            g = g0
+        snap = orc.snapshot()
+        gn, ge = eng.decode_step(tok)
+        gconf = eng.debug_conf().astype(np.float64)
+        r = orc.decode_step(tok, eval_heads=exit_enabled)
+        if not np.array_equal(ge, r.exit_layers):
+            forced = []
+            for s in range(len(tok)):
+                if ge[s] != r.exit_layers[s]:
+                    # the first checkpoint where the two sides decided differently
+                    c = ck.index(min(x for x in (ge[s], r.exit_layers[s]) if x in ck))
+                    co = r.conf[s, c]
+                    assert not np.isnan(co)
+                    assert abs(co - g[c]) < REL_WINDOW * abs(g[c]), (
+                        "step %d seq %d: exit %d (GPU) vs %d (oracle), conf %.6g gamma %.6g"
+                        % (k, s, ge[s], r.exit_layers[s], co, g[c]))
+                    st.exit_mismatch += 1
+                forced.append(int(ge[s]) if ge[s] in ck else -1)
+            orc.restore(snap)
+            r = orc.decode_step(tok, forced_exit=forced, eval_heads=exit_enabled)
+        # confidences agree wherever both evaluated the head
+        both = ~np.isnan(r.conf) & ~np.isnan(gconf)
+        assert np.array_equal(np.isnan(r.conf), np.isnan(gconf)), (k, r.conf, gconf)
+        if both.any():
+            rel = np.abs(gconf[both] - r.conf[both]) / r.conf[both]
+            st.max_conf_rel = max(st.max_conf_rel, float(rel.max()))
+            assert rel.max() < CONF_REL_TOL, (k, gconf, r.conf)
+            gmat = np.broadcast_to(g, r.conf.shape)
+            dist = np.abs(r.conf[both] - gmat[both])
+            st.decisions += int(both.sum())
+            st.in_abs_window += int((dist < ABS_WINDOW).sum())
+            st.in_rel_window += int((dist < REL_WINDOW * np.abs(gmat[both])).sum())
+        if check_hidden:
+            for j in range(L):
+                gh = eng.debug_hidden(j)
+                for s in range(len(tok)):
+                    e = rel_l2(gh[s], r.hidden[j, s])
+                    st.max_hidden_rel = max(st.max_hidden_rel, e)
+                    assert e < HIDDEN_TOL, (k, j, s, e)
+        for s in range(len(tok)):
+            if gn[s] != r.next_tokens[s]:
+                assert r.margins[s] < MARGIN_WINDOW, (k, s, gn[s], r.next_tokens[s], r.margins[s])
+                st.token_mismatch += 1
+        st.gpu_exits.append(ge.copy())
+        st.gpu_tokens.append(gn.copy())
+        tok = gn.copy()
+        st.steps += 1
+    return st
+
+
+def check_kv(eng: ee.DecodeEngine, orc: oracle.Oracle, tol: float = 2e-2):
+    """Every written slot holds finite bf16 K/V (no 0xFFFF sentinel) that match
+    the oracle's history, and the block tables agree bit for bit."""
+    L = orc.cfg.n_layers
+    worst = 0.0
+    for s in range(len(orc.seqs)):
+        assert list(eng.debug_block_table(s)) == orc.seqs[s].blocks
+        P = orc.seqs[s].pos
+        assert eng.seq_pos(s) == P
+        for j in range(L):
+            for p in range(P):
+                k, v = eng.debug_kv(s, j, p)
+                assert not (k == 0xFFFF).any() and not (v == 0xFFFF).any(), (s, j, p)
+                kf = oracle.bf16_to_f64(k)
+                vf = oracle.bf16_to_f64(v)
+                ek = rel_l2(kf, orc.K[s][j, p].reshape(-1))
+                ev = rel_l2(vf, orc.V[s][j, p].reshape(-1))
+                worst = max(worst, ek, ev)
+                assert ek < tol and ev < tol, (s, j, p, ek, ev)
+    return worst
