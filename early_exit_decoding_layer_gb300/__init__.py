@@ -310,6 +310,16 @@ class DecodeEngine:
 
 # ---------------------------------------------------------------- single kernels
 
+def pair_order(x):
+    """Columns of x [..., K] (K % 8 == 0) rearranged into the kernels' activation
+    pair order: within each run of 8 the order is 0,4,1,5,2,6,3,7."""
+    K = x.shape[-1]
+    idx = np.arange(K)
+    j = idx % 8
+    src = (idx - j) + np.where(j % 2 == 0, j // 2, 4 + j // 2)
+    return x[..., src]
+
+
 def _stream(stream=None) -> int:
     import torch
     return (stream or torch.cuda.current_stream()).cuda_stream
@@ -332,8 +342,10 @@ def quantize_int4(w, stream=None):
     return packed, scales
 
 
-def linear_bf16(x, w, err=None, stream=None):
+def linear_bf16(x_f16, w, err=None, stream=None):
+    """x_f16 [M, K] fp16 bits in pair order, w [N, K] bf16 bits -> y [M, N] fp32."""
     import torch
+    x = x_f16
     M, K = x.shape
     N = w.shape[0]
     y = torch.empty((M, N), dtype=torch.float32, device=x.device)
@@ -343,6 +355,7 @@ def linear_bf16(x, w, err=None, stream=None):
 
 
 def linear_int4(x_f16, packed, scales, err=None, stream=None):
+    """x_f16 [M, K] fp16 bits in pair order, packed [N, K/2], scales [N, S] -> y fp32."""
     import torch
     M, K = x_f16.shape
     N = packed.shape[0]
@@ -359,7 +372,7 @@ def attention_scratch_bytes(B, n_heads, n_kv_heads, head_dim) -> int:
 
 def attention(q, kcache, vcache, block_table, pos, n_heads, n_kv_heads, head_dim, scratch=None,
               err=None, stream=None):
-    """q [B, Hq*hd] fp32; caches [blocks, Hkv, 16, hd] bf16 bits; block_table [B, W] int32;
+    """q [B, Hq*hd] fp32; caches [blocks, Hkv, 16, hd] fp16 bits; block_table [B, W] int32;
     pos [B] int32.  Returns o [B, Hq*hd] fp32."""
     import torch
     B = q.shape[0]
@@ -379,7 +392,7 @@ def head_scratch_bytes(M) -> int:
 
 
 def vocab_head(u, E, scratch=None, err=None, stream=None):
-    """u [M, d] bf16 bits, E [V, d] bf16 bits -> (conf [M] fp32, argmax [M] int32)."""
+    """u [M, d] fp16 bits in pair order, E [V, d] bf16 bits -> (conf [M] fp32, argmax [M] int32)."""
     import torch
     M, d = u.shape
     V = E.shape[0]

@@ -44,10 +44,10 @@ struct StepOut {
 // ------------------------------------------------------------------ GEMV
 enum Epi : int32_t {
   EPI_F32 = 0,     // out_f32[seq * out_stride + n] = y
-  EPI_QKV = 1,     // RoPE on q/k row pairs, q -> q_out, k/v -> paged cache
+  EPI_QKV = 1,     // RoPE on q/k row pairs, q -> q_out, k/v (fp16) -> paged cache
   EPI_RESID = 2,   // h[seq, n] += y (+ debug copy)
-  EPI_SWIGLU = 3,  // rows (2i, 2i+1) = (gate_i, up_i) -> x_out[seq, i] = silu(g) u
-  EPI_X = 4,       // x_out[seq, n] = y (bf16 and fp16 copies)
+  EPI_SWIGLU = 3,  // rows (2i, 2i+1) = (gate_i, up_i) -> x_out[seq, i] = silu(g) u (fp16)
+  EPI_X = 4,       // x_out[seq, n] = y (fp16, pair order)
   EPI_HEAD = 5,    // vocabulary head: per-row softmax statistics and argmax
 };
 
@@ -65,8 +65,7 @@ struct LinearParams {
   const int32_t* list_exit;  // rows on the int4 weights (may be null)
   int32_t m_direct_full;     // used when list_full == null
   int32_t m_direct_exit;     // used when list_exit == null
-  // activations by sequence id: bf16 for bf16 weights, fp16 (permuted runs of 8) for int4
-  const uint16_t* xb;
+  // activations by sequence id, fp16 in pair order (runs of 8: 0,4,1,5,2,6,3,7)
   const uint16_t* xh;
   int32_t x_stride;
   int32_t epi;
@@ -75,7 +74,7 @@ struct LinearParams {
   int32_t out_stride;
   // EPI_QKV
   float* q_out;              // [seq][Hq*hd]
-  uint16_t* kc;              // this layer's K cache [blocks][Hkv][16][hd]
+  uint16_t* kc;              // this layer's K cache [blocks][Hkv][16][hd] fp16
   uint16_t* vc;
   const int32_t* block_table;
   int32_t bt_stride;
@@ -87,8 +86,7 @@ struct LinearParams {
   int32_t h_stride;
   float* hdbg;               // [seq][h_stride] copy when *dbg_flag != 0
   const int32_t* dbg_flag;
-  // EPI_SWIGLU / EPI_X
-  uint16_t* xb_out;
+  // EPI_SWIGLU / EPI_X (fp16, pair order)
   uint16_t* xh_out;
   int32_t xo_stride;
   // EPI_HEAD
@@ -130,8 +128,7 @@ struct AttnParams {
   float* part;               // scratch partials
   int32_t* counters;         // [batch_slots][Hkv], zero between launches
   float* o_f32;              // [seq][Hq*hd] (op) or null
-  uint16_t* ob;              // bf16 [seq][xo_stride] or null
-  uint16_t* oh;              // fp16, permuted runs of 8, or null
+  uint16_t* oh;              // fp16 in pair order, or null
   int32_t o_stride;
   int32_t* err;
 };
@@ -147,8 +144,7 @@ struct NormParams {
   const uint16_t* g;
   int32_t d;
   float eps;
-  uint16_t* xb;
-  uint16_t* xh;               // may be null
+  uint16_t* xh;               // fp16, pair order
   int32_t x_stride;
 };
 cudaError_t launch_rmsnorm(const NormParams& p, int batch_slots, bool pdl, cudaStream_t st);

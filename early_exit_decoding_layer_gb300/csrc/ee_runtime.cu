@@ -99,8 +99,8 @@ struct ee_ctx {
   int32_t* pos = nullptr;
   float2* rope = nullptr;
   float* h = nullptr;
-  uint16_t *xb = nullptr, *xh = nullptr, *ab = nullptr, *ah = nullptr, *actb = nullptr,
-           *acth = nullptr, *ub = nullptr;
+  // fp16 activations in the GEMV kernels' pair order, by sequence id
+  uint16_t *xh = nullptr, *ah = nullptr, *acth = nullptr, *uh = nullptr;
   float* q = nullptr;
   float* attn_part = nullptr;
   int32_t* attn_cnt = nullptr;
@@ -215,13 +215,10 @@ size_t carve(ee_ctx* c, const ee_config& cfg, uint8_t* base) {
   int32_t* pos = cv.take<int32_t>(EE_MAX_BATCH);
   float2* rope = cv.take<float2>((size_t)m.maxs * (m.hd / 2));
   float* h = cv.take<float>((size_t)EE_MAX_BATCH * m.d);
-  uint16_t* xb = cv.take<uint16_t>((size_t)EE_MAX_BATCH * m.d);
   uint16_t* xh = cv.take<uint16_t>((size_t)EE_MAX_BATCH * m.d);
-  uint16_t* ab = cv.take<uint16_t>((size_t)EE_MAX_BATCH * m.dq);
   uint16_t* ah = cv.take<uint16_t>((size_t)EE_MAX_BATCH * m.dq);
-  uint16_t* actb = cv.take<uint16_t>((size_t)EE_MAX_BATCH * m.F);
   uint16_t* acth = cv.take<uint16_t>((size_t)EE_MAX_BATCH * m.F);
-  uint16_t* ub = cv.take<uint16_t>((size_t)EE_MAX_BATCH * m.d);
+  uint16_t* uh = cv.take<uint16_t>((size_t)EE_MAX_BATCH * m.d);
   float* q = cv.take<float>((size_t)EE_MAX_BATCH * m.dq);
   float* apart = cv.take<float>((size_t)kAttnSplitSlots * m.hkv * (m.hq / m.hkv) * (m.hd + 2));
   float* hpart = cv.take<float>((size_t)kHeadGridMax * EE_MAX_BATCH * 4);
@@ -250,13 +247,10 @@ size_t carve(ee_ctx* c, const ee_config& cfg, uint8_t* base) {
     c->pos = pos;
     c->rope = rope;
     c->h = h;
-    c->xb = xb;
     c->xh = xh;
-    c->ab = ab;
     c->ah = ah;
-    c->actb = actb;
     c->acth = acth;
-    c->ub = ub;
+    c->uh = uh;
     c->q = q;
     c->attn_part = apart;
     c->head_part = hpart;
@@ -347,7 +341,6 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
     // attention RMSNorm of every participating sequence
     np.list = c->lists->part;
     np.g = w.g_attn;
-    np.xb = c->xb;
     np.xh = c->xh;
     EE_CUDA(c, launch_rmsnorm(np, B, true, st));
     // QKV projection + RoPE + K/V write into the shared paged cache
@@ -360,7 +353,6 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
     p.sstride = sstride_of(m.d);
     p.list_full = c->lists->full;
     p.list_exit = c->lists->exitl;
-    p.xb = c->xb;
     p.xh = c->xh;
     p.x_stride = m.d;
     p.epi = EPI_QKV;
@@ -384,7 +376,6 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
     ap.nsplit = nsplit;
     ap.part = c->attn_part;
     ap.counters = c->attn_cnt;
-    ap.ob = c->ab;
     ap.oh = c->ah;
     ap.o_stride = m.dq;
     ap.err = err;
@@ -399,7 +390,6 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
     p.sstride = sstride_of(m.dq);
     p.list_full = c->lists->full;
     p.list_exit = c->lists->exitl;
-    p.xb = c->ab;
     p.xh = c->ah;
     p.x_stride = m.dq;
     p.epi = EPI_RESID;
@@ -417,11 +407,9 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
     p.sstride = sstride_of(m.d);
     p.list_full = c->lists->full;
     p.list_exit = c->lists->exitl;
-    p.xb = c->xb;
     p.xh = c->xh;
     p.x_stride = m.d;
     p.epi = EPI_SWIGLU;
-    p.xb_out = c->actb;
     p.xh_out = c->acth;
     p.xo_stride = m.F;
     EE_CUDA(c, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
@@ -435,7 +423,6 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
     p.sstride = sstride_of(m.F);
     p.list_full = c->lists->full;
     p.list_exit = c->lists->exitl;
-    p.xb = c->actb;
     p.xh = c->acth;
     p.x_stride = m.F;
     p.epi = EPI_RESID;
@@ -449,7 +436,6 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
       NormParams fp = np;
       fp.list = c->lists->full;
       fp.g = c->g_final;
-      fp.xh = nullptr;
       EE_CUDA(c, launch_rmsnorm(fp, B, true, st));
       p = base;
       p.N = m.d;
@@ -457,10 +443,10 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
       p.w = c->Tt[ci];
       p.list_full = c->lists->full;
       p.list_exit = nullptr;
-      p.xb = c->xb;
+      p.xh = c->xh;
       p.x_stride = m.d;
       p.epi = EPI_X;
-      p.xb_out = c->ub;
+      p.xh_out = c->uh;
       p.xo_stride = m.d;
       EE_CUDA(c, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
       // z = u E^T, conf = max softmax, exit if conf > gamma_c, compact the lists
@@ -469,8 +455,8 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
       p.K = m.d;
       p.w = c->E;
       p.list_full = c->lists->full;
-      p.list_exit = nullptr;
-      p.xb = c->ub;
+      p.list_exit = c->lists->exitl;  // merged into the new exit list; no int4 work (wq is null)
+      p.xh = c->uh;
       p.x_stride = m.d;
       p.epi = EPI_HEAD;
       p.head_mode = HEAD_CHECKPOINT;
@@ -487,7 +473,6 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
   NormParams fp = np;
   fp.list = c->lists->fin;
   fp.g = c->g_final;
-  fp.xh = nullptr;
   EE_CUDA(c, launch_rmsnorm(fp, B, true, st));
   LinearParams p = base;
   p.N = m.V;
@@ -495,7 +480,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
   p.w = c->E;
   p.list_full = c->lists->fin;
   p.list_exit = nullptr;
-  p.xb = c->xb;
+  p.xh = c->xh;
   p.x_stride = m.d;
   p.epi = EPI_HEAD;
   p.head_mode = HEAD_FINAL;
@@ -1044,8 +1029,7 @@ ee_status ee_op_quantize_int4(const uint16_t* w, int32_t rows, int32_t cols, uin
              : EE_ERR_CUDA;
 }
 
-static ee_status op_linear(int32_t M, int32_t N, int32_t K, const uint16_t* xb, const uint16_t* xh,
-                           const uint16_t* w, const uint8_t* q, const uint16_t* s, int32_t sstride, float* y,
+static ee_status op_linear(int32_t M, int32_t N, int32_t K, const uint16_t* xh, const uint16_t* w, const uint8_t* q, const uint16_t* s, int32_t sstride, float* y,
                            int32_t* err, void* stream) {
   if (M < 1 || M > EE_MAX_BATCH || N < 2 || N % 2 || K < 32 || K % 32 || !y) return EE_ERR_INVALID_ARG;
   if (q && ((uintptr_t)q % 16 || (uintptr_t)s % 16 || sstride % 8)) return EE_ERR_INVALID_ARG;
@@ -1061,7 +1045,6 @@ static ee_status op_linear(int32_t M, int32_t N, int32_t K, const uint16_t* xb, 
   p.sstride = sstride;
   p.m_direct_full = w ? M : 0;
   p.m_direct_exit = q ? M : 0;
-  p.xb = xb;
   p.xh = xh;
   p.x_stride = K;
   p.epi = EPI_F32;
@@ -1072,17 +1055,17 @@ static ee_status op_linear(int32_t M, int32_t N, int32_t K, const uint16_t* xb, 
                                                                                            : EE_ERR_CUDA;
 }
 
-ee_status ee_op_linear_bf16(int32_t M, int32_t N, int32_t K, const uint16_t* x, const uint16_t* w, float* y,
-                            int32_t* err_flag, void* stream) {
-  if (!x || !w) return EE_ERR_INVALID_ARG;
-  return op_linear(M, N, K, x, nullptr, w, nullptr, nullptr, 0, y, err_flag, stream);
+ee_status ee_op_linear_bf16(int32_t M, int32_t N, int32_t K, const uint16_t* x_f16, const uint16_t* w,
+                            float* y, int32_t* err_flag, void* stream) {
+  if (!x_f16 || !w) return EE_ERR_INVALID_ARG;
+  return op_linear(M, N, K, x_f16, w, nullptr, nullptr, 0, y, err_flag, stream);
 }
 
 ee_status ee_op_linear_int4(int32_t M, int32_t N, int32_t K, const uint16_t* x_f16, const uint8_t* packed,
                             const uint16_t* scales, int32_t scale_stride, float* y, int32_t* err_flag,
                             void* stream) {
   if (!x_f16 || !packed || !scales || scale_stride < ceil_div(K, EE_QUANT_GROUP)) return EE_ERR_INVALID_ARG;
-  return op_linear(M, N, K, nullptr, x_f16, nullptr, packed, scales, scale_stride, y, err_flag, stream);
+  return op_linear(M, N, K, x_f16, nullptr, packed, scales, scale_stride, y, err_flag, stream);
 }
 
 size_t ee_attention_scratch_bytes(int32_t B, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim) {
@@ -1133,9 +1116,9 @@ size_t ee_head_scratch_bytes(int32_t M) {
   return (size_t)kHeadGridMax * EE_MAX_BATCH * 4 * 4 + kAlign;
 }
 
-ee_status ee_op_vocab_head(int32_t M, int32_t V, int32_t d, const uint16_t* u, const uint16_t* E, float* conf,
+ee_status ee_op_vocab_head(int32_t M, int32_t V, int32_t d, const uint16_t* u_f16, const uint16_t* E, float* conf,
                            int32_t* argmax, void* scratch, int32_t* err_flag, void* stream) {
-  if (M < 1 || M > EE_MAX_BATCH || V < 2 || V % 2 || d < 32 || d % 32 || !u || !E || !conf || !argmax ||
+  if (M < 1 || M > EE_MAX_BATCH || V < 2 || V % 2 || d < 32 || d % 32 || !u_f16 || !E || !conf || !argmax ||
       !scratch)
     return EE_ERR_INVALID_ARG;
   const int sms = device_sms();
@@ -1145,7 +1128,7 @@ ee_status ee_op_vocab_head(int32_t M, int32_t V, int32_t d, const uint16_t* u, c
   p.K = d;
   p.w = E;
   p.m_direct_full = M;
-  p.xb = u;
+  p.xh = u_f16;
   p.x_stride = d;
   p.epi = EPI_HEAD;
   p.head_mode = HEAD_CONF_ARGMAX;

@@ -13,7 +13,7 @@
 // atomic counter, no waiting -- merges the partials and writes the output:
 // o = sum_i acc_i exp(m_i - M) / sum_i l_i exp(m_i - M).
 //
-// Cache layout (one layer): [block][kv head][16 slots][head_dim] bf16.
+// Cache layout (one layer): [block][kv head][16 slots][head_dim] fp16.
 #include <math.h>
 
 #include "ee_common.cuh"
@@ -27,14 +27,13 @@ constexpr int kWarps = 4;
 constexpr int kUnroll = 4;
 
 EE_DEV void to_float8(const uint4& v, float* f) {
-  f[0] = bf16_lo(v.x);
-  f[1] = bf16_hi(v.x);
-  f[2] = bf16_lo(v.y);
-  f[3] = bf16_hi(v.y);
-  f[4] = bf16_lo(v.z);
-  f[5] = bf16_hi(v.z);
-  f[6] = bf16_lo(v.w);
-  f[7] = bf16_hi(v.w);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
 }
 
 // Merge (m2, l2, a2) into (m1, l1, a1).
@@ -214,7 +213,6 @@ __global__ void __launch_bounds__(kWarps * 32) k_attention(const AttnParams p) {
     const float o = a / l;
     const int col = (g * G + h) * HD + dd;
     if (p.o_f32) p.o_f32[(size_t)seq * p.o_stride + col] = o;
-    if (p.ob) p.ob[(size_t)seq * p.o_stride + col] = float_to_bf16_bits(o);
     if (p.oh) p.oh[(size_t)seq * p.o_stride + xh_slot(col)] = float_to_half_bits(o);
   }
   if (tid == 0) p.counters[(size_t)z * hkv + g] = 0;

@@ -1,5 +1,6 @@
 // Skinny GEMV / GEMM for decode: Y[m, n] = sum_k X[m, k] W[n, k] for the few
-// sequences of a step, with the weights streamed once from HBM.
+// sequences of a step, with the weights streamed once from HBM.  Activations
+// are fp16 (the A16 of W4A16), accumulation fp32.
 //
 // One launch serves both sub-batches of a layer: the rows still on the bf16
 // backbone ("full" list) read the bf16 matrix, the rows that exited read the
@@ -14,9 +15,9 @@
 // 1 KB (512 bf16 columns, or 2048 int4 columns plus their 16 scales).  Warp w
 // owns rows (2w, 2w+1) of each 16-row tile, so the pairs that RoPE and SwiGLU
 // combine are reduced by the same warp.  Activations come from L1/L2 (they are
-// a few KB per sequence); the int4 path takes them in fp16, permuted within
-// runs of 8 so that one 16-byte load yields the half2 pairs that match the
-// nibble pairs of a packed word (see xh_slot).
+// a few KB per sequence) in fp16, permuted within runs of 8 so that one
+// 16-byte load yields the half2 pairs that match the nibble pairs of a packed
+// int4 word (see xh_slot); the bf16 path reads the same layout.
 //
 // int4 dequantisation: a packed word holds columns c..c+7 in nibbles 0..7;
 // (w ^ 0x88888888) turns two's complement into offset binary, then
@@ -49,19 +50,23 @@ constexpr size_t kListBytes = 2 * kListLen * sizeof(int32_t);
 constexpr size_t kStatBytes = kConsumerWarps * kMM * 3 * sizeof(float);
 constexpr size_t kSmemBytes = kRingBytes + kBarBytes + kListBytes + kStatBytes;
 
+EE_DEV __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// 8 bf16 weights w0..w7 (natural order) times 8 fp16 activations given in
+// pair order (x0,x4) (x1,x5) (x2,x6) (x3,x7), accumulated in fp32.
 EE_DEV float dot8_bf16(const uint4& w, const uint4& x, float acc) {
-  acc = fmaf(bf16_lo(w.x), bf16_lo(x.x), acc);
-  acc = fmaf(bf16_hi(w.x), bf16_hi(x.x), acc);
-  acc = fmaf(bf16_lo(w.y), bf16_lo(x.y), acc);
-  acc = fmaf(bf16_hi(w.y), bf16_hi(x.y), acc);
-  acc = fmaf(bf16_lo(w.z), bf16_lo(x.z), acc);
-  acc = fmaf(bf16_hi(w.z), bf16_hi(x.z), acc);
-  acc = fmaf(bf16_lo(w.w), bf16_lo(x.w), acc);
-  acc = fmaf(bf16_hi(w.w), bf16_hi(x.w), acc);
+  const float2 x04 = __half22float2(u32_as_h2(x.x)), x15 = __half22float2(u32_as_h2(x.y));
+  const float2 x26 = __half22float2(u32_as_h2(x.z)), x37 = __half22float2(u32_as_h2(x.w));
+  acc = fmaf(bf16_lo(w.x), x04.x, acc);
+  acc = fmaf(bf16_hi(w.x), x15.x, acc);
+  acc = fmaf(bf16_lo(w.y), x26.x, acc);
+  acc = fmaf(bf16_hi(w.y), x37.x, acc);
+  acc = fmaf(bf16_lo(w.z), x04.y, acc);
+  acc = fmaf(bf16_hi(w.z), x15.y, acc);
+  acc = fmaf(bf16_lo(w.w), x26.y, acc);
+  acc = fmaf(bf16_hi(w.w), x37.y, acc);
   return acc;
 }
-
-EE_DEV __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
 // 8 int4 weights (one packed word) times 8 fp16 activations in pair order.
 EE_DEV __half2 dot8_int4(uint32_t word, const uint4& x, __half2 acc) {
@@ -104,15 +109,15 @@ EE_DEV void epi_pair(const LinearParams& p, int seq, int ra, float ya, float yb)
         q[i + (hd >> 1)] = o2;
       } else {
         uint16_t* k = kv_slot(p.kc, p, seq, pos, head);
-        k[i] = float_to_bf16_bits(o1);
-        k[i + (hd >> 1)] = float_to_bf16_bits(o2);
+        k[i] = float_to_half_bits(o1);
+        k[i + (hd >> 1)] = float_to_half_bits(o2);
       }
     } else {
       const int rr = ra - dq - dk;
       const int head = rr / hd, i = rr % hd;
       uint16_t* v = kv_slot(p.vc, p, seq, pos, head);
       const uint32_t packed =
-          uint32_t(float_to_bf16_bits(ya)) | (uint32_t(float_to_bf16_bits(yb)) << 16);
+          uint32_t(float_to_half_bits(ya)) | (uint32_t(float_to_half_bits(yb)) << 16);
       *reinterpret_cast<uint32_t*>(v + i) = packed;
     }
   } else if constexpr (EPI == EPI_RESID) {
@@ -125,17 +130,11 @@ EE_DEV void epi_pair(const LinearParams& p, int seq, int ra, float ya, float yb)
   } else if constexpr (EPI == EPI_SWIGLU) {
     const int i = ra >> 1;
     const float a = ya / (1.0f + expf(-ya)) * yb;
-    p.xb_out[(size_t)seq * p.xo_stride + i] = float_to_bf16_bits(a);
-    if (p.xh_out) p.xh_out[(size_t)seq * p.xo_stride + xh_slot(i)] = float_to_half_bits(a);
+    p.xh_out[(size_t)seq * p.xo_stride + xh_slot(i)] = float_to_half_bits(a);
   } else if constexpr (EPI == EPI_X) {
-    uint16_t* xo = p.xb_out + (size_t)seq * p.xo_stride;
-    xo[ra] = float_to_bf16_bits(ya);
-    xo[ra + 1] = float_to_bf16_bits(yb);
-    if (p.xh_out) {
-      uint16_t* ho = p.xh_out + (size_t)seq * p.xo_stride;
-      ho[xh_slot(ra)] = float_to_half_bits(ya);
-      ho[xh_slot(ra + 1)] = float_to_half_bits(yb);
-    }
+    uint16_t* ho = p.xh_out + (size_t)seq * p.xo_stride;
+    ho[xh_slot(ra)] = float_to_half_bits(ya);
+    ho[xh_slot(ra + 1)] = float_to_half_bits(yb);
   }
 }
 
@@ -296,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
 #pragma unroll
                   for (int m = 0; m < kMM; ++m) {
                     if (m < mc) {
-                      const uint4 xv = ldg_nc_v4(p.xb + (size_t)seqs[m] * p.x_stride + k0);
+                      const uint4 xv = ldg_nc_v4(p.xh + (size_t)seqs[m] * p.x_stride + k0);
                       acc0[m] = dot8_bf16(wa, xv, acc0[m]);
                       acc1[m] = dot8_bf16(wb, xv, acc1[m]);
                     }

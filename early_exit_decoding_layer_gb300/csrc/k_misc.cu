@@ -11,8 +11,8 @@ namespace ee {
 namespace {
 
 // ------------------------------------------------------------------ RMSNorm
-// x = h * rsqrt(mean(h^2) + eps) * g for every listed sequence; writes the
-// bf16 copy and (if requested) the fp16 copy in the int4 kernels' pair order.
+// x = h * rsqrt(mean(h^2) + eps) * g for every listed sequence, written in
+// fp16 in the GEMV kernels' pair order.
 __global__ void __launch_bounds__(256) k_rmsnorm(const NormParams p) {
   __shared__ float red[8];
   grid_dep_wait();
@@ -24,12 +24,17 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const NormParams p) {
   const float* h = p.h + (size_t)seq * p.h_stride;
   const int tid = threadIdx.x;
   float ss = 0.0f;
-  for (int i = tid * 4; i < p.d; i += 256 * 4) {
-    const float4 v = *reinterpret_cast<const float4*>(h + i);
-    ss = fmaf(v.x, v.x, ss);
-    ss = fmaf(v.y, v.y, ss);
-    ss = fmaf(v.z, v.z, ss);
-    ss = fmaf(v.w, v.w, ss);
+  for (int i = tid * 8; i < p.d; i += 256 * 8) {
+    const float4 a = *reinterpret_cast<const float4*>(h + i);
+    const float4 b = *reinterpret_cast<const float4*>(h + i + 4);
+    ss = fmaf(a.x, a.x, ss);
+    ss = fmaf(a.y, a.y, ss);
+    ss = fmaf(a.z, a.z, ss);
+    ss = fmaf(a.w, a.w, ss);
+    ss = fmaf(b.x, b.x, ss);
+    ss = fmaf(b.y, b.y, ss);
+    ss = fmaf(b.z, b.z, ss);
+    ss = fmaf(b.w, b.w, ss);
   }
   ss = warp_sum(ss);
   if ((tid & 31) == 0) red[tid >> 5] = ss;
@@ -38,23 +43,20 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const NormParams p) {
 #pragma unroll
   for (int w = 0; w < 8; ++w) tot += red[w];
   const float r = rsqrtf(tot / (float)p.d + p.eps);
-  uint16_t* xb = p.xb + (size_t)seq * p.x_stride;
-  uint16_t* xh = p.xh ? p.xh + (size_t)seq * p.x_stride : nullptr;
-  for (int i = tid * 4; i < p.d; i += 256 * 4) {
-    const float4 v = *reinterpret_cast<const float4*>(h + i);
-    const uint2 gw = *reinterpret_cast<const uint2*>(p.g + i);
-    const float x0 = v.x * r * bf16_lo(gw.x), x1 = v.y * r * bf16_hi(gw.x);
-    const float x2 = v.z * r * bf16_lo(gw.y), x3 = v.w * r * bf16_hi(gw.y);
-    uint2 o;
-    o.x = uint32_t(float_to_bf16_bits(x0)) | (uint32_t(float_to_bf16_bits(x1)) << 16);
-    o.y = uint32_t(float_to_bf16_bits(x2)) | (uint32_t(float_to_bf16_bits(x3)) << 16);
-    *reinterpret_cast<uint2*>(xb + i) = o;
-    if (xh) {
-      xh[xh_slot(i)] = float_to_half_bits(x0);
-      xh[xh_slot(i + 1)] = float_to_half_bits(x1);
-      xh[xh_slot(i + 2)] = float_to_half_bits(x2);
-      xh[xh_slot(i + 3)] = float_to_half_bits(x3);
-    }
+  uint16_t* xh = p.xh + (size_t)seq * p.x_stride;
+  for (int i = tid * 8; i < p.d; i += 256 * 8) {
+    const float4 a = *reinterpret_cast<const float4*>(h + i);
+    const float4 b = *reinterpret_cast<const float4*>(h + i + 4);
+    const uint4 gw = *reinterpret_cast<const uint4*>(p.g + i);
+    const float x[8] = {a.x * r * bf16_lo(gw.x), a.y * r * bf16_hi(gw.x), a.z * r * bf16_lo(gw.y),
+                        a.w * r * bf16_hi(gw.y), b.x * r * bf16_lo(gw.z), b.y * r * bf16_hi(gw.z),
+                        b.z * r * bf16_lo(gw.w), b.w * r * bf16_hi(gw.w)};
+    uint4 o;  // pair order: (x0,x4) (x1,x5) (x2,x6) (x3,x7)
+    o.x = uint32_t(float_to_half_bits(x[0])) | (uint32_t(float_to_half_bits(x[4])) << 16);
+    o.y = uint32_t(float_to_half_bits(x[1])) | (uint32_t(float_to_half_bits(x[5])) << 16);
+    o.z = uint32_t(float_to_half_bits(x[2])) | (uint32_t(float_to_half_bits(x[6])) << 16);
+    o.w = uint32_t(float_to_half_bits(x[3])) | (uint32_t(float_to_half_bits(x[7])) << 16);
+    *reinterpret_cast<uint4*>(xh + i) = o;
   }
 }
 

@@ -21,6 +21,11 @@
  * "exit" (int4) sub-batch instead of masking exited rows (the dynamic batch
  * regrouping of the CALM article §3.3).
  *
+ * Precision.  Backbone weights, E and T are bf16; exit-layer weights int4
+ * with bf16 scales; activations fed to the projections and the K/V cache are
+ * fp16 (16-bit activations, the A16 of W4A16); accumulation, the residual
+ * stream, softmax and RoPE are fp32.
+ *
  * Conventions.
  *  - Everything on the device lives in one arena that the CALLER allocates
  *    (ee_arena_bytes tells how much); the library never calls cudaMalloc.
@@ -189,7 +194,7 @@ ee_status ee_debug_hidden(ee_ctx *ctx, int32_t layer, float *out);
 /* Exit-head confidences of the last step, [batch, n_checkpoints] fp32, NaN
  * where the head was not evaluated. */
 ee_status ee_debug_conf(ee_ctx *ctx, float *out);
-/* K and V (bf16 bits, [n_kv_heads*head_dim] each, host) stored for sequence
+/* K and V (fp16 bits, [n_kv_heads*head_dim] each, host) stored for sequence
  * seq at layer `layer`, position pos (pos < the sequence's position). */
 ee_status ee_debug_kv(ee_ctx *ctx, int32_t seq, int32_t layer, int32_t pos, uint16_t *k,
                       uint16_t *v);
@@ -213,15 +218,19 @@ ee_status ee_debug_int4(ee_ctx *ctx, int32_t layer, int32_t mat, uint8_t *packed
 ee_status ee_op_quantize_int4(const uint16_t *w, int32_t rows, int32_t cols, uint8_t *packed,
                               uint16_t *scales, int32_t scale_stride, void *stream);
 
+/* Activations.  The kernels carry activations in fp16 (the A16 of W4A16)
+ * and accumulate in fp32.  An activation row of K values is stored in "pair
+ * order": within each run of 8 columns c..c+7 the stored order is
+ * c, c+4, c+1, c+5, c+2, c+6, c+3, c+7, so that one 16-byte load gives the
+ * (c+j, c+j+4) pairs that match the nibble pairs of a packed int4 word. */
+
 /* y[m, n] = sum_k x[m, k] W[n, k] for m < M (M <= EE_MAX_BATCH): bf16 W
- * [N, K], x bf16 [M, K], y fp32 [M, N].  K % 32 == 0, N even. */
-ee_status ee_op_linear_bf16(int32_t M, int32_t N, int32_t K, const uint16_t *x, const uint16_t *w,
-                            float *y, int32_t *err_flag, void *stream);
+ * [N, K], x fp16 [M, K] in pair order, y fp32 [M, N].  K % 32 == 0, N even. */
+ee_status ee_op_linear_bf16(int32_t M, int32_t N, int32_t K, const uint16_t *x_f16,
+                            const uint16_t *w, float *y, int32_t *err_flag, void *stream);
 /* Same with the int4 copy: packed [N, K/2], scales [N, scale_stride] bf16
  * with scale_stride a multiple of 8 and >= ceil(K/128) (entries past
- * ceil(K/128) are read but unused); x is given in fp16 ([M, K] __half bits)
- * as the exit layers take it, in pair order: within each run of 8 columns
- * the stored order is 0,4,1,5,2,6,3,7. */
+ * ceil(K/128) are read but unused); x fp16 [M, K] in pair order. */
 ee_status ee_op_linear_int4(int32_t M, int32_t N, int32_t K, const uint16_t *x_f16,
                             const uint8_t *packed, const uint16_t *scales, int32_t scale_stride,
                             float *y, int32_t *err_flag, void *stream);
@@ -229,8 +238,8 @@ ee_status ee_op_linear_int4(int32_t M, int32_t N, int32_t K, const uint16_t *x_f
 /* Paged GQA decode attention (one query position per sequence, causal over
  * positions 0..pos[s]):  o[s, h*hd + i] = sum_t softmax_t(q_h . k_t / sqrt(hd)) v_t[i]
  * with kv head g = floor(h * Hkv / Hq).
- *   q [B, Hq*hd] fp32; kcache/vcache [n_blocks, Hkv, 16, hd] bf16 (one
- *   layer); block_table [B, bt_stride] int32; pos [B] int32 (the query's
+ *   q [B, Hq*hd] fp32; kcache/vcache [n_blocks, Hkv, 16, hd] fp16 (one
+ *   layer, the layout of the context's shared cache); block_table [B, bt_stride] int32; pos [B] int32 (the query's
  *   position, so ctx = pos + 1); o [B, Hq*hd] fp32.
  * scratch: device buffer of ee_attention_scratch_bytes(B, Hq, Hkv, hd) bytes;
  * its counters must be zero on the first call (ee_create does this for the
@@ -243,12 +252,12 @@ ee_status ee_op_attention(int32_t B, int32_t n_heads, int32_t n_kv_heads, int32_
                           const int32_t *block_table, int32_t bt_stride, const int32_t *pos,
                           float *o, void *scratch, int32_t *err_flag, void *stream);
 
-/* Vocabulary head over M rows: z[m, v] = u[m, :] . E[v, :] (u bf16 [M, d],
- * E bf16 [V, d]); writes conf[m] = max_v softmax(z[m])_v = 1/sum_v exp(z_v - z_max)
+/* Vocabulary head over M rows: z[m, v] = u[m, :] . E[v, :] (u fp16 [M, d]
+ * in pair order, E bf16 [V, d]); writes conf[m] = max_v softmax(z[m])_v = 1/sum_v exp(z_v - z_max)
  * and argmax[m] (lowest index on ties).  scratch: ee_head_scratch_bytes(M)
  * bytes, counters zero on the first call and left zero. */
 size_t ee_head_scratch_bytes(int32_t M);
-ee_status ee_op_vocab_head(int32_t M, int32_t V, int32_t d, const uint16_t *u, const uint16_t *E,
+ee_status ee_op_vocab_head(int32_t M, int32_t V, int32_t d, const uint16_t *u_f16, const uint16_t *E,
                            float *conf, int32_t *argmax, void *scratch, int32_t *err_flag,
                            void *stream);
 

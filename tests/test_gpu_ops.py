@@ -24,14 +24,15 @@ def bf16_bits(x64, rng=None):
 
 
 def half_pair_order(x16):
-    """fp16 activations in the int4 kernels' pair order: within each run of 8
-    columns the order is 0,4,1,5,2,6,3,7."""
+    """fp16 activations in the kernels' pair order: within each run of 8
+    columns the order is 0,4,1,5,2,6,3,7 (written here by scattering)."""
     M, K = x16.shape
     idx = np.arange(K)
     j = idx % 8
     slot = (idx - j) + np.where(j < 4, 2 * j, 2 * (j - 4) + 1)
     out = np.empty_like(x16)
     out[:, slot] = x16
+    assert np.array_equal(ee.pair_order(x16), out)   # the binding's gather agrees
     return out
 
 
@@ -63,10 +64,10 @@ def test_quantize_bit_exact(rows, cols):
 def test_linear_bf16(M, N, K):
     rng = np.random.default_rng(M * 1000 + N + K)
     W = synth.normal_bf16(5, N * 7 + K, (N, K), 0.02)
-    x = bf16_bits(rng.standard_normal((M, K)))
+    x16 = rng.standard_normal((M, K)).astype(np.float16)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    y = ee.linear_bf16(dev(x.view(np.int16)), dev(W.view(np.int16)), err=err).cpu().numpy()
-    xf, Wf = oracle.bf16_to_f64(x), oracle.bf16_to_f64(W)
+    y = ee.linear_bf16(dev(half_pair_order(x16).view(np.int16)), dev(W.view(np.int16)), err=err).cpu().numpy()
+    xf, Wf = x16.astype(np.float64), oracle.bf16_to_f64(W)
     ref = oracle.linear(xf, Wf)
     bound = 1e-5 * (np.abs(xf) @ np.abs(Wf).T) + 1e-7   # fp32 accumulation of exact products
     assert np.all(np.abs(y - ref) <= bound)
@@ -102,7 +103,7 @@ def test_linear_int4(M, N, K):
 # ------------------------------------------------------------------ attention
 
 def paged(rng, B, ctxs, hkv, hd, nblocks_extra=5):
-    """Random bf16 K/V histories scattered over shuffled 16-slot blocks."""
+    """Random fp16 K/V histories scattered over shuffled 16-slot blocks."""
     bps = max((c + 15) // 16 for c in ctxs)
     nblocks = B * bps + nblocks_extra
     order = rng.permutation(nblocks)
@@ -112,8 +113,8 @@ def paged(rng, B, ctxs, hkv, hd, nblocks_extra=5):
     K, V = [], []
     n = 0
     for b in range(B):
-        Kb = bf16_bits(rng.standard_normal((ctxs[b], hkv, hd)))
-        Vb = bf16_bits(rng.standard_normal((ctxs[b], hkv, hd)))
+        Kb = rng.standard_normal((ctxs[b], hkv, hd)).astype(np.float16).view(np.uint16)
+        Vb = rng.standard_normal((ctxs[b], hkv, hd)).astype(np.float16).view(np.uint16)
         for i in range((ctxs[b] + 15) // 16):
             bt[b, i] = order[n]
             n += 1
@@ -142,7 +143,8 @@ def test_attention(B, hq, hkv, hd, ctxs):
                          hq, hkv, hd, scratch=scratch, err=err).cpu().numpy()
         for b in range(B):
             ref = oracle.attention_decode(q[b].astype(np.float64).reshape(hq, hd),
-                                          oracle.bf16_to_f64(K[b]), oracle.bf16_to_f64(V[b]))
+                                          K[b].view(np.float16).astype(np.float64),
+                                          V[b].view(np.float16).astype(np.float64))
             assert np.allclose(o[b].reshape(hq, hd), ref, rtol=1e-4, atol=1e-5), (rep, b)
     assert err.item() == 0
 
@@ -153,10 +155,10 @@ def test_attention(B, hq, hkv, hd, ctxs):
 def test_vocab_head(M, V, d):
     rng = np.random.default_rng(M + V + d)
     E = synth.normal_bf16(9, V + d, (V, d), 0.02)
-    u = bf16_bits(rng.standard_normal((M, d)))
-    conf, arg = ee.vocab_head(dev(u.view(np.int16)), dev(E.view(np.int16)))
+    u16 = rng.standard_normal((M, d)).astype(np.float16)
+    conf, arg = ee.vocab_head(dev(half_pair_order(u16).view(np.int16)), dev(E.view(np.int16)))
     conf, arg = conf.cpu().numpy(), arg.cpu().numpy()
-    z = oracle.linear(oracle.bf16_to_f64(u), oracle.bf16_to_f64(E))
+    z = oracle.linear(u16.astype(np.float64), oracle.bf16_to_f64(E))
     for m in range(M):
         c_ref = oracle.max_softmax(z[m])
         assert abs(conf[m] - c_ref) <= 1e-4 * c_ref
@@ -167,7 +169,7 @@ def test_vocab_head(M, V, d):
     E2 = np.zeros((64, 32), dtype=np.uint16)
     E2[[5, 9, 40], 0] = 0x3F80  # 1.0
     u2 = np.zeros((1, 32), dtype=np.uint16)
-    u2[0, 0] = 0x4000  # 2.0
+    u2[0, 0] = 0x4000  # fp16 2.0 (column 0 stays first in pair order)
     conf, arg = ee.vocab_head(dev(u2.view(np.int16)), dev(E2.view(np.int16)))
     assert arg.item() == 5
     expect = 1.0 / (3 + 61 * math.exp(-2.0))
