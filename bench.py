@@ -1,0 +1,519 @@
+#!/usr/bin/env python
+"""Early-exit greedy decode benchmark (one GB300 per rank).
+
+A step is one ee_decode_step: one early-exit decode of every sequence of the
+batch through the whole hot path (embedding, per layer RMSNorm -> QKV + RoPE
++ shared-KV write -> paged attention -> O + residual -> RMSNorm -> gate/up +
+SwiGLU -> down + residual, the checkpoint exit heads with their decisions and
+sub-batch compaction, the final head).
+
+Default workload: Llama-3.1-8B shape, batch 1, 2048-token prompt, greedy
+decode with thresholds at the 40th percentile of the no-exit confidences of
+the first 8 decode steps.  The same kernels are also timed as the forced
+no-exit baseline.  Weights and prompts are seeded synthetic data.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+        python bench.py --impl reference ...   (the CPU oracle, bounded sample)
+For N > 1 run under torchrun: every rank decodes its own batch (replicas, no
+collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+DEFAULT_WORKLOAD = "llama3.1-8b-b1"
+METRIC = "decoded tokens/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def mat_list(sh):
+    d, dq, dk, F = sh.d_model, sh.n_heads * sh.head_dim, sh.n_kv_heads * sh.head_dim, sh.ffn_dim
+    return {"qkv": (dq + 2 * dk, d), "o": (d, dq), "gateup": (2 * F, d), "down": (d, F)}
+
+
+def w_bytes(N, K, int4):
+    if int4:
+        return N * K // 2 + N * ((K + 127) // 128) * 2
+    return N * K * 2
+
+
+def launch_bytes(sh, ckpts, kind, layer, exits, ctxs):
+    """Algorithmic bytes one launch must read: the weights of the sub-batches
+    it serves (bf16 rows of sequences still on the backbone, int4 rows of
+    exited ones), the head tensors, or the K/V history."""
+    mats = mat_list(sh)
+    if kind in mats:
+        N, K = mats[kind]
+        full = any(e >= layer for e in exits)
+        ex = any(e < layer for e in exits)
+        return full * w_bytes(N, K, False) + ex * w_bytes(N, K, True)
+    d, V = sh.d_model, sh.vocab
+    if kind == "head_t":
+        return d * d * 2
+    if kind in ("head_e", "final_head"):
+        return V * d * 2
+    if kind == "attn":
+        return sum(int(c) * 2 * sh.n_kv_heads * sh.head_dim * 2 for c in ctxs)
+    return 0
+
+
+def step_bytes(sh, ckpts, exits, ctxs, heads):
+    """Bytes a step must read (the workload's roofline rule): for each layer the
+    bf16 weights if any sequence runs it in bf16 and the int4 weights plus
+    scales if any runs it on the exit copy; T and E for every head evaluated;
+    E for the final head; every sequence's K/V history of every layer."""
+    total = 0
+    for j in range(sh.n_layers):
+        for kind in ("qkv", "o", "gateup", "down"):
+            total += launch_bytes(sh, ckpts, kind, j, exits, ctxs)
+        total += launch_bytes(sh, ckpts, "attn", j, exits, ctxs)
+    if heads:
+        for l in ckpts:
+            if any(e >= l for e in exits):
+                total += launch_bytes(sh, ckpts, "head_t", l, exits, ctxs)
+                total += launch_bytes(sh, ckpts, "head_e", l, exits, ctxs)
+    total += launch_bytes(sh, ckpts, "final_head", -1, exits, ctxs)
+    return total
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        cmd = ["nvidia-smi", "--query-gpu=" + self.Q, "--format=csv,noheader,nounits", "-lms", "200"]
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        first = vis.split(",")[0].strip() if vis else ""
+        if first:
+            cmd += ["-i", first]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def dist_init(use_cuda: bool):
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        if use_cuda:
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if use_cuda else "gloo")
+    return rank, world, local
+
+
+def barrier(world, use_cuda):
+    if world > 1:
+        import torch.distributed as dist
+        if use_cuda:
+            import torch
+            dist.barrier(device_ids=[torch.cuda.current_device()])
+        else:
+            dist.barrier()
+
+
+def reduce_max(x: float, world: int, use_cuda: bool) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if use_cuda else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, world: int, use_cuda: bool) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if use_cuda else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- the oracle (CPU)
+
+def oracle_step_sample(w, layers=2, ctx=None, seed=99, timings=None):
+    """Times the CPU oracle's own functions on a bounded sample of one decode
+    step of workload w: `layers` decoder layers at context `ctx` (synthetic K/V
+    history standing in for the prompt), one checkpoint exit head and the final
+    head.  Weight generation and conversion are outside the timing.  Returns
+    (seconds per decode step of one sequence extrapolated to all layers with
+    one head, dict of the parts)."""
+    import oracle
+    sh = w.shape
+    cfg = oracle.ModelConfig.from_shape(sh, w.checkpoints)
+    ctx = ctx or (w.max_prompt() + w.steps // 2)
+    t_layer = []
+    for j in range(layers):
+        Wt = oracle.Weights(cfg, lambda jj: synth.layer_weights(sh, w.seed, jj),
+                            np.zeros((2, sh.d_model), np.uint16), synth.final_gain(sh), [],
+                            cache_bytes=0)
+        lw = Wt.layer(j, False)
+        kh = synth.normal_f32(seed, 7 * j + 1, (ctx + 1, sh.n_kv_heads, sh.head_dim), 1.0).astype(np.float64)
+        vh = synth.normal_f32(seed, 7 * j + 2, (ctx + 1, sh.n_kv_heads, sh.head_dim), 1.0).astype(np.float64)
+        h = synth.normal_f32(seed, 7 * j + 3, (sh.d_model,), 1.0).astype(np.float64)
+        t0 = time.perf_counter()
+        oracle.layer_decode(cfg, lw, h, ctx, kh, vh)
+        t_layer.append(time.perf_counter() - t0)
+        del lw, kh, vh
+    E = oracle.bf16_to_f64(synth.embedding(sh, w.seed))
+    g = oracle.bf16_to_f64(synth.final_gain(sh))
+    T = oracle.bf16_to_f64(synth.exit_transform(sh, w.seed, 0)) if w.checkpoints else None
+    h = synth.normal_f32(seed, 5, (sh.d_model,), 1.0).astype(np.float64)
+    t0 = time.perf_counter()
+    oracle.max_softmax(oracle.head_logits(h, g, E, sh.rms_eps, T))
+    t_head = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.argmax_lowest(oracle.head_logits(h, g, E, sh.rms_eps))
+    t_final = time.perf_counter() - t0
+    parts = {"layer_s": float(np.mean(t_layer)), "exit_head_s": t_head, "final_head_s": t_final,
+             "ctx": ctx}
+    return sh.n_layers * parts["layer_s"] + t_head + t_final, parts
+
+
+def cpu_threads():
+    return os.cpu_count() or 1
+
+
+def run_reference(args):
+    """The oracle, as it stands, on this host's cores: every step is one bounded
+    sample (one decoder layer at the workload's mid context plus the exit and
+    final heads), extrapolated to a whole decode step."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[args.workload]
+    secs = []
+    parts = None
+    t_all = time.perf_counter()
+    for i in range(args.warmup + args.steps):
+        s, parts = oracle_step_sample(w, layers=1, seed=100 + i)
+        if i >= args.warmup:
+            secs.append(s)
+    per_step = statistics.median(secs)
+    value = w.batch / (w.batch * per_step)  # sequences are decoded one after another
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3 * w.batch, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "global_batch": w.batch, "seq_len": w.max_prompt(),
+                   "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+                         "sample": "per step: 1 decoder layer at context %d + exit head + final head "
+                                   "(numpy float64), extrapolated to %d layers; %s"
+                                   % (parts["ctx"], w.shape.n_layers, json.dumps(parts))},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": time.perf_counter() - t_all,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- ours
+
+def load_engine(ee, w, max_batch, max_seq_len, stream):
+    sh = w.shape
+    eng = ee.DecodeEngine(sh, w.checkpoints, max_batch, max_seq_len, stream=stream)
+    for j in range(sh.n_layers):
+        eng.load_layer(j, synth.layer_weights(sh, w.seed, j))
+    eng.load_shared(synth.embedding(sh, w.seed), synth.final_gain(sh),
+                    [synth.exit_transform(sh, w.seed, c) for c in range(len(w.checkpoints))])
+    return eng
+
+
+def calibrate(eng, w, prompts, steps, percentiles):
+    """gamma_l = p-th percentile of the no-exit confidences at checkpoint l over
+    the first `steps` decode steps (one sample per sequence and step)."""
+    eng.set_exit_enabled(True)
+    eng.set_thresholds([np.inf] * len(w.checkpoints))
+    tok = eng.prefill(prompts)
+    confs = []
+    for _ in range(steps):
+        tok, _ = eng.decode_step(tok)
+        confs.append(eng.debug_conf())
+    c = np.concatenate(confs, axis=0)
+    return {p: np.percentile(c, p, axis=0) for p in percentiles}, c
+
+
+def timed_run(eng, w, prompts, steps, warmup, heads, world, profile_steps=0):
+    import torch
+    eng.set_exit_enabled(heads)
+    tok = eng.prefill(prompts)
+    for _ in range(warmup):
+        tok, _ = eng.decode_step(tok)
+    ctx0 = np.array([eng.seq_pos(s) for s in range(len(prompts))])
+    barrier(world, True)
+    torch.cuda.synchronize()
+    clocks = ClockSampler()
+    dev_ms = []
+    exits = []
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        tok, ex = eng.decode_step(tok)
+        dev_ms.append(eng.last_step_ms())
+        exits.append(ex.copy())
+    wall = time.perf_counter() - t0
+    torch.cuda.synchronize()
+    barrier(world, True)
+    clk = clocks.stop()
+    prof = []
+    if profile_steps:
+        eng.set_profile(True)
+        for _ in range(profile_steps):
+            ctx = np.array([eng.seq_pos(s) + 1 for s in range(len(prompts))])
+            tok, ex = eng.decode_step(tok)
+            prof.append((eng.profile_read(), ex.copy(), ctx))
+        eng.set_profile(False)
+    return {"dev_ms": dev_ms, "wall_s": wall, "exits": exits, "ctx0": ctx0, "clocks": clk,
+            "profile": prof}
+
+
+def kernel_roofline(sh, ckpts, prof, peak):
+    """Achieved HBM bandwidth of the GEMV kernel (every projection, exit-head and
+    LM-head launch) and of the attention kernel from the profiled launches."""
+    lin = ("qkv", "o", "gateup", "down", "head_t", "head_e", "final_head")
+    acc = {"linear": [0, 0.0, 0], "attn": [0, 0.0, 0]}
+    per_kind = {}
+    for recs, exits, ctx in prof:
+        for kind, layer, ms in recs:
+            b = launch_bytes(sh, ckpts, kind, layer, exits, ctx)
+            key = "linear" if kind in lin else ("attn" if kind == "attn" else None)
+            pk = per_kind.setdefault(kind, [0, 0.0, 0])
+            pk[0] += b
+            pk[1] += ms
+            pk[2] += 1
+            if key:
+                acc[key][0] += b
+                acc[key][1] += ms
+                acc[key][2] += 1
+    out = {}
+    for k, (b, ms, n) in acc.items():
+        gbs = b / (ms * 1e-3) / 1e9 if ms > 0 else 0.0
+        out[k] = {"bytes_per_launch": b / max(n, 1), "ms_per_launch": ms / max(n, 1),
+                  "achieved_gbs": gbs, "frac": gbs / peak}
+    tot = sum(v[1] for v in per_kind.values())
+    out["share"] = {k: round(v[1] / tot, 4) for k, v in sorted(per_kind.items(), key=lambda x: -x[1][1])}
+    out["ms_per_step_profiled"] = tot / max(len(prof), 1)
+    return out
+
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_init(True)
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    __graft_entry__.build()
+    import early_exit_decoding_layer_gb300 as ee
+
+    w = synth.WORKLOADS[args.workload]
+    sh = w.shape
+    peak, peak_kind = peaks()
+    B = w.batch
+    max_seq = w.max_prompt() + args.warmup + args.steps + w.calib_steps + 16
+    lens, prompts = synth.workload_inputs(w)
+    if rank:  # replicas decode different sequences
+        prompts = synth.prompts(sh, w.seed + 1000 * rank, lens)
+    st = torch.cuda.Stream()
+    t_load = time.perf_counter()
+    eng = load_engine(ee, w, B, max_seq, st)
+    t_load = time.perf_counter() - t_load
+    gammas, calib = calibrate(eng, w, prompts, w.calib_steps, w.gamma_percentiles)
+
+    runs = {}
+    for pct in w.gamma_percentiles:
+        eng.set_thresholds(gammas[pct])
+        runs[pct] = timed_run(eng, w, prompts, args.steps, args.warmup, True, world,
+                              profile_steps=args.profile_steps)
+    base = timed_run(eng, w, prompts, args.steps, args.warmup, False, world,
+                     profile_steps=args.profile_steps)
+
+    def summarize(r, heads):
+        dev_s = sum(r["dev_ms"]) / 1e3
+        max_dev = reduce_max(dev_s, world, True)
+        max_wall = reduce_max(r["wall_s"], world, True)
+        tokens = B * args.steps * world
+        bytes_total = 0
+        for k, ex in enumerate(r["exits"]):
+            ctx = r["ctx0"] + k + 1
+            bytes_total += step_bytes(sh, w.checkpoints, ex, ctx, heads)
+        hist = {}
+        for ex in r["exits"]:
+            for e in ex:
+                hist[int(e)] = hist.get(int(e), 0) + 1
+        return {"value": tokens / max_dev, "e2e": tokens / max_wall, "ms_per_step": 1e3 * max_dev / args.steps,
+                "bytes_per_step": bytes_total / args.steps,
+                "step_roofline_frac_8tbs": bytes_total / dev_s / 8e12,
+                "step_roofline_frac_measured": bytes_total / dev_s / (peak * 1e9),
+                "exit_hist": dict(sorted(hist.items())), "clocks": r["clocks"]}
+
+    main = summarize(runs[w.gamma_percentiles[0]], True)
+    nox = summarize(base, False)
+    prof_main = runs[w.gamma_percentiles[0]]["profile"]
+    kr = kernel_roofline(sh, w.checkpoints, prof_main, peak) if prof_main else None
+    kr_base = kernel_roofline(sh, w.checkpoints, base["profile"], peak) if base["profile"] else None
+    h2d, d2h, launches = eng.step_io(B, True)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        s_step, parts = oracle_step_sample(w, layers=args.cpu_layers)
+        cpu = {"value": 1.0 / s_step, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+               "sample": "%d decoder layers at context %d + exit head + final head of one sequence "
+                         "(numpy float64, weights prepared outside the timing), extrapolated to %d "
+                         "layers; parts %s" % (args.cpu_layers, parts["ctx"], sh.n_layers, json.dumps(parts))}
+
+    if rank == 0:
+        clk = main["clocks"]
+        line = {
+            "metric": METRIC, "value": main["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": main["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded random-init weights N(0,0.02), uniform random prompts)",
+            "config": {"workload": w.name, "model": sh.name, "global_batch": B * world,
+                       "seq_len": w.max_prompt(), "parallelism": "replicas" if world > 1 else "single",
+                       "gamma_percentile": w.gamma_percentiles[0],
+                       "gamma": [float(x) for x in gammas[w.gamma_percentiles[0]]],
+                       "l2": "inputs larger than L2 (weights %.1f GB/step streamed)" % (main["bytes_per_step"] / 1e9)},
+            "e2e": {"value": main["e2e"], "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches * args.steps,
+            "roofline": None,
+            "cpu_baseline": cpu,
+            "clocks": {"sm_mhz": clk.get("sm_mhz"), "sm_max_mhz": clk.get("sm_max_mhz"),
+                       "reasons": clk.get("reasons")},
+            "no_exit": {"value": nox["value"], "ms_per_step": nox["ms_per_step"], "e2e": nox["e2e"],
+                        "bytes_per_step": nox["bytes_per_step"],
+                        "step_roofline_frac_8tbs": nox["step_roofline_frac_8tbs"],
+                        "step_roofline_frac_measured": nox["step_roofline_frac_measured"],
+                        "clocks": nox["clocks"], "kernel": kr_base},
+            "speedup_vs_no_exit": main["value"] / nox["value"],
+            "step_roofline": {"bytes_per_step": main["bytes_per_step"],
+                              "frac_8tbs": main["step_roofline_frac_8tbs"],
+                              "frac_measured": main["step_roofline_frac_measured"]},
+            "exit_hist": main["exit_hist"],
+            "load_s": t_load,
+        }
+        if kr:
+            k = kr["linear"]
+            line["roofline"] = {"bound": "hbm", "kernel": "k_linear (GEMV, all launches of a step)",
+                                "achieved": k["achieved_gbs"], "peak": peak,
+                                "peak_kind": peak_kind, "unit": "GB/s", "frac": k["frac"],
+                                "traffic": None, "bytes_per_launch": k["bytes_per_launch"],
+                                "ms_per_launch": k["ms_per_launch"]}
+            line["kernels"] = kr
+        for pct in w.gamma_percentiles[1:]:
+            extra = summarize(runs[pct], True)
+            line.setdefault("other_gammas", {})[str(pct)] = {
+                "value": extra["value"], "ms_per_step": extra["ms_per_step"],
+                "exit_hist": extra["exit_hist"], "gamma": [float(x) for x in gammas[pct]]}
+        print(json.dumps(line), flush=True)
+    eng.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_dry_dist(args):
+    """Multi-rank plumbing without a GPU (gloo): each rank reports made-up
+    per-rank times; rank 0 prints the aggregate line."""
+    rank, world, _ = dist_init(False)
+    B, K = 4, args.steps
+    my_time = 1.0 + 0.5 * rank
+    barrier(world, False)
+    t = reduce_max(my_time, world, False)
+    tok = reduce_sum(B * K, world, False)
+    if rank == 0:
+        print(json.dumps({"metric": METRIC, "value": tok / t, "n_gpus": world, "max_time_s": t,
+                          "tokens": tok, "scaling": "weak"}), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--profile-steps", type=int, default=3)
+    ap.add_argument("--cpu-layers", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dry-dist", action="store_true", help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.dry_dist:
+        return run_dry_dist(args)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

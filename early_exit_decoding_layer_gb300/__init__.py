@@ -33,8 +33,11 @@ EXPORTS = (
     "ee_set_debug", "ee_debug_hidden", "ee_debug_conf", "ee_debug_kv", "ee_debug_block_table",
     "ee_debug_int4", "ee_op_quantize_int4", "ee_op_linear_bf16", "ee_op_linear_int4",
     "ee_attention_scratch_bytes", "ee_op_attention", "ee_head_scratch_bytes",
-    "ee_op_vocab_head",
+    "ee_op_vocab_head", "ee_step_io", "ee_set_profile", "ee_profile_read", "ee_last_step_ms",
 )
+
+KINDS = ("begin", "norm", "qkv", "attn", "o", "gateup", "down", "head_norm", "head_t", "head_e",
+         "final_norm", "final_head")
 
 
 class EEError(RuntimeError):
@@ -62,6 +65,10 @@ class EELayerWeights(ctypes.Structure):
 
 class EESharedWeights(ctypes.Structure):
     _fields_ = [("embed", c_vp), ("g_final", c_vp), ("exit_T", P(c_vp))]
+
+
+class EELaunchRecord(ctypes.Structure):
+    _fields_ = [("kind", c_i32), ("layer", c_i32), ("ms", c_f32)]
 
 
 class EEWeights(ctypes.Structure):
@@ -110,6 +117,10 @@ def load_library(path: str = LIB_PATH):
                                   c_vp, c_vp]),
         "ee_head_scratch_bytes": (c_sz, [i32]),
         "ee_op_vocab_head": (i32, [i32, i32, i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
+        "ee_step_io": (i32, [c_vp, i32, i32, P(c_sz), P(c_sz), P(i32)]),
+        "ee_set_profile": (i32, [c_vp, i32]),
+        "ee_profile_read": (i32, [c_vp, P(EELaunchRecord), i32, P(i32)]),
+        "ee_last_step_ms": (i32, [c_vp, P(c_f32)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -155,7 +166,10 @@ class DecodeEngine:
     """One early-exit decoding context on one GPU (see include/ee.h)."""
 
     def __init__(self, shape, checkpoints: Sequence[int], max_batch: int, max_seq_len: int,
-                 device: int = 0):
+                 device: int = 0, stream=None):
+        """stream: a torch.cuda.Stream to queue all work on (default: the
+        current stream if it is not the legacy default stream, else a stream
+        the library creates)."""
         import torch
 
         self.lib = load_library()
@@ -174,7 +188,10 @@ class DecodeEngine:
         with torch.cuda.device(self.device):
             self._arena = torch.empty(nbytes + 256, dtype=torch.uint8, device=self.device)
             base = (self._arena.data_ptr() + 255) // 256 * 256
-            stream = torch.cuda.current_stream(self.device).cuda_stream
+            if stream is None:
+                stream = torch.cuda.current_stream(self.device)
+            self.stream = stream
+            stream = stream.cuda_stream
             ctx = c_vp()
             st = self.lib.ee_create(ctypes.byref(self.cfg), base, nbytes, stream, ctypes.byref(ctx))
         if st != 0:
@@ -268,6 +285,29 @@ class DecodeEngine:
         b, p = c_i32(), c_i32()
         self._check(self.lib.ee_seq_info(self.ctx, ctypes.byref(b), seq, ctypes.byref(p)))
         return p.value
+
+    def step_io(self, batch: int, heads: bool):
+        """(h2d bytes, d2h bytes, kernel launches) of one decode step."""
+        h, d, n = c_sz(), c_sz(), c_i32()
+        self._check(self.lib.ee_step_io(self.ctx, batch, 1 if heads else 0, ctypes.byref(h),
+                                        ctypes.byref(d), ctypes.byref(n)))
+        return h.value, d.value, n.value
+
+    def last_step_ms(self) -> float:
+        ms = c_f32()
+        self._check(self.lib.ee_last_step_ms(self.ctx, ctypes.byref(ms)))
+        return ms.value
+
+    def set_profile(self, profile: bool):
+        self._check(self.lib.ee_set_profile(self.ctx, 1 if profile else 0))
+
+    def profile_read(self):
+        """[(kind name, layer, ms)] of the last profiled step's launches."""
+        n = c_i32()
+        self._check(self.lib.ee_profile_read(self.ctx, None, 0, ctypes.byref(n)))
+        recs = (EELaunchRecord * max(1, n.value))()
+        self._check(self.lib.ee_profile_read(self.ctx, recs, n.value, ctypes.byref(n)))
+        return [(KINDS[r.kind], r.layer, r.ms) for r in recs[: n.value]]
 
     # -- inspection ----------------------------------------------------------
     def debug_hidden(self, layer: int) -> np.ndarray:

@@ -32,12 +32,13 @@ struct StepDesc {
   int32_t debug;                    // keep per-layer hidden states
 };
 
-// Device -> host step outputs (one copy per step).
+// Device -> host step outputs.  One copy per step of the head of the struct
+// up to the confidences of the batch's sequences.
 struct StepOut {
-  int32_t next_token[EE_MAX_BATCH];
-  int32_t exit_layer[EE_MAX_BATCH];
   int32_t err;                      // first device error code, 0 if none
   int32_t pad[3];
+  int32_t next_token[EE_MAX_BATCH];
+  int32_t exit_layer[EE_MAX_BATCH];
   float conf[EE_MAX_BATCH * EE_MAX_CHECKPOINTS];  // [seq][checkpoint], NaN = not evaluated
 };
 

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdarg.h>
+#include <stddef.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -21,6 +22,8 @@ using namespace ee;
 namespace {
 
 constexpr size_t kAlign = 256;
+
+size_t step_d2h_bytes(int B) { return offsetof(StepOut, conf) + (size_t)B * EE_MAX_CHECKPOINTS * sizeof(float); }
 constexpr int kHeadGridMax = 256;       // CTAs of a vocabulary-head launch (<= SMs)
 constexpr int kAttnSplitSlots = 1024;   // batch x splits capacity of the attention scratch
 
@@ -86,8 +89,11 @@ struct ee_ctx {
   Dims m;
   int dev = 0, num_sms = 0;
   cudaStream_t user_stream = nullptr;
-  cudaStream_t st = nullptr;
+  cudaStream_t st = nullptr;   // the caller's stream, or our own if the caller gave NULL
+  bool own_stream = false;
   cudaEvent_t ev = nullptr;
+  cudaEvent_t step_ev[2] = {nullptr, nullptr};
+  float last_step_ms = 0.0f;
   uint8_t* arena = nullptr;
   size_t arena_bytes = 0;
 
@@ -130,6 +136,12 @@ struct ee_ctx {
   int exit_enabled = 1, use_graph = 1, debug = 0;
   bool cuda_broken = false;
   std::map<std::pair<int, int>, cudaGraphExec_t> graphs;
+  // profiling: events around each launch of a step
+  int profile = 0;
+  std::vector<cudaEvent_t> prof_ev;
+  std::vector<std::pair<int, int>> prof_tag;  // (kind, layer) per launch of the last step
+  std::vector<float> prof_ms;
+  int launches[2] = {0, 0};                   // kernels per step without / with heads
   std::string err;
 };
 
@@ -284,15 +296,60 @@ struct DeviceGuard {
 
 // Orders our stream after everything already queued on the caller's stream.
 ee_status join_user_stream(ee_ctx* c) {
+  if (!c->own_stream) return EE_OK;
   EE_CUDA(c, cudaEventRecord(c->ev, c->user_stream));
   EE_CUDA(c, cudaStreamWaitEvent(c->st, c->ev, 0));
   return EE_OK;
 }
 
+// Launch bookkeeping of one step: counts launches and, in profile mode,
+// records an event before the first and after every launch.
+struct LaunchLog {
+  ee_ctx* c;
+  bool prof;
+  int n = 0;
+  LaunchLog(ee_ctx* cc, bool p) : c(cc), prof(p) {
+    if (prof) c->prof_tag.clear();
+  }
+  ee_status before() {
+    if (!prof) return EE_OK;
+    if (n == 0) {
+      if ((int)c->prof_ev.size() < 1 && add_event() != EE_OK) return EE_ERR_CUDA;
+      EE_CUDA(c, cudaEventRecord(c->prof_ev[0], c->st));
+    }
+    return EE_OK;
+  }
+  ee_status after(int kind, int layer) {
+    ++n;
+    if (!prof) return EE_OK;
+    while ((int)c->prof_ev.size() < n + 1)
+      if (add_event() != EE_OK) return EE_ERR_CUDA;
+    EE_CUDA(c, cudaEventRecord(c->prof_ev[n], c->st));
+    c->prof_tag.emplace_back(kind, layer);
+    return EE_OK;
+  }
+  ee_status add_event() {
+    cudaEvent_t e;
+    EE_CUDA(c, cudaEventCreate(&e));
+    c->prof_ev.push_back(e);
+    return EE_OK;
+  }
+};
+
+#define EE_LAUNCH(log, kind, layer, call) \
+  do {                                    \
+    ee_status s_ = (log).before();        \
+    if (s_ != EE_OK) return s_;           \
+    EE_CUDA(c, (call));                   \
+    s_ = (log).after((kind), (layer));    \
+    if (s_ != EE_OK) return s_;           \
+  } while (0)
+
 // ---------------------------------------------------------------- step enqueue
-ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
+ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
   const Dims& m = c->m;
   cudaStream_t st = c->st;
+  LaunchLog log(c, prof);
   EE_CUDA(c, cudaMemcpyAsync(c->desc_dev, c->desc_host, sizeof(StepDesc), cudaMemcpyHostToDevice, st));
 
   BeginParams bp = {};
@@ -309,7 +366,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
   bp.n_layers = m.L;
   bp.n_ckpt = m.nck;
   bp.dbg_flag = c->dbg_flag;
-  EE_CUDA(c, launch_step_begin(bp, B, st));
+  EE_LAUNCH(log, EE_K_BEGIN, -1, launch_step_begin(bp, B, st));
 
   int32_t* err = &c->out_dev->err;
   const int nsplit = attention_nsplit(B, m.hkv, c->num_sms);
@@ -342,7 +399,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
     np.list = c->lists->part;
     np.g = w.g_attn;
     np.xh = c->xh;
-    EE_CUDA(c, launch_rmsnorm(np, B, true, st));
+    EE_LAUNCH(log, EE_K_NORM, j, launch_rmsnorm(np, B, true, st));
     // QKV projection + RoPE + K/V write into the shared paged cache
     LinearParams p = base;
     p.N = m.nqkv;
@@ -359,7 +416,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
     p.q_out = c->q;
     p.kc = c->kcache + (size_t)j * m.kv_layer_elems;
     p.vc = c->vcache + (size_t)j * m.kv_layer_elems;
-    EE_CUDA(c, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
+    EE_LAUNCH(log, EE_K_QKV, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
     // decode attention
     AttnParams ap = {};
     ap.list = c->lists->part;
@@ -379,7 +436,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
     ap.oh = c->ah;
     ap.o_stride = m.dq;
     ap.err = err;
-    EE_CUDA(c, launch_attention(ap, B, true, st));
+    EE_LAUNCH(log, EE_K_ATTN, j, launch_attention(ap, B, true, st));
     // O projection + residual
     p = base;
     p.N = m.d;
@@ -393,10 +450,10 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
     p.xh = c->ah;
     p.x_stride = m.dq;
     p.epi = EPI_RESID;
-    EE_CUDA(c, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
+    EE_LAUNCH(log, EE_K_O, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
     // FFN RMSNorm
     np.g = w.g_ffn;
-    EE_CUDA(c, launch_rmsnorm(np, B, true, st));
+    EE_LAUNCH(log, EE_K_NORM, j, launch_rmsnorm(np, B, true, st));
     // gate/up + SwiGLU
     p = base;
     p.N = 2 * m.F;
@@ -412,7 +469,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
     p.epi = EPI_SWIGLU;
     p.xh_out = c->acth;
     p.xo_stride = m.F;
-    EE_CUDA(c, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
+    EE_LAUNCH(log, EE_K_GATEUP, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
     // down projection + residual (+ per-layer copy in debug mode)
     p = base;
     p.N = m.d;
@@ -427,7 +484,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
     p.x_stride = m.F;
     p.epi = EPI_RESID;
     p.hdbg = c->hdbg + (size_t)j * EE_MAX_BATCH * m.d;
-    EE_CUDA(c, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
+    EE_LAUNCH(log, EE_K_DOWN, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
 
     const auto ck = std::find(c->ckpts.begin(), c->ckpts.end(), j);
     if (heads && ck != c->ckpts.end()) {
@@ -436,7 +493,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
       NormParams fp = np;
       fp.list = c->lists->full;
       fp.g = c->g_final;
-      EE_CUDA(c, launch_rmsnorm(fp, B, true, st));
+      EE_LAUNCH(log, EE_K_HEAD_NORM, j, launch_rmsnorm(fp, B, true, st));
       p = base;
       p.N = m.d;
       p.K = m.d;
@@ -448,7 +505,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
       p.epi = EPI_X;
       p.xh_out = c->uh;
       p.xo_stride = m.d;
-      EE_CUDA(c, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
+      EE_LAUNCH(log, EE_K_HEAD_T, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
       // z = u E^T, conf = max softmax, exit if conf > gamma_c, compact the lists
       p = base;
       p.N = m.V;
@@ -466,14 +523,15 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
       p.exit_layer = c->out_dev->exit_layer;
       p.ckpt_index = ci;
       p.ckpt_layer = j;
-      EE_CUDA(c, launch_linear(p, std::min(linear_grid(p.N, c->num_sms), kHeadGridMax), true, st));
+      EE_LAUNCH(log, EE_K_HEAD_E, j,
+                launch_linear(p, std::min(linear_grid(p.N, c->num_sms), kHeadGridMax), true, st));
     }
   }
   // final LM head: argmax of RMSNorm_final(h) E^T
   NormParams fp = np;
   fp.list = c->lists->fin;
   fp.g = c->g_final;
-  EE_CUDA(c, launch_rmsnorm(fp, B, true, st));
+  EE_LAUNCH(log, EE_K_FINAL_NORM, -1, launch_rmsnorm(fp, B, true, st));
   LinearParams p = base;
   p.N = m.V;
   p.K = m.d;
@@ -486,19 +544,37 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads) {
   p.head_mode = HEAD_FINAL;
   p.head_counter = c->head_cnt;
   p.argmax_out = c->out_dev->next_token;
-  EE_CUDA(c, launch_linear(p, std::min(linear_grid(p.N, c->num_sms), kHeadGridMax), true, st));
-  EE_CUDA(c, cudaMemcpyAsync(c->out_host, c->out_dev, sizeof(StepOut), cudaMemcpyDeviceToHost, st));
+  EE_LAUNCH(log, EE_K_FINAL_HEAD, -1,
+            launch_linear(p, std::min(linear_grid(p.N, c->num_sms), kHeadGridMax), true, st));
+  EE_CUDA(c, cudaMemcpyAsync(c->out_host, c->out_dev, step_d2h_bytes(B), cudaMemcpyDeviceToHost, st));
+  c->launches[heads ? 1 : 0] = log.n;
   return EE_OK;
 }
 
-ee_status run_step(ee_ctx* c, int B, bool heads) {
+// One step in profile mode: eager launches with an event pair around each.
+ee_status run_step_profiled(ee_ctx* c, int B, bool heads) {
+  const ee_status s = enqueue_step(c, B, heads, true);
+  if (s != EE_OK) return s;
+  EE_CUDA(c, cudaStreamSynchronize(c->st));
+  c->prof_ms.assign(c->prof_tag.size(), 0.0f);
+  for (size_t i = 0; i < c->prof_tag.size(); ++i)
+    EE_CUDA(c, cudaEventElapsedTime(&c->prof_ms[i], c->prof_ev[i], c->prof_ev[i + 1]));
+  c->last_step_ms = 0.0f;
+  for (float v : c->prof_ms) c->last_step_ms += v;
+  return EE_OK;
+}
+
+// One step replayed from the graph of (B, heads) -- captured on first use --
+// or launched eagerly, timed by an event pair on the context's stream.
+ee_status run_step_timed(ee_ctx* c, int B, bool heads) {
+  EE_CUDA(c, cudaEventRecord(c->step_ev[0], c->st));
   if (c->use_graph) {
     const auto key = std::make_pair(B, heads ? 1 : 0);
     auto it = c->graphs.find(key);
     if (it == c->graphs.end()) {
       cudaGraph_t g = nullptr;
       EE_CUDA(c, cudaStreamBeginCapture(c->st, cudaStreamCaptureModeThreadLocal));
-      const ee_status s = enqueue_step(c, B, heads);
+      const ee_status s = enqueue_step(c, B, heads, false);
       const cudaError_t e = cudaStreamEndCapture(c->st, &g);
       if (s != EE_OK) {
         if (g) cudaGraphDestroy(g);
@@ -514,10 +590,18 @@ ee_status run_step(ee_ctx* c, int B, bool heads) {
     }
     EE_CUDA(c, cudaGraphLaunch(it->second, c->st));
   } else {
-    const ee_status s = enqueue_step(c, B, heads);
+    const ee_status s = enqueue_step(c, B, heads, false);
     if (s != EE_OK) return s;
   }
+  EE_CUDA(c, cudaEventRecord(c->step_ev[1], c->st));
   EE_CUDA(c, cudaStreamSynchronize(c->st));
+  EE_CUDA(c, cudaEventElapsedTime(&c->last_step_ms, c->step_ev[0], c->step_ev[1]));
+  return EE_OK;
+}
+
+ee_status run_step(ee_ctx* c, int B, bool heads) {
+  const ee_status s = c->profile ? run_step_profiled(c, B, heads) : run_step_timed(c, B, heads);
+  if (s != EE_OK) return s;
   if (c->out_host->err != 0)
     return fail(c, EE_ERR_DEVICE_TIMEOUT,
                 "a bounded device wait gave up (code %d: 1 = stage fill, 2 = stage drain, 3 = exit drain)",
@@ -647,8 +731,15 @@ ee_status ee_create(const ee_config* cfg, void* dev_arena, size_t arena_bytes, v
     return bail(EE_ERR_CUDA);
   if (c->num_sms > kHeadGridMax) c->num_sms = kHeadGridMax;
   if (linear_prepare() != cudaSuccess) return bail(EE_ERR_CUDA);
-  if (cudaStreamCreateWithFlags(&c->st, cudaStreamNonBlocking) != cudaSuccess) return bail(EE_ERR_CUDA);
+  if (c->user_stream) {
+    c->st = c->user_stream;
+  } else {
+    if (cudaStreamCreateWithFlags(&c->st, cudaStreamNonBlocking) != cudaSuccess) return bail(EE_ERR_CUDA);
+    c->own_stream = true;
+  }
   if (cudaEventCreateWithFlags(&c->ev, cudaEventDisableTiming) != cudaSuccess) return bail(EE_ERR_CUDA);
+  if (cudaEventCreate(&c->step_ev[0]) != cudaSuccess || cudaEventCreate(&c->step_ev[1]) != cudaSuccess)
+    return bail(EE_ERR_CUDA);
   if (cudaHostAlloc((void**)&c->desc_host, sizeof(StepDesc), cudaHostAllocDefault) != cudaSuccess ||
       cudaHostAlloc((void**)&c->out_host, sizeof(StepOut), cudaHostAllocDefault) != cudaSuccess)
     return bail(EE_ERR_CUDA);
@@ -686,11 +777,14 @@ ee_status ee_create(const ee_config* cfg, void* dev_arena, size_t arena_bytes, v
 void ee_destroy(ee_ctx* c) {
   if (!c) return;
   for (auto& kv : c->graphs) cudaGraphExecDestroy(kv.second);
+  for (auto e : c->prof_ev) cudaEventDestroy(e);
   if (c->st) cudaStreamSynchronize(c->st);
   if (c->desc_host) cudaFreeHost(c->desc_host);
   if (c->out_host) cudaFreeHost(c->out_host);
   if (c->ev) cudaEventDestroy(c->ev);
-  if (c->st) cudaStreamDestroy(c->st);
+  for (auto e : c->step_ev)
+    if (e) cudaEventDestroy(e);
+  if (c->st && c->own_stream) cudaStreamDestroy(c->st);
   delete c;
 }
 
@@ -798,6 +892,40 @@ ee_status ee_set_exit_enabled(ee_ctx* c, int32_t enabled) {
 ee_status ee_set_use_graph(ee_ctx* c, int32_t use_graph) {
   if (!c) return EE_ERR_INVALID_ARG;
   c->use_graph = use_graph ? 1 : 0;
+  return EE_OK;
+}
+
+ee_status ee_last_step_ms(const ee_ctx* c, float* ms) {
+  if (!c || !ms) return EE_ERR_INVALID_ARG;
+  *ms = c->last_step_ms;
+  return EE_OK;
+}
+
+ee_status ee_set_profile(ee_ctx* c, int32_t profile) {
+  if (!c) return EE_ERR_INVALID_ARG;
+  c->profile = profile ? 1 : 0;
+  return EE_OK;
+}
+
+ee_status ee_profile_read(ee_ctx* c, ee_launch_record* out, int32_t cap, int32_t* n) {
+  if (!c || !n) return EE_ERR_INVALID_ARG;
+  *n = (int32_t)c->prof_ms.size();
+  if (out)
+    for (int i = 0; i < *n && i < cap; ++i)
+      out[i] = ee_launch_record{c->prof_tag[i].first, c->prof_tag[i].second, c->prof_ms[i]};
+  return EE_OK;
+}
+
+ee_status ee_step_io(const ee_ctx* c, int32_t batch, int32_t heads, size_t* h2d, size_t* d2h,
+                     int32_t* launches) {
+  if (!c || batch < 1 || batch > EE_MAX_BATCH) return EE_ERR_INVALID_ARG;
+  if (h2d) *h2d = sizeof(StepDesc);
+  if (d2h) *d2h = step_d2h_bytes(batch);
+  if (launches) {
+    // begin + per layer (2 norms, QKV, attention, O, gate/up, down) + heads + final norm/head
+    const int with_heads = heads && c->m.nck > 0;
+    *launches = 1 + 7 * c->m.L + (with_heads ? 3 * c->m.nck : 0) + 2;
+  }
   return EE_OK;
 }
 

@@ -129,8 +129,11 @@ size_t ee_arena_bytes(const ee_config *cfg);
 
 /* Validates cfg (before any CUDA call), carves the caller's arena
  * (dev_arena, 256-byte aligned, >= ee_arena_bytes(cfg)) and binds the
- * context to the current device and to `stream` (a cudaStream_t, NULL = the
- * legacy default stream).  The arena must outlive the context. */
+ * context to the current device.  All work is queued on `stream` (a
+ * cudaStream_t, not the legacy default stream, which cannot be captured into
+ * a graph); with stream = NULL the context creates its own non-blocking
+ * stream and orders it after the legacy default stream at every call.  The
+ * arena and the stream must outlive the context. */
 ee_status ee_create(const ee_config *cfg, void *dev_arena, size_t arena_bytes, void *stream,
                     ee_ctx **out);
 void ee_destroy(ee_ctx *ctx);
@@ -183,6 +186,45 @@ ee_status ee_reset(ee_ctx *ctx);
 /* Number of active sequences and the position (tokens in the cache) of
  * sequence seq. */
 ee_status ee_seq_info(const ee_ctx *ctx, int32_t *batch, int32_t seq, int32_t *pos);
+
+/* Device time of the last prefill/decode step: CUDA events recorded on the
+ * context's stream right before and after the step's work (the graph replay,
+ * with its two small copies).  In profile mode, the sum of the launches. */
+ee_status ee_last_step_ms(const ee_ctx *ctx, float *ms);
+
+/* Bytes one decode step copies host -> device and device -> host for a batch
+ * of `batch` sequences, and the number of kernels it launches with exit heads
+ * enabled (heads = 1) or not.  No CUDA call. */
+ee_status ee_step_io(const ee_ctx *ctx, int32_t batch, int32_t heads, size_t *h2d_bytes,
+                     size_t *d2h_bytes, int32_t *launches);
+
+/* Kinds of kernel launch in a decode step (ee_launch_record.kind). */
+enum {
+  EE_K_BEGIN = 0,      /* embedding gather, positions, lists            */
+  EE_K_NORM = 1,       /* attention / FFN RMSNorm                       */
+  EE_K_QKV = 2,        /* QKV GEMV + RoPE + K/V write                   */
+  EE_K_ATTN = 3,       /* decode attention                              */
+  EE_K_O = 4,          /* O GEMV + residual                             */
+  EE_K_GATEUP = 5,     /* gate/up GEMV + SwiGLU                         */
+  EE_K_DOWN = 6,       /* down GEMV + residual                          */
+  EE_K_HEAD_NORM = 7,  /* checkpoint: final-norm of the full sub-batch  */
+  EE_K_HEAD_T = 8,     /* checkpoint: u = n T GEMV                      */
+  EE_K_HEAD_E = 9,     /* checkpoint: vocabulary head + exit decision   */
+  EE_K_FINAL_NORM = 10,
+  EE_K_FINAL_HEAD = 11 /* final LM head, argmax                          */
+};
+typedef struct {
+  int32_t kind;   /* EE_K_* */
+  int32_t layer;  /* decoder layer, or -1 */
+  float ms;       /* device time between events around the launch */
+} ee_launch_record;
+
+/* profile = 1: the following decode steps run without the CUDA graph and
+ * with a CUDA event pair around every kernel launch (this serialises the
+ * launches, so step times are longer than without profiling);
+ * ee_profile_read returns the last step's launches in order. */
+ee_status ee_set_profile(ee_ctx *ctx, int32_t profile);
+ee_status ee_profile_read(ee_ctx *ctx, ee_launch_record *out, int32_t cap, int32_t *n);
 
 /* ------------------------------------------------- inspection (tests, tools) */
 

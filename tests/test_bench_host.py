@@ -1,0 +1,77 @@
+"""Host logic of bench.py: the roofline byte model against the workload's
+stated per-step figures, and the multi-rank replica path over gloo (CPU)."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+import bench
+import synth
+from tests.conftest import ROOT
+
+
+def test_step_bytes_8b_b1_no_exit():
+    w = synth.WORKLOADS["llama3.1-8b-b1"]
+    sh = w.shape
+    L = sh.n_layers
+    # bf16 layer: QKV 6144x4096 + O 4096x4096 + gate/up 28672x4096 + down 4096x14336, 2 B each
+    assert sum(bench.w_bytes(N, K, False) for N, K in bench.mat_list(sh).values()) == 436207616
+    ctx = 2048 + 128
+    b = bench.step_bytes(sh, w.checkpoints, [L - 1], [ctx], heads=False)
+    expect = 32 * 436207616 + 128256 * 4096 * 2 + 32 * ctx * 2 * 8 * 128 * 2
+    assert b == expect
+    assert 15.2e9 < b < 15.4e9       # the workload's 15.3 GB no-exit figure
+
+
+def test_step_bytes_exit_at_first_checkpoint():
+    w = synth.WORKLOADS["llama3.1-8b-b1"]
+    sh = w.shape
+    ctx = 2176
+    b = bench.step_bytes(sh, w.checkpoints, [4], [ctx], heads=True)
+    bf16 = 436207616
+    int4 = sum(bench.w_bytes(N, K, True) for N, K in bench.mat_list(sh).values())
+    assert int4 == 112459776
+    E, T = 128256 * 4096 * 2, 4096 * 4096 * 2
+    assert b == 5 * bf16 + 27 * int4 + (T + E) + E + 32 * ctx * 4096
+    assert 7.5e9 < b < 7.8e9         # the workload's 7.64 GB bound
+
+
+def test_step_bytes_mixed_batch_reads_each_matrix_once():
+    w = synth.WORKLOADS["llama3.1-8b-b32"]
+    sh = w.shape
+    # one sequence never exits, one exits at 4: every layer reads bf16, layers 5.. also int4
+    b = bench.step_bytes(sh, w.checkpoints, [31, 4], [100, 100], heads=True)
+    bf16 = 436207616
+    int4 = 112459776
+    E, T = 128256 * 4096 * 2, 4096 * 4096 * 2
+    heads = 7 * (T + E)   # the non-exiting sequence is scored at every checkpoint
+    kv = 2 * 32 * 100 * 4096
+    assert b == 32 * bf16 + 27 * int4 + heads + E + kv
+
+
+def free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+@pytest.mark.timeout(300)
+def test_replicas_world_size_2_gloo():
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes", "1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(free_port()),
+           os.path.join(ROOT, "bench.py"), "--dry-dist", "--gpus", "2", "--steps", "10",
+           "--warmup", "3"]
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    r = subprocess.run(cmd, capture_output=True, text=True, cwd=ROOT, env=env, timeout=280)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1   # rank 0 alone prints
+    out = json.loads(lines[0])
+    assert out["n_gpus"] == 2
+    assert out["max_time_s"] == 1.5          # the slower rank sets the time
+    assert out["value"] == pytest.approx(2 * 4 * 10 / 1.5)
