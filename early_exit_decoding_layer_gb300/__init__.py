@@ -112,9 +112,9 @@ def load_library(path: str = LIB_PATH):
         "ee_op_quantize_int4": (i32, [c_vp, i32, i32, c_vp, c_vp, i32, c_vp]),
         "ee_op_linear_bf16": (i32, [i32, i32, i32, c_vp, c_vp, c_vp, c_vp, c_vp]),
         "ee_op_linear_int4": (i32, [i32, i32, i32, c_vp, c_vp, c_vp, i32, c_vp, c_vp, c_vp]),
-        "ee_attention_scratch_bytes": (c_sz, [i32, i32, i32, i32]),
-        "ee_op_attention": (i32, [i32, i32, i32, i32, c_vp, c_vp, c_vp, c_vp, i32, c_vp, c_vp, c_vp,
-                                  c_vp, c_vp]),
+        "ee_attention_scratch_bytes": (c_sz, [i32, i32, i32, i32, i32]),
+        "ee_op_attention": (i32, [i32, i32, i32, i32, i32, c_vp, c_vp, c_vp, c_vp, i32, c_vp, c_vp,
+                                  c_vp, c_vp, c_vp]),
         "ee_head_scratch_bytes": (c_sz, [i32]),
         "ee_op_vocab_head": (i32, [i32, i32, i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]),
         "ee_step_io": (i32, [c_vp, i32, i32, P(c_sz), P(c_sz), P(i32)]),
@@ -406,21 +406,21 @@ def linear_int4(x_f16, packed, scales, err=None, stream=None):
     return y
 
 
-def attention_scratch_bytes(B, n_heads, n_kv_heads, head_dim) -> int:
-    return int(load_library().ee_attention_scratch_bytes(B, n_heads, n_kv_heads, head_dim))
+def attention_scratch_bytes(B, n_heads, n_kv_heads, head_dim, max_ctx) -> int:
+    return int(load_library().ee_attention_scratch_bytes(B, n_heads, n_kv_heads, head_dim, max_ctx))
 
 
-def attention(q, kcache, vcache, block_table, pos, n_heads, n_kv_heads, head_dim, scratch=None,
-              err=None, stream=None):
+def attention(q, kcache, vcache, block_table, pos, n_heads, n_kv_heads, head_dim, max_ctx,
+              scratch=None, err=None, stream=None):
     """q [B, Hq*hd] fp32; caches [blocks, Hkv, 16, hd] fp16 bits; block_table [B, W] int32;
     pos [B] int32.  Returns o [B, Hq*hd] fp32."""
     import torch
     B = q.shape[0]
     if scratch is None:
-        scratch = torch.zeros(attention_scratch_bytes(B, n_heads, n_kv_heads, head_dim),
+        scratch = torch.zeros(attention_scratch_bytes(B, n_heads, n_kv_heads, head_dim, max_ctx),
                               dtype=torch.uint8, device=q.device)
     o = torch.empty((B, n_heads * head_dim), dtype=torch.float32, device=q.device)
-    _raise(load_library().ee_op_attention(B, n_heads, n_kv_heads, head_dim, _ptr(q), _ptr(kcache),
+    _raise(load_library().ee_op_attention(B, n_heads, n_kv_heads, head_dim, max_ctx, _ptr(q), _ptr(kcache),
                                           _ptr(vcache), _ptr(block_table), block_table.shape[1],
                                           _ptr(pos), _ptr(o), _ptr(scratch), _ptr(err),
                                           _stream(stream)), "ee_op_attention")

@@ -56,6 +56,8 @@ enum HeadMode : int32_t { HEAD_CONF_ARGMAX = 0, HEAD_CHECKPOINT = 1, HEAD_FINAL 
 
 struct LinearParams {
   int32_t N, K;
+  int32_t nstages;           // ring stages (linear_plan_smem)
+  int32_t xs_rows;           // > 0: activations of up to xs_rows sequences staged in smem
   // weights: bf16 [N, K]; int4 packed [N, K/2] with bf16 scales [N, sstride]
   const uint16_t* w;
   const uint8_t* wq;
@@ -108,6 +110,9 @@ size_t linear_smem_bytes();
 // Sets the kernels' shared-memory attributes on the current device (call once
 // per device before the first launch, outside stream capture).
 cudaError_t linear_prepare();
+// Chooses the ring depth and whether the activations of the step's rows (at
+// most max_rows sequences) are staged in shared memory.
+void linear_plan_smem(LinearParams& p, int max_rows);
 // Launches the GEMV on `grid` CTAs (grid <= number of SMs).  pdl: launch
 // with programmatic stream serialisation.
 cudaError_t launch_linear(const LinearParams& p, int grid, bool pdl, cudaStream_t st);
@@ -125,7 +130,8 @@ struct AttnParams {
   const int32_t* block_table;
   int32_t bt_stride;
   const int32_t* pos;        // query position by sequence id (ctx = pos + 1)
-  int32_t nsplit;
+  int32_t nsplit;            // CTAs per (sequence, kv head): attention_nsplit(max context)
+  int32_t bpc;               // 16-slot blocks per CTA: attention_blocks_per_cta(head_dim)
   float* part;               // scratch partials
   int32_t* counters;         // [batch_slots][Hkv], zero between launches
   float* o_f32;              // [seq][Hq*hd] (op) or null
@@ -135,7 +141,10 @@ struct AttnParams {
 };
 size_t attention_part_floats(int batch_slots, int n_heads, int n_kv_heads, int head_dim, int nsplit);
 cudaError_t launch_attention(const AttnParams& p, int batch_slots, bool pdl, cudaStream_t st);
-int attention_nsplit(int batch, int n_kv_heads, int num_sms);
+int attention_blocks_per_cta(int head_dim);
+int attention_nsplit(int max_ctx, int head_dim);
+int attention_max_split();
+cudaError_t attention_prepare();
 
 // ------------------------------------------------------------------ small kernels
 struct NormParams {

@@ -25,7 +25,6 @@ constexpr size_t kAlign = 256;
 
 size_t step_d2h_bytes(int B) { return offsetof(StepOut, conf) + (size_t)B * EE_MAX_CHECKPOINTS * sizeof(float); }
 constexpr int kHeadGridMax = 256;       // CTAs of a vocabulary-head launch (<= SMs)
-constexpr int kAttnSplitSlots = 1024;   // batch x splits capacity of the attention scratch
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -184,6 +183,8 @@ const char* validate_config(const ee_config* c) {
   if (c->kv_block != EE_KV_BLOCK) return "kv_block must be 16";
   if (c->max_batch < 1 || c->max_batch > EE_MAX_BATCH) return "max_batch must be in [1, 64]";
   if (c->max_seq_len < 2) return "max_seq_len must be >= 2";
+  if (attention_nsplit(c->max_seq_len, c->head_dim) > attention_max_split())
+    return "max_seq_len too large for the attention kernel";
   if (!(c->rms_eps > 0.0f) || !(c->rope_theta > 0.0f)) return "rms_eps and rope_theta must be > 0";
   if (c->n_checkpoints < 0 || c->n_checkpoints > EE_MAX_CHECKPOINTS) return "n_checkpoints out of range";
   if (c->n_checkpoints > 0 && !c->checkpoint_layers) return "checkpoint_layers is NULL";
@@ -232,7 +233,8 @@ size_t carve(ee_ctx* c, const ee_config& cfg, uint8_t* base) {
   uint16_t* acth = cv.take<uint16_t>((size_t)EE_MAX_BATCH * m.F);
   uint16_t* uh = cv.take<uint16_t>((size_t)EE_MAX_BATCH * m.d);
   float* q = cv.take<float>((size_t)EE_MAX_BATCH * m.dq);
-  float* apart = cv.take<float>((size_t)kAttnSplitSlots * m.hkv * (m.hq / m.hkv) * (m.hd + 2));
+  float* apart = cv.take<float>(
+      attention_part_floats(m.maxb, m.hq, m.hkv, m.hd, attention_nsplit(m.maxs, m.hd)));
   float* hpart = cv.take<float>((size_t)kHeadGridMax * EE_MAX_BATCH * 4);
   float* hdbg = cv.take<float>((size_t)m.L * EE_MAX_BATCH * m.d);
   StepDesc* desc = cv.take<StepDesc>(1);
@@ -369,7 +371,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
   EE_LAUNCH(log, EE_K_BEGIN, -1, launch_step_begin(bp, B, st));
 
   int32_t* err = &c->out_dev->err;
-  const int nsplit = attention_nsplit(B, m.hkv, c->num_sms);
+  const int nsplit = attention_nsplit(m.maxs, m.hd);
 
   NormParams np = {};
   np.h = c->h;
@@ -416,6 +418,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.q_out = c->q;
     p.kc = c->kcache + (size_t)j * m.kv_layer_elems;
     p.vc = c->vcache + (size_t)j * m.kv_layer_elems;
+    linear_plan_smem(p, B);
     EE_LAUNCH(log, EE_K_QKV, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
     // decode attention
     AttnParams ap = {};
@@ -431,6 +434,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     ap.bt_stride = m.bps;
     ap.pos = c->pos;
     ap.nsplit = nsplit;
+    ap.bpc = attention_blocks_per_cta(m.hd);
     ap.part = c->attn_part;
     ap.counters = c->attn_cnt;
     ap.oh = c->ah;
@@ -450,6 +454,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.xh = c->ah;
     p.x_stride = m.dq;
     p.epi = EPI_RESID;
+    linear_plan_smem(p, B);
     EE_LAUNCH(log, EE_K_O, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
     // FFN RMSNorm
     np.g = w.g_ffn;
@@ -469,6 +474,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.epi = EPI_SWIGLU;
     p.xh_out = c->acth;
     p.xo_stride = m.F;
+    linear_plan_smem(p, B);
     EE_LAUNCH(log, EE_K_GATEUP, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
     // down projection + residual (+ per-layer copy in debug mode)
     p = base;
@@ -484,6 +490,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.x_stride = m.F;
     p.epi = EPI_RESID;
     p.hdbg = c->hdbg + (size_t)j * EE_MAX_BATCH * m.d;
+    linear_plan_smem(p, B);
     EE_LAUNCH(log, EE_K_DOWN, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
 
     const auto ck = std::find(c->ckpts.begin(), c->ckpts.end(), j);
@@ -505,6 +512,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
       p.epi = EPI_X;
       p.xh_out = c->uh;
       p.xo_stride = m.d;
+      linear_plan_smem(p, B);
       EE_LAUNCH(log, EE_K_HEAD_T, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
       // z = u E^T, conf = max softmax, exit if conf > gamma_c, compact the lists
       p = base;
@@ -523,6 +531,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
       p.exit_layer = c->out_dev->exit_layer;
       p.ckpt_index = ci;
       p.ckpt_layer = j;
+      linear_plan_smem(p, B);
       EE_LAUNCH(log, EE_K_HEAD_E, j,
                 launch_linear(p, std::min(linear_grid(p.N, c->num_sms), kHeadGridMax), true, st));
     }
@@ -544,6 +553,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
   p.head_mode = HEAD_FINAL;
   p.head_counter = c->head_cnt;
   p.argmax_out = c->out_dev->next_token;
+  linear_plan_smem(p, B);
   EE_LAUNCH(log, EE_K_FINAL_HEAD, -1,
             launch_linear(p, std::min(linear_grid(p.N, c->num_sms), kHeadGridMax), true, st));
   EE_CUDA(c, cudaMemcpyAsync(c->out_host, c->out_dev, step_d2h_bytes(B), cudaMemcpyDeviceToHost, st));
@@ -730,7 +740,7 @@ ee_status ee_create(const ee_config* cfg, void* dev_arena, size_t arena_bytes, v
   if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->dev) != cudaSuccess)
     return bail(EE_ERR_CUDA);
   if (c->num_sms > kHeadGridMax) c->num_sms = kHeadGridMax;
-  if (linear_prepare() != cudaSuccess) return bail(EE_ERR_CUDA);
+  if (linear_prepare() != cudaSuccess || attention_prepare() != cudaSuccess) return bail(EE_ERR_CUDA);
   if (c->user_stream) {
     c->st = c->user_stream;
   } else {
@@ -1179,6 +1189,7 @@ static ee_status op_linear(int32_t M, int32_t N, int32_t K, const uint16_t* xh, 
   p.out_f32 = y;
   p.out_stride = N;
   p.err = err;
+  linear_plan_smem(p, M);
   return launch_linear(p, linear_grid(N, sms), false, (cudaStream_t)stream) == cudaSuccess ? EE_OK
                                                                                            : EE_ERR_CUDA;
 }
@@ -1196,19 +1207,24 @@ ee_status ee_op_linear_int4(int32_t M, int32_t N, int32_t K, const uint16_t* x_f
   return op_linear(M, N, K, x_f16, nullptr, packed, scales, scale_stride, y, err_flag, stream);
 }
 
-size_t ee_attention_scratch_bytes(int32_t B, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim) {
-  if (B < 1 || B > EE_MAX_BATCH || n_kv_heads < 1 || n_heads % n_kv_heads) return 0;
-  const int nsplit = attention_nsplit(B, n_kv_heads, kHeadGridMax);
+size_t ee_attention_scratch_bytes(int32_t B, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                  int32_t max_ctx) {
+  if (B < 1 || B > EE_MAX_BATCH || n_kv_heads < 1 || n_heads % n_kv_heads || max_ctx < 1 ||
+      (head_dim != 64 && head_dim != 128))
+    return 0;
+  const int nsplit = attention_nsplit(max_ctx, head_dim);
+  if (nsplit > attention_max_split()) return 0;
   return align_up(attention_part_floats(B, n_heads, n_kv_heads, head_dim, nsplit) * 4, kAlign) +
          (size_t)EE_MAX_BATCH * n_kv_heads * 4;
 }
 
-ee_status ee_op_attention(int32_t B, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, const float* q,
-                          const uint16_t* kcache, const uint16_t* vcache, const int32_t* block_table,
-                          int32_t bt_stride, const int32_t* pos, float* o, void* scratch, int32_t* err_flag,
-                          void* stream) {
+ee_status ee_op_attention(int32_t B, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, int32_t max_ctx,
+                          const float* q, const uint16_t* kcache, const uint16_t* vcache,
+                          const int32_t* block_table, int32_t bt_stride, const int32_t* pos, float* o,
+                          void* scratch, int32_t* err_flag, void* stream) {
   if (B < 1 || B > EE_MAX_BATCH || n_kv_heads < 1 || n_heads % n_kv_heads || (head_dim != 64 && head_dim != 128))
     return EE_ERR_INVALID_ARG;
+  if (max_ctx < 1 || attention_nsplit(max_ctx, head_dim) > attention_max_split()) return EE_ERR_INVALID_ARG;
   const int G = n_heads / n_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return EE_ERR_INVALID_ARG;
   if (!q || !kcache || !vcache || !block_table || !pos || !o || !scratch || bt_stride < 1)
@@ -1227,10 +1243,10 @@ ee_status ee_op_attention(int32_t B, int32_t n_heads, int32_t n_kv_heads, int32_
   p.block_table = block_table;
   p.bt_stride = bt_stride;
   p.pos = pos;
-  p.nsplit = attention_nsplit(B, n_kv_heads, sms);
-  const size_t pbytes =
-      align_up(attention_part_floats(B, n_heads, n_kv_heads, head_dim,
-                                     attention_nsplit(B, n_kv_heads, kHeadGridMax)) * 4, kAlign);
+  if (attention_prepare() != cudaSuccess) return EE_ERR_CUDA;
+  p.nsplit = attention_nsplit(max_ctx, head_dim);
+  p.bpc = attention_blocks_per_cta(head_dim);
+  const size_t pbytes = align_up(attention_part_floats(B, n_heads, n_kv_heads, head_dim, p.nsplit) * 4, kAlign);
   p.part = (float*)scratch;
   p.counters = (int32_t*)((uint8_t*)scratch + pbytes);
   p.o_f32 = o;
@@ -1265,6 +1281,7 @@ ee_status ee_op_vocab_head(int32_t M, int32_t V, int32_t d, const uint16_t* u_f1
   p.conf_out = conf;
   p.argmax_out = argmax;
   p.err = err_flag;
+  linear_plan_smem(p, M);
   return launch_linear(p, std::min(linear_grid(V, sms), kHeadGridMax), false, (cudaStream_t)stream) ==
                  cudaSuccess
              ? EE_OK

@@ -1,17 +1,23 @@
 // Split-K GQA decode attention over the paged KV cache.
 //
 // One query position per sequence attends over positions 0..pos (causal).
-// The grid is (split, kv head, sequence slot).  A CTA takes one contiguous
-// slice of the context for one kv head and serves all Hq/Hkv query heads of
-// that group from one read of each K and V row.  Lanes own 8 head dims (one
-// 16-byte load per row), hd/8 lanes form a token group, and each warp works
-// on 32/(hd/8) tokens at a time, four tokens per group in flight.  Scores are
-// reduced across the token group with xor shuffles; the softmax is online
-// (running max m, sum l, weighted values acc).  Token groups, then warps, are
-// merged in registers and shared memory; the CTA writes one partial
-// (m, l, acc) and the last CTA of each (sequence, kv head) -- found with an
-// atomic counter, no waiting -- merges the partials and writes the output:
-// o = sum_i acc_i exp(m_i - M) / sum_i l_i exp(m_i - M).
+// The grid is (split, kv head, sequence slot).  A CTA owns up to BPC whole
+// 16-slot blocks of one sequence's context for one kv head and serves all
+// Hq/Hkv query heads of that group from one read of each K and V row.
+//
+// Data movement: the CTA's K and V tiles ([16][hd] fp16 each, contiguous in
+// the cache) are bulk-copied into shared memory by one thread.  Blocks that
+// hold only earlier positions were written by earlier steps, so their copies
+// are issued before the grid dependency wait and overlap the QKV projection
+// still running; the block holding the current position is copied after it.
+//
+// Compute: lanes own 8 head dims (one 16-byte shared load per row); hd/8
+// lanes form a token group; scores are reduced across the group with xor
+// shuffles and the softmax is online (running max m, sum l, weighted values
+// acc).  Token groups, then warps, are merged; the CTA writes one partial
+// (acc, m, l) per head, and the last CTA of each (sequence, kv head) -- found
+// with an atomic counter, nothing waits -- merges the partials:
+// o = sum_i acc_i exp(m_i - M) / sum_i l_i exp(m_i - M), M = max_i m_i.
 //
 // Cache layout (one layer): [block][kv head][16 slots][head_dim] fp16.
 #include <math.h>
@@ -24,7 +30,9 @@ namespace ee {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kUnroll = 4;
+constexpr int kThreadsA = kWarps * 32;
+constexpr int kKvSmem = 64 * 1024;  // K + V tiles of one CTA
+constexpr int kMaxSplit = 128;
 
 EE_DEV void to_float8(const uint4& v, float* f) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -55,12 +63,22 @@ EE_DEV void merge_state(float& m1, float& l1, float* a1, float m2, float l2, con
   m1 = m;
 }
 
+template <int HD>
+constexpr int blocks_per_cta() {
+  return kKvSmem / (2 * 16 * HD * 2);
+}
+
 template <int HD, int G>
-__global__ void __launch_bounds__(kWarps * 32) k_attention(const AttnParams p) {
+__global__ void __launch_bounds__(kThreadsA) k_attention(const AttnParams p) {
   constexpr int LPT = HD / 8;    // lanes per token
   constexpr int TPW = 32 / LPT;  // tokens per warp step
-  constexpr int PSZ = G * (HD + 2);
-  __shared__ float sm_part[kWarps][PSZ];
+  constexpr int TILE = 16 * HD;  // elements of one (block, kv head) tile
+  constexpr int BPC = blocks_per_cta<HD>();
+  constexpr int PSZ = G * HD + ((2 * G + 3) / 4) * 4;  // partial: acc [G][HD], m [G], l [G] (16-B rows)
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint16_t* Ks = reinterpret_cast<uint16_t*>(smem);
+  uint16_t* Vs = Ks + BPC * TILE;
+  __shared__ __align__(8) uint64_t bar;
   __shared__ int s_last;
 
   const int split = blockIdx.x, g = blockIdx.y, z = blockIdx.z;
@@ -68,15 +86,44 @@ __global__ void __launch_bounds__(kWarps * 32) k_attention(const AttnParams p) {
   const int sub = lane / LPT, dl = lane % LPT;
   const int hkv = p.n_kv_heads;
 
+  // The list, the positions and the block-table entries of earlier blocks
+  // were written at least two launches back: safe before the dependency wait.
+  const int count = p.list ? ld_volatile_i32(p.list) : p.m_direct;
+  const bool active = z < count;
+  int seq = 0, ctx = 0, b0 = 0, b1 = 0, last = -1;
+  if (active) {
+    seq = p.list ? ld_volatile_i32(p.list + 1 + z) : z;
+    ctx = ld_volatile_i32(p.pos + seq) + 1;
+    const int nb = (ctx + 15) >> 4;
+    b0 = split * p.bpc;
+    b1 = min(nb, b0 + p.bpc);
+    last = nb - 1;
+  }
+  const bool have = active && b0 < b1;
+  const int32_t* bt = p.block_table + (size_t)seq * p.bt_stride;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const uint64_t pol = l2_evict_first_policy();
+  if (tid == 0 && have) {
+    mbar_arrive_expect_tx(&bar, (uint32_t)(b1 - b0) * 2 * TILE * 2);
+    for (int b = b0; b < b1; ++b) {
+      if (b == last) continue;
+      const size_t off = ((size_t)ld_volatile_i32(bt + b) * hkv + g) * TILE;
+      bulk_g2s(Ks + (b - b0) * TILE, p.kc + off, TILE * 2, &bar, pol);
+      bulk_g2s(Vs + (b - b0) * TILE, p.vc + off, TILE * 2, &bar, pol);
+    }
+  }
   grid_dep_wait();
   grid_dep_launch();
-  const int count = p.list ? ld_volatile_i32(p.list) : p.m_direct;
-  if (z >= count) return;
-  const int seq = p.list ? p.list[1 + z] : z;
-  const int ctx = p.pos[seq] + 1;
-  const int per = (ctx + p.nsplit - 1) / p.nsplit;
-  const int t0 = split * per;
-  const int t1 = min(ctx, t0 + per);
+  if (tid == 0 && have && last >= b0 && last < b1) {
+    const size_t off = ((size_t)ld_volatile_i32(bt + last) * hkv + g) * TILE;
+    bulk_g2s(Ks + (last - b0) * TILE, p.kc + off, TILE * 2, &bar, pol);
+    bulk_g2s(Vs + (last - b0) * TILE, p.vc + off, TILE * 2, &bar, pol);
+  }
+  if (!active) return;
 
   const float scale = rsqrtf((float)HD);
   float q[G][8];
@@ -103,30 +150,18 @@ __global__ void __launch_bounds__(kWarps * 32) k_attention(const AttnParams p) {
     for (int i = 0; i < 8; ++i) acc[h][i] = 0.0f;
   }
 
-  const int32_t* bt = p.block_table + (size_t)seq * p.bt_stride;
-  constexpr int kStep = kWarps * TPW;  // tokens per CTA step
-  for (int base = t0 + warp * TPW; base < t1; base += kStep * kUnroll) {
-    uint4 kr[kUnroll], vr[kUnroll];
-    bool valid[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int t = base + u * kStep + sub;
-      valid[u] = t < t1;
-      if (valid[u]) {
-        const int block = bt[t >> 4];
-        const size_t off = ((((size_t)block * hkv + g) * 16) + (t & 15)) * HD + dl * 8;
-        kr[u] = ldg_nc_v4(p.kc + off);
-        vr[u] = ldg_nc_v4(p.vc + off);
-      } else {
-        kr[u] = make_uint4(0, 0, 0, 0);
-        vr[u] = kr[u];
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+  bool ok = true;
+  if (have) ok = mbar_wait_bounded(&bar, 0, p.err, DERR_FULL_WAIT);
+  if (have && !ok) mbar_wait_bounded(&bar, 0, p.err, DERR_DRAIN_WAIT);  // copies land before reuse
+  if (have && ok) {
+    const int t0 = b0 * 16, t1 = min(ctx, b1 * 16);
+    for (int base = t0 + warp * TPW; base < t1; base += kWarps * TPW) {
+      const int t = base + sub;
+      const bool valid = t < t1;
+      const int row = valid ? t - t0 : 0;
       float kf[8], vf[8];
-      to_float8(kr[u], kf);
-      to_float8(vr[u], vf);
+      to_float8(*reinterpret_cast<const uint4*>(Ks + row * HD + dl * 8), kf);
+      to_float8(*reinterpret_cast<const uint4*>(Vs + row * HD + dl * 8), vf);
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         float s = 0.0f;
@@ -134,7 +169,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_attention(const AttnParams p) {
         for (int i = 0; i < 8; ++i) s = fmaf(q[h][i], kf[i], s);
 #pragma unroll
         for (int o = LPT / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (valid[u]) {
+        if (valid) {
           const float mn = fmaxf(mrun[h], s);
           const float c = expf(mrun[h] - mn);
           const float e = expf(s - mn);
@@ -160,34 +195,37 @@ __global__ void __launch_bounds__(kWarps * 32) k_attention(const AttnParams p) {
       merge_state<8>(mrun[h], lrun[h], acc[h], m2, l2, a2);
     }
   }
+  __syncthreads();  // the K/V tiles are no longer read: reuse the space
+  float* wpart = reinterpret_cast<float*>(smem);  // [warp][PSZ]
   if (sub == 0) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      float* dst = sm_part[warp] + h * (HD + 2);
+      float* dst = wpart + warp * PSZ;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) dst[dl * 8 + i] = acc[h][i];
+      for (int i = 0; i < 8; ++i) dst[h * HD + dl * 8 + i] = acc[h][i];
       if (dl == 0) {
-        dst[HD] = mrun[h];
-        dst[HD + 1] = lrun[h];
+        dst[G * HD + h] = mrun[h];
+        dst[G * HD + G + h] = lrun[h];
       }
     }
   }
   __syncthreads();
 
-  // CTA partial: merge the warps (thread i handles head i / HD, dim i % HD)
+  // CTA partial: merge the warps
   float* part = p.part + (((size_t)z * hkv + g) * p.nsplit + split) * PSZ;
-  for (int idx = tid; idx < G * HD; idx += kWarps * 32) {
-    const int h = idx / HD, dd = idx % HD;
+  for (int idx = tid; idx < G * HD; idx += kThreadsA) {
+    const int h = idx / HD;
     float m = -INFINITY, l = 0.0f, a = 0.0f;
+#pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      const float* src = sm_part[w] + h * (HD + 2);
-      float a2 = src[dd];
-      merge_state<1>(m, l, &a, src[HD], src[HD + 1], &a2);
+      const float* src = wpart + w * PSZ;
+      float a2 = src[idx];
+      merge_state<1>(m, l, &a, src[G * HD + h], src[G * HD + G + h], &a2);
     }
-    part[h * (HD + 2) + dd] = a;
-    if (dd == 0) {
-      part[h * (HD + 2) + HD] = m;
-      part[h * (HD + 2) + HD + 1] = l;
+    part[idx] = a;
+    if (idx % HD == 0) {
+      part[G * HD + h] = m;
+      part[G * HD + G + h] = l;
     }
   }
   __syncthreads();
@@ -200,30 +238,80 @@ __global__ void __launch_bounds__(kWarps * 32) k_attention(const AttnParams p) {
   if (!s_last) return;
   __threadfence();
 
-  // last CTA of this (sequence, kv head): merge all splits
-  const float* parts = p.part + (((size_t)z * hkv + g) * p.nsplit) * PSZ;
-  for (int idx = tid; idx < G * HD; idx += kWarps * 32) {
-    const int h = idx / HD, dd = idx % HD;
-    float m = -INFINITY, l = 0.0f, a = 0.0f;
-    for (int s = 0; s < p.nsplit; ++s) {
-      const float* src = parts + (size_t)s * PSZ + h * (HD + 2);
-      float a2 = __ldcg(src + dd);
-      merge_state<1>(m, l, &a, __ldcg(src + HD), __ldcg(src + HD + 1), &a2);
+  // last CTA of this (sequence, kv head): merge the splits.  Warp w takes
+  // heads w, w+4, ...: M = max m, weights exp(m - M), L = sum weight * l.
+  const float* parts = p.part + ((size_t)z * hkv + g) * p.nsplit * PSZ;
+  float* wts = reinterpret_cast<float*>(smem);  // [split][G]
+  float* inv_l = wts + kMaxSplit * G;           // [G]
+  for (int h = warp; h < G; h += kWarps) {
+    float mloc = -INFINITY;
+    for (int s = lane; s < p.nsplit; s += 32) {
+      const float l = __ldcg(parts + (size_t)s * PSZ + G * HD + G + h);
+      if (l > 0.0f) mloc = fmaxf(mloc, __ldcg(parts + (size_t)s * PSZ + G * HD + h));
     }
-    const float o = a / l;
-    const int col = (g * G + h) * HD + dd;
-    if (p.o_f32) p.o_f32[(size_t)seq * p.o_stride + col] = o;
-    if (p.oh) p.oh[(size_t)seq * p.o_stride + xh_slot(col)] = float_to_half_bits(o);
+    const float M = warp_max(mloc);
+    float lsum = 0.0f;
+    for (int s = lane; s < p.nsplit; s += 32) {
+      const float l = __ldcg(parts + (size_t)s * PSZ + G * HD + G + h);
+      const float w = l > 0.0f ? expf(__ldcg(parts + (size_t)s * PSZ + G * HD + h) - M) : 0.0f;
+      wts[s * G + h] = w;
+      lsum += w * l;
+    }
+    lsum = warp_sum(lsum);
+    if (lane == 0) inv_l[h] = 1.0f / lsum;
+  }
+  __syncthreads();
+  for (int i4 = tid; i4 < G * HD / 4; i4 += kThreadsA) {
+    const int h = (i4 * 4) / HD;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    int s = 0;
+    for (; s + 8 <= p.nsplit; s += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldcg(reinterpret_cast<const float4*>(parts + (size_t)(s + u) * PSZ) + i4);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float w = wts[(s + u) * G + h];
+        o.x = fmaf(w, v[u].x, o.x);
+        o.y = fmaf(w, v[u].y, o.y);
+        o.z = fmaf(w, v[u].z, o.z);
+        o.w = fmaf(w, v[u].w, o.w);
+      }
+    }
+    for (; s < p.nsplit; ++s) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(parts + (size_t)s * PSZ) + i4);
+      const float w = wts[s * G + h];
+      o.x = fmaf(w, v.x, o.x);
+      o.y = fmaf(w, v.y, o.y);
+      o.z = fmaf(w, v.z, o.z);
+      o.w = fmaf(w, v.w, o.w);
+    }
+    const float il = inv_l[h];
+    const float ov[4] = {o.x * il, o.y * il, o.z * il, o.w * il};
+    const int col0 = g * G * HD + i4 * 4;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (p.o_f32) p.o_f32[(size_t)seq * p.o_stride + col0 + u] = ov[u];
+      if (p.oh) p.oh[(size_t)seq * p.o_stride + xh_slot(col0 + u)] = float_to_half_bits(ov[u]);
+    }
   }
   if (tid == 0) p.counters[(size_t)z * hkv + g] = 0;
 }
 
 template <int HD, int G>
+cudaError_t set_attr_t() {
+  static_assert(kMaxSplit * G * 4 + G * 4 <= kKvSmem, "merge scratch");
+  static_assert(kWarps * (G * HD + 8 * G) * 4 <= kKvSmem, "warp partials");
+  return cudaFuncSetAttribute(k_attention<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvSmem);
+}
+
+template <int HD, int G>
 cudaError_t launch_t(const AttnParams& p, int batch_slots, bool pdl, cudaStream_t st) {
+  constexpr size_t smem = kKvSmem;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.nsplit, p.n_kv_heads, batch_slots);
-  cfg.blockDim = dim3(kWarps * 32);
-  cfg.dynamicSmemBytes = 0;
+  cfg.blockDim = dim3(kThreadsA);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -235,20 +323,41 @@ cudaError_t launch_t(const AttnParams& p, int batch_slots, bool pdl, cudaStream_
 
 }  // namespace
 
+int attention_blocks_per_cta(int head_dim) { return head_dim == 64 ? blocks_per_cta<64>() : blocks_per_cta<128>(); }
+
 size_t attention_part_floats(int batch_slots, int n_heads, int n_kv_heads, int head_dim, int nsplit) {
   const int G = n_heads / n_kv_heads;
-  return (size_t)batch_slots * n_kv_heads * nsplit * G * (head_dim + 2);
+  return (size_t)batch_slots * n_kv_heads * nsplit * (G * head_dim + ((2 * G + 3) / 4) * 4);
 }
 
-int attention_nsplit(int batch, int n_kv_heads, int num_sms) {
-  int s = (4 * num_sms + n_kv_heads * batch - 1) / (n_kv_heads * batch);
-  if (s < 1) s = 1;
-  if (s > 128) s = 128;
-  return s;
+int attention_max_split() { return kMaxSplit; }
+
+cudaError_t attention_prepare() {
+  cudaError_t e;
+#define EE_ATT_ATTR(HD_, G_) \
+  if ((e = set_attr_t<HD_, G_>()) != cudaSuccess) return e;
+  EE_ATT_ATTR(64, 1)
+  EE_ATT_ATTR(64, 2)
+  EE_ATT_ATTR(64, 4)
+  EE_ATT_ATTR(64, 8)
+  EE_ATT_ATTR(128, 1)
+  EE_ATT_ATTR(128, 2)
+  EE_ATT_ATTR(128, 4)
+  EE_ATT_ATTR(128, 8)
+#undef EE_ATT_ATTR
+  return cudaSuccess;
+}
+
+int attention_nsplit(int max_ctx, int head_dim) {
+  const int nb = (max_ctx + 15) / 16;
+  const int bpc = attention_blocks_per_cta(head_dim);
+  return (nb + bpc - 1) / bpc;
 }
 
 cudaError_t launch_attention(const AttnParams& p, int batch_slots, bool pdl, cudaStream_t st) {
   const int G = p.n_heads / p.n_kv_heads;
+  if (p.nsplit < 1 || p.nsplit > kMaxSplit || p.bpc != attention_blocks_per_cta(p.head_dim))
+    return cudaErrorInvalidValue;
 #define EE_ATT_CASE(HD_, G_) \
   if (p.head_dim == HD_ && G == G_) return launch_t<HD_, G_>(p, batch_slots, pdl, st);
   EE_ATT_CASE(64, 1)

@@ -39,16 +39,19 @@ constexpr int kTileRows = 2 * kConsumerWarps;
 constexpr int kChunkBytes = 1024;
 constexpr int kScaleBytes = 32;
 constexpr int kStageBytes = kTileRows * (kChunkBytes + kScaleBytes);
-constexpr int kStages = 6;
+constexpr int kMaxStages = 6;
 constexpr int kMM = 8;  // sequences per pass over the weights
 constexpr int kBfChunk = kChunkBytes / 2;  // bf16 columns per stage row
 constexpr int kQChunk = kChunkBytes * 2;   // int4 columns per stage row
 
-constexpr size_t kRingBytes = size_t(kStages) * kStageBytes;
-constexpr size_t kBarBytes = 2 * kStages * sizeof(uint64_t);
-constexpr size_t kListBytes = 2 * kListLen * sizeof(int32_t);
-constexpr size_t kStatBytes = kConsumerWarps * kMM * 3 * sizeof(float);
-constexpr size_t kSmemBytes = kRingBytes + kBarBytes + kListBytes + kStatBytes;
+// Shared memory: a small header (barriers, lists, head statistics), then the
+// activations of the step's rows when they are staged (XS mode), then the ring.
+constexpr size_t kHeaderBytes = 1536;
+constexpr size_t kXsMaxBytes = 48 * 1024;
+constexpr size_t kSmemTarget = 112 * 1024;  // two CTAs per SM: the next kernel's CTA can prefetch
+constexpr size_t kSmemMax = kHeaderBytes + kXsMaxBytes + size_t(kMaxStages) * kStageBytes;
+static_assert((2 * kMaxStages + 1) * 8 + 2 * kListLen * 4 + kConsumerWarps * kMM * 3 * 4 <= kHeaderBytes,
+              "header overflow");
 
 EE_DEV __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
@@ -165,23 +168,68 @@ EE_DEV Stat stat_merge(Stat a, Stat b) {
 
 EE_DEV void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory"); }
 
-template <int EPI>
+// Iteration order shared by the producer and the consumers: phase (0 bf16
+// rows, 1 int4 rows), pass over at most kMM sequences, 16-row tile of the
+// CTA's rows, K chunk.  Each iteration fills one ring stage.
+struct Plan {
+  int r0, r1, ntiles, nc[2], passes[2];
+  EE_DEV int rows(int t) const { return min(kTileRows, r1 - (r0 + t * kTileRows)); }
+  EE_DEV uint32_t total() const {
+    return (uint32_t)(passes[0] * ntiles * nc[0] + passes[1] * ntiles * nc[1]);
+  }
+};
+
+// Issues the bulk copies of one ring stage (weights and, for int4, scales).
+EE_DEV void issue_stage(const LinearParams& p, const Plan& pl, int phase, int t, int c, uint8_t* sbase,
+                        uint64_t* bar, uint64_t pol) {
+  const int tr0 = pl.r0 + t * kTileRows;
+  const int rows = pl.rows(t);
+  if (phase == 0) {
+    const int ce = min(kBfChunk, p.K - c * kBfChunk);
+    const uint32_t cb = ce * 2;
+    mbar_arrive_expect_tx(bar, rows * cb);
+    for (int r = 0; r < rows; ++r)
+      bulk_g2s(sbase + r * kChunkBytes, p.w + (size_t)(tr0 + r) * p.K + c * kBfChunk, cb, bar, pol);
+  } else {
+    const int ce = min(kQChunk, p.K - c * kQChunk);
+    const uint32_t cb = ce / 2;
+    const int ng = (ce + EE_QUANT_GROUP - 1) / EE_QUANT_GROUP;
+    const uint32_t sb = ((ng * 2 + 15) / 16) * 16;
+    mbar_arrive_expect_tx(bar, rows * (cb + sb));
+    for (int r = 0; r < rows; ++r) {
+      bulk_g2s(sbase + r * kChunkBytes, p.wq + (size_t)(tr0 + r) * (p.K / 2) + (size_t)c * (kQChunk / 2),
+               cb, bar, pol);
+      bulk_g2s(sbase + kTileRows * kChunkBytes + r * kScaleBytes,
+               p.ws + (size_t)(tr0 + r) * p.sstride + c * (kQChunk / EE_QUANT_GROUP), sb, bar, pol);
+    }
+  }
+}
+
+// XS = true: the activations of all the step's rows (at most p.xs_rows
+// sequences) are bulk-copied into shared memory once, after the dependency
+// wait, while the weight stream already runs; XS = false: activations are
+// read from global memory (L1/L2) at every stage.
+template <int EPI, bool XS>
 __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRingBytes);
-  uint64_t* empty = full + kStages;
-  int32_t* lf = reinterpret_cast<int32_t*>(empty + kStages);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* xbar = empty + kMaxStages;
+  int32_t* lf = reinterpret_cast<int32_t*>(smem + 128);
   int32_t* le = lf + kListLen;
-  float* hst = reinterpret_cast<float*>(le + kListLen);
+  float* hst = reinterpret_cast<float*>(smem + 128 + 2 * kListLen * 4 + 8);
+  uint8_t* xs = smem + kHeaderBytes;
+  uint8_t* ring = xs + (XS ? (size_t)p.xs_rows * p.K * 2 : 0);
+  const int nst = p.nstages;
   __shared__ int s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < nst; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
+    mbar_init(xbar, 1);
     fence_mbar_init();
   }
   // Lists were written at least two launches back (see grid_dep_wait), so
@@ -194,95 +242,98 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
 
   const int nf = p.w ? min(lf[0], EE_MAX_BATCH) : 0;
   const int ne = p.wq ? min(le[0], EE_MAX_BATCH) : 0;
-  const int npairs = p.N >> 1;
-  const int r0 = 2 * (int)(((long long)blockIdx.x * npairs) / gridDim.x);
-  const int r1 = 2 * (int)(((long long)(blockIdx.x + 1) * npairs) / gridDim.x);
-  const int ntiles = (r1 - r0 + kTileRows - 1) / kTileRows;
-  const int nc_b = (p.K + kBfChunk - 1) / kBfChunk;
-  const int nc_q = (p.K + kQChunk - 1) / kQChunk;
-  const int passes_b = (nf + kMM - 1) / kMM;
-  const int passes_q = (ne + kMM - 1) / kMM;
+  const int nx = nf + ne;  // XS mode: rows staged (full rows first, then exit rows)
+  Plan pl;
+  {
+    const int npairs = p.N >> 1;
+    pl.r0 = 2 * (int)(((long long)blockIdx.x * npairs) / gridDim.x);
+    pl.r1 = 2 * (int)(((long long)(blockIdx.x + 1) * npairs) / gridDim.x);
+    pl.ntiles = (pl.r1 - pl.r0 + kTileRows - 1) / kTileRows;
+    pl.nc[0] = (p.K + kBfChunk - 1) / kBfChunk;
+    pl.nc[1] = (p.K + kQChunk - 1) / kQChunk;
+    pl.passes[0] = (nf + kMM - 1) / kMM;
+    pl.passes[1] = (ne + kMM - 1) / kMM;
+  }
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
+      const uint32_t total = pl.total();
+      const uint32_t prefill = total < (uint32_t)nst ? total : (uint32_t)nst;
+      bool xdone = !XS;
+      auto stage_x = [&]() {
+        // activations are written by the previous kernel: copy them after the wait
+        grid_dep_wait();
+        if (nx > 0) {
+          const uint32_t rb = (uint32_t)p.K * 2;
+          mbar_arrive_expect_tx(xbar, nx * rb);
+          for (int m = 0; m < nx; ++m) {
+            const int seq = m < nf ? lf[1 + m] : le[1 + m - nf];
+            bulk_g2s(xs + (size_t)m * rb, p.xh + (size_t)seq * p.x_stride, rb, xbar, pol);
+          }
+        }
+        xdone = true;
+      };
       uint32_t it = 0;
       bool ok = true;
       for (int phase = 0; phase < 2 && ok; ++phase) {
-        const int passes = phase == 0 ? passes_b : passes_q;
-        const int nc = phase == 0 ? nc_b : nc_q;
-        for (int pass = 0; pass < passes && ok; ++pass) {
-          for (int t = 0; t < ntiles && ok; ++t) {
-            const int tr0 = r0 + t * kTileRows;
-            const int rows = min(kTileRows, r1 - tr0);
-            for (int c = 0; c < nc; ++c, ++it) {
-              const int st = it % kStages;
-              const uint32_t n = it / kStages;
+        for (int pass = 0; pass < pl.passes[phase] && ok; ++pass) {
+          for (int t = 0; t < pl.ntiles && ok; ++t) {
+            for (int c = 0; c < pl.nc[phase]; ++c, ++it) {
+              if (!xdone && it == prefill) stage_x();
+              const int st = it % nst;
+              const uint32_t n = it / nst;
               if (n > 0 && !mbar_wait_bounded(&empty[st], (n - 1) & 1, p.err, DERR_EMPTY_WAIT)) {
                 ok = false;
                 break;
               }
-              uint8_t* sbase = ring + (size_t)st * kStageBytes;
-              if (phase == 0) {
-                const int ce = min(kBfChunk, p.K - c * kBfChunk);
-                const uint32_t cb = ce * 2;
-                mbar_arrive_expect_tx(&full[st], rows * cb);
-                for (int r = 0; r < rows; ++r)
-                  bulk_g2s(sbase + r * kChunkBytes, p.w + (size_t)(tr0 + r) * p.K + c * kBfChunk, cb,
-                           &full[st], pol);
-              } else {
-                const int ce = min(kQChunk, p.K - c * kQChunk);
-                const uint32_t cb = ce / 2;
-                const int ng = (ce + EE_QUANT_GROUP - 1) / EE_QUANT_GROUP;
-                const uint32_t sb = ((ng * 2 + 15) / 16) * 16;
-                mbar_arrive_expect_tx(&full[st], rows * (cb + sb));
-                for (int r = 0; r < rows; ++r) {
-                  bulk_g2s(sbase + r * kChunkBytes,
-                           p.wq + (size_t)(tr0 + r) * (p.K / 2) + (size_t)c * (kQChunk / 2), cb,
-                           &full[st], pol);
-                  bulk_g2s(sbase + kTileRows * kChunkBytes + r * kScaleBytes,
-                           p.ws + (size_t)(tr0 + r) * p.sstride + c * (kQChunk / EE_QUANT_GROUP), sb,
-                           &full[st], pol);
-                }
-              }
+              issue_stage(p, pl, phase, t, c, ring + (size_t)st * kStageBytes, &full[st], pol);
             }
           }
         }
       }
+      if (!xdone) stage_x();
       // every copy this thread issued lands before the CTA may exit
-      const uint32_t j0 = it > (uint32_t)kStages ? it - kStages : 0;
+      const uint32_t j0 = it > (uint32_t)nst ? it - nst : 0;
       for (uint32_t j = j0; j < it; ++j)
-        mbar_wait_bounded(&full[j % kStages], (j / kStages) & 1, p.err, DERR_DRAIN_WAIT);
+        mbar_wait_bounded(&full[j % nst], (j / nst) & 1, p.err, DERR_DRAIN_WAIT);
+      if (XS && nx > 0) mbar_wait_bounded(xbar, 0, p.err, DERR_DRAIN_WAIT);
     }
   } else {
     // ------------------------------------------------------------ consumers
     grid_dep_wait();
     grid_dep_launch();
-    uint32_t it = 0;
     bool ok = true;
+    if (XS && nx > 0) ok = mbar_wait_bounded(xbar, 0, p.err, DERR_FULL_WAIT);
+    uint32_t it = 0;
     for (int phase = 0; phase < 2; ++phase) {
-      const int passes = phase == 0 ? passes_b : passes_q;
       const int nlist = phase == 0 ? nf : ne;
       const int32_t* lst = phase == 0 ? lf : le;
-      const int nc = phase == 0 ? nc_b : nc_q;
-      for (int pass = 0; pass < passes; ++pass) {
+      const int nc = pl.nc[phase];
+      const int xbase = phase == 0 ? 0 : nf;  // XS row of the phase's first sequence
+      for (int pass = 0; pass < pl.passes[phase]; ++pass) {
         const int m0 = pass * kMM;
         const int mc = min(kMM, nlist - m0);
         int seqs[kMM];
+        const uint16_t* xrow[kMM];
 #pragma unroll
-        for (int m = 0; m < kMM; ++m) seqs[m] = lst[1 + m0 + min(m, mc - 1)];
+        for (int m = 0; m < kMM; ++m) {
+          const int mm = min(m, mc - 1);
+          seqs[m] = lst[1 + m0 + mm];
+          xrow[m] = XS ? reinterpret_cast<const uint16_t*>(xs) + (size_t)(xbase + m0 + mm) * p.K
+                       : p.xh + (size_t)seqs[m] * p.x_stride;
+        }
         Stat stat = {-INFINITY, 0.0f, 0x7fffffff};
-        for (int t = 0; t < ntiles; ++t) {
-          const int tr0 = r0 + t * kTileRows;
-          const int rows = min(kTileRows, r1 - tr0);
-          const bool have = 2 * warp < rows;
+        for (int t = 0; t < pl.ntiles; ++t) {
+          const int tr0 = pl.r0 + t * kTileRows;
+          const bool have = 2 * warp < pl.rows(t);
           float acc0[kMM], acc1[kMM];
 #pragma unroll
           for (int m = 0; m < kMM; ++m) acc0[m] = acc1[m] = 0.0f;
           for (int c = 0; c < nc; ++c, ++it) {
-            const int st = it % kStages;
-            if (ok) ok = mbar_wait_bounded(&full[st], (it / kStages) & 1, p.err, DERR_FULL_WAIT);
+            const int st = it % nst;
+            if (ok) ok = mbar_wait_bounded(&full[st], (it / nst) & 1, p.err, DERR_FULL_WAIT);
             if (ok && have) {
               const uint8_t* sa = ring + (size_t)st * kStageBytes + (2 * warp) * kChunkBytes;
               const uint8_t* sb = sa + kChunkBytes;
@@ -295,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
 #pragma unroll
                   for (int m = 0; m < kMM; ++m) {
                     if (m < mc) {
-                      const uint4 xv = ldg_nc_v4(p.xh + (size_t)seqs[m] * p.x_stride + k0);
+                      const uint4 xv = XS ? *reinterpret_cast<const uint4*>(xrow[m] + k0)
+                                          : ldg_nc_v4(xrow[m] + k0);
                       acc0[m] = dot8_bf16(wa, xv, acc0[m]);
                       acc1[m] = dot8_bf16(wb, xv, acc1[m]);
                     }
@@ -315,9 +367,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
 #pragma unroll
                   for (int m = 0; m < kMM; ++m) {
                     if (m < mc) {
-                      const uint16_t* xp = p.xh + (size_t)seqs[m] * p.x_stride + k0;
-                      const uint4 x0 = ldg_nc_v4(xp), x1 = ldg_nc_v4(xp + 8);
-                      const uint4 x2 = ldg_nc_v4(xp + 16), x3 = ldg_nc_v4(xp + 24);
+                      const uint16_t* xp = xrow[m] + k0;
+                      uint4 x0, x1, x2, x3;
+                      if (XS) {
+                        x0 = *reinterpret_cast<const uint4*>(xp);
+                        x1 = *reinterpret_cast<const uint4*>(xp + 8);
+                        x2 = *reinterpret_cast<const uint4*>(xp + 16);
+                        x3 = *reinterpret_cast<const uint4*>(xp + 24);
+                      } else {
+                        x0 = ldg_nc_v4(xp);
+                        x1 = ldg_nc_v4(xp + 8);
+                        x2 = ldg_nc_v4(xp + 16);
+                        x3 = ldg_nc_v4(xp + 24);
+                      }
                       __half2 ha = __float2half2_rn(0.0f), hb = ha;
                       ha = dot8_int4(qa.x, x0, ha);
                       hb = dot8_int4(qb.x, x0, hb);
@@ -458,7 +520,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
 
 template <int EPI>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(k_linear<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(k_linear<EPI, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSmemMax);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_linear<EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax);
 }
 
 template <int EPI>
@@ -466,19 +531,36 @@ cudaError_t launch_one(const LinearParams& p, int grid, bool pdl, cudaStream_t s
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = kHeaderBytes + (p.xs_rows > 0 ? (size_t)p.xs_rows * p.K * 2 : 0) +
+                         (size_t)p.nstages * kStageBytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_linear<EPI>, p);
+  if (p.xs_rows > 0) return cudaLaunchKernelEx(&cfg, k_linear<EPI, true>, p);
+  return cudaLaunchKernelEx(&cfg, k_linear<EPI, false>, p);
 }
 
 }  // namespace
 
-size_t linear_smem_bytes() { return kSmemBytes; }
+size_t linear_smem_bytes() { return kSmemMax; }
+
+void linear_plan_smem(LinearParams& p, int max_rows) {
+  const size_t xb = (size_t)max_rows * p.K * 2;
+  int nst = kMaxStages;
+  bool xs = max_rows <= kMM && xb <= kXsMaxBytes;
+  if (xs) {
+    const size_t room = kSmemTarget - kHeaderBytes - xb;
+    nst = (int)(room / kStageBytes);
+    if (nst > kMaxStages) nst = kMaxStages;
+    if (nst < 4) xs = false;
+  }
+  if (!xs) nst = kMaxStages;
+  p.xs_rows = xs ? max_rows : 0;
+  p.nstages = nst;
+}
 
 cudaError_t linear_prepare() {
   cudaError_t e;

@@ -70,7 +70,8 @@ typedef enum {
 
 /* Model shape and runtime limits.
  * Requirements: d_model, n_heads*head_dim and ffn_dim multiples of 32;
- * head_dim even and <= 256; n_heads a multiple of n_kv_heads;
+ * head_dim 64 or 128; n_heads / n_kv_heads in {1, 2, 4, 8}; vocab even;
+ * max_seq_len <= 16384;
  * quant_group == 128; kv_block == 16; 1 <= max_batch <= EE_MAX_BATCH;
  * checkpoint_layers strictly ascending, each in [0, n_layers-2]. */
 typedef struct {
@@ -278,19 +279,20 @@ ee_status ee_op_linear_int4(int32_t M, int32_t N, int32_t K, const uint16_t *x_f
                             float *y, int32_t *err_flag, void *stream);
 
 /* Paged GQA decode attention (one query position per sequence, causal over
- * positions 0..pos[s]):  o[s, h*hd + i] = sum_t softmax_t(q_h . k_t / sqrt(hd)) v_t[i]
+ * positions 0..pos[s], pos[s] + 1 <= max_ctx <= 16384):  o[s, h*hd + i] = sum_t softmax_t(q_h . k_t / sqrt(hd)) v_t[i]
  * with kv head g = floor(h * Hkv / Hq).
  *   q [B, Hq*hd] fp32; kcache/vcache [n_blocks, Hkv, 16, hd] fp16 (one
  *   layer, the layout of the context's shared cache); block_table [B, bt_stride] int32; pos [B] int32 (the query's
  *   position, so ctx = pos + 1); o [B, Hq*hd] fp32.
- * scratch: device buffer of ee_attention_scratch_bytes(B, Hq, Hkv, hd) bytes;
+ * scratch: device buffer of ee_attention_scratch_bytes(B, Hq, Hkv, hd, max_ctx) bytes;
  * its counters must be zero on the first call (ee_create does this for the
  * context's own scratch; for this entry point, zero it once with cudaMemset)
  * and are left at zero by every call. */
 size_t ee_attention_scratch_bytes(int32_t B, int32_t n_heads, int32_t n_kv_heads,
-                                  int32_t head_dim);
+                                  int32_t head_dim, int32_t max_ctx);
 ee_status ee_op_attention(int32_t B, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
-                          const float *q, const uint16_t *kcache, const uint16_t *vcache,
+                          int32_t max_ctx, const float *q, const uint16_t *kcache,
+                          const uint16_t *vcache,
                           const int32_t *block_table, int32_t bt_stride, const int32_t *pos,
                           float *o, void *scratch, int32_t *err_flag, void *stream);
 

@@ -69,8 +69,10 @@ def test_op_argument_validation(lib):
     assert lib.ee_op_linear_bf16(1, 7, 64, 16, 16, 16, None, None) == 1
     assert lib.ee_op_linear_bf16(1, 8, 40, 16, 16, 16, None, None) == 1
     assert lib.ee_op_linear_int4(1, 8, 256, 16, 16, 16, 1, 16, None, None) == 1
-    assert lib.ee_op_attention(1, 4, 3, 64, 16, 16, 16, 16, 1, 16, 16, 16, None, None) == 1
+    assert lib.ee_op_attention(1, 4, 3, 64, 100, 16, 16, 16, 16, 1, 16, 16, 16, None, None) == 1
+    assert lib.ee_op_attention(1, 4, 2, 64, 1 << 20, 16, 16, 16, 16, 1, 16, 16, 16, None, None) == 1
     assert lib.ee_op_vocab_head(1, 7, 64, 16, 16, 16, 16, 16, None, None) == 1
     assert lib.ee_op_quantize_int4(16, 4, 40, 16, 16, 2, None) == 1
-    assert lib.ee_attention_scratch_bytes(0, 4, 2, 64) == 0
+    assert lib.ee_attention_scratch_bytes(0, 4, 2, 64, 100) == 0
+    assert lib.ee_attention_scratch_bytes(1, 4, 2, 64, 100) > 0
     assert lib.ee_head_scratch_bytes(1) > 0

@@ -129,7 +129,7 @@ def paged(rng, B, ctxs, hkv, hd, nblocks_extra=5):
 @pytest.mark.parametrize("B,hq,hkv,hd,ctxs", [
     (1, 4, 2, 64, [1]), (1, 4, 2, 64, [15]), (1, 4, 2, 64, [16]), (1, 4, 2, 64, [17]),
     (3, 32, 8, 64, [300, 1, 47]), (1, 32, 8, 128, [2304]), (2, 64, 8, 128, [4100, 33]),
-    (4, 8, 8, 128, [5, 64, 129, 1000]),
+    (4, 8, 8, 128, [5, 64, 129, 1000]), (2, 16, 16, 64, [700, 16]), (1, 64, 8, 128, [1]),
 ])
 def test_attention(B, hq, hkv, hd, ctxs):
     rng = np.random.default_rng(B * 7 + hq + hd + sum(ctxs))
@@ -137,10 +137,11 @@ def test_attention(B, hq, hkv, hd, ctxs):
     q = rng.standard_normal((B, hq * hd)).astype(np.float32)
     pos = np.array(ctxs, dtype=np.int32) - 1
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    scratch = torch.zeros(ee.attention_scratch_bytes(B, hq, hkv, hd), dtype=torch.uint8, device="cuda")
+    max_ctx = max(ctxs) + 37
+    scratch = torch.zeros(ee.attention_scratch_bytes(B, hq, hkv, hd, max_ctx), dtype=torch.uint8, device="cuda")
     for rep in range(2):  # the second call checks that the counters were left at zero
         o = ee.attention(dev(q), dev(kc.view(np.int16)), dev(vc.view(np.int16)), dev(bt), dev(pos),
-                         hq, hkv, hd, scratch=scratch, err=err).cpu().numpy()
+                         hq, hkv, hd, max_ctx, scratch=scratch, err=err).cpu().numpy()
         for b in range(B):
             ref = oracle.attention_decode(q[b].astype(np.float64).reshape(hq, hd),
                                           K[b].view(np.float16).astype(np.float64),
