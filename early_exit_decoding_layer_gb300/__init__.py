@@ -374,7 +374,7 @@ def quantize_int4(w, stream=None):
     """w: bf16 bits [rows, cols] (torch.int16/uint16 CUDA tensor) -> (packed uint8, scales int16)."""
     import torch
     rows, cols = w.shape
-    sstride = ((cols + 127) // 128 + 7) // 8 * 8
+    sstride = (cols + 127) // 128
     packed = torch.empty((rows, cols // 2), dtype=torch.uint8, device=w.device)
     scales = torch.zeros((rows, sstride), dtype=torch.int16, device=w.device)
     _raise(load_library().ee_op_quantize_int4(_ptr(w), rows, cols, _ptr(packed), _ptr(scales), sstride,

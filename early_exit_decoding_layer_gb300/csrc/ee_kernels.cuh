@@ -56,13 +56,15 @@ enum HeadMode : int32_t { HEAD_CONF_ARGMAX = 0, HEAD_CHECKPOINT = 1, HEAD_FINAL 
 
 struct LinearParams {
   int32_t N, K;
-  int32_t nstages;           // ring stages (linear_plan_smem)
-  int32_t xs_rows;           // > 0: activations of up to xs_rows sequences staged in smem
+  int32_t max_rows;          // upper bound of the list counts (sequences of the step)
+  // filled by launch_linear: ring stages, staged activation rows (0: read from
+  // global), sequences per pass, per-row sum capacity
+  int32_t nstages, xs_rows, mcap, rows_cap;
   // weights: bf16 [N, K]; int4 packed [N, K/2] with bf16 scales [N, sstride]
   const uint16_t* w;
   const uint8_t* wq;
   const uint16_t* ws;
-  int32_t sstride;
+  int32_t sstride;           // scale row stride (elements); ceil(K/128) keeps rows unpadded
   // rows: either lists (count + ids) or a direct count with ids 0..m_direct-1
   const int32_t* list_full;  // rows on the bf16 weights (may be null)
   const int32_t* list_exit;  // rows on the int4 weights (may be null)
@@ -110,9 +112,6 @@ size_t linear_smem_bytes();
 // Sets the kernels' shared-memory attributes on the current device (call once
 // per device before the first launch, outside stream capture).
 cudaError_t linear_prepare();
-// Chooses the ring depth and whether the activations of the step's rows (at
-// most max_rows sequences) are staged in shared memory.
-void linear_plan_smem(LinearParams& p, int max_rows);
 // Launches the GEMV on `grid` CTAs (grid <= number of SMs).  pdl: launch
 // with programmatic stream serialisation.
 cudaError_t launch_linear(const LinearParams& p, int grid, bool pdl, cudaStream_t st);

@@ -28,7 +28,7 @@ constexpr int kHeadGridMax = 256;       // CTAs of a vocabulary-head launch (<= 
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
-int sstride_of(int K) { return (int)align_up((size_t)ceil_div(K, EE_QUANT_GROUP), 8); }
+int sstride_of(int K) { return (int)ceil_div(K, EE_QUANT_GROUP); }
 
 struct Carver {
   uint8_t* base;
@@ -418,7 +418,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.q_out = c->q;
     p.kc = c->kcache + (size_t)j * m.kv_layer_elems;
     p.vc = c->vcache + (size_t)j * m.kv_layer_elems;
-    linear_plan_smem(p, B);
+    p.max_rows = B;
     EE_LAUNCH(log, EE_K_QKV, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
     // decode attention
     AttnParams ap = {};
@@ -454,7 +454,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.xh = c->ah;
     p.x_stride = m.dq;
     p.epi = EPI_RESID;
-    linear_plan_smem(p, B);
+    p.max_rows = B;
     EE_LAUNCH(log, EE_K_O, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
     // FFN RMSNorm
     np.g = w.g_ffn;
@@ -474,7 +474,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.epi = EPI_SWIGLU;
     p.xh_out = c->acth;
     p.xo_stride = m.F;
-    linear_plan_smem(p, B);
+    p.max_rows = B;
     EE_LAUNCH(log, EE_K_GATEUP, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
     // down projection + residual (+ per-layer copy in debug mode)
     p = base;
@@ -490,7 +490,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.x_stride = m.F;
     p.epi = EPI_RESID;
     p.hdbg = c->hdbg + (size_t)j * EE_MAX_BATCH * m.d;
-    linear_plan_smem(p, B);
+    p.max_rows = B;
     EE_LAUNCH(log, EE_K_DOWN, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
 
     const auto ck = std::find(c->ckpts.begin(), c->ckpts.end(), j);
@@ -512,7 +512,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
       p.epi = EPI_X;
       p.xh_out = c->uh;
       p.xo_stride = m.d;
-      linear_plan_smem(p, B);
+      p.max_rows = B;
       EE_LAUNCH(log, EE_K_HEAD_T, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
       // z = u E^T, conf = max softmax, exit if conf > gamma_c, compact the lists
       p = base;
@@ -531,7 +531,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
       p.exit_layer = c->out_dev->exit_layer;
       p.ckpt_index = ci;
       p.ckpt_layer = j;
-      linear_plan_smem(p, B);
+      p.max_rows = B;
       EE_LAUNCH(log, EE_K_HEAD_E, j,
                 launch_linear(p, std::min(linear_grid(p.N, c->num_sms), kHeadGridMax), true, st));
     }
@@ -553,7 +553,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
   p.head_mode = HEAD_FINAL;
   p.head_counter = c->head_cnt;
   p.argmax_out = c->out_dev->next_token;
-  linear_plan_smem(p, B);
+  p.max_rows = B;
   EE_LAUNCH(log, EE_K_FINAL_HEAD, -1,
             launch_linear(p, std::min(linear_grid(p.N, c->num_sms), kHeadGridMax), true, st));
   EE_CUDA(c, cudaMemcpyAsync(c->out_host, c->out_dev, step_d2h_bytes(B), cudaMemcpyDeviceToHost, st));
@@ -1170,7 +1170,7 @@ ee_status ee_op_quantize_int4(const uint16_t* w, int32_t rows, int32_t cols, uin
 static ee_status op_linear(int32_t M, int32_t N, int32_t K, const uint16_t* xh, const uint16_t* w, const uint8_t* q, const uint16_t* s, int32_t sstride, float* y,
                            int32_t* err, void* stream) {
   if (M < 1 || M > EE_MAX_BATCH || N < 2 || N % 2 || K < 32 || K % 32 || !y) return EE_ERR_INVALID_ARG;
-  if (q && ((uintptr_t)q % 16 || (uintptr_t)s % 16 || sstride % 8)) return EE_ERR_INVALID_ARG;
+  if (q && ((uintptr_t)q % 16 || (uintptr_t)s % 16)) return EE_ERR_INVALID_ARG;
   if (w && (uintptr_t)w % 16) return EE_ERR_INVALID_ARG;
   const int sms = device_sms();
   if (sms <= 0) return EE_ERR_CUDA;
@@ -1189,7 +1189,7 @@ static ee_status op_linear(int32_t M, int32_t N, int32_t K, const uint16_t* xh, 
   p.out_f32 = y;
   p.out_stride = N;
   p.err = err;
-  linear_plan_smem(p, M);
+  p.max_rows = M;
   return launch_linear(p, linear_grid(N, sms), false, (cudaStream_t)stream) == cudaSuccess ? EE_OK
                                                                                            : EE_ERR_CUDA;
 }
@@ -1281,7 +1281,7 @@ ee_status ee_op_vocab_head(int32_t M, int32_t V, int32_t d, const uint16_t* u_f1
   p.conf_out = conf;
   p.argmax_out = argmax;
   p.err = err_flag;
-  linear_plan_smem(p, M);
+  p.max_rows = M;
   return launch_linear(p, std::min(linear_grid(V, sms), kHeadGridMax), false, (cudaStream_t)stream) ==
                  cudaSuccess
              ? EE_OK

@@ -8,16 +8,25 @@
 // group of 128 input columns, dequantised in registers and never written
 // back).  An empty list reads no byte of its matrix.
 //
-// Data flow per CTA (persistent, one per SM): warp 8 is a producer whose lane
-// 0 streams the CTA's contiguous row range through a 6-stage shared-memory
-// ring with bulk asynchronous copies (cp.async.bulk, completion counted on
-// mbarriers, L2 evict-first); warps 0-7 consume.  A stage holds 16 rows x
-// 1 KB (512 bf16 columns, or 2048 int4 columns plus their 16 scales).  Warp w
-// owns rows (2w, 2w+1) of each 16-row tile, so the pairs that RoPE and SwiGLU
-// combine are reduced by the same warp.  Activations come from L1/L2 (they are
-// a few KB per sequence) in fp16, permuted within runs of 8 so that one
-// 16-byte load yields the half2 pairs that match the nibble pairs of a packed
-// int4 word (see xh_slot); the bf16 path reads the same layout.
+// Data flow per CTA (persistent, one per SM): each CTA owns a contiguous,
+// pair-aligned range of output rows, which is one contiguous byte range of the
+// row-major weights.  Warp 8's lane 0 streams that range through a ring of
+// shared-memory stages, each filled by ONE 16 KB bulk asynchronous copy
+// (cp.async.bulk, completion counted on an mbarrier, L2 evict-first; plus one
+// 512-byte copy of the stage's int4 scales): the copy engine reaches HBM peak
+// only with large requests (1 KB requests stall near 2.5 TB/s on GB300).  The
+// weights of the first stages are requested before the grid dependency wait,
+// so they stream while the previous kernel finishes; the activations of the
+// step's rows (fp16, a few KB per sequence) are bulk-copied into shared memory
+// after it.  Warps 0-7 consume: each takes an eighth of a stage, maps every
+// 16-byte vector back to (row, column), accumulates per row in registers and
+// adds each row's partial into per-row sums in shared memory (one warp
+// reduction when the warp's slice lies in one row).  The epilogue (RoPE + KV
+// write, SwiGLU, residual add, head statistics) runs once over the CTA's rows.
+//
+// Activations are stored in "pair order" (within each run of 8 columns:
+// 0,4,1,5,2,6,3,7, see xh_slot) so that one 16-byte load yields the half2
+// pairs that match the nibble pairs of a packed int4 word.
 //
 // int4 dequantisation: a packed word holds columns c..c+7 in nibbles 0..7;
 // (w ^ 0x88888888) turns two's complement into offset binary, then
@@ -34,24 +43,22 @@ namespace ee {
 namespace {
 
 constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kTileRows = 2 * kConsumerWarps;
-constexpr int kChunkBytes = 1024;
-constexpr int kScaleBytes = 32;
-constexpr int kStageBytes = kTileRows * (kChunkBytes + kScaleBytes);
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;
+constexpr int kStageW = 16384;  // weight bytes per stage: one bulk copy
+constexpr int kStageS = 512;    // int4 scale bytes per stage (16 KB of nibbles = 256 groups)
+constexpr int kStageBytes = kStageW + kStageS;
 constexpr int kMaxStages = 6;
 constexpr int kMM = 8;  // sequences per pass over the weights
-constexpr int kBfChunk = kChunkBytes / 2;  // bf16 columns per stage row
-constexpr int kQChunk = kChunkBytes * 2;   // int4 columns per stage row
 
-// Shared memory: a small header (barriers, lists, head statistics), then the
-// activations of the step's rows when they are staged (XS mode), then the ring.
+// Shared memory: header (barriers, lists, head statistics), the staged
+// activations (XS mode), the per-row sums [rows][mcap], then the ring.
 constexpr size_t kHeaderBytes = 1536;
 constexpr size_t kXsMaxBytes = 48 * 1024;
 constexpr size_t kSmemTarget = 112 * 1024;  // two CTAs per SM: the next kernel's CTA can prefetch
-constexpr size_t kSmemMax = kHeaderBytes + kXsMaxBytes + size_t(kMaxStages) * kStageBytes;
-static_assert((2 * kMaxStages + 1) * 8 + 2 * kListLen * 4 + kConsumerWarps * kMM * 3 * 4 <= kHeaderBytes,
-              "header overflow");
+constexpr size_t kSmemMax = 227 * 1024;
+static_assert((2 * kMaxStages + 1) * 8 <= 128, "barriers");
+static_assert(128 + 2 * kListLen * 4 + 8 + kConsumerWarps * kMM * 3 * 4 <= kHeaderBytes, "header overflow");
 
 EE_DEV __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
@@ -168,47 +175,53 @@ EE_DEV Stat stat_merge(Stat a, Stat b) {
 
 EE_DEV void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory"); }
 
-// Iteration order shared by the producer and the consumers: phase (0 bf16
-// rows, 1 int4 rows), pass over at most kMM sequences, 16-row tile of the
-// CTA's rows, K chunk.  Each iteration fills one ring stage.
+// Per-CTA plan shared by the producer and the consumers.  Phase 0 streams
+// the bf16 rows [r0, r1) (K*2 bytes each), phase 1 their int4 copy (K/2
+// bytes each); each phase runs one pass per group of at most mcap sequences.
 struct Plan {
-  int r0, r1, ntiles, nc[2], passes[2];
-  EE_DEV int rows(int t) const { return min(kTileRows, r1 - (r0 + t * kTileRows)); }
-  EE_DEV uint32_t total() const {
-    return (uint32_t)(passes[0] * ntiles * nc[0] + passes[1] * ntiles * nc[1]);
-  }
+  int r0, r1, mcap;
+  int nst[2], passes[2];
+  long long rbytes[2];
+  bool sc_staged;  // int4 scales flatten with the weights (K % 512 == 0, unpadded rows)
 };
 
-// Issues the bulk copies of one ring stage (weights and, for int4, scales).
-EE_DEV void issue_stage(const LinearParams& p, const Plan& pl, int phase, int t, int c, uint8_t* sbase,
+EE_DEV void issue_stage(const LinearParams& p, const Plan& pl, int phase, int s, uint8_t* sbase,
                         uint64_t* bar, uint64_t pol) {
-  const int tr0 = pl.r0 + t * kTileRows;
-  const int rows = pl.rows(t);
+  const long long off = (long long)s * kStageW;
+  const uint32_t bytes = (uint32_t)min((long long)kStageW, pl.rbytes[phase] - off);
   if (phase == 0) {
-    const int ce = min(kBfChunk, p.K - c * kBfChunk);
-    const uint32_t cb = ce * 2;
-    mbar_arrive_expect_tx(bar, rows * cb);
-    for (int r = 0; r < rows; ++r)
-      bulk_g2s(sbase + r * kChunkBytes, p.w + (size_t)(tr0 + r) * p.K + c * kBfChunk, cb, bar, pol);
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(sbase, reinterpret_cast<const uint8_t*>(p.w + (size_t)pl.r0 * p.K) + off, bytes, bar, pol);
   } else {
-    const int ce = min(kQChunk, p.K - c * kQChunk);
-    const uint32_t cb = ce / 2;
-    const int ng = (ce + EE_QUANT_GROUP - 1) / EE_QUANT_GROUP;
-    const uint32_t sb = ((ng * 2 + 15) / 16) * 16;
-    mbar_arrive_expect_tx(bar, rows * (cb + sb));
-    for (int r = 0; r < rows; ++r) {
-      bulk_g2s(sbase + r * kChunkBytes, p.wq + (size_t)(tr0 + r) * (p.K / 2) + (size_t)c * (kQChunk / 2),
-               cb, bar, pol);
-      bulk_g2s(sbase + kTileRows * kChunkBytes + r * kScaleBytes,
-               p.ws + (size_t)(tr0 + r) * p.sstride + c * (kQChunk / EE_QUANT_GROUP), sb, bar, pol);
-    }
+    const uint32_t sb = pl.sc_staged ? bytes / 32 : 0;  // one bf16 scale per 64 bytes of nibbles
+    mbar_arrive_expect_tx(bar, bytes + sb);
+    bulk_g2s(sbase, p.wq + (size_t)pl.r0 * (p.K / 2) + off, bytes, bar, pol);
+    if (sb)
+      bulk_g2s(sbase + kStageW, p.ws + (size_t)pl.r0 * p.sstride + (size_t)s * (kStageW / 64), sb, bar, pol);
   }
 }
 
-// XS = true: the activations of all the step's rows (at most p.xs_rows
-// sequences) are bulk-copied into shared memory once, after the dependency
-// wait, while the weight stream already runs; XS = false: activations are
-// read from global memory (L1/L2) at every stage.
+// Adds a lane's per-row partials to the CTA's row sums: one warp reduction
+// when every active lane holds the same row, otherwise one atomic per lane.
+EE_DEV void flush_rows(float* rowsum, int mcap, int mc, int row, float* acc, int lane) {
+  const int rmax = __reduce_max_sync(0xffffffffu, row);
+  const bool uniform = __all_sync(0xffffffffu, row == rmax || row < 0);
+  if (uniform) {
+    if (rmax < 0) return;
+#pragma unroll
+    for (int m = 0; m < kMM; ++m) {
+      if (m < mc) {
+        const float v = warp_sum(acc[m]);
+        if (lane == 0) atomicAdd(&rowsum[rmax * mcap + m], v);
+      }
+    }
+  } else if (row >= 0) {
+#pragma unroll
+    for (int m = 0; m < kMM; ++m)
+      if (m < mc) atomicAdd(&rowsum[row * mcap + m], acc[m]);
+  }
+}
+
 template <int EPI, bool XS>
 __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -219,7 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
   int32_t* le = lf + kListLen;
   float* hst = reinterpret_cast<float*>(smem + 128 + 2 * kListLen * 4 + 8);
   uint8_t* xs = smem + kHeaderBytes;
-  uint8_t* ring = xs + (XS ? (size_t)p.xs_rows * p.K * 2 : 0);
+  float* rowsum = reinterpret_cast<float*>(xs + (XS ? (size_t)p.xs_rows * p.K * 2 : 0));
+  uint8_t* ring = reinterpret_cast<uint8_t*>(rowsum) + (size_t)p.rows_cap * p.mcap * 4;
   const int nst = p.nstages;
   __shared__ int s_last;
 
@@ -248,18 +262,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
     const int npairs = p.N >> 1;
     pl.r0 = 2 * (int)(((long long)blockIdx.x * npairs) / gridDim.x);
     pl.r1 = 2 * (int)(((long long)(blockIdx.x + 1) * npairs) / gridDim.x);
-    pl.ntiles = (pl.r1 - pl.r0 + kTileRows - 1) / kTileRows;
-    pl.nc[0] = (p.K + kBfChunk - 1) / kBfChunk;
-    pl.nc[1] = (p.K + kQChunk - 1) / kQChunk;
-    pl.passes[0] = (nf + kMM - 1) / kMM;
-    pl.passes[1] = (ne + kMM - 1) / kMM;
+    pl.mcap = p.mcap;
+    pl.rbytes[0] = (long long)(pl.r1 - pl.r0) * p.K * 2;
+    pl.rbytes[1] = (long long)(pl.r1 - pl.r0) * (p.K / 2);
+    pl.nst[0] = (int)((pl.rbytes[0] + kStageW - 1) / kStageW);
+    pl.nst[1] = (int)((pl.rbytes[1] + kStageW - 1) / kStageW);
+    pl.passes[0] = (nf + pl.mcap - 1) / pl.mcap;
+    pl.passes[1] = (ne + pl.mcap - 1) / pl.mcap;
+    pl.sc_staged = (p.K % 512 == 0) && (p.sstride * EE_QUANT_GROUP == p.K);
   }
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
-      const uint32_t total = pl.total();
+      const uint32_t total =
+          (uint32_t)(pl.passes[0] * pl.nst[0] + pl.passes[1] * pl.nst[1]);
       const uint32_t prefill = total < (uint32_t)nst ? total : (uint32_t)nst;
       bool xdone = !XS;
       auto stage_x = [&]() {
@@ -279,17 +297,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
       bool ok = true;
       for (int phase = 0; phase < 2 && ok; ++phase) {
         for (int pass = 0; pass < pl.passes[phase] && ok; ++pass) {
-          for (int t = 0; t < pl.ntiles && ok; ++t) {
-            for (int c = 0; c < pl.nc[phase]; ++c, ++it) {
-              if (!xdone && it == prefill) stage_x();
-              const int st = it % nst;
-              const uint32_t n = it / nst;
-              if (n > 0 && !mbar_wait_bounded(&empty[st], (n - 1) & 1, p.err, DERR_EMPTY_WAIT)) {
-                ok = false;
-                break;
-              }
-              issue_stage(p, pl, phase, t, c, ring + (size_t)st * kStageBytes, &full[st], pol);
+          for (int s = 0; s < pl.nst[phase]; ++s, ++it) {
+            if (!xdone && it == prefill) stage_x();
+            const int st = it % nst;
+            const uint32_t n = it / nst;
+            if (n > 0 && !mbar_wait_bounded(&empty[st], (n - 1) & 1, p.err, DERR_EMPTY_WAIT)) {
+              ok = false;
+              break;
             }
+            issue_stage(p, pl, phase, s, ring + (size_t)st * kStageBytes, &full[st], pol);
           }
         }
       }
@@ -306,15 +322,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
     grid_dep_launch();
     bool ok = true;
     if (XS && nx > 0) ok = mbar_wait_bounded(xbar, 0, p.err, DERR_FULL_WAIT);
+    const int nrows = pl.r1 - pl.r0;
     uint32_t it = 0;
     for (int phase = 0; phase < 2; ++phase) {
       const int nlist = phase == 0 ? nf : ne;
       const int32_t* lst = phase == 0 ? lf : le;
-      const int nc = pl.nc[phase];
       const int xbase = phase == 0 ? 0 : nf;  // XS row of the phase's first sequence
+      const int vec_elems = phase == 0 ? 8 : 32;
       for (int pass = 0; pass < pl.passes[phase]; ++pass) {
-        const int m0 = pass * kMM;
-        const int mc = min(kMM, nlist - m0);
+        const int m0 = pass * pl.mcap;
+        const int mc = min(pl.mcap, nlist - m0);
         int seqs[kMM];
         const uint16_t* xrow[kMM];
 #pragma unroll
@@ -324,123 +341,139 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
           xrow[m] = XS ? reinterpret_cast<const uint16_t*>(xs) + (size_t)(xbase + m0 + mm) * p.K
                        : p.xh + (size_t)seqs[m] * p.x_stride;
         }
-        Stat stat = {-INFINITY, 0.0f, 0x7fffffff};
-        for (int t = 0; t < pl.ntiles; ++t) {
-          const int tr0 = pl.r0 + t * kTileRows;
-          const bool have = 2 * warp < pl.rows(t);
-          float acc0[kMM], acc1[kMM];
+        for (int i = tid; i < nrows * pl.mcap; i += kConsumers) rowsum[i] = 0.0f;
+        consumer_bar();
+        for (int s = 0; s < pl.nst[phase]; ++s, ++it) {
+          const int st = it % nst;
+          if (ok) ok = mbar_wait_bounded(&full[st], (it / nst) & 1, p.err, DERR_FULL_WAIT);
+          ok = __all_sync(0xffffffffu, ok);  // the row flush below is warp-collective
+          if (ok) {
+            const uint8_t* sw = ring + (size_t)st * kStageBytes;
+            const long long off = (long long)s * kStageW;
+            const int nbytes = (int)min((long long)kStageW, pl.rbytes[phase] - off);
+            const int nv = nbytes >> 4;
+            const int vb = (int)(((long long)nv * warp) / kConsumerWarps);
+            const int ve = (int)(((long long)nv * (warp + 1)) / kConsumerWarps);
+            // (row, column) of this lane's first vector; later vectors step by 32
+            const int e0 = (int)(phase == 0 ? off / 2 : off * 2) + (vb + lane) * vec_elems;
+            int row = e0 / p.K;
+            int k = e0 - row * p.K;
+            const int step = 32 * vec_elems;
+            int cur = -1;
+            float acc[kMM];
 #pragma unroll
-          for (int m = 0; m < kMM; ++m) acc0[m] = acc1[m] = 0.0f;
-          for (int c = 0; c < nc; ++c, ++it) {
-            const int st = it % nst;
-            if (ok) ok = mbar_wait_bounded(&full[st], (it / nst) & 1, p.err, DERR_FULL_WAIT);
-            if (ok && have) {
-              const uint8_t* sa = ring + (size_t)st * kStageBytes + (2 * warp) * kChunkBytes;
-              const uint8_t* sb = sa + kChunkBytes;
+            for (int m = 0; m < kMM; ++m) acc[m] = 0.0f;
+            for (int v = vb + lane; v < ve; v += 32, k += step) {
+              while (k >= p.K) {
+                k -= p.K;
+                ++row;
+              }
+              if (row != cur) {
+                if (cur >= 0) {
+#pragma unroll
+                  for (int m = 0; m < kMM; ++m)
+                    if (m < mc) atomicAdd(&rowsum[cur * pl.mcap + m], acc[m]);
+                }
+                cur = row;
+#pragma unroll
+                for (int m = 0; m < kMM; ++m) acc[m] = 0.0f;
+              }
+              const uint4 wv = *reinterpret_cast<const uint4*>(sw + (size_t)v * 16);
               if (phase == 0) {
-                const int nvec = min(kBfChunk, p.K - c * kBfChunk) >> 3;
-                for (int v = lane; v < nvec; v += 32) {
-                  const uint4 wa = *reinterpret_cast<const uint4*>(sa + v * 16);
-                  const uint4 wb = *reinterpret_cast<const uint4*>(sb + v * 16);
-                  const int k0 = c * kBfChunk + v * 8;
 #pragma unroll
-                  for (int m = 0; m < kMM; ++m) {
-                    if (m < mc) {
-                      const uint4 xv = XS ? *reinterpret_cast<const uint4*>(xrow[m] + k0)
-                                          : ldg_nc_v4(xrow[m] + k0);
-                      acc0[m] = dot8_bf16(wa, xv, acc0[m]);
-                      acc1[m] = dot8_bf16(wb, xv, acc1[m]);
-                    }
+                for (int m = 0; m < kMM; ++m) {
+                  if (m < mc) {
+                    const uint4 xv = XS ? *reinterpret_cast<const uint4*>(xrow[m] + k) : ldg_nc_v4(xrow[m] + k);
+                    acc[m] = dot8_bf16(wv, xv, acc[m]);
                   }
                 }
               } else {
-                const int nvec = min(kQChunk, p.K - c * kQChunk) >> 5;
-                const uint16_t* sca = reinterpret_cast<const uint16_t*>(
-                    ring + (size_t)st * kStageBytes + kTileRows * kChunkBytes + (2 * warp) * kScaleBytes);
-                const uint16_t* scb = sca + kScaleBytes / 2;
-                for (int v = lane; v < nvec; v += 32) {
-                  const uint4 qa = *reinterpret_cast<const uint4*>(sa + v * 16);
-                  const uint4 qb = *reinterpret_cast<const uint4*>(sb + v * 16);
-                  const float s_a = bf16_bits_to_float(sca[v >> 2]);
-                  const float s_b = bf16_bits_to_float(scb[v >> 2]);
-                  const int k0 = c * kQChunk + v * 32;
+                const float sc =
+                    pl.sc_staged
+                        ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(sw + kStageW)[v >> 2])
+                        : bf16_bits_to_float(__ldg(p.ws + (size_t)(pl.r0 + row) * p.sstride + k / EE_QUANT_GROUP));
 #pragma unroll
-                  for (int m = 0; m < kMM; ++m) {
-                    if (m < mc) {
-                      const uint16_t* xp = xrow[m] + k0;
-                      uint4 x0, x1, x2, x3;
-                      if (XS) {
-                        x0 = *reinterpret_cast<const uint4*>(xp);
-                        x1 = *reinterpret_cast<const uint4*>(xp + 8);
-                        x2 = *reinterpret_cast<const uint4*>(xp + 16);
-                        x3 = *reinterpret_cast<const uint4*>(xp + 24);
-                      } else {
-                        x0 = ldg_nc_v4(xp);
-                        x1 = ldg_nc_v4(xp + 8);
-                        x2 = ldg_nc_v4(xp + 16);
-                        x3 = ldg_nc_v4(xp + 24);
-                      }
-                      __half2 ha = __float2half2_rn(0.0f), hb = ha;
-                      ha = dot8_int4(qa.x, x0, ha);
-                      hb = dot8_int4(qb.x, x0, hb);
-                      ha = dot8_int4(qa.y, x1, ha);
-                      hb = dot8_int4(qb.y, x1, hb);
-                      ha = dot8_int4(qa.z, x2, ha);
-                      hb = dot8_int4(qb.z, x2, hb);
-                      ha = dot8_int4(qa.w, x3, ha);
-                      hb = dot8_int4(qb.w, x3, hb);
-                      const float2 fa = __half22float2(ha), fb = __half22float2(hb);
-                      acc0[m] = fmaf(s_a, fa.x + fa.y, acc0[m]);
-                      acc1[m] = fmaf(s_b, fb.x + fb.y, acc1[m]);
+                for (int m = 0; m < kMM; ++m) {
+                  if (m < mc) {
+                    const uint16_t* xp = xrow[m] + k;
+                    uint4 x0, x1, x2, x3;
+                    if (XS) {
+                      x0 = *reinterpret_cast<const uint4*>(xp);
+                      x1 = *reinterpret_cast<const uint4*>(xp + 8);
+                      x2 = *reinterpret_cast<const uint4*>(xp + 16);
+                      x3 = *reinterpret_cast<const uint4*>(xp + 24);
+                    } else {
+                      x0 = ldg_nc_v4(xp);
+                      x1 = ldg_nc_v4(xp + 8);
+                      x2 = ldg_nc_v4(xp + 16);
+                      x3 = ldg_nc_v4(xp + 24);
                     }
+                    __half2 h = __float2half2_rn(0.0f);
+                    h = dot8_int4(wv.x, x0, h);
+                    h = dot8_int4(wv.y, x1, h);
+                    h = dot8_int4(wv.z, x2, h);
+                    h = dot8_int4(wv.w, x3, h);
+                    const float2 f = __half22float2(h);
+                    acc[m] = fmaf(sc, f.x + f.y, acc[m]);
                   }
                 }
               }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[st]);
+            flush_rows(rowsum, pl.mcap, mc, cur, acc, lane);
           }
-          if (have) {
-            const int ra = tr0 + 2 * warp;
-#pragma unroll
-            for (int m = 0; m < kMM; ++m) {
-              if (m < mc) {
-                const float ya = warp_sum(acc0[m]);
-                const float yb = warp_sum(acc1[m]);
-                if constexpr (EPI == EPI_HEAD) {
-                  if (lane == m) {
-                    stat_push(stat, ya, ra);
-                    stat_push(stat, yb, ra + 1);
-                  }
-                } else {
-                  if (lane == m) epi_pair<EPI>(p, seqs[m], ra, ya, yb);
-                }
-              }
-            }
-          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[st]);
         }
+        consumer_bar();  // every row sum of this pass is complete
         if constexpr (EPI == EPI_HEAD) {
-          // combine the 8 warps' statistics of this pass; one partial per CTA and row
-          if (lane < kMM) {
-            float* hs = hst + (warp * kMM + lane) * 3;
-            hs[0] = stat.mx;
-            hs[1] = stat.sum;
-            hs[2] = __int_as_float(stat.arg);
+          Stat stat[kMM];
+#pragma unroll
+          for (int m = 0; m < kMM; ++m) stat[m] = Stat{-INFINITY, 0.0f, 0x7fffffff};
+          for (int r = tid; r < nrows; r += kConsumers) {
+#pragma unroll
+            for (int m = 0; m < kMM; ++m)
+              if (m < mc) stat_push(stat[m], rowsum[r * pl.mcap + m], pl.r0 + r);
+          }
+#pragma unroll
+          for (int m = 0; m < kMM; ++m) {
+            if (m < mc) {
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) {
+                Stat t;
+                t.mx = __shfl_xor_sync(0xffffffffu, stat[m].mx, o);
+                t.sum = __shfl_xor_sync(0xffffffffu, stat[m].sum, o);
+                t.arg = __shfl_xor_sync(0xffffffffu, stat[m].arg, o);
+                stat[m] = stat_merge(stat[m], t);
+              }
+              if (lane == 0) {
+                float* hs = hst + (warp * kMM + m) * 3;
+                hs[0] = stat[m].mx;
+                hs[1] = stat[m].sum;
+                hs[2] = __int_as_float(stat[m].arg);
+              }
+            }
           }
           consumer_bar();
           if (warp == 0 && lane < mc) {
-            Stat s = {-INFINITY, 0.0f, 0x7fffffff};
+            Stat sm = {-INFINITY, 0.0f, 0x7fffffff};
             for (int w = 0; w < kConsumerWarps; ++w) {
               const float* hs = hst + (w * kMM + lane) * 3;
-              s = stat_merge(s, Stat{hs[0], hs[1], __float_as_int(hs[2])});
+              sm = stat_merge(sm, Stat{hs[0], hs[1], __float_as_int(hs[2])});
             }
             float* dst = p.head_part + ((size_t)blockIdx.x * EE_MAX_BATCH + m0 + lane) * 4;
-            dst[0] = s.mx;
-            dst[1] = s.sum;
-            dst[2] = __int_as_float(s.arg);
+            dst[0] = sm.mx;
+            dst[1] = sm.sum;
+            dst[2] = __int_as_float(sm.arg);
           }
-          consumer_bar();
+        } else {
+          const int npr = nrows >> 1;
+          for (int i = tid; i < npr * mc; i += kConsumers) {
+            const int pr = i / mc, m = i - pr * mc;
+            epi_pair<EPI>(p, seqs[m], pl.r0 + 2 * pr, rowsum[(2 * pr) * pl.mcap + m],
+                          rowsum[(2 * pr + 1) * pl.mcap + m]);
+          }
         }
+        consumer_bar();  // row sums are reused by the next pass
       }
     }
   }
@@ -532,7 +565,7 @@ cudaError_t launch_one(const LinearParams& p, int grid, bool pdl, cudaStream_t s
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kHeaderBytes + (p.xs_rows > 0 ? (size_t)p.xs_rows * p.K * 2 : 0) +
-                         (size_t)p.nstages * kStageBytes;
+                         (size_t)p.rows_cap * p.mcap * 4 + (size_t)p.nstages * kStageBytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -547,17 +580,32 @@ cudaError_t launch_one(const LinearParams& p, int grid, bool pdl, cudaStream_t s
 
 size_t linear_smem_bytes() { return kSmemMax; }
 
-void linear_plan_smem(LinearParams& p, int max_rows) {
+// Shared-memory plan of one launch: per-row sums for the CTA's rows, the
+// activations staged when they fit (at most kMM sequences, 48 KB), and as
+// many ring stages as keep the CTA within the two-CTAs-per-SM budget.
+static void plan_smem(LinearParams& p, int grid) {
+  const int max_rows = p.max_rows < 1 ? 1 : p.max_rows;
+  p.mcap = max_rows < kMM ? max_rows : kMM;
+  const int npairs = p.N / 2;
+  p.rows_cap = 2 * ((npairs + grid - 1) / grid);
+  const size_t rs = ((size_t)p.rows_cap * p.mcap * 4 + 15) / 16 * 16;
+  p.rows_cap = (int)(rs / 4 / p.mcap);
   const size_t xb = (size_t)max_rows * p.K * 2;
-  int nst = kMaxStages;
+  const size_t fixed = kHeaderBytes + rs;
   bool xs = max_rows <= kMM && xb <= kXsMaxBytes;
+  int nst = kMaxStages;
   if (xs) {
-    const size_t room = kSmemTarget - kHeaderBytes - xb;
-    nst = (int)(room / kStageBytes);
+    const long long room = (long long)kSmemTarget - (long long)(fixed + xb);
+    nst = room > 0 ? (int)(room / kStageBytes) : 0;
     if (nst > kMaxStages) nst = kMaxStages;
     if (nst < 4) xs = false;
   }
-  if (!xs) nst = kMaxStages;
+  if (!xs) {
+    const long long room = (long long)kSmemTarget - (long long)fixed;
+    nst = room > 0 ? (int)(room / kStageBytes) : 0;
+    if (nst > kMaxStages) nst = kMaxStages;
+    if (nst < 2) nst = 2;
+  }
   p.xs_rows = xs ? max_rows : 0;
   p.nstages = nst;
 }
@@ -573,11 +621,16 @@ cudaError_t linear_prepare() {
 }
 
 int linear_grid(int N, int num_sms) {
-  const int tiles = (N + kTileRows - 1) / kTileRows;
-  return tiles < num_sms ? (tiles > 0 ? tiles : 1) : num_sms;
+  const int pairs = N / 2;
+  return pairs < num_sms ? (pairs > 0 ? pairs : 1) : num_sms;
 }
 
-cudaError_t launch_linear(const LinearParams& p, int grid, bool pdl, cudaStream_t st) {
+cudaError_t launch_linear(const LinearParams& p_in, int grid, bool pdl, cudaStream_t st) {
+  LinearParams p = p_in;
+  plan_smem(p, grid);
+  const size_t smem = kHeaderBytes + (p.xs_rows > 0 ? (size_t)p.xs_rows * p.K * 2 : 0) +
+                      (size_t)p.rows_cap * p.mcap * 4 + (size_t)p.nstages * kStageBytes;
+  if (smem > kSmemMax) return cudaErrorInvalidConfiguration;
   switch (p.epi) {
     case EPI_F32: return launch_one<EPI_F32>(p, grid, pdl, st);
     case EPI_QKV: return launch_one<EPI_QKV>(p, grid, pdl, st);

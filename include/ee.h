@@ -272,8 +272,8 @@ ee_status ee_op_quantize_int4(const uint16_t *w, int32_t rows, int32_t cols, uin
 ee_status ee_op_linear_bf16(int32_t M, int32_t N, int32_t K, const uint16_t *x_f16,
                             const uint16_t *w, float *y, int32_t *err_flag, void *stream);
 /* Same with the int4 copy: packed [N, K/2], scales [N, scale_stride] bf16
- * with scale_stride a multiple of 8 and >= ceil(K/128) (entries past
- * ceil(K/128) are read but unused); x fp16 [M, K] in pair order. */
+ * with scale_stride >= ceil(K/128) (scale_stride = K/128 with K % 512 == 0
+ * lets the scales stream with the weights); x fp16 [M, K] in pair order. */
 ee_status ee_op_linear_int4(int32_t M, int32_t N, int32_t K, const uint16_t *x_f16,
                             const uint8_t *packed, const uint16_t *scales, int32_t scale_stride,
                             float *y, int32_t *err_flag, void *stream);
