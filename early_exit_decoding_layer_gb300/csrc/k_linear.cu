@@ -56,7 +56,7 @@ constexpr int kMM = 8;  // sequences per pass over the weights
 constexpr size_t kHeaderBytes = 1536;
 constexpr size_t kXsMaxBytes = 48 * 1024;
 constexpr size_t kSmemTarget = 112 * 1024;  // two CTAs per SM: the next kernel's CTA can prefetch
-constexpr size_t kSmemMax = 227 * 1024;
+constexpr size_t kSmemMax = 160 * 1024;  // attribute; every plan stays below it
 static_assert((2 * kMaxStages + 1) * 8 <= 128, "barriers");
 static_assert(128 + 2 * kListLen * 4 + 8 + kConsumerWarps * kMM * 3 * 4 <= kHeaderBytes, "header overflow");
 
