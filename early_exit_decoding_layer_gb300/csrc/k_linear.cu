@@ -175,6 +175,12 @@ EE_DEV Stat stat_merge(Stat a, Stat b) {
 
 EE_DEV void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory"); }
 
+// Bytes of the per-row sums, rounded up so that the ring behind them starts on
+// a 16-byte boundary (bulk copies need it).
+__host__ __device__ inline size_t rowsum_bytes(int rows_cap, int mcap) {
+  return ((size_t)rows_cap * mcap * 4 + 15) / 16 * 16;
+}
+
 // Per-CTA plan shared by the producer and the consumers.  Phase 0 streams
 // the bf16 rows [r0, r1) (K*2 bytes each), phase 1 their int4 copy (K/2
 // bytes each); each phase runs one pass per group of at most mcap sequences.
@@ -233,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
   float* hst = reinterpret_cast<float*>(smem + 128 + 2 * kListLen * 4 + 8);
   uint8_t* xs = smem + kHeaderBytes;
   float* rowsum = reinterpret_cast<float*>(xs + (XS ? (size_t)p.xs_rows * p.K * 2 : 0));
-  uint8_t* ring = reinterpret_cast<uint8_t*>(rowsum) + (size_t)p.rows_cap * p.mcap * 4;
+  uint8_t* ring = reinterpret_cast<uint8_t*>(rowsum) + rowsum_bytes(p.rows_cap, p.mcap);
   const int nst = p.nstages;
   __shared__ int s_last;
 
@@ -565,7 +571,7 @@ cudaError_t launch_one(const LinearParams& p, int grid, bool pdl, cudaStream_t s
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kHeaderBytes + (p.xs_rows > 0 ? (size_t)p.xs_rows * p.K * 2 : 0) +
-                         (size_t)p.rows_cap * p.mcap * 4 + (size_t)p.nstages * kStageBytes;
+                         rowsum_bytes(p.rows_cap, p.mcap) + (size_t)p.nstages * kStageBytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -588,8 +594,7 @@ static void plan_smem(LinearParams& p, int grid) {
   p.mcap = max_rows < kMM ? max_rows : kMM;
   const int npairs = p.N / 2;
   p.rows_cap = 2 * ((npairs + grid - 1) / grid);
-  const size_t rs = ((size_t)p.rows_cap * p.mcap * 4 + 15) / 16 * 16;
-  p.rows_cap = (int)(rs / 4 / p.mcap);
+  const size_t rs = rowsum_bytes(p.rows_cap, p.mcap);
   const size_t xb = (size_t)max_rows * p.K * 2;
   const size_t fixed = kHeaderBytes + rs;
   bool xs = max_rows <= kMM && xb <= kXsMaxBytes;
@@ -629,7 +634,7 @@ cudaError_t launch_linear(const LinearParams& p_in, int grid, bool pdl, cudaStre
   LinearParams p = p_in;
   plan_smem(p, grid);
   const size_t smem = kHeaderBytes + (p.xs_rows > 0 ? (size_t)p.xs_rows * p.K * 2 : 0) +
-                      (size_t)p.rows_cap * p.mcap * 4 + (size_t)p.nstages * kStageBytes;
+                      rowsum_bytes(p.rows_cap, p.mcap) + (size_t)p.nstages * kStageBytes;
   if (smem > kSmemMax) return cudaErrorInvalidConfiguration;
   switch (p.epi) {
     case EPI_F32: return launch_one<EPI_F32>(p, grid, pdl, st);
