@@ -116,6 +116,8 @@ cudaError_t linear_prepare();
 // with programmatic stream serialisation.
 cudaError_t launch_linear(const LinearParams& p, int grid, bool pdl, cudaStream_t st);
 int linear_grid(int N, int num_sms);
+// True if rows of K bf16 or int4 weights can be streamed in row-aligned stages.
+bool linear_shape_ok(int K);
 
 // ------------------------------------------------------------------ attention
 struct AttnParams {

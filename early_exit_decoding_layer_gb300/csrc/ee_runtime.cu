@@ -183,6 +183,9 @@ const char* validate_config(const ee_config* c) {
   if (c->kv_block != EE_KV_BLOCK) return "kv_block must be 16";
   if (c->max_batch < 1 || c->max_batch > EE_MAX_BATCH) return "max_batch must be in [1, 64]";
   if (c->max_seq_len < 2) return "max_seq_len must be >= 2";
+  if (!linear_shape_ok(c->d_model) || !linear_shape_ok(c->n_heads * c->head_dim) ||
+      !linear_shape_ok(c->ffn_dim))
+    return "a projection width is not supported by the GEMV stage geometry";
   if (attention_nsplit(c->max_seq_len, c->head_dim) > attention_max_split())
     return "max_seq_len too large for the attention kernel";
   if (!(c->rms_eps > 0.0f) || !(c->rope_theta > 0.0f)) return "rms_eps and rope_theta must be > 0";
@@ -1169,7 +1172,7 @@ ee_status ee_op_quantize_int4(const uint16_t* w, int32_t rows, int32_t cols, uin
 
 static ee_status op_linear(int32_t M, int32_t N, int32_t K, const uint16_t* xh, const uint16_t* w, const uint8_t* q, const uint16_t* s, int32_t sstride, float* y,
                            int32_t* err, void* stream) {
-  if (M < 1 || M > EE_MAX_BATCH || N < 2 || N % 2 || K < 32 || K % 32 || !y) return EE_ERR_INVALID_ARG;
+  if (M < 1 || M > EE_MAX_BATCH || N < 2 || N % 2 || !linear_shape_ok(K) || !y) return EE_ERR_INVALID_ARG;
   if (q && ((uintptr_t)q % 16 || (uintptr_t)s % 16)) return EE_ERR_INVALID_ARG;
   if (w && (uintptr_t)w % 16) return EE_ERR_INVALID_ARG;
   const int sms = device_sms();
@@ -1262,7 +1265,7 @@ size_t ee_head_scratch_bytes(int32_t M) {
 
 ee_status ee_op_vocab_head(int32_t M, int32_t V, int32_t d, const uint16_t* u_f16, const uint16_t* E, float* conf,
                            int32_t* argmax, void* scratch, int32_t* err_flag, void* stream) {
-  if (M < 1 || M > EE_MAX_BATCH || V < 2 || V % 2 || d < 32 || d % 32 || !u_f16 || !E || !conf || !argmax ||
+  if (M < 1 || M > EE_MAX_BATCH || V < 2 || V % 2 || !linear_shape_ok(d) || !u_f16 || !E || !conf || !argmax ||
       !scratch)
     return EE_ERR_INVALID_ARG;
   const int sms = device_sms();

@@ -53,12 +53,14 @@ constexpr int kMM = 8;  // sequences per pass over the weights
 
 // Shared memory: header (barriers, lists, head statistics), the staged
 // activations (XS mode), the per-row sums [rows][mcap], then the ring.
-constexpr size_t kHeaderBytes = 1536;
+constexpr size_t kHeaderBytes = 2176;
 constexpr size_t kXsMaxBytes = 48 * 1024;
 constexpr size_t kSmemTarget = 112 * 1024;  // two CTAs per SM: the next kernel's CTA can prefetch
 constexpr size_t kSmemMax = 160 * 1024;  // attribute; every plan stays below it
 static_assert((2 * kMaxStages + 1) * 8 <= 128, "barriers");
-static_assert(128 + 2 * kListLen * 4 + 8 + kConsumerWarps * kMM * 3 * 4 <= kHeaderBytes, "header overflow");
+constexpr size_t kSlotOff = 1536;  // per-stage warp partials: [2][warps][kMM] floats, then [2][warps] row ids
+static_assert(128 + 2 * kListLen * 4 + 8 + kConsumerWarps * kMM * 3 * 4 <= kSlotOff, "header overflow");
+static_assert(kSlotOff + 2 * kConsumerWarps * kMM * 4 + 2 * kConsumerWarps * 4 <= kHeaderBytes, "slots");
 
 EE_DEV __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
@@ -181,6 +183,51 @@ __host__ __device__ inline size_t rowsum_bytes(int rows_cap, int mcap) {
   return ((size_t)rows_cap * mcap * 4 + 15) / 16 * 16;
 }
 
+// Stage geometry of one phase, aligned to rows of rb bytes so that each
+// warp's eighth of a stage ("slice") lies inside one row (case A: a row is
+// one or more whole stages, or a stage holds 1, 2 or 4 rows) or is made of q
+// whole rows (case B: small rows, a stage holds a multiple of 8 rows).
+struct Geo {
+  int rb;       // bytes per row
+  int S;        // bytes per full stage
+  bool caseA;
+  int slice;    // case A: bytes per warp slice (multiple of 16)
+  int q;        // case B: rows per warp slice
+};
+
+__host__ __device__ inline Geo make_geo(int rb) {
+  Geo g;
+  g.rb = rb;
+  g.slice = 0;
+  g.q = 0;
+  if (rb >= kStageW) {
+    int n = (rb + kStageW - 1) / kStageW;
+    while (rb % (n * 128) != 0 && n < 64) ++n;
+    g.S = rb / n;
+    g.caseA = true;
+    g.slice = g.S / 8;
+  } else {
+    int nr = kStageW / rb;
+    if (nr >= 8) {
+      nr -= nr % 8;
+      g.caseA = false;
+      g.q = nr / 8;
+    } else {
+      nr = nr >= 4 ? 4 : (nr >= 2 ? 2 : 1);
+      g.caseA = true;
+    }
+    g.S = nr * rb;
+    if (g.caseA) g.slice = g.S / 8;
+  }
+  return g;
+}
+
+__host__ __device__ inline bool geo_ok(const Geo& g) {
+  if (g.S <= 0 || g.S > kStageW || g.S % 16) return false;
+  if (g.caseA) return g.slice % 16 == 0 && (g.rb % g.S == 0 || g.S % g.rb == 0);
+  return g.rb % 16 == 0;
+}
+
 // Per-CTA plan shared by the producer and the consumers.  Phase 0 streams
 // the bf16 rows [r0, r1) (K*2 bytes each), phase 1 their int4 copy (K/2
 // bytes each); each phase runs one pass per group of at most mcap sequences.
@@ -188,13 +235,15 @@ struct Plan {
   int r0, r1, mcap;
   int nst[2], passes[2];
   long long rbytes[2];
-  bool sc_staged;  // int4 scales flatten with the weights (K % 512 == 0, unpadded rows)
+  Geo geo[2];
+  bool sc_staged;  // int4 scales stream with the weights (one 16-byte-aligned slice per stage)
 };
 
 EE_DEV void issue_stage(const LinearParams& p, const Plan& pl, int phase, int s, uint8_t* sbase,
                         uint64_t* bar, uint64_t pol) {
-  const long long off = (long long)s * kStageW;
-  const uint32_t bytes = (uint32_t)min((long long)kStageW, pl.rbytes[phase] - off);
+  const long long S = pl.geo[phase].S;
+  const long long off = (long long)s * S;
+  const uint32_t bytes = (uint32_t)min(S, pl.rbytes[phase] - off);
   if (phase == 0) {
     mbar_arrive_expect_tx(bar, bytes);
     bulk_g2s(sbase, reinterpret_cast<const uint8_t*>(p.w + (size_t)pl.r0 * p.K) + off, bytes, bar, pol);
@@ -203,28 +252,49 @@ EE_DEV void issue_stage(const LinearParams& p, const Plan& pl, int phase, int s,
     mbar_arrive_expect_tx(bar, bytes + sb);
     bulk_g2s(sbase, p.wq + (size_t)pl.r0 * (p.K / 2) + off, bytes, bar, pol);
     if (sb)
-      bulk_g2s(sbase + kStageW, p.ws + (size_t)pl.r0 * p.sstride + (size_t)s * (kStageW / 64), sb, bar, pol);
+      bulk_g2s(sbase + kStageW, p.ws + (size_t)pl.r0 * p.sstride + (size_t)(off / 64), sb, bar, pol);
   }
 }
 
-// Adds a lane's per-row partials to the CTA's row sums: one warp reduction
-// when every active lane holds the same row, otherwise one atomic per lane.
-EE_DEV void flush_rows(float* rowsum, int mcap, int mc, int row, float* acc, int lane) {
-  const int rmax = __reduce_max_sync(0xffffffffu, row);
-  const bool uniform = __all_sync(0xffffffffu, row == rmax || row < 0);
-  if (uniform) {
-    if (rmax < 0) return;
+// Dot products of one stage vector (16 bytes of weights) with the mc
+// activation rows at column k, accumulated into acc[m].
+template <bool XS>
+EE_DEV void vec_dot(int phase, const uint4& wv, float sc, const uint16_t* const* xrow, int k, int mc,
+                    float* acc) {
+  if (phase == 0) {
 #pragma unroll
     for (int m = 0; m < kMM; ++m) {
       if (m < mc) {
-        const float v = warp_sum(acc[m]);
-        if (lane == 0) atomicAdd(&rowsum[rmax * mcap + m], v);
+        const uint4 xv = XS ? *reinterpret_cast<const uint4*>(xrow[m] + k) : ldg_nc_v4(xrow[m] + k);
+        acc[m] = dot8_bf16(wv, xv, acc[m]);
       }
     }
-  } else if (row >= 0) {
+  } else {
 #pragma unroll
-    for (int m = 0; m < kMM; ++m)
-      if (m < mc) atomicAdd(&rowsum[row * mcap + m], acc[m]);
+    for (int m = 0; m < kMM; ++m) {
+      if (m < mc) {
+        const uint16_t* xp = xrow[m] + k;
+        uint4 x0, x1, x2, x3;
+        if (XS) {
+          x0 = *reinterpret_cast<const uint4*>(xp);
+          x1 = *reinterpret_cast<const uint4*>(xp + 8);
+          x2 = *reinterpret_cast<const uint4*>(xp + 16);
+          x3 = *reinterpret_cast<const uint4*>(xp + 24);
+        } else {
+          x0 = ldg_nc_v4(xp);
+          x1 = ldg_nc_v4(xp + 8);
+          x2 = ldg_nc_v4(xp + 16);
+          x3 = ldg_nc_v4(xp + 24);
+        }
+        __half2 h = __float2half2_rn(0.0f);
+        h = dot8_int4(wv.x, x0, h);
+        h = dot8_int4(wv.y, x1, h);
+        h = dot8_int4(wv.z, x2, h);
+        h = dot8_int4(wv.w, x3, h);
+        const float2 f = __half22float2(h);
+        acc[m] = fmaf(sc, f.x + f.y, acc[m]);
+      }
+    }
   }
 }
 
@@ -237,6 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
   int32_t* lf = reinterpret_cast<int32_t*>(smem + 128);
   int32_t* le = lf + kListLen;
   float* hst = reinterpret_cast<float*>(smem + 128 + 2 * kListLen * 4 + 8);
+  float* slot = reinterpret_cast<float*>(smem + kSlotOff);
+  int32_t* slot_row = reinterpret_cast<int32_t*>(slot + 2 * kConsumerWarps * kMM);
   uint8_t* xs = smem + kHeaderBytes;
   float* rowsum = reinterpret_cast<float*>(xs + (XS ? (size_t)p.xs_rows * p.K * 2 : 0));
   uint8_t* ring = reinterpret_cast<uint8_t*>(rowsum) + rowsum_bytes(p.rows_cap, p.mcap);
@@ -269,13 +341,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
     pl.r0 = 2 * (int)(((long long)blockIdx.x * npairs) / gridDim.x);
     pl.r1 = 2 * (int)(((long long)(blockIdx.x + 1) * npairs) / gridDim.x);
     pl.mcap = p.mcap;
+    pl.geo[0] = make_geo(p.K * 2);
+    pl.geo[1] = make_geo(p.K / 2);
     pl.rbytes[0] = (long long)(pl.r1 - pl.r0) * p.K * 2;
     pl.rbytes[1] = (long long)(pl.r1 - pl.r0) * (p.K / 2);
-    pl.nst[0] = (int)((pl.rbytes[0] + kStageW - 1) / kStageW);
-    pl.nst[1] = (int)((pl.rbytes[1] + kStageW - 1) / kStageW);
+    pl.nst[0] = (int)((pl.rbytes[0] + pl.geo[0].S - 1) / pl.geo[0].S);
+    pl.nst[1] = (int)((pl.rbytes[1] + pl.geo[1].S - 1) / pl.geo[1].S);
     pl.passes[0] = (nf + pl.mcap - 1) / pl.mcap;
     pl.passes[1] = (ne + pl.mcap - 1) / pl.mcap;
-    pl.sc_staged = (p.K % 512 == 0) && (p.sstride * EE_QUANT_GROUP == p.K);
+    pl.sc_staged = (p.K % 512 == 0) && (p.sstride * EE_QUANT_GROUP == p.K) && (pl.geo[1].S % 512 == 0);
   }
 
   if (warp == kConsumerWarps) {
@@ -347,88 +421,89 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
           xrow[m] = XS ? reinterpret_cast<const uint16_t*>(xs) + (size_t)(xbase + m0 + mm) * p.K
                        : p.xh + (size_t)seqs[m] * p.x_stride;
         }
-        for (int i = tid; i < nrows * pl.mcap; i += kConsumers) rowsum[i] = 0.0f;
-        consumer_bar();
+        const Geo& g = pl.geo[phase];
+        const int esz_num = phase == 0 ? 1 : 4, esz_den = phase == 0 ? 2 : 1;  // elements = bytes * num / den
         for (int s = 0; s < pl.nst[phase]; ++s, ++it) {
           const int st = it % nst;
+          const int buf = it & 1;
           if (ok) ok = mbar_wait_bounded(&full[st], (it / nst) & 1, p.err, DERR_FULL_WAIT);
-          ok = __all_sync(0xffffffffu, ok);  // the row flush below is warp-collective
-          if (ok) {
-            const uint8_t* sw = ring + (size_t)st * kStageBytes;
-            const long long off = (long long)s * kStageW;
-            const int nbytes = (int)min((long long)kStageW, pl.rbytes[phase] - off);
-            const int nv = nbytes >> 4;
-            const int vb = (int)(((long long)nv * warp) / kConsumerWarps);
-            const int ve = (int)(((long long)nv * (warp + 1)) / kConsumerWarps);
-            // (row, column) of this lane's first vector; later vectors step by 32
-            const int e0 = (int)(phase == 0 ? off / 2 : off * 2) + (vb + lane) * vec_elems;
-            int row = e0 / p.K;
-            int k = e0 - row * p.K;
-            const int step = 32 * vec_elems;
-            int cur = -1;
+          ok = __all_sync(0xffffffffu, ok);
+          const uint8_t* sw = ring + (size_t)st * kStageBytes;
+          const long long off = (long long)s * g.S;
+          const int bytes = (int)min((long long)g.S, pl.rbytes[phase] - off);
+          if (g.caseA) {
+            // this warp's slice lies inside one row: one partial per sequence
+            const int sb = warp * g.slice;
+            int row = -1, first = 0;
             float acc[kMM];
 #pragma unroll
             for (int m = 0; m < kMM; ++m) acc[m] = 0.0f;
-            for (int v = vb + lane; v < ve; v += 32, k += step) {
-              while (k >= p.K) {
-                k -= p.K;
-                ++row;
+            if (ok && sb < bytes) {
+              const long long ob = off + sb;
+              row = (int)(ob / g.rb);
+              const int kb = (int)(ob - (long long)row * g.rb);
+              first = kb == 0;
+              const int k0 = kb * esz_num / esz_den;
+              for (int v = lane; v < g.slice / 16; v += 32) {
+                const uint4 wv = *reinterpret_cast<const uint4*>(sw + sb + v * 16);
+                const int k = k0 + v * vec_elems;
+                float sc = 0.0f;
+                if (phase == 1)
+                  sc = pl.sc_staged
+                           ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(sw + kStageW)[(sb + v * 16) >> 6])
+                           : bf16_bits_to_float(__ldg(p.ws + (size_t)(pl.r0 + row) * p.sstride + k / EE_QUANT_GROUP));
+                vec_dot<XS>(phase, wv, sc, xrow, k, mc, acc);
               }
-              if (row != cur) {
-                if (cur >= 0) {
+            }
 #pragma unroll
-                  for (int m = 0; m < kMM; ++m)
-                    if (m < mc) atomicAdd(&rowsum[cur * pl.mcap + m], acc[m]);
-                }
-                cur = row;
-#pragma unroll
-                for (int m = 0; m < kMM; ++m) acc[m] = 0.0f;
+            for (int m = 0; m < kMM; ++m) {
+              if (m < mc) {
+                const float v = warp_sum(acc[m]);
+                if (lane == 0) slot[(buf * kConsumerWarps + warp) * kMM + m] = v;
               }
-              const uint4 wv = *reinterpret_cast<const uint4*>(sw + (size_t)v * 16);
-              if (phase == 0) {
+            }
+            if (lane == 0) slot_row[buf * kConsumerWarps + warp] = row >= 0 ? (row << 1) | first : -1;
+          } else if (ok) {
+            // this warp's slice is q whole rows: each row's sum is complete here
+            const int row0 = (int)(off / g.rb);
+            const int nrs = bytes / g.rb;
+            for (int rr = warp * g.q; rr < min(nrs, (warp + 1) * g.q); ++rr) {
+              float acc[kMM];
 #pragma unroll
-                for (int m = 0; m < kMM; ++m) {
-                  if (m < mc) {
-                    const uint4 xv = XS ? *reinterpret_cast<const uint4*>(xrow[m] + k) : ldg_nc_v4(xrow[m] + k);
-                    acc[m] = dot8_bf16(wv, xv, acc[m]);
-                  }
-                }
-              } else {
-                const float sc =
-                    pl.sc_staged
-                        ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(sw + kStageW)[v >> 2])
-                        : bf16_bits_to_float(__ldg(p.ws + (size_t)(pl.r0 + row) * p.sstride + k / EE_QUANT_GROUP));
+              for (int m = 0; m < kMM; ++m) acc[m] = 0.0f;
+              const int rbase = rr * g.rb;
+              for (int v = lane; v < g.rb / 16; v += 32) {
+                const uint4 wv = *reinterpret_cast<const uint4*>(sw + rbase + v * 16);
+                const int k = v * vec_elems;
+                float sc = 0.0f;
+                if (phase == 1)
+                  sc = pl.sc_staged
+                           ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(sw + kStageW)[(rbase + v * 16) >> 6])
+                           : bf16_bits_to_float(__ldg(p.ws + (size_t)(pl.r0 + row0 + rr) * p.sstride + k / EE_QUANT_GROUP));
+                vec_dot<XS>(phase, wv, sc, xrow, k, mc, acc);
+              }
 #pragma unroll
-                for (int m = 0; m < kMM; ++m) {
-                  if (m < mc) {
-                    const uint16_t* xp = xrow[m] + k;
-                    uint4 x0, x1, x2, x3;
-                    if (XS) {
-                      x0 = *reinterpret_cast<const uint4*>(xp);
-                      x1 = *reinterpret_cast<const uint4*>(xp + 8);
-                      x2 = *reinterpret_cast<const uint4*>(xp + 16);
-                      x3 = *reinterpret_cast<const uint4*>(xp + 24);
-                    } else {
-                      x0 = ldg_nc_v4(xp);
-                      x1 = ldg_nc_v4(xp + 8);
-                      x2 = ldg_nc_v4(xp + 16);
-                      x3 = ldg_nc_v4(xp + 24);
-                    }
-                    __half2 h = __float2half2_rn(0.0f);
-                    h = dot8_int4(wv.x, x0, h);
-                    h = dot8_int4(wv.y, x1, h);
-                    h = dot8_int4(wv.z, x2, h);
-                    h = dot8_int4(wv.w, x3, h);
-                    const float2 f = __half22float2(h);
-                    acc[m] = fmaf(sc, f.x + f.y, acc[m]);
-                  }
+              for (int m = 0; m < kMM; ++m) {
+                if (m < mc) {
+                  const float v = warp_sum(acc[m]);
+                  if (lane == 0) rowsum[(row0 + rr) * pl.mcap + m] = v;
                 }
               }
             }
-            flush_rows(rowsum, pl.mcap, mc, cur, acc, lane);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[st]);
+          consumer_bar();
+          if (g.caseA && warp == 0 && lane < mc) {
+            // fold the warps' partials into the row sums in a fixed order
+            for (int w = 0; w < kConsumerWarps; ++w) {
+              const int rf = slot_row[buf * kConsumerWarps + w];
+              if (rf < 0) continue;
+              float* dst = &rowsum[(rf >> 1) * pl.mcap + lane];
+              const float v = slot[(buf * kConsumerWarps + w) * kMM + lane];
+              *dst = (rf & 1) ? v : *dst + v;
+            }
+          }
         }
         consumer_bar();  // every row sum of this pass is complete
         if constexpr (EPI == EPI_HEAD) {
@@ -623,6 +698,11 @@ cudaError_t linear_prepare() {
   if ((e = set_smem_attr<EPI_SWIGLU>()) != cudaSuccess) return e;
   if ((e = set_smem_attr<EPI_X>()) != cudaSuccess) return e;
   return set_smem_attr<EPI_HEAD>();
+}
+
+bool linear_shape_ok(int K) {
+  if (K < 32 || K % 32) return false;
+  return geo_ok(make_geo(K * 2)) && geo_ok(make_geo(K / 2));
 }
 
 int linear_grid(int N, int num_sms) {
