@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
                        : p.xh + (size_t)seqs[m] * p.x_stride;
         }
         const Geo& g = pl.geo[phase];
-        const int esz_num = phase == 0 ? 1 : 4, esz_den = phase == 0 ? 2 : 1;  // elements = bytes * num / den
+        const int esz_num = phase == 0 ? 1 : 2, esz_den = phase == 0 ? 2 : 1;  // elements = bytes * num / den
         for (int s = 0; s < pl.nst[phase]; ++s, ++it) {
           const int st = it % nst;
           const int buf = it & 1;
