@@ -53,14 +53,12 @@ constexpr int kMM = 8;  // sequences per pass over the weights
 
 // Shared memory: header (barriers, lists, head statistics), the staged
 // activations (XS mode), the per-row sums [rows][mcap], then the ring.
-constexpr size_t kHeaderBytes = 2176;
+constexpr size_t kHeaderBytes = 1536;
 constexpr size_t kXsMaxBytes = 48 * 1024;
 constexpr size_t kSmemTarget = 112 * 1024;  // two CTAs per SM: the next kernel's CTA can prefetch
 constexpr size_t kSmemMax = 160 * 1024;  // attribute; every plan stays below it
 static_assert((2 * kMaxStages + 1) * 8 <= 128, "barriers");
-constexpr size_t kSlotOff = 1536;  // per-stage warp partials: [2][warps][kMM] floats, then [2][warps] row ids
-static_assert(128 + 2 * kListLen * 4 + 8 + kConsumerWarps * kMM * 3 * 4 <= kSlotOff, "header overflow");
-static_assert(kSlotOff + 2 * kConsumerWarps * kMM * 4 + 2 * kConsumerWarps * 4 <= kHeaderBytes, "slots");
+static_assert(128 + 2 * kListLen * 4 + 8 + kConsumerWarps * kMM * 3 * 4 <= kHeaderBytes, "header overflow");
 
 EE_DEV __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
@@ -183,49 +181,36 @@ __host__ __device__ inline size_t rowsum_bytes(int rows_cap, int mcap) {
   return ((size_t)rows_cap * mcap * 4 + 15) / 16 * 16;
 }
 
-// Stage geometry of one phase, aligned to rows of rb bytes so that each
-// warp's eighth of a stage ("slice") lies inside one row (case A: a row is
-// one or more whole stages, or a stage holds 1, 2 or 4 rows) or is made of q
-// whole rows (case B: small rows, a stage holds a multiple of 8 rows).
+// Stage geometry of one phase.  Rows of rb bytes are never split across
+// warps: row r of a CTA belongs to consumer warp r % 8.  A stage is either nr
+// whole rows (rb <= 16 KB) or one of nparts equal parts of a row (rb > 16 KB).
 struct Geo {
-  int rb;       // bytes per row
-  int S;        // bytes per full stage
-  bool caseA;
-  int slice;    // case A: bytes per warp slice (multiple of 16)
-  int q;        // case B: rows per warp slice
+  int rb;      // bytes per row
+  int S;       // bytes per full stage
+  int nr;      // whole rows per stage, or 0 when a stage is part of a row
+  int nparts;  // stages per row when nr == 0
 };
 
 __host__ __device__ inline Geo make_geo(int rb) {
   Geo g;
   g.rb = rb;
-  g.slice = 0;
-  g.q = 0;
-  if (rb >= kStageW) {
-    int n = (rb + kStageW - 1) / kStageW;
-    while (rb % (n * 128) != 0 && n < 64) ++n;
-    g.S = rb / n;
-    g.caseA = true;
-    g.slice = g.S / 8;
+  if (rb <= kStageW) {
+    g.nr = kStageW / rb;
+    g.nparts = 1;
+    g.S = g.nr * rb;
   } else {
-    int nr = kStageW / rb;
-    if (nr >= 8) {
-      nr -= nr % 8;
-      g.caseA = false;
-      g.q = nr / 8;
-    } else {
-      nr = nr >= 4 ? 4 : (nr >= 2 ? 2 : 1);
-      g.caseA = true;
-    }
-    g.S = nr * rb;
-    if (g.caseA) g.slice = g.S / 8;
+    int n = (rb + kStageW - 1) / kStageW;
+    while ((rb % n != 0 || (rb / n) % 16 != 0) && n < 64) ++n;
+    g.nr = 0;
+    g.nparts = n;
+    g.S = rb / n;
   }
   return g;
 }
 
 __host__ __device__ inline bool geo_ok(const Geo& g) {
-  if (g.S <= 0 || g.S > kStageW || g.S % 16) return false;
-  if (g.caseA) return g.slice % 16 == 0 && (g.rb % g.S == 0 || g.S % g.rb == 0);
-  return g.rb % 16 == 0;
+  return g.S > 0 && g.S <= kStageW && g.S % 16 == 0 && g.rb % 16 == 0 &&
+         (g.nr > 0 || g.S * g.nparts == g.rb);
 }
 
 // Per-CTA plan shared by the producer and the consumers.  Phase 0 streams
@@ -307,8 +292,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
   int32_t* lf = reinterpret_cast<int32_t*>(smem + 128);
   int32_t* le = lf + kListLen;
   float* hst = reinterpret_cast<float*>(smem + 128 + 2 * kListLen * 4 + 8);
-  float* slot = reinterpret_cast<float*>(smem + kSlotOff);
-  int32_t* slot_row = reinterpret_cast<int32_t*>(slot + 2 * kConsumerWarps * kMM);
   uint8_t* xs = smem + kHeaderBytes;
   float* rowsum = reinterpret_cast<float*>(xs + (XS ? (size_t)p.xs_rows * p.K * 2 : 0));
   uint8_t* ring = reinterpret_cast<uint8_t*>(rowsum) + rowsum_bytes(p.rows_cap, p.mcap);
@@ -408,7 +391,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
       const int nlist = phase == 0 ? nf : ne;
       const int32_t* lst = phase == 0 ? lf : le;
       const int xbase = phase == 0 ? 0 : nf;  // XS row of the phase's first sequence
-      const int vec_elems = phase == 0 ? 8 : 32;
       for (int pass = 0; pass < pl.passes[phase]; ++pass) {
         const int m0 = pass * pl.mcap;
         const int mc = min(pl.mcap, nlist - m0);
@@ -422,88 +404,78 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
                        : p.xh + (size_t)seqs[m] * p.x_stride;
         }
         const Geo& g = pl.geo[phase];
-        const int esz_num = phase == 0 ? 1 : 2, esz_den = phase == 0 ? 2 : 1;  // elements = bytes * num / den
+        const int epb = phase == 0 ? 1 : 4;  // elements per 2 bytes: bf16 1, int4 4
+        float acc[kMM];  // carried across the parts of a row longer than a stage
+#pragma unroll
+        for (int m = 0; m < kMM; ++m) acc[m] = 0.0f;
         for (int s = 0; s < pl.nst[phase]; ++s, ++it) {
           const int st = it % nst;
-          const int buf = it & 1;
+          // every warp waits for every stage, so that its arrival on the empty
+          // barrier below always belongs to this use of the stage
           if (ok) ok = mbar_wait_bounded(&full[st], (it / nst) & 1, p.err, DERR_FULL_WAIT);
           ok = __all_sync(0xffffffffu, ok);
           const uint8_t* sw = ring + (size_t)st * kStageBytes;
           const long long off = (long long)s * g.S;
           const int bytes = (int)min((long long)g.S, pl.rbytes[phase] - off);
-          if (g.caseA) {
-            // this warp's slice lies inside one row: one partial per sequence
-            const int sb = warp * g.slice;
-            int row = -1, first = 0;
-            float acc[kMM];
+          if (ok) {
+            if (g.nr > 0) {
+              const int row0 = s * g.nr, nrs = bytes / g.rb;
+              for (int rr = (warp - row0 % kConsumerWarps + kConsumerWarps) % kConsumerWarps; rr < nrs;
+                   rr += kConsumerWarps) {
+                const int row = row0 + rr;
+                const int rbase = rr * g.rb;
 #pragma unroll
-            for (int m = 0; m < kMM; ++m) acc[m] = 0.0f;
-            if (ok && sb < bytes) {
-              const long long ob = off + sb;
-              row = (int)(ob / g.rb);
-              const int kb = (int)(ob - (long long)row * g.rb);
-              first = kb == 0;
-              const int k0 = kb * esz_num / esz_den;
-              for (int v = lane; v < g.slice / 16; v += 32) {
-                const uint4 wv = *reinterpret_cast<const uint4*>(sw + sb + v * 16);
-                const int k = k0 + v * vec_elems;
-                float sc = 0.0f;
-                if (phase == 1)
-                  sc = pl.sc_staged
-                           ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(sw + kStageW)[(sb + v * 16) >> 6])
-                           : bf16_bits_to_float(__ldg(p.ws + (size_t)(pl.r0 + row) * p.sstride + k / EE_QUANT_GROUP));
-                vec_dot<XS>(phase, wv, sc, xrow, k, mc, acc);
+                for (int m = 0; m < kMM; ++m) acc[m] = 0.0f;
+                for (int v = lane; v < g.rb / 16; v += 32) {
+                  const uint4 wv = *reinterpret_cast<const uint4*>(sw + rbase + v * 16);
+                  const int k = v * 8 * epb;
+                  float sc = 0.0f;
+                  if (phase == 1)
+                    sc = pl.sc_staged
+                             ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(sw + kStageW)[(rbase + v * 16) >> 6])
+                             : bf16_bits_to_float(__ldg(p.ws + (size_t)(pl.r0 + row) * p.sstride + k / EE_QUANT_GROUP));
+                  vec_dot<XS>(phase, wv, sc, xrow, k, mc, acc);
+                }
+#pragma unroll
+                for (int m = 0; m < kMM; ++m) {
+                  if (m < mc) {
+                    const float t = warp_sum(acc[m]);
+                    if (lane == 0) rowsum[row * pl.mcap + m] = t;
+                  }
+                }
               }
-            }
+            } else {
+              const int row = s / g.nparts, part = s % g.nparts;
+              if (row % kConsumerWarps == warp) {
+                if (part == 0) {
 #pragma unroll
-            for (int m = 0; m < kMM; ++m) {
-              if (m < mc) {
-                const float v = warp_sum(acc[m]);
-                if (lane == 0) slot[(buf * kConsumerWarps + warp) * kMM + m] = v;
-              }
-            }
-            if (lane == 0) slot_row[buf * kConsumerWarps + warp] = row >= 0 ? (row << 1) | first : -1;
-          } else if (ok) {
-            // this warp's slice is q whole rows: each row's sum is complete here
-            const int row0 = (int)(off / g.rb);
-            const int nrs = bytes / g.rb;
-            for (int rr = warp * g.q; rr < min(nrs, (warp + 1) * g.q); ++rr) {
-              float acc[kMM];
+                  for (int m = 0; m < kMM; ++m) acc[m] = 0.0f;
+                }
+                const int kb = part * g.S;  // byte offset of the part within its row
+                for (int v = lane; v < bytes / 16; v += 32) {
+                  const uint4 wv = *reinterpret_cast<const uint4*>(sw + v * 16);
+                  const int k = (kb + v * 16) / 2 * epb;
+                  float sc = 0.0f;
+                  if (phase == 1)
+                    sc = pl.sc_staged
+                             ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(sw + kStageW)[(v * 16) >> 6])
+                             : bf16_bits_to_float(__ldg(p.ws + (size_t)(pl.r0 + row) * p.sstride + k / EE_QUANT_GROUP));
+                  vec_dot<XS>(phase, wv, sc, xrow, k, mc, acc);
+                }
+                if (part == g.nparts - 1) {
 #pragma unroll
-              for (int m = 0; m < kMM; ++m) acc[m] = 0.0f;
-              const int rbase = rr * g.rb;
-              for (int v = lane; v < g.rb / 16; v += 32) {
-                const uint4 wv = *reinterpret_cast<const uint4*>(sw + rbase + v * 16);
-                const int k = v * vec_elems;
-                float sc = 0.0f;
-                if (phase == 1)
-                  sc = pl.sc_staged
-                           ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(sw + kStageW)[(rbase + v * 16) >> 6])
-                           : bf16_bits_to_float(__ldg(p.ws + (size_t)(pl.r0 + row0 + rr) * p.sstride + k / EE_QUANT_GROUP));
-                vec_dot<XS>(phase, wv, sc, xrow, k, mc, acc);
-              }
-#pragma unroll
-              for (int m = 0; m < kMM; ++m) {
-                if (m < mc) {
-                  const float v = warp_sum(acc[m]);
-                  if (lane == 0) rowsum[(row0 + rr) * pl.mcap + m] = v;
+                  for (int m = 0; m < kMM; ++m) {
+                    if (m < mc) {
+                      const float t = warp_sum(acc[m]);
+                      if (lane == 0) rowsum[row * pl.mcap + m] = t;
+                    }
+                  }
                 }
               }
             }
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[st]);
-          consumer_bar();
-          if (g.caseA && warp == 0 && lane < mc) {
-            // fold the warps' partials into the row sums in a fixed order
-            for (int w = 0; w < kConsumerWarps; ++w) {
-              const int rf = slot_row[buf * kConsumerWarps + w];
-              if (rf < 0) continue;
-              float* dst = &rowsum[(rf >> 1) * pl.mcap + lane];
-              const float v = slot[(buf * kConsumerWarps + w) * kMM + lane];
-              *dst = (rf & 1) ? v : *dst + v;
-            }
-          }
         }
         consumer_bar();  // every row sum of this pass is complete
         if constexpr (EPI == EPI_HEAD) {
