@@ -97,6 +97,12 @@ EE_DEV void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes, uint6
       : "memory");
 }
 
+// Asks the memory system to bring `bytes` (multiple of 16, 16-byte aligned
+// address) of global memory into L2; nothing is written to shared memory.
+EE_DEV void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Programmatic dependent launch.  Every kernel of a step follows one rule:
 // it reads nothing a kernel before it wrote and writes nothing before
 // grid_dep_wait(), except data that the kernel two launches back or earlier

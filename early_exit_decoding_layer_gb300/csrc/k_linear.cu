@@ -8,21 +8,18 @@
 // group of 128 input columns, dequantised in registers and never written
 // back).  An empty list reads no byte of its matrix.
 //
-// Data flow per CTA (persistent, one per SM): each CTA owns a contiguous,
-// pair-aligned range of output rows, which is one contiguous byte range of the
-// row-major weights.  Warp 8's lane 0 streams that range through a ring of
-// shared-memory stages, each filled by ONE 16 KB bulk asynchronous copy
-// (cp.async.bulk, completion counted on an mbarrier, L2 evict-first; plus one
-// 512-byte copy of the stage's int4 scales): the copy engine reaches HBM peak
-// only with large requests (1 KB requests stall near 2.5 TB/s on GB300).  The
-// weights of the first stages are requested before the grid dependency wait,
-// so they stream while the previous kernel finishes; the activations of the
-// step's rows (fp16, a few KB per sequence) are bulk-copied into shared memory
-// after it.  Warps 0-7 consume: each takes an eighth of a stage, maps every
-// 16-byte vector back to (row, column), accumulates per row in registers and
-// adds each row's partial into per-row sums in shared memory (one warp
-// reduction when the warp's slice lies in one row).  The epilogue (RoPE + KV
-// write, SwiGLU, residual add, head statistics) runs once over the CTA's rows.
+// Data flow: one CTA of 8 warps per SM owns a balanced, pair-aligned range of
+// output rows; warp w owns the CTA's rows w, w+8, ... and streams each of them
+// with coalesced 16-byte loads (a warp reads 512 contiguous bytes per load
+// instruction) straight into registers, double-buffered in batches of 8
+// vectors per lane so that 16 loads per lane (64 KB per SM) are in flight --
+// what the HBM needs to run at peak.  The first batch is requested before the
+// grid dependency wait (weights never change), so the stream starts while the
+// previous kernel drains; the activations of the step's rows (fp16, a few KB
+// per sequence), written by that kernel, are copied into shared memory after
+// the wait.  A warp finishes each of its rows alone (one warp reduction), so
+// results do not depend on timing.  The epilogue (RoPE + KV write, SwiGLU,
+// residual add, head statistics) runs once over the CTA's rows.
 //
 // Activations are stored in "pair order" (within each run of 8 columns:
 // 0,4,1,5,2,6,3,7, see xh_slot) so that one 16-byte load yields the half2
@@ -42,23 +39,18 @@ namespace ee {
 
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;
-constexpr int kStageW = 16384;  // weight bytes per stage: one bulk copy
-constexpr int kStageS = 512;    // int4 scale bytes per stage (16 KB of nibbles = 256 groups)
-constexpr int kStageBytes = kStageW + kStageS;
-constexpr int kMaxStages = 6;
-constexpr int kMM = 8;  // sequences per pass over the weights
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kBatch = 8;  // 16-byte vectors per lane per batch (two batches in flight)
+constexpr int kMM = 8;     // sequences per pass over the weights
+constexpr size_t kPrefetchBytes = 128 * 1024;  // weights pulled into L2 before the dependency wait
 
-// Shared memory: header (barriers, lists, head statistics), the staged
-// activations (XS mode), the per-row sums [rows][mcap], then the ring.
+// Shared memory: header (lists, head statistics), the staged activations
+// (XS mode), then the per-row sums [rows][mcap].
 constexpr size_t kHeaderBytes = 1536;
-constexpr size_t kXsMaxBytes = 48 * 1024;
-constexpr size_t kSmemTarget = 112 * 1024;  // two CTAs per SM: the next kernel's CTA can prefetch
-constexpr size_t kSmemMax = 160 * 1024;  // attribute; every plan stays below it
-static_assert((2 * kMaxStages + 1) * 8 <= 128, "barriers");
-static_assert(128 + 2 * kListLen * 4 + 8 + kConsumerWarps * kMM * 3 * 4 <= kHeaderBytes, "header overflow");
+constexpr size_t kXsMaxBytes = 64 * 1024;
+constexpr size_t kSmemMax = 120 * 1024;
+static_assert(2 * kListLen * 4 + 16 + kWarps * kMM * 3 * 4 <= kHeaderBytes, "header overflow");
 
 EE_DEV __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
@@ -173,90 +165,59 @@ EE_DEV Stat stat_merge(Stat a, Stat b) {
   return r;
 }
 
-EE_DEV void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory"); }
-
-// Bytes of the per-row sums, rounded up so that the ring behind them starts on
-// a 16-byte boundary (bulk copies need it).
-__host__ __device__ inline size_t rowsum_bytes(int rows_cap, int mcap) {
-  return ((size_t)rows_cap * mcap * 4 + 15) / 16 * 16;
+EE_DEV uint16_t ldg_u16(const uint16_t* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
 }
 
-// Stage geometry of one phase.  Rows of rb bytes are never split across
-// warps: row r of a CTA belongs to consumer warp r % 8.  A stage is either nr
-// whole rows (rb <= 16 KB) or one of nparts equal parts of a row (rb > 16 KB).
-struct Geo {
-  int rb;      // bytes per row
-  int S;       // bytes per full stage
-  int nr;      // whole rows per stage, or 0 when a stage is part of a row
-  int nparts;  // stages per row when nr == 0
-};
-
-__host__ __device__ inline Geo make_geo(int rb) {
-  Geo g;
-  g.rb = rb;
-  if (rb <= kStageW) {
-    g.nr = kStageW / rb;
-    g.nparts = 1;
-    g.S = g.nr * rb;
-  } else {
-    int n = (rb + kStageW - 1) / kStageW;
-    while ((rb % n != 0 || (rb / n) % 16 != 0) && n < 64) ++n;
-    g.nr = 0;
-    g.nparts = n;
-    g.S = rb / n;
-  }
-  return g;
-}
-
-__host__ __device__ inline bool geo_ok(const Geo& g) {
-  return g.S > 0 && g.S <= kStageW && g.S % 16 == 0 && g.rb % 16 == 0 &&
-         (g.nr > 0 || g.S * g.nparts == g.rb);
-}
-
-// Per-CTA plan shared by the producer and the consumers.  Phase 0 streams
-// the bf16 rows [r0, r1) (K*2 bytes each), phase 1 their int4 copy (K/2
-// bytes each); each phase runs one pass per group of at most mcap sequences.
 struct Plan {
   int r0, r1, mcap;
-  int nst[2], passes[2];
-  long long rbytes[2];
-  Geo geo[2];
-  bool sc_staged;  // int4 scales stream with the weights (one 16-byte-aligned slice per stage)
+  int passes[2];
 };
 
-EE_DEV void issue_stage(const LinearParams& p, const Plan& pl, int phase, int s, uint8_t* sbase,
-                        uint64_t* bar, uint64_t pol) {
-  const long long S = pl.geo[phase].S;
-  const long long off = (long long)s * S;
-  const uint32_t bytes = (uint32_t)min(S, pl.rbytes[phase] - off);
-  if (phase == 0) {
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_g2s(sbase, reinterpret_cast<const uint8_t*>(p.w + (size_t)pl.r0 * p.K) + off, bytes, bar, pol);
-  } else {
-    const uint32_t sb = pl.sc_staged ? bytes / 32 : 0;  // one bf16 scale per 64 bytes of nibbles
-    mbar_arrive_expect_tx(bar, bytes + sb);
-    bulk_g2s(sbase, p.wq + (size_t)pl.r0 * (p.K / 2) + off, bytes, bar, pol);
-    if (sb)
-      bulk_g2s(sbase + kStageW, p.ws + (size_t)pl.r0 * p.sstride + (size_t)(off / 64), sb, bar, pol);
+// Loads one batch of this warp's stream: positions base + 32 j + lane
+// (j < kBatch) of the concatenation of the warp's rows, nv vectors each
+// (nv % 32 == 0, so the 32 positions of one j lie in one row).
+template <int PH>
+EE_DEV void load_batch(const LinearParams& p, const Plan& pl, int warp, int lane, int nv, int total,
+                       int base, uint4* buf, uint16_t* sbuf) {
+  const size_t rstride = PH == 0 ? (size_t)p.K * 2 : (size_t)p.K / 2;
+  const uint8_t* wbase = PH == 0 ? reinterpret_cast<const uint8_t*>(p.w) : p.wq;
+  int ri = base / nv;
+  int v = base - ri * nv + lane;
+#pragma unroll
+  for (int j = 0; j < kBatch; ++j) {
+    if (base + 32 * j < total) {
+      const int row = pl.r0 + warp + kWarps * ri;
+      buf[j] = ldg_nc_v4(wbase + (size_t)row * rstride + (size_t)v * 16);
+      if (PH == 1) sbuf[j] = ldg_u16(p.ws + (size_t)row * p.sstride + (v >> 2));
+    } else {
+      buf[j] = make_uint4(0, 0, 0, 0);
+      if (PH == 1) sbuf[j] = 0;
+    }
+    v += 32;
+    if (v >= nv) {
+      v -= nv;
+      ++ri;
+    }
   }
 }
 
-// Dot products of one stage vector (16 bytes of weights) with the mc
-// activation rows at column k, accumulated into acc[m].
-template <bool XS>
-EE_DEV void vec_dot(int phase, const uint4& wv, float sc, const uint16_t* const* xrow, int k, int mc,
-                    float* acc) {
-  if (phase == 0) {
+template <int PH, bool XS, int MMAX>
+EE_DEV void dot_vec(const uint4& wv, uint16_t sbits, const uint16_t* const* xrow, int k, int mc, float* acc) {
+  if (PH == 0) {
 #pragma unroll
-    for (int m = 0; m < kMM; ++m) {
+    for (int m = 0; m < MMAX; ++m) {
       if (m < mc) {
         const uint4 xv = XS ? *reinterpret_cast<const uint4*>(xrow[m] + k) : ldg_nc_v4(xrow[m] + k);
         acc[m] = dot8_bf16(wv, xv, acc[m]);
       }
     }
   } else {
+    const float sc = bf16_bits_to_float(sbits);
 #pragma unroll
-    for (int m = 0; m < kMM; ++m) {
+    for (int m = 0; m < MMAX; ++m) {
       if (m < mc) {
         const uint16_t* xp = xrow[m] + k;
         uint4 x0, x1, x2, x3;
@@ -283,30 +244,97 @@ EE_DEV void vec_dot(int phase, const uint4& wv, float sc, const uint16_t* const*
   }
 }
 
-template <int EPI, bool XS>
-__global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
+template <int MMAX>
+EE_DEV void flush_row(float* rowsum, int mcap, int row_local, int mc, float* acc, int lane) {
+#pragma unroll
+  for (int m = 0; m < MMAX; ++m) {
+    if (m < mc) {
+      const float t = warp_sum(acc[m]);
+      if (lane == 0) rowsum[row_local * mcap + m] = t;
+    }
+    acc[m] = 0.0f;
+  }
+}
+
+template <int PH, bool XS, int MMAX>
+EE_DEV void compute_batch(const uint4* w, const uint16_t* sc, int base, int total, int nv, int epv,
+                          int& cur, const uint16_t* const* xrow, int mc, float* acc, float* rowsum,
+                          int mcap, int warp, int lane) {
+  int ri = base / nv;
+  int v0 = base - ri * nv;  // warp-uniform vector index of lane 0
+#pragma unroll
+  for (int j = 0; j < kBatch; ++j) {
+    if (base + 32 * j < total) {
+      if (ri != cur) {
+        flush_row<MMAX>(rowsum, mcap, warp + kWarps * cur, mc, acc, lane);
+        cur = ri;
+      }
+      dot_vec<PH, XS, MMAX>(w[j], sc[j], xrow, (v0 + lane) * epv, mc, acc);
+    }
+    v0 += 32;
+    if (v0 >= nv) {
+      v0 -= nv;
+      ++ri;
+    }
+  }
+}
+
+// Streams this warp's rows of one phase (PH 0: bf16 weights, 1: int4) for
+// the mc sequences of one pass and writes each row's sums into rowsum.
+template <int PH, bool XS, int MMAX>
+EE_DEV void stream_rows(const LinearParams& p, const Plan& pl, int warp, int lane, int mc,
+                        const uint16_t* const* xrow, float* rowsum) {
+  const int nrows = pl.r1 - pl.r0;
+  const int nrw = nrows > warp ? (nrows - warp + kWarps - 1) / kWarps : 0;  // rows of this warp
+  const int nv = PH == 0 ? p.K / 8 : p.K / 32;                             // vectors per row
+  const int epv = PH == 0 ? 8 : 32;                                        // elements per vector
+  float acc[MMAX];
+#pragma unroll
+  for (int m = 0; m < MMAX; ++m) acc[m] = 0.0f;
+  if (nv % 32 == 0) {
+    // 32 consecutive positions of the warp's stream lie in one row
+    const int total = nrw * nv;
+    const int bstep = 32 * kBatch;
+    uint4 a[kBatch], b[kBatch];
+    uint16_t sa[kBatch], sb[kBatch];
+    load_batch<PH>(p, pl, warp, lane, nv, total, 0, a, sa);
+    int cur = 0;
+    for (int base = 0; base < total; base += 2 * bstep) {
+      if (base + bstep < total) load_batch<PH>(p, pl, warp, lane, nv, total, base + bstep, b, sb);
+      compute_batch<PH, XS, MMAX>(a, sa, base, total, nv, epv, cur, xrow, mc, acc, rowsum, pl.mcap, warp, lane);
+      if (base + 2 * bstep < total) load_batch<PH>(p, pl, warp, lane, nv, total, base + 2 * bstep, a, sa);
+      if (base + bstep < total)
+        compute_batch<PH, XS, MMAX>(b, sb, base + bstep, total, nv, epv, cur, xrow, mc, acc, rowsum, pl.mcap,
+                                    warp, lane);
+    }
+    if (nrw > 0) flush_row<MMAX>(rowsum, pl.mcap, warp + kWarps * cur, mc, acc, lane);
+  } else {
+    // short or odd rows: one row at a time, lanes stride over its vectors
+    const size_t rstride = PH == 0 ? (size_t)p.K * 2 : (size_t)p.K / 2;
+    const uint8_t* wbase = PH == 0 ? reinterpret_cast<const uint8_t*>(p.w) : p.wq;
+    for (int ri = 0; ri < nrw; ++ri) {
+      const int row = pl.r0 + warp + kWarps * ri;
+      for (int v = lane; v < nv; v += 32) {
+        const uint4 wv = ldg_nc_v4(wbase + (size_t)row * rstride + (size_t)v * 16);
+        const uint16_t sbits = PH == 1 ? ldg_u16(p.ws + (size_t)row * p.sstride + (v >> 2)) : 0;
+        dot_vec<PH, XS, MMAX>(wv, sbits, xrow, v * epv, mc, acc);
+      }
+      flush_row<MMAX>(rowsum, pl.mcap, warp + kWarps * ri, mc, acc, lane);
+    }
+  }
+}
+
+template <int EPI, bool XS, int MMAX>
+__global__ void __launch_bounds__(kThreads, MMAX == 1 ? 2 : 1) k_linear(const LinearParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + kMaxStages;
-  uint64_t* xbar = empty + kMaxStages;
-  int32_t* lf = reinterpret_cast<int32_t*>(smem + 128);
+  int32_t* lf = reinterpret_cast<int32_t*>(smem);
   int32_t* le = lf + kListLen;
-  float* hst = reinterpret_cast<float*>(smem + 128 + 2 * kListLen * 4 + 8);
+  float* hst = reinterpret_cast<float*>(smem + 2 * kListLen * 4 + 16);
   uint8_t* xs = smem + kHeaderBytes;
   float* rowsum = reinterpret_cast<float*>(xs + (XS ? (size_t)p.xs_rows * p.K * 2 : 0));
-  uint8_t* ring = reinterpret_cast<uint8_t*>(rowsum) + rowsum_bytes(p.rows_cap, p.mcap);
-  const int nst = p.nstages;
   __shared__ int s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0) {
-    for (int s = 0; s < nst; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
-    }
-    mbar_init(xbar, 1);
-    fence_mbar_init();
-  }
   // Lists were written at least two launches back (see grid_dep_wait), so
   // they may be read before this grid's dependency wait.
   if (tid < kListLen) {
@@ -324,210 +352,114 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
     pl.r0 = 2 * (int)(((long long)blockIdx.x * npairs) / gridDim.x);
     pl.r1 = 2 * (int)(((long long)(blockIdx.x + 1) * npairs) / gridDim.x);
     pl.mcap = p.mcap;
-    pl.geo[0] = make_geo(p.K * 2);
-    pl.geo[1] = make_geo(p.K / 2);
-    pl.rbytes[0] = (long long)(pl.r1 - pl.r0) * p.K * 2;
-    pl.rbytes[1] = (long long)(pl.r1 - pl.r0) * (p.K / 2);
-    pl.nst[0] = (int)((pl.rbytes[0] + pl.geo[0].S - 1) / pl.geo[0].S);
-    pl.nst[1] = (int)((pl.rbytes[1] + pl.geo[1].S - 1) / pl.geo[1].S);
     pl.passes[0] = (nf + pl.mcap - 1) / pl.mcap;
     pl.passes[1] = (ne + pl.mcap - 1) / pl.mcap;
-    pl.sc_staged = (p.K % 512 == 0) && (p.sstride * EE_QUANT_GROUP == p.K) && (pl.geo[1].S % 512 == 0);
   }
+  const int nrows = pl.r1 - pl.r0;
 
-  if (warp == kConsumerWarps) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint64_t pol = l2_evict_first_policy();
-      const uint32_t total =
-          (uint32_t)(pl.passes[0] * pl.nst[0] + pl.passes[1] * pl.nst[1]);
-      const uint32_t prefill = total < (uint32_t)nst ? total : (uint32_t)nst;
-      bool xdone = !XS;
-      auto stage_x = [&]() {
-        // activations are written by the previous kernel: copy them after the wait
-        grid_dep_wait();
-        if (nx > 0) {
-          const uint32_t rb = (uint32_t)p.K * 2;
-          mbar_arrive_expect_tx(xbar, nx * rb);
-          for (int m = 0; m < nx; ++m) {
-            const int seq = m < nf ? lf[1 + m] : le[1 + m - nf];
-            bulk_g2s(xs + (size_t)m * rb, p.xh + (size_t)seq * p.x_stride, rb, xbar, pol);
-          }
-        }
-        xdone = true;
-      };
-      uint32_t it = 0;
-      bool ok = true;
-      for (int phase = 0; phase < 2 && ok; ++phase) {
-        for (int pass = 0; pass < pl.passes[phase] && ok; ++pass) {
-          for (int s = 0; s < pl.nst[phase]; ++s, ++it) {
-            if (!xdone && it == prefill) stage_x();
-            const int st = it % nst;
-            const uint32_t n = it / nst;
-            if (n > 0 && !mbar_wait_bounded(&empty[st], (n - 1) & 1, p.err, DERR_EMPTY_WAIT)) {
-              ok = false;
-              break;
-            }
-            issue_stage(p, pl, phase, s, ring + (size_t)st * kStageBytes, &full[st], pol);
-          }
-        }
+  // Weights do not depend on the previous kernel: pull the start of this
+  // CTA's rows into L2 now, while that kernel drains.
+  if (tid == 0) {
+    const int ph = pl.passes[0] > 0 ? 0 : (pl.passes[1] > 0 ? 1 : -1);
+    if (ph >= 0) {
+      const size_t rb = ph == 0 ? (size_t)p.K * 2 : (size_t)p.K / 2;
+      const uint8_t* base = (ph == 0 ? reinterpret_cast<const uint8_t*>(p.w) : p.wq) + (size_t)pl.r0 * rb;
+      const size_t total = (size_t)nrows * rb;
+      const size_t want = total < kPrefetchBytes ? total : kPrefetchBytes;
+      for (size_t o = 0; o < want; o += 16384) {
+        const uint32_t n = (uint32_t)((want - o) < 16384 ? (want - o) : 16384);
+        prefetch_l2(base + o, n);
       }
-      if (!xdone) stage_x();
-      // every copy this thread issued lands before the CTA may exit
-      const uint32_t j0 = it > (uint32_t)nst ? it - nst : 0;
-      for (uint32_t j = j0; j < it; ++j)
-        mbar_wait_bounded(&full[j % nst], (j / nst) & 1, p.err, DERR_DRAIN_WAIT);
-      if (XS && nx > 0) mbar_wait_bounded(xbar, 0, p.err, DERR_DRAIN_WAIT);
     }
-  } else {
-    // ------------------------------------------------------------ consumers
-    grid_dep_wait();
-    grid_dep_launch();
-    bool ok = true;
-    if (XS && nx > 0) ok = mbar_wait_bounded(xbar, 0, p.err, DERR_FULL_WAIT);
-    const int nrows = pl.r1 - pl.r0;
-    uint32_t it = 0;
-    for (int phase = 0; phase < 2; ++phase) {
-      const int nlist = phase == 0 ? nf : ne;
-      const int32_t* lst = phase == 0 ? lf : le;
-      const int xbase = phase == 0 ? 0 : nf;  // XS row of the phase's first sequence
-      for (int pass = 0; pass < pl.passes[phase]; ++pass) {
-        const int m0 = pass * pl.mcap;
-        const int mc = min(pl.mcap, nlist - m0);
-        int seqs[kMM];
-        const uint16_t* xrow[kMM];
+  }
+  grid_dep_wait();
+  grid_dep_launch();
+  if (XS && nx > 0) {
+    // the activations of the step's rows, written by the previous kernel
+    const int v16 = p.K / 8;  // 16-byte vectors per row
+    for (int i = tid; i < nx * v16; i += kThreads) {
+      const int m = i / v16, c = i - m * v16;
+      const int seq = m < nf ? lf[1 + m] : le[1 + m - nf];
+      reinterpret_cast<uint4*>(xs)[i] = *reinterpret_cast<const uint4*>(p.xh + (size_t)seq * p.x_stride + c * 8);
+    }
+  }
+  __syncthreads();
+
+  for (int phase = 0; phase < 2; ++phase) {
+    const int nlist = phase == 0 ? nf : ne;
+    const int32_t* lst = phase == 0 ? lf : le;
+    const int xbase = phase == 0 ? 0 : nf;  // XS row of the phase's first sequence
+    for (int pass = 0; pass < pl.passes[phase]; ++pass) {
+      const int m0 = pass * pl.mcap;
+      const int mc = min(pl.mcap, nlist - m0);
+      const uint16_t* xrow[MMAX];
 #pragma unroll
-        for (int m = 0; m < kMM; ++m) {
-          const int mm = min(m, mc - 1);
-          seqs[m] = lst[1 + m0 + mm];
-          xrow[m] = XS ? reinterpret_cast<const uint16_t*>(xs) + (size_t)(xbase + m0 + mm) * p.K
-                       : p.xh + (size_t)seqs[m] * p.x_stride;
-        }
-        const Geo& g = pl.geo[phase];
-        const int epb = phase == 0 ? 1 : 4;  // elements per 2 bytes: bf16 1, int4 4
-        float acc[kMM];  // carried across the parts of a row longer than a stage
-#pragma unroll
-        for (int m = 0; m < kMM; ++m) acc[m] = 0.0f;
-        for (int s = 0; s < pl.nst[phase]; ++s, ++it) {
-          const int st = it % nst;
-          // every warp waits for every stage, so that its arrival on the empty
-          // barrier below always belongs to this use of the stage
-          if (ok) ok = mbar_wait_bounded(&full[st], (it / nst) & 1, p.err, DERR_FULL_WAIT);
-          ok = __all_sync(0xffffffffu, ok);
-          const uint8_t* sw = ring + (size_t)st * kStageBytes;
-          const long long off = (long long)s * g.S;
-          const int bytes = (int)min((long long)g.S, pl.rbytes[phase] - off);
-          if (ok) {
-            if (g.nr > 0) {
-              const int row0 = s * g.nr, nrs = bytes / g.rb;
-              for (int rr = (warp - row0 % kConsumerWarps + kConsumerWarps) % kConsumerWarps; rr < nrs;
-                   rr += kConsumerWarps) {
-                const int row = row0 + rr;
-                const int rbase = rr * g.rb;
-#pragma unroll
-                for (int m = 0; m < kMM; ++m) acc[m] = 0.0f;
-                for (int v = lane; v < g.rb / 16; v += 32) {
-                  const uint4 wv = *reinterpret_cast<const uint4*>(sw + rbase + v * 16);
-                  const int k = v * 8 * epb;
-                  float sc = 0.0f;
-                  if (phase == 1)
-                    sc = pl.sc_staged
-                             ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(sw + kStageW)[(rbase + v * 16) >> 6])
-                             : bf16_bits_to_float(__ldg(p.ws + (size_t)(pl.r0 + row) * p.sstride + k / EE_QUANT_GROUP));
-                  vec_dot<XS>(phase, wv, sc, xrow, k, mc, acc);
-                }
-#pragma unroll
-                for (int m = 0; m < kMM; ++m) {
-                  if (m < mc) {
-                    const float t = warp_sum(acc[m]);
-                    if (lane == 0) rowsum[row * pl.mcap + m] = t;
-                  }
-                }
-              }
-            } else {
-              const int row = s / g.nparts, part = s % g.nparts;
-              if (row % kConsumerWarps == warp) {
-                if (part == 0) {
-#pragma unroll
-                  for (int m = 0; m < kMM; ++m) acc[m] = 0.0f;
-                }
-                const int kb = part * g.S;  // byte offset of the part within its row
-                for (int v = lane; v < bytes / 16; v += 32) {
-                  const uint4 wv = *reinterpret_cast<const uint4*>(sw + v * 16);
-                  const int k = (kb + v * 16) / 2 * epb;
-                  float sc = 0.0f;
-                  if (phase == 1)
-                    sc = pl.sc_staged
-                             ? bf16_bits_to_float(reinterpret_cast<const uint16_t*>(sw + kStageW)[(v * 16) >> 6])
-                             : bf16_bits_to_float(__ldg(p.ws + (size_t)(pl.r0 + row) * p.sstride + k / EE_QUANT_GROUP));
-                  vec_dot<XS>(phase, wv, sc, xrow, k, mc, acc);
-                }
-                if (part == g.nparts - 1) {
-#pragma unroll
-                  for (int m = 0; m < kMM; ++m) {
-                    if (m < mc) {
-                      const float t = warp_sum(acc[m]);
-                      if (lane == 0) rowsum[row * pl.mcap + m] = t;
-                    }
-                  }
-                }
-              }
-            }
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[st]);
-        }
-        consumer_bar();  // every row sum of this pass is complete
-        if constexpr (EPI == EPI_HEAD) {
-          Stat stat[kMM];
-#pragma unroll
-          for (int m = 0; m < kMM; ++m) stat[m] = Stat{-INFINITY, 0.0f, 0x7fffffff};
-          for (int r = tid; r < nrows; r += kConsumers) {
-#pragma unroll
-            for (int m = 0; m < kMM; ++m)
-              if (m < mc) stat_push(stat[m], rowsum[r * pl.mcap + m], pl.r0 + r);
-          }
-#pragma unroll
-          for (int m = 0; m < kMM; ++m) {
-            if (m < mc) {
-#pragma unroll
-              for (int o = 16; o > 0; o >>= 1) {
-                Stat t;
-                t.mx = __shfl_xor_sync(0xffffffffu, stat[m].mx, o);
-                t.sum = __shfl_xor_sync(0xffffffffu, stat[m].sum, o);
-                t.arg = __shfl_xor_sync(0xffffffffu, stat[m].arg, o);
-                stat[m] = stat_merge(stat[m], t);
-              }
-              if (lane == 0) {
-                float* hs = hst + (warp * kMM + m) * 3;
-                hs[0] = stat[m].mx;
-                hs[1] = stat[m].sum;
-                hs[2] = __int_as_float(stat[m].arg);
-              }
-            }
-          }
-          consumer_bar();
-          if (warp == 0 && lane < mc) {
-            Stat sm = {-INFINITY, 0.0f, 0x7fffffff};
-            for (int w = 0; w < kConsumerWarps; ++w) {
-              const float* hs = hst + (w * kMM + lane) * 3;
-              sm = stat_merge(sm, Stat{hs[0], hs[1], __float_as_int(hs[2])});
-            }
-            float* dst = p.head_part + ((size_t)blockIdx.x * EE_MAX_BATCH + m0 + lane) * 4;
-            dst[0] = sm.mx;
-            dst[1] = sm.sum;
-            dst[2] = __int_as_float(sm.arg);
-          }
-        } else {
-          const int npr = nrows >> 1;
-          for (int i = tid; i < npr * mc; i += kConsumers) {
-            const int pr = i / mc, m = i - pr * mc;
-            epi_pair<EPI>(p, seqs[m], pl.r0 + 2 * pr, rowsum[(2 * pr) * pl.mcap + m],
-                          rowsum[(2 * pr + 1) * pl.mcap + m]);
-          }
-        }
-        consumer_bar();  // row sums are reused by the next pass
+      for (int m = 0; m < MMAX; ++m) {
+        const int mm = min(m, mc - 1);
+        xrow[m] = XS ? reinterpret_cast<const uint16_t*>(xs) + (size_t)(xbase + m0 + mm) * p.K
+                     : p.xh + (size_t)lst[1 + m0 + mm] * p.x_stride;
       }
+      if (phase == 0)
+        stream_rows<0, XS, MMAX>(p, pl, warp, lane, mc, xrow, rowsum);
+      else
+        stream_rows<1, XS, MMAX>(p, pl, warp, lane, mc, xrow, rowsum);
+      __syncthreads();  // every row sum of this pass is complete
+      if constexpr (EPI == EPI_HEAD) {
+        Stat stat[MMAX];
+#pragma unroll
+        for (int m = 0; m < MMAX; ++m) stat[m] = Stat{-INFINITY, 0.0f, 0x7fffffff};
+        for (int r = tid; r < nrows; r += kThreads) {
+#pragma unroll
+          for (int m = 0; m < MMAX; ++m)
+            if (m < mc) stat_push(stat[m], rowsum[r * pl.mcap + m], pl.r0 + r);
+        }
+#pragma unroll
+        for (int m = 0; m < MMAX; ++m) {
+          if (m < mc) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              Stat t;
+              t.mx = __shfl_xor_sync(0xffffffffu, stat[m].mx, o);
+              t.sum = __shfl_xor_sync(0xffffffffu, stat[m].sum, o);
+              t.arg = __shfl_xor_sync(0xffffffffu, stat[m].arg, o);
+              stat[m] = stat_merge(stat[m], t);
+            }
+            if (lane == 0) {
+              float* hs = hst + (warp * kMM + m) * 3;
+              hs[0] = stat[m].mx;
+              hs[1] = stat[m].sum;
+              hs[2] = __int_as_float(stat[m].arg);
+            }
+          }
+        }
+        __syncthreads();
+        if (warp == 0 && lane < mc) {
+          Stat sm = {-INFINITY, 0.0f, 0x7fffffff};
+          for (int w = 0; w < kWarps; ++w) {
+            const float* hs = hst + (w * kMM + lane) * 3;
+            sm = stat_merge(sm, Stat{hs[0], hs[1], __float_as_int(hs[2])});
+          }
+          float* dst = p.head_part + ((size_t)blockIdx.x * EE_MAX_BATCH + m0 + lane) * 4;
+          dst[0] = sm.mx;
+          dst[1] = sm.sum;
+          dst[2] = __int_as_float(sm.arg);
+        }
+      } else {
+        int seqs_m[MMAX];
+#pragma unroll
+        for (int m = 0; m < MMAX; ++m) seqs_m[m] = lst[1 + m0 + min(m, mc - 1)];
+        const int npr = nrows >> 1;
+        for (int i = tid; i < npr * mc; i += kThreads) {
+          const int pr = i / mc, m = i - pr * mc;
+          int seq = seqs_m[0];
+#pragma unroll
+          for (int mm = 1; mm < MMAX; ++mm)
+            if (mm == m) seq = seqs_m[mm];
+          epi_pair<EPI>(p, seq, pl.r0 + 2 * pr, rowsum[(2 * pr) * pl.mcap + m],
+                        rowsum[(2 * pr + 1) * pl.mcap + m]);
+        }
+      }
+      __syncthreads();  // row sums are reused by the next pass
     }
   }
 
@@ -544,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
     __threadfence();
     float* res = hst;  // reuse: [m] (conf, argmax)
     const int nrows = nf;
-    for (int m = warp; m < nrows; m += kConsumerWarps + 1) {
+    for (int m = warp; m < nrows; m += kWarps) {
       Stat s = {-INFINITY, 0.0f, 0x7fffffff};
       for (int c = lane; c < (int)gridDim.x; c += 32) {
         const float* src = p.head_part + ((size_t)c * EE_MAX_BATCH + m) * 4;
@@ -606,10 +538,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
 
 template <int EPI>
 cudaError_t set_smem_attr() {
-  cudaError_t e = cudaFuncSetAttribute(k_linear<EPI, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemMax);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_linear<EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax);
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(k_linear<EPI, false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kSmemMax)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(k_linear<EPI, true, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kSmemMax)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(k_linear<EPI, false, kMM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kSmemMax)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(k_linear<EPI, true, kMM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)kSmemMax);
+}
+
+size_t smem_of(const LinearParams& p) {
+  return kHeaderBytes + (p.xs_rows > 0 ? (size_t)p.xs_rows * p.K * 2 : 0) + (size_t)p.rows_cap * p.mcap * 4;
 }
 
 template <int EPI>
@@ -617,50 +561,37 @@ cudaError_t launch_one(const LinearParams& p, int grid, bool pdl, cudaStream_t s
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kHeaderBytes + (p.xs_rows > 0 ? (size_t)p.xs_rows * p.K * 2 : 0) +
-                         rowsum_bytes(p.rows_cap, p.mcap) + (size_t)p.nstages * kStageBytes;
+  cfg.dynamicSmemBytes = smem_of(p);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (p.xs_rows > 0) return cudaLaunchKernelEx(&cfg, k_linear<EPI, true>, p);
-  return cudaLaunchKernelEx(&cfg, k_linear<EPI, false>, p);
+  if (p.mcap == 1) {
+    if (p.xs_rows > 0) return cudaLaunchKernelEx(&cfg, k_linear<EPI, true, 1>, p);
+    return cudaLaunchKernelEx(&cfg, k_linear<EPI, false, 1>, p);
+  }
+  if (p.xs_rows > 0) return cudaLaunchKernelEx(&cfg, k_linear<EPI, true, kMM>, p);
+  return cudaLaunchKernelEx(&cfg, k_linear<EPI, false, kMM>, p);
+}
+
+// Shared-memory plan of one launch: per-row sums for the CTA's rows and the
+// activations of the step's rows when they fit.
+void plan_smem(LinearParams& p, int grid) {
+  const int max_rows = p.max_rows < 1 ? 1 : p.max_rows;
+  p.mcap = max_rows < kMM ? max_rows : kMM;
+  const int npairs = p.N / 2;
+  p.rows_cap = 2 * ((npairs + grid - 1) / grid);
+  const size_t xb = (size_t)max_rows * p.K * 2;
+  const bool xs = max_rows <= kMM && xb <= kXsMaxBytes;
+  p.xs_rows = xs ? max_rows : 0;
+  p.nstages = 0;
 }
 
 }  // namespace
 
 size_t linear_smem_bytes() { return kSmemMax; }
-
-// Shared-memory plan of one launch: per-row sums for the CTA's rows, the
-// activations staged when they fit (at most kMM sequences, 48 KB), and as
-// many ring stages as keep the CTA within the two-CTAs-per-SM budget.
-static void plan_smem(LinearParams& p, int grid) {
-  const int max_rows = p.max_rows < 1 ? 1 : p.max_rows;
-  p.mcap = max_rows < kMM ? max_rows : kMM;
-  const int npairs = p.N / 2;
-  p.rows_cap = 2 * ((npairs + grid - 1) / grid);
-  const size_t rs = rowsum_bytes(p.rows_cap, p.mcap);
-  const size_t xb = (size_t)max_rows * p.K * 2;
-  const size_t fixed = kHeaderBytes + rs;
-  bool xs = max_rows <= kMM && xb <= kXsMaxBytes;
-  int nst = kMaxStages;
-  if (xs) {
-    const long long room = (long long)kSmemTarget - (long long)(fixed + xb);
-    nst = room > 0 ? (int)(room / kStageBytes) : 0;
-    if (nst > kMaxStages) nst = kMaxStages;
-    if (nst < 4) xs = false;
-  }
-  if (!xs) {
-    const long long room = (long long)kSmemTarget - (long long)fixed;
-    nst = room > 0 ? (int)(room / kStageBytes) : 0;
-    if (nst > kMaxStages) nst = kMaxStages;
-    if (nst < 2) nst = 2;
-  }
-  p.xs_rows = xs ? max_rows : 0;
-  p.nstages = nst;
-}
 
 cudaError_t linear_prepare() {
   cudaError_t e;
@@ -672,10 +603,7 @@ cudaError_t linear_prepare() {
   return set_smem_attr<EPI_HEAD>();
 }
 
-bool linear_shape_ok(int K) {
-  if (K < 32 || K % 32) return false;
-  return geo_ok(make_geo(K * 2)) && geo_ok(make_geo(K / 2));
-}
+bool linear_shape_ok(int K) { return K >= 32 && K % 32 == 0; }
 
 int linear_grid(int N, int num_sms) {
   const int pairs = N / 2;
@@ -685,9 +613,7 @@ int linear_grid(int N, int num_sms) {
 cudaError_t launch_linear(const LinearParams& p_in, int grid, bool pdl, cudaStream_t st) {
   LinearParams p = p_in;
   plan_smem(p, grid);
-  const size_t smem = kHeaderBytes + (p.xs_rows > 0 ? (size_t)p.xs_rows * p.K * 2 : 0) +
-                      rowsum_bytes(p.rows_cap, p.mcap) + (size_t)p.nstages * kStageBytes;
-  if (smem > kSmemMax) return cudaErrorInvalidConfiguration;
+  if (smem_of(p) > kSmemMax) return cudaErrorInvalidConfiguration;
   switch (p.epi) {
     case EPI_F32: return launch_one<EPI_F32>(p, grid, pdl, st);
     case EPI_QKV: return launch_one<EPI_QKV>(p, grid, pdl, st);
