@@ -103,6 +103,23 @@ EE_DEV void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Per-thread asynchronous 16-byte copy global -> shared (bypasses L1);
+// completion is tracked per thread with commit/wait groups.
+EE_DEV void cp_async16(void* dst_smem, const void* src_gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src_gmem)
+               : "memory");
+}
+EE_DEV void cp_async16_hint(void* dst_smem, const void* src_gmem, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_addr(dst_smem)),
+               "l"(src_gmem), "l"(policy)
+               : "memory");
+}
+EE_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+EE_DEV void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Programmatic dependent launch.  Every kernel of a step follows one rule:
 // it reads nothing a kernel before it wrote and writes nothing before
 // grid_dep_wait(), except data that the kernel two launches back or earlier

@@ -41,15 +41,19 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kBatch = 8;  // 16-byte vectors per lane per batch (two batches in flight)
+constexpr int kBatch = 8;  // 16-byte vectors per lane per batch
 constexpr int kMM = 8;     // sequences per pass over the weights
-constexpr size_t kPrefetchBytes = 128 * 1024;  // weights pulled into L2 before the dependency wait
+constexpr size_t kPrefetchBytes = 128 * 1024;  // per CTA: next kernel's weights pulled into L2
 
 // Shared memory: header (lists, head statistics), the staged activations
-// (XS mode), then the per-row sums [rows][mcap].
+// (XS mode), the per-row sums [rows][mcap], then per-warp copy rings of
+// nslots batches (kBatch vectors of 16 bytes per lane, plus 16 bytes of int4
+// scales per vector slot).
 constexpr size_t kHeaderBytes = 1536;
 constexpr size_t kXsMaxBytes = 64 * 1024;
-constexpr size_t kSmemMax = 120 * 1024;
+constexpr size_t kSmemMax = 227 * 1024 - 1024;
+constexpr int kMaxSlots = 4;
+constexpr size_t kSlotBytes = (size_t)kBatch * 512 + kBatch * 16;  // one warp, one batch
 static_assert(2 * kListLen * 4 + 16 + kWarps * kMM * 3 * 4 <= kHeaderBytes, "header overflow");
 
 EE_DEV __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
@@ -176,29 +180,28 @@ struct Plan {
   int passes[2];
 };
 
-// Loads one batch of this warp's stream: positions base + 32 j + lane
-// (j < kBatch) of the concatenation of the warp's rows, nv vectors each
-// (nv % 32 == 0, so the 32 positions of one j lie in one row).
+// Copies one batch of this warp's stream into its ring slot: positions
+// base + 32 j + lane (j < kBatch) of the concatenation of the warp's rows, nv
+// vectors each (nv % 32 == 0, so the 32 positions of one j lie in one row).
+// For int4 with K % 1024 == 0, lane j also copies the 8 scales of slot j.
 template <int PH>
-EE_DEV void load_batch(const LinearParams& p, const Plan& pl, int warp, int lane, int nv, int total,
-                       int base, uint4* buf, uint16_t* sbuf) {
+EE_DEV void issue_batch(const LinearParams& p, const Plan& pl, int warp, int lane, int nv, int total,
+                        int base, uint8_t* slot, bool sc_async, uint64_t pol) {
   const size_t rstride = PH == 0 ? (size_t)p.K * 2 : (size_t)p.K / 2;
   const uint8_t* wbase = PH == 0 ? reinterpret_cast<const uint8_t*>(p.w) : p.wq;
   int ri = base / nv;
-  int v = base - ri * nv + lane;
+  int v0 = base - ri * nv;
 #pragma unroll
   for (int j = 0; j < kBatch; ++j) {
     if (base + 32 * j < total) {
       const int row = pl.r0 + warp + kWarps * ri;
-      buf[j] = ldg_nc_v4(wbase + (size_t)row * rstride + (size_t)v * 16);
-      if (PH == 1) sbuf[j] = ldg_u16(p.ws + (size_t)row * p.sstride + (v >> 2));
-    } else {
-      buf[j] = make_uint4(0, 0, 0, 0);
-      if (PH == 1) sbuf[j] = 0;
+      cp_async16_hint(slot + j * 512 + lane * 16, wbase + (size_t)row * rstride + (size_t)(v0 + lane) * 16, pol);
+      if (PH == 1 && sc_async && lane == j)
+        cp_async16(slot + kBatch * 512 + j * 16, p.ws + (size_t)row * p.sstride + (v0 >> 2));
     }
-    v += 32;
-    if (v >= nv) {
-      v -= nv;
+    v0 += 32;
+    if (v0 >= nv) {
+      v0 -= nv;
       ++ri;
     }
   }
@@ -257,19 +260,25 @@ EE_DEV void flush_row(float* rowsum, int mcap, int row_local, int mc, float* acc
 }
 
 template <int PH, bool XS, int MMAX>
-EE_DEV void compute_batch(const uint4* w, const uint16_t* sc, int base, int total, int nv, int epv,
-                          int& cur, const uint16_t* const* xrow, int mc, float* acc, float* rowsum,
-                          int mcap, int warp, int lane) {
+EE_DEV void compute_batch(const LinearParams& p, const Plan& pl, const uint8_t* slot, bool sc_async, int base,
+                          int total, int nv, int& cur, const uint16_t* const* xrow, int mc, float* acc,
+                          float* rowsum, int warp, int lane) {
+  const int epv = PH == 0 ? 8 : 32;  // elements per vector
   int ri = base / nv;
   int v0 = base - ri * nv;  // warp-uniform vector index of lane 0
 #pragma unroll
   for (int j = 0; j < kBatch; ++j) {
     if (base + 32 * j < total) {
       if (ri != cur) {
-        flush_row<MMAX>(rowsum, mcap, warp + kWarps * cur, mc, acc, lane);
+        flush_row<MMAX>(rowsum, pl.mcap, warp + kWarps * cur, mc, acc, lane);
         cur = ri;
       }
-      dot_vec<PH, XS, MMAX>(w[j], sc[j], xrow, (v0 + lane) * epv, mc, acc);
+      const uint4 wv = *reinterpret_cast<const uint4*>(slot + j * 512 + lane * 16);
+      uint16_t sbits = 0;
+      if (PH == 1)
+        sbits = sc_async ? reinterpret_cast<const uint16_t*>(slot + kBatch * 512 + j * 16)[lane >> 2]
+                         : ldg_u16(p.ws + (size_t)(pl.r0 + warp + kWarps * ri) * p.sstride + ((v0 + lane) >> 2));
+      dot_vec<PH, XS, MMAX>(wv, sbits, xrow, (v0 + lane) * epv, mc, acc);
     }
     v0 += 32;
     if (v0 >= nv) {
@@ -279,35 +288,66 @@ EE_DEV void compute_batch(const uint4* w, const uint16_t* sc, int base, int tota
   }
 }
 
+EE_DEV void wait_slots(int nslots) {
+  if (nslots >= 4)
+    cp_async_wait<3>();
+  else if (nslots == 3)
+    cp_async_wait<2>();
+  else
+    cp_async_wait<1>();
+}
+
+// The first nslots - 1 batches of a warp's stream (weights only, so they may
+// be requested before the grid dependency wait).
+template <int PH>
+EE_DEV void stream_prologue(const LinearParams& p, const Plan& pl, int warp, int lane, uint8_t* ring,
+                            bool sc_async, uint64_t pol) {
+  const int nrows = pl.r1 - pl.r0;
+  const int nrw = nrows > warp ? (nrows - warp + kWarps - 1) / kWarps : 0;
+  const int nv = PH == 0 ? p.K / 8 : p.K / 32;
+  if (nv % 32 != 0) return;
+  const int total = nrw * nv;
+  for (int b = 0; b < p.nslots - 1; ++b) {
+    if (b * 32 * kBatch < total)
+      issue_batch<PH>(p, pl, warp, lane, nv, total, b * 32 * kBatch, ring + (size_t)b * kSlotBytes, sc_async, pol);
+    cp_async_commit();
+  }
+}
+
 // Streams this warp's rows of one phase (PH 0: bf16 weights, 1: int4) for
 // the mc sequences of one pass and writes each row's sums into rowsum.
+// `pre`: stream_prologue already ran for this pass.
 template <int PH, bool XS, int MMAX>
 EE_DEV void stream_rows(const LinearParams& p, const Plan& pl, int warp, int lane, int mc,
-                        const uint16_t* const* xrow, float* rowsum) {
+                        const uint16_t* const* xrow, float* rowsum, uint8_t* ring, bool sc_async, bool pre,
+                        uint64_t pol) {
   const int nrows = pl.r1 - pl.r0;
   const int nrw = nrows > warp ? (nrows - warp + kWarps - 1) / kWarps : 0;  // rows of this warp
   const int nv = PH == 0 ? p.K / 8 : p.K / 32;                             // vectors per row
-  const int epv = PH == 0 ? 8 : 32;                                        // elements per vector
   float acc[MMAX];
 #pragma unroll
   for (int m = 0; m < MMAX; ++m) acc[m] = 0.0f;
   if (nv % 32 == 0) {
-    // 32 consecutive positions of the warp's stream lie in one row
     const int total = nrw * nv;
     const int bstep = 32 * kBatch;
-    uint4 a[kBatch], b[kBatch];
-    uint16_t sa[kBatch], sb[kBatch];
-    load_batch<PH>(p, pl, warp, lane, nv, total, 0, a, sa);
+    const int nb = (total + bstep - 1) / bstep;
+    const int ns = p.nslots;
+    if (!pre) stream_prologue<PH>(p, pl, warp, lane, ring, sc_async, pol);
     int cur = 0;
-    for (int base = 0; base < total; base += 2 * bstep) {
-      if (base + bstep < total) load_batch<PH>(p, pl, warp, lane, nv, total, base + bstep, b, sb);
-      compute_batch<PH, XS, MMAX>(a, sa, base, total, nv, epv, cur, xrow, mc, acc, rowsum, pl.mcap, warp, lane);
-      if (base + 2 * bstep < total) load_batch<PH>(p, pl, warp, lane, nv, total, base + 2 * bstep, a, sa);
-      if (base + bstep < total)
-        compute_batch<PH, XS, MMAX>(b, sb, base + bstep, total, nv, epv, cur, xrow, mc, acc, rowsum, pl.mcap,
-                                    warp, lane);
+    for (int b = 0; b < nb; ++b) {
+      const int bn = b + ns - 1;
+      if (bn < nb)
+        issue_batch<PH>(p, pl, warp, lane, nv, total, bn * bstep, ring + (size_t)(bn % ns) * kSlotBytes, sc_async,
+                        pol);
+      cp_async_commit();
+      wait_slots(ns);  // batch b has landed
+      __syncwarp();
+      compute_batch<PH, XS, MMAX>(p, pl, ring + (size_t)(b % ns) * kSlotBytes, sc_async, b * bstep, total, nv, cur,
+                                  xrow, mc, acc, rowsum, warp, lane);
+      __syncwarp();  // the slot is refilled next iteration
     }
     if (nrw > 0) flush_row<MMAX>(rowsum, pl.mcap, warp + kWarps * cur, mc, acc, lane);
+    cp_async_wait<0>();
   } else {
     // short or odd rows: one row at a time, lanes stride over its vectors
     const size_t rstride = PH == 0 ? (size_t)p.K * 2 : (size_t)p.K / 2;
@@ -317,7 +357,7 @@ EE_DEV void stream_rows(const LinearParams& p, const Plan& pl, int warp, int lan
       for (int v = lane; v < nv; v += 32) {
         const uint4 wv = ldg_nc_v4(wbase + (size_t)row * rstride + (size_t)v * 16);
         const uint16_t sbits = PH == 1 ? ldg_u16(p.ws + (size_t)row * p.sstride + (v >> 2)) : 0;
-        dot_vec<PH, XS, MMAX>(wv, sbits, xrow, v * epv, mc, acc);
+        dot_vec<PH, XS, MMAX>(wv, sbits, xrow, v * (PH == 0 ? 8 : 32), mc, acc);
       }
       flush_row<MMAX>(rowsum, pl.mcap, warp + kWarps * ri, mc, acc, lane);
     }
@@ -325,13 +365,14 @@ EE_DEV void stream_rows(const LinearParams& p, const Plan& pl, int warp, int lan
 }
 
 template <int EPI, bool XS, int MMAX>
-__global__ void __launch_bounds__(kThreads, MMAX == 1 ? 2 : 1) k_linear(const LinearParams p) {
+__global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   int32_t* lf = reinterpret_cast<int32_t*>(smem);
   int32_t* le = lf + kListLen;
   float* hst = reinterpret_cast<float*>(smem + 2 * kListLen * 4 + 16);
   uint8_t* xs = smem + kHeaderBytes;
   float* rowsum = reinterpret_cast<float*>(xs + (XS ? (size_t)p.xs_rows * p.K * 2 : 0));
+  uint8_t* rings = reinterpret_cast<uint8_t*>(rowsum) + (((size_t)p.rows_cap * p.mcap * 4 + 15) / 16 * 16);
   __shared__ int s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -357,21 +398,13 @@ __global__ void __launch_bounds__(kThreads, MMAX == 1 ? 2 : 1) k_linear(const Li
   }
   const int nrows = pl.r1 - pl.r0;
 
-  // Weights do not depend on the previous kernel: pull the start of this
-  // CTA's rows into L2 now, while that kernel drains.
-  if (tid == 0) {
-    const int ph = pl.passes[0] > 0 ? 0 : (pl.passes[1] > 0 ? 1 : -1);
-    if (ph >= 0) {
-      const size_t rb = ph == 0 ? (size_t)p.K * 2 : (size_t)p.K / 2;
-      const uint8_t* base = (ph == 0 ? reinterpret_cast<const uint8_t*>(p.w) : p.wq) + (size_t)pl.r0 * rb;
-      const size_t total = (size_t)nrows * rb;
-      const size_t want = total < kPrefetchBytes ? total : kPrefetchBytes;
-      for (size_t o = 0; o < want; o += 16384) {
-        const uint32_t n = (uint32_t)((want - o) < 16384 ? (want - o) : 16384);
-        prefetch_l2(base + o, n);
-      }
-    }
-  }
+  uint8_t* ring = rings + (size_t)warp * p.nslots * kSlotBytes;
+  const uint64_t pol = l2_evict_first_policy();
+  const bool sc_async = p.K % 1024 == 0 && p.sstride * EE_QUANT_GROUP == p.K;
+  // Weights do not depend on the previous kernel: start this warp's stream now.
+  const int first_phase = pl.passes[0] > 0 ? 0 : (pl.passes[1] > 0 ? 1 : -1);
+  if (first_phase == 0) stream_prologue<0>(p, pl, warp, lane, ring, sc_async, pol);
+  if (first_phase == 1) stream_prologue<1>(p, pl, warp, lane, ring, sc_async, pol);
   grid_dep_wait();
   grid_dep_launch();
   if (XS && nx > 0) {
@@ -399,10 +432,11 @@ __global__ void __launch_bounds__(kThreads, MMAX == 1 ? 2 : 1) k_linear(const Li
         xrow[m] = XS ? reinterpret_cast<const uint16_t*>(xs) + (size_t)(xbase + m0 + mm) * p.K
                      : p.xh + (size_t)lst[1 + m0 + mm] * p.x_stride;
       }
+      const bool pre = phase == first_phase && pass == 0;
       if (phase == 0)
-        stream_rows<0, XS, MMAX>(p, pl, warp, lane, mc, xrow, rowsum);
+        stream_rows<0, XS, MMAX>(p, pl, warp, lane, mc, xrow, rowsum, ring, sc_async, pre, pol);
       else
-        stream_rows<1, XS, MMAX>(p, pl, warp, lane, mc, xrow, rowsum);
+        stream_rows<1, XS, MMAX>(p, pl, warp, lane, mc, xrow, rowsum, ring, sc_async, pre, pol);
       __syncthreads();  // every row sum of this pass is complete
       if constexpr (EPI == EPI_HEAD) {
         Stat stat[MMAX];
@@ -460,6 +494,26 @@ __global__ void __launch_bounds__(kThreads, MMAX == 1 ? 2 : 1) k_linear(const Li
         }
       }
       __syncthreads();  // row sums are reused by the next pass
+    }
+  }
+
+  // Pull the start of the next kernel's weights (the same CTA index's rows)
+  // into L2 while the other CTAs finish.
+  if (tid == 0 && (p.next_w || p.next_wq)) {
+    const int ngrid = p.next_grid > 0 ? p.next_grid : (int)gridDim.x;
+    if ((int)blockIdx.x < ngrid) {
+      const int npairs = p.next_N >> 1;
+      const int nr0 = 2 * (int)(((long long)blockIdx.x * npairs) / ngrid);
+      const int nr1 = 2 * (int)(((long long)(blockIdx.x + 1) * npairs) / ngrid);
+      for (int ph = 0; ph < 2; ++ph) {
+        if (ph == 0 ? (p.next_w == nullptr || nf == 0) : (p.next_wq == nullptr || ne == 0)) continue;
+        const size_t rb = ph == 0 ? (size_t)p.next_K * 2 : (size_t)p.next_K / 2;
+        const uint8_t* base =
+            (ph == 0 ? reinterpret_cast<const uint8_t*>(p.next_w) : p.next_wq) + (size_t)nr0 * rb;
+        const size_t tot = (size_t)(nr1 - nr0) * rb;
+        const size_t want = tot < kPrefetchBytes ? tot : kPrefetchBytes;
+        for (size_t o = 0; o < want; o += 16384) prefetch_l2(base + o, (uint32_t)((want - o) < 16384 ? (want - o) : 16384));
+      }
     }
   }
 
@@ -553,7 +607,8 @@ cudaError_t set_smem_attr() {
 }
 
 size_t smem_of(const LinearParams& p) {
-  return kHeaderBytes + (p.xs_rows > 0 ? (size_t)p.xs_rows * p.K * 2 : 0) + (size_t)p.rows_cap * p.mcap * 4;
+  return kHeaderBytes + (p.xs_rows > 0 ? (size_t)p.xs_rows * p.K * 2 : 0) +
+         ((size_t)p.rows_cap * p.mcap * 4 + 15) / 16 * 16 + (size_t)kWarps * p.nslots * kSlotBytes;
 }
 
 template <int EPI>
@@ -586,7 +641,8 @@ void plan_smem(LinearParams& p, int grid) {
   const size_t xb = (size_t)max_rows * p.K * 2;
   const bool xs = max_rows <= kMM && xb <= kXsMaxBytes;
   p.xs_rows = xs ? max_rows : 0;
-  p.nstages = 0;
+  p.nslots = kMaxSlots;
+  while (p.nslots > 2 && smem_of(p) > kSmemMax) --p.nslots;
 }
 
 }  // namespace
