@@ -18,6 +18,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libee.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
+# EE_NVCC_EXTRA="-DEE_CHECKED" builds the self-checking debug variant of the kernels.
+NVCC_FLAGS += os.environ.get("EE_NVCC_EXTRA", "").split()
 
 
 def nvcc() -> str:

@@ -639,8 +639,9 @@ ee_status run_step(ee_ctx* c, int B, bool heads) {
   if (s != EE_OK) return s;
   if (c->out_host->err != 0)
     return fail(c, EE_ERR_DEVICE_TIMEOUT,
-                "a bounded device wait gave up (code %d: 1 = stage fill, 2 = stage drain, 3 = exit drain)",
-                c->out_host->err);
+                "device error code %d (1 = stage fill, 2 = stage drain, 3 = exit drain; >= 10: a checked "
+                "access was refused) info %d %d",
+                c->out_host->err, c->out_host->pad[0], c->out_host->pad[1]);
   return EE_OK;
 }
 

@@ -43,7 +43,6 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kBatch = 8;  // 16-byte vectors per lane per batch
 constexpr int kMM = 8;     // sequences per pass over the weights
-constexpr size_t kPrefetchBytes = 128 * 1024;  // per CTA: next kernel's weights pulled into L2
 
 // Shared memory: header (lists, head statistics), the staged activations
 // (XS mode), the per-row sums [rows][mcap], then per-warp copy rings of
@@ -52,6 +51,7 @@ constexpr size_t kPrefetchBytes = 128 * 1024;  // per CTA: next kernel's weights
 constexpr size_t kHeaderBytes = 1536;
 constexpr size_t kXsMaxBytes = 64 * 1024;
 constexpr size_t kSmemMax = 227 * 1024 - 1024;
+constexpr size_t kSmemPair = 112 * 1024;  // two CTAs per SM
 constexpr int kMaxSlots = 4;
 constexpr size_t kSlotBytes = (size_t)kBatch * 512 + kBatch * 16;  // one warp, one batch
 static_assert(2 * kListLen * 4 + 16 + kWarps * kMM * 3 * 4 <= kHeaderBytes, "header overflow");
@@ -184,6 +184,27 @@ struct Plan {
 // base + 32 j + lane (j < kBatch) of the concatenation of the warp's rows, nv
 // vectors each (nv % 32 == 0, so the 32 positions of one j lie in one row).
 // For int4 with K % 1024 == 0, lane j also copies the 8 scales of slot j.
+#ifdef EE_CHECKED
+// Debug builds: every asynchronous access is checked; a bad one is recorded
+// (site code in err[0], value in err[1..2]) and skipped.
+EE_DEV uint32_t dyn_smem_size() {
+  uint32_t v;
+  asm volatile("mov.u32 %0, %dynamic_smem_size;" : "=r"(v));
+  return v;
+}
+extern __shared__ __align__(1024) uint8_t smem_base_sym[];
+EE_DEV bool check_ok(int32_t* err, bool ok, int site, long long v1, long long v2) {
+  if (!ok && err && atomicCAS(err, 0, site) == 0) {
+    err[1] = (int32_t)v1;
+    err[2] = (int32_t)v2;
+  }
+  return ok;
+}
+#define EE_CHECK(err, cond, site, v1, v2) check_ok((err), (cond), (site), (long long)(v1), (long long)(v2))
+#else
+#define EE_CHECK(err, cond, site, v1, v2) true
+#endif
+
 template <int PH>
 EE_DEV void issue_batch(const LinearParams& p, const Plan& pl, int warp, int lane, int nv, int total,
                         int base, uint8_t* slot, bool sc_async, uint64_t pol) {
@@ -195,9 +216,21 @@ EE_DEV void issue_batch(const LinearParams& p, const Plan& pl, int warp, int lan
   for (int j = 0; j < kBatch; ++j) {
     if (base + 32 * j < total) {
       const int row = pl.r0 + warp + kWarps * ri;
-      cp_async16_hint(slot + j * 512 + lane * 16, wbase + (size_t)row * rstride + (size_t)(v0 + lane) * 16, pol);
-      if (PH == 1 && sc_async && lane == j)
-        cp_async16(slot + kBatch * 512 + j * 16, p.ws + (size_t)row * p.sstride + (v0 >> 2));
+      uint8_t* dst = slot + j * 512 + lane * 16;
+      const uint8_t* src = wbase + (size_t)row * rstride + (size_t)(v0 + lane) * 16;
+#ifdef EE_CHECKED
+      const uint32_t so = smem_addr(dst) - smem_addr(smem_base_sym);
+      const bool okd = EE_CHECK(p.err, so % 16 == 0 && so + 16 <= dyn_smem_size(), 11, so, dyn_smem_size());
+      const bool oks = EE_CHECK(p.err, ((uintptr_t)src & 15) == 0 && row >= pl.r0 && row < pl.r1 && v0 + lane < nv,
+                                12, row, v0 + lane);
+      if (okd && oks)
+#endif
+        cp_async16(dst, src);
+      if (PH == 1 && sc_async && lane == j) {
+        const uint16_t* ssrc = p.ws + (size_t)row * p.sstride + (v0 >> 2);
+        if (EE_CHECK(p.err, ((uintptr_t)ssrc & 15) == 0, 13, row, v0))
+          cp_async16(slot + kBatch * 512 + j * 16, ssrc);
+      }
     }
     v0 += 32;
     if (v0 >= nv) {
@@ -413,6 +446,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
     for (int i = tid; i < nx * v16; i += kThreads) {
       const int m = i / v16, c = i - m * v16;
       const int seq = m < nf ? lf[1 + m] : le[1 + m - nf];
+#ifdef EE_CHECKED
+      if (!EE_CHECK(p.err, (size_t)(i + 1) * 16 <= (size_t)p.xs_rows * p.K * 2 && seq >= 0 && seq < EE_MAX_BATCH, 15,
+                    i, seq))
+        continue;
+#endif
       reinterpret_cast<uint4*>(xs)[i] = *reinterpret_cast<const uint4*>(p.xh + (size_t)seq * p.x_stride + c * 8);
     }
   }
@@ -494,26 +532,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
         }
       }
       __syncthreads();  // row sums are reused by the next pass
-    }
-  }
-
-  // Pull the start of the next kernel's weights (the same CTA index's rows)
-  // into L2 while the other CTAs finish.
-  if (tid == 0 && (p.next_w || p.next_wq)) {
-    const int ngrid = p.next_grid > 0 ? p.next_grid : (int)gridDim.x;
-    if ((int)blockIdx.x < ngrid) {
-      const int npairs = p.next_N >> 1;
-      const int nr0 = 2 * (int)(((long long)blockIdx.x * npairs) / ngrid);
-      const int nr1 = 2 * (int)(((long long)(blockIdx.x + 1) * npairs) / ngrid);
-      for (int ph = 0; ph < 2; ++ph) {
-        if (ph == 0 ? (p.next_w == nullptr || nf == 0) : (p.next_wq == nullptr || ne == 0)) continue;
-        const size_t rb = ph == 0 ? (size_t)p.next_K * 2 : (size_t)p.next_K / 2;
-        const uint8_t* base =
-            (ph == 0 ? reinterpret_cast<const uint8_t*>(p.next_w) : p.next_wq) + (size_t)nr0 * rb;
-        const size_t tot = (size_t)(nr1 - nr0) * rb;
-        const size_t want = tot < kPrefetchBytes ? tot : kPrefetchBytes;
-        for (size_t o = 0; o < want; o += 16384) prefetch_l2(base + o, (uint32_t)((want - o) < 16384 ? (want - o) : 16384));
-      }
     }
   }
 
@@ -641,8 +659,12 @@ void plan_smem(LinearParams& p, int grid) {
   const size_t xb = (size_t)max_rows * p.K * 2;
   const bool xs = max_rows <= kMM && xb <= kXsMaxBytes;
   p.xs_rows = xs ? max_rows : 0;
-  p.nslots = kMaxSlots;
-  while (p.nslots > 2 && smem_of(p) > kSmemMax) --p.nslots;
+  // Three slots (two batches in flight per lane, 64 KB per SM) in a CTA small
+  // enough that the next kernel's CTA fits beside it and starts its stream
+  // before this one ends; fewer when that does not fit.
+  p.nslots = 3;
+  while (p.nslots > 2 && smem_of(p) > kSmemPair) --p.nslots;
+  if (smem_of(p) > kSmemMax) p.nslots = 2;
 }
 
 }  // namespace
