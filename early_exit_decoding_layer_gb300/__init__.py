@@ -34,6 +34,7 @@ EXPORTS = (
     "ee_debug_int4", "ee_op_quantize_int4", "ee_op_linear_bf16", "ee_op_linear_int4",
     "ee_attention_scratch_bytes", "ee_op_attention", "ee_head_scratch_bytes",
     "ee_op_vocab_head", "ee_step_io", "ee_set_profile", "ee_profile_read", "ee_last_step_ms",
+    "ee_op_attention_noalloc",
 )
 
 KINDS = ("begin", "norm", "qkv", "attn", "o", "gateup", "down", "head_norm", "head_t", "head_e",
@@ -121,6 +122,8 @@ def load_library(path: str = LIB_PATH):
         "ee_set_profile": (i32, [c_vp, i32]),
         "ee_profile_read": (i32, [c_vp, P(EELaunchRecord), i32, P(i32)]),
         "ee_last_step_ms": (i32, [c_vp, P(c_f32)]),
+        "ee_op_attention_noalloc": (i32, [i32, i32, i32, i32, i32, c_vp, c_vp, c_vp, c_vp, i32, c_vp,
+                                          c_vp, c_vp, c_vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -424,6 +427,25 @@ def attention(q, kcache, vcache, block_table, pos, n_heads, n_kv_heads, head_dim
                                           _ptr(vcache), _ptr(block_table), block_table.shape[1],
                                           _ptr(pos), _ptr(o), _ptr(scratch), _ptr(err),
                                           _stream(stream)), "ee_op_attention")
+    return o
+
+
+ATTN_STATIC_SCRATCH_BYTES = 4 << 20  # EE_ATTN_STATIC_SCRATCH_BYTES
+
+
+def attention_noalloc(q, kcache, vcache, block_table, pos, n_heads, n_kv_heads, head_dim, max_ctx,
+                      out=None, err=None, stream=None):
+    """ee_op_attention_noalloc: attention() with the library's fixed scratch array
+    instead of a caller buffer.  The C call allocates nothing; pass `out`
+    ([B, Hq*hd] fp32) to keep this wrapper from allocating the result either."""
+    import torch
+    B = q.shape[0]
+    o = out if out is not None else torch.empty((B, n_heads * head_dim), dtype=torch.float32,
+                                                device=q.device)
+    _raise(load_library().ee_op_attention_noalloc(B, n_heads, n_kv_heads, head_dim, max_ctx, _ptr(q),
+                                                  _ptr(kcache), _ptr(vcache), _ptr(block_table),
+                                                  block_table.shape[1], _ptr(pos), _ptr(o), _ptr(err),
+                                                  _stream(stream)), "ee_op_attention_noalloc")
     return o
 
 

@@ -305,6 +305,37 @@ ee_status ee_op_vocab_head(int32_t M, int32_t V, int32_t d, const uint16_t *u_f1
                            float *conf, int32_t *argmax, void *scratch, int32_t *err_flag,
                            void *stream);
 
+/* ---- attention without a caller-provided scratch buffer ------------------
+ * Not part of the early-exit method: the pages have no counterpart.  It is
+ * for callers that cannot allocate device memory, or hand the library a
+ * buffer, at the time they call: a host whose caching allocator has already
+ * reserved the device's free memory (a cudaMalloc from outside it may fail or
+ * synchronise the device), or one that allows no allocation after start-up.
+ *
+ * Same operation, arguments, layouts and results as ee_op_attention, minus
+ * `scratch`.  The scratch is a fixed array of EE_ATTN_STATIC_SCRATCH_BYTES
+ * inside the library; the call allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library call).  A shape whose ee_attention_scratch_bytes(...)
+ * exceeds that size returns EE_ERR_CAPACITY without touching the device (for
+ * Llama-3.1-8B heads, Hq 32, Hkv 8, hd 128, it fits B = 1 at every max_ctx up
+ * to 16384, and B <= 15 at max_ctx 2048).  Invalid shapes return
+ * EE_ERR_INVALID_ARG.
+ *
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before capturing any stream into a graph.
+ *  - Each call zeroes the array's merge counters on `stream` (cudaMemsetAsync)
+ *    and then launches the kernel; it returns without waiting for either.
+ *  - The array is shared by every call on a device and keeps the last call's
+ *    partial results.  Calls that overlap in time on one device (from two
+ *    streams or host threads) race on it: order them, e.g. on one stream. */
+#define EE_ATTN_STATIC_SCRATCH_BYTES (4u << 20)
+ee_status ee_op_attention_noalloc(int32_t B, int32_t n_heads, int32_t n_kv_heads,
+                                  int32_t head_dim, int32_t max_ctx, const float *q,
+                                  const uint16_t *kcache, const uint16_t *vcache,
+                                  const int32_t *block_table, int32_t bt_stride,
+                                  const int32_t *pos, float *o, int32_t *err_flag, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
