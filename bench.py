@@ -299,7 +299,7 @@ def calibrate(eng, w, prompts, steps, percentiles):
     return {p: np.percentile(c, p, axis=0) for p in percentiles}, c
 
 
-def timed_run(eng, w, prompts, steps, warmup, heads, world, profile_steps=0):
+def timed_run(eng, w, prompts, steps, warmup, heads, world, profile_steps=0, ncu_region=False):
     import torch
     eng.set_exit_enabled(heads)
     tok = eng.prefill(prompts)
@@ -311,6 +311,8 @@ def timed_run(eng, w, prompts, steps, warmup, heads, world, profile_steps=0):
     clocks = ClockSampler()
     dev_ms = []
     exits = []
+    if ncu_region:  # a profiler started with --profile-from-start off captures only these steps
+        torch.cuda.profiler.start()
     t0 = time.perf_counter()
     for _ in range(steps):
         tok, ex = eng.decode_step(tok)
@@ -318,6 +320,8 @@ def timed_run(eng, w, prompts, steps, warmup, heads, world, profile_steps=0):
         exits.append(ex.copy())
     wall = time.perf_counter() - t0
     torch.cuda.synchronize()
+    if ncu_region:
+        torch.cuda.profiler.stop()
     barrier(world, True)
     clk = clocks.stop()
     prof = []
@@ -388,9 +392,9 @@ def run_ours(args):
     for pct in w.gamma_percentiles:
         eng.set_thresholds(gammas[pct])
         runs[pct] = timed_run(eng, w, prompts, args.steps, args.warmup, True, world,
-                              profile_steps=args.profile_steps)
+                              profile_steps=args.profile_steps, ncu_region=args.ncu_region)
     base = timed_run(eng, w, prompts, args.steps, args.warmup, False, world,
-                     profile_steps=args.profile_steps)
+                     profile_steps=args.profile_steps, ncu_region=args.ncu_region)
 
     def summarize(r, heads):
         dev_s = sum(r["dev_ms"]) / 1e3
@@ -504,6 +508,8 @@ def main():
     ap.add_argument("--profile-steps", type=int, default=3)
     ap.add_argument("--cpu-layers", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-region", action="store_true",
+                    help="bracket the timed steps with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
     ap.add_argument("--dry-dist", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.warmup < 3:

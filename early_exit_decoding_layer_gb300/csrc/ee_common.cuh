@@ -79,12 +79,6 @@ EE_DEV uint64_t l2_evict_first_policy() {
   return pol;
 }
 
-EE_DEV uint64_t l2_evict_last_policy() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
 // global memory into this CTA's shared memory; completion is counted in
 // bytes on `bar` (whose expected transaction count the caller has raised).
@@ -95,29 +89,6 @@ EE_DEV void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes, uint6
       "%2, [%3], %4;" ::"r"(smem_addr(dst_smem)),
       "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
-}
-
-// Asks the memory system to bring `bytes` (multiple of 16, 16-byte aligned
-// address) of global memory into L2; nothing is written to shared memory.
-EE_DEV void prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
-// Per-thread asynchronous 16-byte copy global -> shared (bypasses L1);
-// completion is tracked per thread with commit/wait groups.
-EE_DEV void cp_async16(void* dst_smem, const void* src_gmem) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src_gmem)
-               : "memory");
-}
-EE_DEV void cp_async16_hint(void* dst_smem, const void* src_gmem, uint64_t policy) {
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_addr(dst_smem)),
-               "l"(src_gmem), "l"(policy)
-               : "memory");
-}
-EE_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-EE_DEV void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Programmatic dependent launch.  Every kernel of a step follows one rule:
@@ -137,6 +108,16 @@ EE_DEV int32_t ld_volatile_i32(const int32_t* p) {
 EE_DEV uint4 ldg_nc_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Streaming 16-byte load of data read once per launch (weights): not kept in
+// L1, with a 256-byte L2 fetch granule.
+EE_DEV uint4 ldg_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;

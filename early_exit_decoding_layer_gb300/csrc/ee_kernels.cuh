@@ -57,14 +57,9 @@ enum HeadMode : int32_t { HEAD_CONF_ARGMAX = 0, HEAD_CHECKPOINT = 1, HEAD_FINAL 
 struct LinearParams {
   int32_t N, K;
   int32_t max_rows;          // upper bound of the list counts (sequences of the step)
-  // filled by launch_linear: copy-ring slots per warp, staged activation rows
-  // (0: read from global), sequences per pass, per-row sum capacity
-  int32_t nslots, xs_rows, mcap, rows_cap;
-  // the next kernel's matrix, whose first rows per CTA are pulled into L2 at
-  // the end of this launch (null: none); next_grid 0 = this launch's grid
-  const uint16_t* next_w;
-  const uint8_t* next_wq;
-  int32_t next_N, next_K, next_grid;
+  // filled by launch_linear: staged activation rows (0: read from global),
+  // sequences per pass, per-row sum capacity
+  int32_t xs_rows, mcap, rows_cap;
   // weights: bf16 [N, K]; int4 packed [N, K/2] with bf16 scales [N, sstride]
   const uint16_t* w;
   const uint8_t* wq;

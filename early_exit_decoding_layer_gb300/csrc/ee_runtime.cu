@@ -350,14 +350,6 @@ struct LaunchLog {
     if (s_ != EE_OK) return s_;           \
   } while (0)
 
-void set_next(LinearParams& p, const uint16_t* w, const uint8_t* wq, int N, int K) {
-  p.next_w = w;
-  p.next_wq = wq;
-  p.next_N = N;
-  p.next_K = K;
-  p.next_grid = 0;
-}
-
 // ---------------------------------------------------------------- step enqueue
 ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
   const Dims& m = c->m;
@@ -429,7 +421,6 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.q_out = c->q;
     p.kc = c->kcache + (size_t)j * m.kv_layer_elems;
     p.vc = c->vcache + (size_t)j * m.kv_layer_elems;
-    set_next(p, w.wo, w.o.q, m.d, m.dq);
     p.max_rows = B;
     EE_LAUNCH(log, EE_K_QKV, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
     // decode attention
@@ -466,7 +457,6 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.xh = c->ah;
     p.x_stride = m.dq;
     p.epi = EPI_RESID;
-    set_next(p, w.wgu, w.gu.q, 2 * m.F, m.d);
     p.max_rows = B;
     EE_LAUNCH(log, EE_K_O, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
     // FFN RMSNorm
@@ -487,7 +477,6 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.epi = EPI_SWIGLU;
     p.xh_out = c->acth;
     p.xo_stride = m.F;
-    set_next(p, w.wd, w.d.q, m.d, m.F);
     p.max_rows = B;
     EE_LAUNCH(log, EE_K_GATEUP, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
     // down projection + residual (+ per-layer copy in debug mode)
@@ -504,15 +493,6 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.x_stride = m.F;
     p.epi = EPI_RESID;
     p.hdbg = c->hdbg + (size_t)j * EE_MAX_BATCH * m.d;
-    {
-      const auto ckn = std::find(c->ckpts.begin(), c->ckpts.end(), j);
-      if (heads && ckn != c->ckpts.end())
-        set_next(p, c->Tt[ckn - c->ckpts.begin()], nullptr, m.d, m.d);
-      else if (j + 1 < m.L)
-        set_next(p, c->layers[j + 1].wqkv, c->layers[j + 1].qkv.q, m.nqkv, m.d);
-      else
-        set_next(p, c->E, nullptr, m.V, m.d);
-    }
     p.max_rows = B;
     EE_LAUNCH(log, EE_K_DOWN, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
 
@@ -535,7 +515,6 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
       p.epi = EPI_X;
       p.xh_out = c->uh;
       p.xo_stride = m.d;
-      set_next(p, c->E, nullptr, m.V, m.d);
       p.max_rows = B;
       EE_LAUNCH(log, EE_K_HEAD_T, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
       // z = u E^T, conf = max softmax, exit if conf > gamma_c, compact the lists
@@ -555,7 +534,6 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
       p.exit_layer = c->out_dev->exit_layer;
       p.ckpt_index = ci;
       p.ckpt_layer = j;
-      if (j + 1 < m.L) set_next(p, c->layers[j + 1].wqkv, c->layers[j + 1].qkv.q, m.nqkv, m.d);
       p.max_rows = B;
       EE_LAUNCH(log, EE_K_HEAD_E, j,
                 launch_linear(p, std::min(linear_grid(p.N, c->num_sms), kHeadGridMax), true, st));

@@ -8,18 +8,19 @@
 // group of 128 input columns, dequantised in registers and never written
 // back).  An empty list reads no byte of its matrix.
 //
-// Data flow: one CTA of 8 warps per SM owns a balanced, pair-aligned range of
-// output rows; warp w owns the CTA's rows w, w+8, ... and streams each of them
-// with coalesced 16-byte loads (a warp reads 512 contiguous bytes per load
-// instruction) straight into registers, double-buffered in batches of 8
-// vectors per lane so that 16 loads per lane (64 KB per SM) are in flight --
-// what the HBM needs to run at peak.  The first batch is requested before the
-// grid dependency wait (weights never change), so the stream starts while the
-// previous kernel drains; the activations of the step's rows (fp16, a few KB
-// per sequence), written by that kernel, are copied into shared memory after
-// the wait.  A warp finishes each of its rows alone (one warp reduction), so
-// results do not depend on timing.  The epilogue (RoPE + KV write, SwiGLU,
-// residual add, head statistics) runs once over the CTA's rows.
+// Data flow: one CTA of 16 warps per SM owns a balanced, pair-aligned range
+// of output rows; warp w owns the CTA's rows w, w+16, ... and walks them as
+// one stream of 16-byte vectors, 32 at a time (a warp reads 512 contiguous
+// bytes per load instruction), straight into registers.  Two batches of 8
+// vectors per lane alternate: the loads of the next batch are issued before
+// the current one is consumed, so up to 64 KB per SM are in flight -- what
+// HBM3e needs to stream near its peak.  The first batch is requested before
+// the grid dependency wait (weights never change), so the stream starts
+// while the previous kernel drains; the activations of the step's rows (fp16,
+// a few KB per sequence), written by that kernel, are copied into shared
+// memory after the wait.  A warp finishes each of its rows alone (one warp
+// reduction), so results do not depend on timing.  The epilogue (RoPE + KV
+// write, SwiGLU, residual add, head statistics) runs once over the CTA's rows.
 //
 // Activations are stored in "pair order" (within each run of 8 columns:
 // 0,4,1,5,2,6,3,7, see xh_slot) so that one 16-byte load yields the half2
@@ -39,21 +40,16 @@ namespace ee {
 
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kBatch = 8;  // 16-byte vectors per lane per batch
 constexpr int kMM = 8;     // sequences per pass over the weights
 
 // Shared memory: header (lists, head statistics), the staged activations
-// (XS mode), the per-row sums [rows][mcap], then per-warp copy rings of
-// nslots batches (kBatch vectors of 16 bytes per lane, plus 16 bytes of int4
-// scales per vector slot).
-constexpr size_t kHeaderBytes = 1536;
+// (XS mode), then the per-row sums [rows][mcap].
+constexpr size_t kHeaderBytes = 3072;
 constexpr size_t kXsMaxBytes = 64 * 1024;
 constexpr size_t kSmemMax = 227 * 1024 - 1024;
-constexpr size_t kSmemPair = 112 * 1024;  // two CTAs per SM
-constexpr int kMaxSlots = 4;
-constexpr size_t kSlotBytes = (size_t)kBatch * 512 + kBatch * 16;  // one warp, one batch
 static_assert(2 * kListLen * 4 + 16 + kWarps * kMM * 3 * 4 <= kHeaderBytes, "header overflow");
 
 EE_DEV __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
@@ -180,19 +176,9 @@ struct Plan {
   int passes[2];
 };
 
-// Copies one batch of this warp's stream into its ring slot: positions
-// base + 32 j + lane (j < kBatch) of the concatenation of the warp's rows, nv
-// vectors each (nv % 32 == 0, so the 32 positions of one j lie in one row).
-// For int4 with K % 1024 == 0, lane j also copies the 8 scales of slot j.
 #ifdef EE_CHECKED
-// Debug builds: every asynchronous access is checked; a bad one is recorded
-// (site code in err[0], value in err[1..2]) and skipped.
-EE_DEV uint32_t dyn_smem_size() {
-  uint32_t v;
-  asm volatile("mov.u32 %0, %dynamic_smem_size;" : "=r"(v));
-  return v;
-}
-extern __shared__ __align__(1024) uint8_t smem_base_sym[];
+// Debug builds: the staging copies are checked; a bad one is recorded (site
+// code in err[0], values in err[1..2]) and skipped.
 EE_DEV bool check_ok(int32_t* err, bool ok, int site, long long v1, long long v2) {
   if (!ok && err && atomicCAS(err, 0, site) == 0) {
     err[1] = (int32_t)v1;
@@ -205,74 +191,101 @@ EE_DEV bool check_ok(int32_t* err, bool ok, int site, long long v1, long long v2
 #define EE_CHECK(err, cond, site, v1, v2) true
 #endif
 
+// One warp's share of a phase: its rows r0 + warp + kWarps * i (i < nrw) of
+// the bf16 matrix (PH 0) or of the packed int4 matrix (PH 1), nv 16-byte
+// vectors each.
+struct Stream {
+  const uint8_t* base;
+  size_t rstride;  // bytes per row
+  int nv, nrw, row0;
+};
+
 template <int PH>
-EE_DEV void issue_batch(const LinearParams& p, const Plan& pl, int warp, int lane, int nv, int total,
-                        int base, uint8_t* slot, bool sc_async, uint64_t pol) {
-  const size_t rstride = PH == 0 ? (size_t)p.K * 2 : (size_t)p.K / 2;
-  const uint8_t* wbase = PH == 0 ? reinterpret_cast<const uint8_t*>(p.w) : p.wq;
-  int ri = base / nv;
-  int v0 = base - ri * nv;
+EE_DEV Stream make_stream(const LinearParams& p, const Plan& pl, int warp) {
+  Stream s;
+  s.base = PH == 0 ? reinterpret_cast<const uint8_t*>(p.w) : p.wq;
+  s.rstride = PH == 0 ? (size_t)p.K * 2 : (size_t)p.K / 2;
+  s.nv = PH == 0 ? p.K / 8 : p.K / 32;
+  const int nrows = pl.r1 - pl.r0;
+  s.nrw = nrows > warp ? (nrows - warp + kWarps - 1) / kWarps : 0;
+  s.row0 = pl.r0 + warp;
+  return s;
+}
+
+// Streams are walked 32 vectors at a time (nv % 32 == 0), so the 32 lanes of
+// one step always lie in one row and a warp reads 512 contiguous bytes.
+// Position in a warp's stream: its ri-th row, vector v0 + lane.
+struct Cursor {
+  int ri, v0;
+};
+
+// Load-side position: the cursor plus this lane's weight (and scale) address.
+struct LoadCursor {
+  int ri, v0;
+  const uint8_t* wp;
+  const uint16_t* sp;
+};
+
+template <int PH>
+EE_DEV LoadCursor load_start(const LinearParams& p, const Stream& st, int lane) {
+  LoadCursor c;
+  c.ri = 0;
+  c.v0 = 0;
+  c.wp = st.base + (size_t)st.row0 * st.rstride + (size_t)lane * 16;
+  c.sp = PH == 1 ? p.ws + (size_t)st.row0 * p.sstride + (lane >> 2) : nullptr;
+  return c;
+}
+
+// kBatch vectors per lane (and, for int4, their scales, two per word).
+template <int PH>
+struct Batch {
+  uint4 w[kBatch];
+  uint32_t s[PH == 1 ? kBatch / 2 : 1];
+};
+
+template <int PH>
+EE_DEV void load_batch(const LinearParams& p, const Stream& st, LoadCursor& c, Batch<PH>& b) {
 #pragma unroll
   for (int j = 0; j < kBatch; ++j) {
-    if (base + 32 * j < total) {
-      const int row = pl.r0 + warp + kWarps * ri;
-      uint8_t* dst = slot + j * 512 + lane * 16;
-      const uint8_t* src = wbase + (size_t)row * rstride + (size_t)(v0 + lane) * 16;
-#ifdef EE_CHECKED
-      const uint32_t so = smem_addr(dst) - smem_addr(smem_base_sym);
-      const bool okd = EE_CHECK(p.err, so % 16 == 0 && so + 16 <= dyn_smem_size(), 11, so, dyn_smem_size());
-      const bool oks = EE_CHECK(p.err, ((uintptr_t)src & 15) == 0 && row >= pl.r0 && row < pl.r1 && v0 + lane < nv,
-                                12, row, v0 + lane);
-      if (okd && oks)
-#endif
-        cp_async16(dst, src);
-      if (PH == 1 && sc_async && lane == j) {
-        const uint16_t* ssrc = p.ws + (size_t)row * p.sstride + (v0 >> 2);
-        if (EE_CHECK(p.err, ((uintptr_t)ssrc & 15) == 0, 13, row, v0))
-          cp_async16(slot + kBatch * 512 + j * 16, ssrc);
+    if (c.ri < st.nrw) {
+      b.w[j] = ldg_stream_v4(c.wp);
+      if constexpr (PH == 1) {
+        const uint32_t sv = ldg_u16(c.sp);
+        b.s[j >> 1] = (j & 1) ? (b.s[j >> 1] | (sv << 16)) : sv;
       }
     }
-    v0 += 32;
-    if (v0 >= nv) {
-      v0 -= nv;
-      ++ri;
+    c.v0 += 32;
+    c.wp += 512;
+    if constexpr (PH == 1) c.sp += 8;
+    if (c.v0 >= st.nv) {
+      c.v0 = 0;
+      ++c.ri;
+      c.wp += (size_t)kWarps * st.rstride - (size_t)st.nv * 16;
+      if constexpr (PH == 1) c.sp += (size_t)kWarps * p.sstride - st.nv / 4;
     }
   }
 }
 
-template <int PH, bool XS, int MMAX>
-EE_DEV void dot_vec(const uint4& wv, uint16_t sbits, const uint16_t* const* xrow, int k, int mc, float* acc) {
-  if (PH == 0) {
+// Activations of the pass's sequences: row m starts at xb + xoff[m] (fp16, pair order).
+template <int PH, int MMAX>
+EE_DEV void dot_vec(const uint4& wv, uint32_t sbits, const uint16_t* xb, const int32_t* xoff, int k, int mc,
+                    float* acc) {
+  if constexpr (PH == 0) {
 #pragma unroll
     for (int m = 0; m < MMAX; ++m) {
-      if (m < mc) {
-        const uint4 xv = XS ? *reinterpret_cast<const uint4*>(xrow[m] + k) : ldg_nc_v4(xrow[m] + k);
-        acc[m] = dot8_bf16(wv, xv, acc[m]);
-      }
+      if (m < mc) acc[m] = dot8_bf16(wv, *reinterpret_cast<const uint4*>(xb + xoff[m] + k), acc[m]);
     }
   } else {
-    const float sc = bf16_bits_to_float(sbits);
+    const float sc = __uint_as_float(sbits << 16);
 #pragma unroll
     for (int m = 0; m < MMAX; ++m) {
       if (m < mc) {
-        const uint16_t* xp = xrow[m] + k;
-        uint4 x0, x1, x2, x3;
-        if (XS) {
-          x0 = *reinterpret_cast<const uint4*>(xp);
-          x1 = *reinterpret_cast<const uint4*>(xp + 8);
-          x2 = *reinterpret_cast<const uint4*>(xp + 16);
-          x3 = *reinterpret_cast<const uint4*>(xp + 24);
-        } else {
-          x0 = ldg_nc_v4(xp);
-          x1 = ldg_nc_v4(xp + 8);
-          x2 = ldg_nc_v4(xp + 16);
-          x3 = ldg_nc_v4(xp + 24);
-        }
+        const uint4* xp = reinterpret_cast<const uint4*>(xb + xoff[m] + k);
         __half2 h = __float2half2_rn(0.0f);
-        h = dot8_int4(wv.x, x0, h);
-        h = dot8_int4(wv.y, x1, h);
-        h = dot8_int4(wv.z, x2, h);
-        h = dot8_int4(wv.w, x3, h);
+        h = dot8_int4(wv.x, xp[0], h);
+        h = dot8_int4(wv.y, xp[1], h);
+        h = dot8_int4(wv.z, xp[2], h);
+        h = dot8_int4(wv.w, xp[3], h);
         const float2 f = __half22float2(h);
         acc[m] = fmaf(sc, f.x + f.y, acc[m]);
       }
@@ -292,108 +305,175 @@ EE_DEV void flush_row(float* rowsum, int mcap, int row_local, int mc, float* acc
   }
 }
 
-template <int PH, bool XS, int MMAX>
-EE_DEV void compute_batch(const LinearParams& p, const Plan& pl, const uint8_t* slot, bool sc_async, int base,
-                          int total, int nv, int& cur, const uint16_t* const* xrow, int mc, float* acc,
-                          float* rowsum, int warp, int lane) {
+template <int PH, int MMAX>
+EE_DEV void compute_batch(const Stream& st, Cursor& c, const Batch<PH>& b, int& cur, const uint16_t* xb,
+                          const int32_t* xoff, int mc, int mcap, float* acc, float* rowsum, int warp, int lane) {
   const int epv = PH == 0 ? 8 : 32;  // elements per vector
-  int ri = base / nv;
-  int v0 = base - ri * nv;  // warp-uniform vector index of lane 0
 #pragma unroll
   for (int j = 0; j < kBatch; ++j) {
-    if (base + 32 * j < total) {
-      if (ri != cur) {
-        flush_row<MMAX>(rowsum, pl.mcap, warp + kWarps * cur, mc, acc, lane);
-        cur = ri;
+    if (c.ri < st.nrw) {
+      if (c.ri != cur) {
+        flush_row<MMAX>(rowsum, mcap, warp + kWarps * cur, mc, acc, lane);
+        cur = c.ri;
       }
-      const uint4 wv = *reinterpret_cast<const uint4*>(slot + j * 512 + lane * 16);
-      uint16_t sbits = 0;
-      if (PH == 1)
-        sbits = sc_async ? reinterpret_cast<const uint16_t*>(slot + kBatch * 512 + j * 16)[lane >> 2]
-                         : ldg_u16(p.ws + (size_t)(pl.r0 + warp + kWarps * ri) * p.sstride + ((v0 + lane) >> 2));
-      dot_vec<PH, XS, MMAX>(wv, sbits, xrow, (v0 + lane) * epv, mc, acc);
+      const uint32_t sbits = PH == 1 ? (b.s[j >> 1] >> (16 * (j & 1))) & 0xFFFFu : 0u;
+      dot_vec<PH, MMAX>(b.w[j], sbits, xb, xoff, (c.v0 + lane) * epv, mc, acc);
     }
-    v0 += 32;
-    if (v0 >= nv) {
-      v0 -= nv;
-      ++ri;
+    c.v0 += 32;
+    if (c.v0 >= st.nv) {
+      c.v0 = 0;
+      ++c.ri;
     }
   }
 }
 
-EE_DEV void wait_slots(int nslots) {
-  if (nslots >= 4)
-    cp_async_wait<3>();
-  else if (nslots == 3)
-    cp_async_wait<2>();
-  else
-    cp_async_wait<1>();
-}
-
-// The first nslots - 1 batches of a warp's stream (weights only, so they may
-// be requested before the grid dependency wait).
-template <int PH>
-EE_DEV void stream_prologue(const LinearParams& p, const Plan& pl, int warp, int lane, uint8_t* ring,
-                            bool sc_async, uint64_t pol) {
-  const int nrows = pl.r1 - pl.r0;
-  const int nrw = nrows > warp ? (nrows - warp + kWarps - 1) / kWarps : 0;
-  const int nv = PH == 0 ? p.K / 8 : p.K / 32;
-  if (nv % 32 != 0) return;
-  const int total = nrw * nv;
-  for (int b = 0; b < p.nslots - 1; ++b) {
-    if (b * 32 * kBatch < total)
-      issue_batch<PH>(p, pl, warp, lane, nv, total, b * 32 * kBatch, ring + (size_t)b * kSlotBytes, sc_async, pol);
-    cp_async_commit();
-  }
-}
-
-// Streams this warp's rows of one phase (PH 0: bf16 weights, 1: int4) for
-// the mc sequences of one pass and writes each row's sums into rowsum.
-// `pre`: stream_prologue already ran for this pass.
-template <int PH, bool XS, int MMAX>
-EE_DEV void stream_rows(const LinearParams& p, const Plan& pl, int warp, int lane, int mc,
-                        const uint16_t* const* xrow, float* rowsum, uint8_t* ring, bool sc_async, bool pre,
-                        uint64_t pol) {
-  const int nrows = pl.r1 - pl.r0;
-  const int nrw = nrows > warp ? (nrows - warp + kWarps - 1) / kWarps : 0;  // rows of this warp
-  const int nv = PH == 0 ? p.K / 8 : p.K / 32;                             // vectors per row
+// Streams this warp's rows of one phase for the mc sequences of one pass and
+// writes each row's sums into rowsum.  Two register batches alternate: the
+// next batch's loads are issued before the current one is consumed.  `pre`:
+// batch 0 was loaded into `a` (load cursor `lc`) before the dependency wait.
+template <int PH, int MMAX>
+EE_DEV void stream_rows(const LinearParams& p, const Plan& pl, int warp, int lane, int mc, const uint16_t* xb,
+                        const int32_t* xoff, float* rowsum, Batch<PH>& a, LoadCursor& lc, bool pre) {
+  const Stream st = make_stream<PH>(p, pl, warp);
   float acc[MMAX];
 #pragma unroll
   for (int m = 0; m < MMAX; ++m) acc[m] = 0.0f;
-  if (nv % 32 == 0) {
-    const int total = nrw * nv;
-    const int bstep = 32 * kBatch;
-    const int nb = (total + bstep - 1) / bstep;
-    const int ns = p.nslots;
-    if (!pre) stream_prologue<PH>(p, pl, warp, lane, ring, sc_async, pol);
-    int cur = 0;
-    for (int b = 0; b < nb; ++b) {
-      const int bn = b + ns - 1;
-      if (bn < nb)
-        issue_batch<PH>(p, pl, warp, lane, nv, total, bn * bstep, ring + (size_t)(bn % ns) * kSlotBytes, sc_async,
-                        pol);
-      cp_async_commit();
-      wait_slots(ns);  // batch b has landed
-      __syncwarp();
-      compute_batch<PH, XS, MMAX>(p, pl, ring + (size_t)(b % ns) * kSlotBytes, sc_async, b * bstep, total, nv, cur,
-                                  xrow, mc, acc, rowsum, warp, lane);
-      __syncwarp();  // the slot is refilled next iteration
+  if (st.nv % 32 == 0) {
+    const int nb = (st.nrw * st.nv + 32 * kBatch - 1) / (32 * kBatch);
+    if (!pre) {
+      lc = load_start<PH>(p, st, lane);
+      load_batch<PH>(p, st, lc, a);
     }
-    if (nrw > 0) flush_row<MMAX>(rowsum, pl.mcap, warp + kWarps * cur, mc, acc, lane);
-    cp_async_wait<0>();
+    Cursor cc = {0, 0};
+    int cur = 0;
+    Batch<PH> b;
+    for (int i = 0; i < nb; i += 2) {
+      if (i + 1 < nb) load_batch<PH>(p, st, lc, b);
+      compute_batch<PH, MMAX>(st, cc, a, cur, xb, xoff, mc, pl.mcap, acc, rowsum, warp, lane);
+      if (i + 2 < nb) load_batch<PH>(p, st, lc, a);
+      if (i + 1 < nb) compute_batch<PH, MMAX>(st, cc, b, cur, xb, xoff, mc, pl.mcap, acc, rowsum, warp, lane);
+    }
+    if (st.nrw > 0) flush_row<MMAX>(rowsum, pl.mcap, warp + kWarps * cur, mc, acc, lane);
   } else {
     // short or odd rows: one row at a time, lanes stride over its vectors
-    const size_t rstride = PH == 0 ? (size_t)p.K * 2 : (size_t)p.K / 2;
-    const uint8_t* wbase = PH == 0 ? reinterpret_cast<const uint8_t*>(p.w) : p.wq;
-    for (int ri = 0; ri < nrw; ++ri) {
-      const int row = pl.r0 + warp + kWarps * ri;
-      for (int v = lane; v < nv; v += 32) {
-        const uint4 wv = ldg_nc_v4(wbase + (size_t)row * rstride + (size_t)v * 16);
-        const uint16_t sbits = PH == 1 ? ldg_u16(p.ws + (size_t)row * p.sstride + (v >> 2)) : 0;
-        dot_vec<PH, XS, MMAX>(wv, sbits, xrow, v * (PH == 0 ? 8 : 32), mc, acc);
+    for (int ri = 0; ri < st.nrw; ++ri) {
+      const int row = st.row0 + kWarps * ri;
+      for (int v = lane; v < st.nv; v += 32) {
+        const uint4 wv = ldg_stream_v4(st.base + (size_t)row * st.rstride + (size_t)v * 16);
+        const uint32_t sbits = PH == 1 ? ldg_u16(p.ws + (size_t)row * p.sstride + (v >> 2)) : 0u;
+        dot_vec<PH, MMAX>(wv, sbits, xb, xoff, v * (PH == 0 ? 8 : 32), mc, acc);
       }
       flush_row<MMAX>(rowsum, pl.mcap, warp + kWarps * ri, mc, acc, lane);
     }
+  }
+}
+
+// Epilogue of one pass: the CTA's row sums for sequences m0 .. m0 + mc - 1
+// of list `lst` are complete in rowsum.
+template <int EPI, int MMAX>
+EE_DEV void pass_epilogue(const LinearParams& p, const Plan& pl, const int32_t* lst, int m0, int mc,
+                          const float* rowsum, float* hst, int nrows, int tid, int warp, int lane) {
+  if constexpr (EPI == EPI_HEAD) {
+    Stat stat[MMAX];
+#pragma unroll
+    for (int m = 0; m < MMAX; ++m) stat[m] = Stat{-INFINITY, 0.0f, 0x7fffffff};
+    for (int r = tid; r < nrows; r += kThreads) {
+#pragma unroll
+      for (int m = 0; m < MMAX; ++m)
+        if (m < mc) stat_push(stat[m], rowsum[r * pl.mcap + m], pl.r0 + r);
+    }
+#pragma unroll
+    for (int m = 0; m < MMAX; ++m) {
+      if (m < mc) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          Stat t;
+          t.mx = __shfl_xor_sync(0xffffffffu, stat[m].mx, o);
+          t.sum = __shfl_xor_sync(0xffffffffu, stat[m].sum, o);
+          t.arg = __shfl_xor_sync(0xffffffffu, stat[m].arg, o);
+          stat[m] = stat_merge(stat[m], t);
+        }
+        if (lane == 0) {
+          float* hs = hst + (warp * kMM + m) * 3;
+          hs[0] = stat[m].mx;
+          hs[1] = stat[m].sum;
+          hs[2] = __int_as_float(stat[m].arg);
+        }
+      }
+    }
+    __syncthreads();
+    if (warp == 0 && lane < mc) {
+      Stat sm = {-INFINITY, 0.0f, 0x7fffffff};
+      for (int w = 0; w < kWarps; ++w) {
+        const float* hs = hst + (w * kMM + lane) * 3;
+        sm = stat_merge(sm, Stat{hs[0], hs[1], __float_as_int(hs[2])});
+      }
+      float* dst = p.head_part + ((size_t)blockIdx.x * EE_MAX_BATCH + m0 + lane) * 4;
+      dst[0] = sm.mx;
+      dst[1] = sm.sum;
+      dst[2] = __int_as_float(sm.arg);
+    }
+  } else {
+    int seqs_m[MMAX];
+#pragma unroll
+    for (int m = 0; m < MMAX; ++m) seqs_m[m] = lst[1 + m0 + min(m, mc - 1)];
+    const int npr = nrows >> 1;
+    for (int i = tid; i < npr * mc; i += kThreads) {
+      const int pr = i / mc, m = i - pr * mc;
+      int seq = seqs_m[0];
+#pragma unroll
+      for (int mm = 1; mm < MMAX; ++mm)
+        if (mm == m) seq = seqs_m[mm];
+      epi_pair<EPI>(p, seq, pl.r0 + 2 * pr, rowsum[(2 * pr) * pl.mcap + m],
+                    rowsum[(2 * pr + 1) * pl.mcap + m]);
+    }
+  }
+}
+
+// Everything up to the first pass: the dependency wait, then the step's
+// activations copied into shared memory (XS mode).
+template <bool XS>
+EE_DEV void wait_and_stage(const LinearParams& p, const int32_t* lf, const int32_t* le, int nf, int nx,
+                           uint8_t* xs, int tid) {
+  grid_dep_wait();
+  grid_dep_launch();
+  if (XS && nx > 0) {
+    // the activations of the step's rows, written by the previous kernel
+    const int v16 = p.K / 8;  // 16-byte vectors per row
+    for (int i = tid; i < nx * v16; i += kThreads) {
+      const int m = i / v16, c = i - m * v16;
+      const int seq = m < nf ? lf[1 + m] : le[1 + m - nf];
+#ifdef EE_CHECKED
+      if (!EE_CHECK(p.err, (size_t)(i + 1) * 16 <= (size_t)p.xs_rows * p.K * 2 && seq >= 0 && seq < EE_MAX_BATCH, 15,
+                    i, seq))
+        continue;
+#endif
+      reinterpret_cast<uint4*>(xs)[i] = *reinterpret_cast<const uint4*>(p.xh + (size_t)seq * p.x_stride + c * 8);
+    }
+  }
+  __syncthreads();
+}
+
+// All passes of one phase (PH 0: the full list on bf16 weights, PH 1: the
+// exit list on int4 weights).
+template <int EPI, bool XS, int MMAX, int PH>
+EE_DEV void run_phase(const LinearParams& p, const Plan& pl, const int32_t* lst, int nlist, int xbase,
+                      const uint8_t* xs, float* rowsum, float* hst, int nrows, int tid, int warp, int lane,
+                      Batch<PH>& a, LoadCursor& lc, bool pre) {
+  for (int pass = 0; pass < pl.passes[PH]; ++pass) {
+    const int m0 = pass * pl.mcap;
+    const int mc = min(pl.mcap, nlist - m0);
+    const uint16_t* xb = XS ? reinterpret_cast<const uint16_t*>(xs) : p.xh;
+    int32_t xoff[MMAX];
+#pragma unroll
+    for (int m = 0; m < MMAX; ++m) {
+      const int mm = min(m, mc - 1);
+      xoff[m] = XS ? (xbase + m0 + mm) * p.K : lst[1 + m0 + mm] * p.x_stride;
+    }
+    stream_rows<PH, MMAX>(p, pl, warp, lane, mc, xb, xoff, rowsum, a, lc, pre && pass == 0);
+    __syncthreads();  // every row sum of this pass is complete
+    pass_epilogue<EPI, MMAX>(p, pl, lst, m0, mc, rowsum, hst, nrows, tid, warp, lane);
+    __syncthreads();  // row sums are reused by the next pass
   }
 }
 
@@ -405,7 +485,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
   float* hst = reinterpret_cast<float*>(smem + 2 * kListLen * 4 + 16);
   uint8_t* xs = smem + kHeaderBytes;
   float* rowsum = reinterpret_cast<float*>(xs + (XS ? (size_t)p.xs_rows * p.K * 2 : 0));
-  uint8_t* rings = reinterpret_cast<uint8_t*>(rowsum) + (((size_t)p.rows_cap * p.mcap * 4 + 15) / 16 * 16);
   __shared__ int s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -431,110 +510,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
   }
   const int nrows = pl.r1 - pl.r0;
 
-  uint8_t* ring = rings + (size_t)warp * p.nslots * kSlotBytes;
-  const uint64_t pol = l2_evict_first_policy();
-  const bool sc_async = p.K % 1024 == 0 && p.sstride * EE_QUANT_GROUP == p.K;
-  // Weights do not depend on the previous kernel: start this warp's stream now.
-  const int first_phase = pl.passes[0] > 0 ? 0 : (pl.passes[1] > 0 ? 1 : -1);
-  if (first_phase == 0) stream_prologue<0>(p, pl, warp, lane, ring, sc_async, pol);
-  if (first_phase == 1) stream_prologue<1>(p, pl, warp, lane, ring, sc_async, pol);
-  grid_dep_wait();
-  grid_dep_launch();
-  if (XS && nx > 0) {
-    // the activations of the step's rows, written by the previous kernel
-    const int v16 = p.K / 8;  // 16-byte vectors per row
-    for (int i = tid; i < nx * v16; i += kThreads) {
-      const int m = i / v16, c = i - m * v16;
-      const int seq = m < nf ? lf[1 + m] : le[1 + m - nf];
-#ifdef EE_CHECKED
-      if (!EE_CHECK(p.err, (size_t)(i + 1) * 16 <= (size_t)p.xs_rows * p.K * 2 && seq >= 0 && seq < EE_MAX_BATCH, 15,
-                    i, seq))
-        continue;
-#endif
-      reinterpret_cast<uint4*>(xs)[i] = *reinterpret_cast<const uint4*>(p.xh + (size_t)seq * p.x_stride + c * 8);
+  // Weights do not depend on the previous kernel: the first batch of this
+  // warp's stream is requested before the dependency wait.
+  if (pl.passes[0] > 0) {
+    Batch<0> a;
+    LoadCursor lc;
+    const Stream st = make_stream<0>(p, pl, warp);
+    const bool pre = st.nv % 32 == 0;
+    if (pre) {
+      lc = load_start<0>(p, st, lane);
+      load_batch<0>(p, st, lc, a);
     }
-  }
-  __syncthreads();
-
-  for (int phase = 0; phase < 2; ++phase) {
-    const int nlist = phase == 0 ? nf : ne;
-    const int32_t* lst = phase == 0 ? lf : le;
-    const int xbase = phase == 0 ? 0 : nf;  // XS row of the phase's first sequence
-    for (int pass = 0; pass < pl.passes[phase]; ++pass) {
-      const int m0 = pass * pl.mcap;
-      const int mc = min(pl.mcap, nlist - m0);
-      const uint16_t* xrow[MMAX];
-#pragma unroll
-      for (int m = 0; m < MMAX; ++m) {
-        const int mm = min(m, mc - 1);
-        xrow[m] = XS ? reinterpret_cast<const uint16_t*>(xs) + (size_t)(xbase + m0 + mm) * p.K
-                     : p.xh + (size_t)lst[1 + m0 + mm] * p.x_stride;
-      }
-      const bool pre = phase == first_phase && pass == 0;
-      if (phase == 0)
-        stream_rows<0, XS, MMAX>(p, pl, warp, lane, mc, xrow, rowsum, ring, sc_async, pre, pol);
-      else
-        stream_rows<1, XS, MMAX>(p, pl, warp, lane, mc, xrow, rowsum, ring, sc_async, pre, pol);
-      __syncthreads();  // every row sum of this pass is complete
-      if constexpr (EPI == EPI_HEAD) {
-        Stat stat[MMAX];
-#pragma unroll
-        for (int m = 0; m < MMAX; ++m) stat[m] = Stat{-INFINITY, 0.0f, 0x7fffffff};
-        for (int r = tid; r < nrows; r += kThreads) {
-#pragma unroll
-          for (int m = 0; m < MMAX; ++m)
-            if (m < mc) stat_push(stat[m], rowsum[r * pl.mcap + m], pl.r0 + r);
-        }
-#pragma unroll
-        for (int m = 0; m < MMAX; ++m) {
-          if (m < mc) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-              Stat t;
-              t.mx = __shfl_xor_sync(0xffffffffu, stat[m].mx, o);
-              t.sum = __shfl_xor_sync(0xffffffffu, stat[m].sum, o);
-              t.arg = __shfl_xor_sync(0xffffffffu, stat[m].arg, o);
-              stat[m] = stat_merge(stat[m], t);
-            }
-            if (lane == 0) {
-              float* hs = hst + (warp * kMM + m) * 3;
-              hs[0] = stat[m].mx;
-              hs[1] = stat[m].sum;
-              hs[2] = __int_as_float(stat[m].arg);
-            }
-          }
-        }
-        __syncthreads();
-        if (warp == 0 && lane < mc) {
-          Stat sm = {-INFINITY, 0.0f, 0x7fffffff};
-          for (int w = 0; w < kWarps; ++w) {
-            const float* hs = hst + (w * kMM + lane) * 3;
-            sm = stat_merge(sm, Stat{hs[0], hs[1], __float_as_int(hs[2])});
-          }
-          float* dst = p.head_part + ((size_t)blockIdx.x * EE_MAX_BATCH + m0 + lane) * 4;
-          dst[0] = sm.mx;
-          dst[1] = sm.sum;
-          dst[2] = __int_as_float(sm.arg);
-        }
-      } else {
-        int seqs_m[MMAX];
-#pragma unroll
-        for (int m = 0; m < MMAX; ++m) seqs_m[m] = lst[1 + m0 + min(m, mc - 1)];
-        const int npr = nrows >> 1;
-        for (int i = tid; i < npr * mc; i += kThreads) {
-          const int pr = i / mc, m = i - pr * mc;
-          int seq = seqs_m[0];
-#pragma unroll
-          for (int mm = 1; mm < MMAX; ++mm)
-            if (mm == m) seq = seqs_m[mm];
-          epi_pair<EPI>(p, seq, pl.r0 + 2 * pr, rowsum[(2 * pr) * pl.mcap + m],
-                        rowsum[(2 * pr + 1) * pl.mcap + m]);
-        }
-      }
-      __syncthreads();  // row sums are reused by the next pass
+    wait_and_stage<XS>(p, lf, le, nf, nx, xs, tid);
+    run_phase<EPI, XS, MMAX, 0>(p, pl, lf, nf, 0, xs, rowsum, hst, nrows, tid, warp, lane, a, lc, pre);
+    if (pl.passes[1] > 0) {
+      Batch<1> a1;
+      LoadCursor lc1;
+      run_phase<EPI, XS, MMAX, 1>(p, pl, le, ne, nf, xs, rowsum, hst, nrows, tid, warp, lane, a1, lc1, false);
     }
+  } else {
+    Batch<1> a;
+    LoadCursor lc;
+    const Stream st = make_stream<1>(p, pl, warp);
+    const bool pre = pl.passes[1] > 0 && st.nv % 32 == 0;
+    if (pre) {
+      lc = load_start<1>(p, st, lane);
+      load_batch<1>(p, st, lc, a);
+    }
+    wait_and_stage<XS>(p, lf, le, nf, nx, xs, tid);
+    run_phase<EPI, XS, MMAX, 1>(p, pl, le, ne, nf, xs, rowsum, hst, nrows, tid, warp, lane, a, lc, pre);
   }
-
   if constexpr (EPI == EPI_HEAD) {
     // Last CTA to finish merges the per-CTA partials (no spin wait: a counter).
     __syncthreads();
@@ -625,8 +630,7 @@ cudaError_t set_smem_attr() {
 }
 
 size_t smem_of(const LinearParams& p) {
-  return kHeaderBytes + (p.xs_rows > 0 ? (size_t)p.xs_rows * p.K * 2 : 0) +
-         ((size_t)p.rows_cap * p.mcap * 4 + 15) / 16 * 16 + (size_t)kWarps * p.nslots * kSlotBytes;
+  return kHeaderBytes + (p.xs_rows > 0 ? (size_t)p.xs_rows * p.K * 2 : 0) + (size_t)p.rows_cap * p.mcap * 4;
 }
 
 template <int EPI>
@@ -659,12 +663,6 @@ void plan_smem(LinearParams& p, int grid) {
   const size_t xb = (size_t)max_rows * p.K * 2;
   const bool xs = max_rows <= kMM && xb <= kXsMaxBytes;
   p.xs_rows = xs ? max_rows : 0;
-  // Three slots (two batches in flight per lane, 64 KB per SM) in a CTA small
-  // enough that the next kernel's CTA fits beside it and starts its stream
-  // before this one ends; fewer when that does not fit.
-  p.nslots = 3;
-  while (p.nslots > 2 && smem_of(p) > kSmemPair) --p.nslots;
-  if (smem_of(p) > kSmemMax) p.nslots = 2;
 }
 
 }  // namespace
