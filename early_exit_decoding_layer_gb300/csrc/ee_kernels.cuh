@@ -68,11 +68,21 @@ struct LinearParams {
   // rows: either lists (count + ids) or a direct count with ids 0..m_direct-1
   const int32_t* list_full;  // rows on the bf16 weights (may be null)
   const int32_t* list_exit;  // rows on the int4 weights (may be null)
+  // nonzero: the previous launch wrote the lists, so they are read only after
+  // the grid dependency wait (and no weights are requested before it)
+  int32_t lists_after_wait;
   int32_t m_direct_full;     // used when list_full == null
   int32_t m_direct_exit;     // used when list_exit == null
   // activations by sequence id, fp16 in pair order (runs of 8: 0,4,1,5,2,6,3,7)
   const uint16_t* xh;
   int32_t x_stride;
+  // RMSNorm applied while staging (only when linear_stages_x() holds): the
+  // staged row is fp16(h * rsqrt(mean(h^2) + eps) * g) from the fp32 residual
+  // stream instead of xh (null: stage xh as is)
+  const float* norm_h;
+  int32_t norm_stride;
+  const uint16_t* norm_g;
+  float norm_eps;
   int32_t epi;
   // EPI_F32
   float* out_f32;
@@ -118,6 +128,9 @@ cudaError_t launch_linear(const LinearParams& p, int grid, bool pdl, cudaStream_
 int linear_grid(int N, int num_sms);
 // True if rows of K bf16 or int4 weights can be streamed in row-aligned stages.
 bool linear_shape_ok(int K);
+// True when a launch over at most max_rows sequences stages its activations
+// in shared memory (and so can apply RMSNorm itself).
+bool linear_stages_x(int max_rows, int K);
 
 // ------------------------------------------------------------------ attention
 struct AttnParams {

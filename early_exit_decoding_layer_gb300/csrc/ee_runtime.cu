@@ -398,13 +398,26 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
   base.head_part = c->head_part;
   base.gamma = c->gamma_dev;
 
+  // With at most a few sequences the GEMV stages its activations in shared
+  // memory and applies each RMSNorm itself; otherwise a norm kernel runs first.
+  const bool fuse_norm = linear_stages_x(B, m.d);
+  auto norm_on_stage = [&](LinearParams& lp, const uint16_t* g) {
+    lp.norm_h = c->h;
+    lp.norm_stride = m.d;
+    lp.norm_g = g;
+    lp.norm_eps = c->cfg.rms_eps;
+  };
+  bool lists_just_written = true;  // by the step-begin kernel
+
   for (int j = 0; j < m.L; ++j) {
     const LayerBufs& w = c->layers[j];
     // attention RMSNorm of every participating sequence
-    np.list = c->lists->part;
-    np.g = w.g_attn;
-    np.xh = c->xh;
-    EE_LAUNCH(log, EE_K_NORM, j, launch_rmsnorm(np, B, true, st));
+    if (!fuse_norm) {
+      np.list = c->lists->part;
+      np.g = w.g_attn;
+      np.xh = c->xh;
+      EE_LAUNCH(log, EE_K_NORM, j, launch_rmsnorm(np, B, true, st));
+    }
     // QKV projection + RoPE + K/V write into the shared paged cache
     LinearParams p = base;
     p.N = m.nqkv;
@@ -417,12 +430,17 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.list_exit = c->lists->exitl;
     p.xh = c->xh;
     p.x_stride = m.d;
+    if (fuse_norm) {
+      norm_on_stage(p, w.g_attn);
+      p.lists_after_wait = lists_just_written ? 1 : 0;
+    }
     p.epi = EPI_QKV;
     p.q_out = c->q;
     p.kc = c->kcache + (size_t)j * m.kv_layer_elems;
     p.vc = c->vcache + (size_t)j * m.kv_layer_elems;
     p.max_rows = B;
     EE_LAUNCH(log, EE_K_QKV, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
+    lists_just_written = false;
     // decode attention
     AttnParams ap = {};
     ap.list = c->lists->part;
@@ -460,8 +478,10 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.max_rows = B;
     EE_LAUNCH(log, EE_K_O, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
     // FFN RMSNorm
-    np.g = w.g_ffn;
-    EE_LAUNCH(log, EE_K_NORM, j, launch_rmsnorm(np, B, true, st));
+    if (!fuse_norm) {
+      np.g = w.g_ffn;
+      EE_LAUNCH(log, EE_K_NORM, j, launch_rmsnorm(np, B, true, st));
+    }
     // gate/up + SwiGLU
     p = base;
     p.N = 2 * m.F;
@@ -474,6 +494,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.list_exit = c->lists->exitl;
     p.xh = c->xh;
     p.x_stride = m.d;
+    if (fuse_norm) norm_on_stage(p, w.g_ffn);
     p.epi = EPI_SWIGLU;
     p.xh_out = c->acth;
     p.xo_stride = m.F;
@@ -500,10 +521,12 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     if (heads && ck != c->ckpts.end()) {
       const int ci = (int)(ck - c->ckpts.begin());
       // u = RMSNorm_final(h) T_c for the sequences still on the backbone
-      NormParams fp = np;
-      fp.list = c->lists->full;
-      fp.g = c->g_final;
-      EE_LAUNCH(log, EE_K_HEAD_NORM, j, launch_rmsnorm(fp, B, true, st));
+      if (!fuse_norm) {
+        NormParams fp = np;
+        fp.list = c->lists->full;
+        fp.g = c->g_final;
+        EE_LAUNCH(log, EE_K_HEAD_NORM, j, launch_rmsnorm(fp, B, true, st));
+      }
       p = base;
       p.N = m.d;
       p.K = m.d;
@@ -512,6 +535,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
       p.list_exit = nullptr;
       p.xh = c->xh;
       p.x_stride = m.d;
+      if (fuse_norm) norm_on_stage(p, c->g_final);
       p.epi = EPI_X;
       p.xh_out = c->uh;
       p.xo_stride = m.d;
@@ -537,13 +561,16 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
       p.max_rows = B;
       EE_LAUNCH(log, EE_K_HEAD_E, j,
                 launch_linear(p, std::min(linear_grid(p.N, c->num_sms), kHeadGridMax), true, st));
+      lists_just_written = true;  // compacted by the exit head
     }
   }
   // final LM head: argmax of RMSNorm_final(h) E^T
-  NormParams fp = np;
-  fp.list = c->lists->fin;
-  fp.g = c->g_final;
-  EE_LAUNCH(log, EE_K_FINAL_NORM, -1, launch_rmsnorm(fp, B, true, st));
+  if (!fuse_norm) {
+    NormParams fp = np;
+    fp.list = c->lists->fin;
+    fp.g = c->g_final;
+    EE_LAUNCH(log, EE_K_FINAL_NORM, -1, launch_rmsnorm(fp, B, true, st));
+  }
   LinearParams p = base;
   p.N = m.V;
   p.K = m.d;
@@ -552,6 +579,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
   p.list_exit = nullptr;
   p.xh = c->xh;
   p.x_stride = m.d;
+  if (fuse_norm) norm_on_stage(p, c->g_final);
   p.epi = EPI_HEAD;
   p.head_mode = HEAD_FINAL;
   p.head_counter = c->head_cnt;
@@ -936,9 +964,11 @@ ee_status ee_step_io(const ee_ctx* c, int32_t batch, int32_t heads, size_t* h2d,
   if (h2d) *h2d = sizeof(StepDesc);
   if (d2h) *d2h = step_d2h_bytes(batch);
   if (launches) {
-    // begin + per layer (2 norms, QKV, attention, O, gate/up, down) + heads + final norm/head
+    // begin + per layer (2 norms unless the GEMVs apply them, QKV, attention,
+    // O, gate/up, down) + heads (norm, T, E) + final norm and head
     const int with_heads = heads && c->m.nck > 0;
-    *launches = 1 + 7 * c->m.L + (with_heads ? 3 * c->m.nck : 0) + 2;
+    const int norms = linear_stages_x(batch, c->m.d) ? 0 : 1;
+    *launches = 1 + (5 + 2 * norms) * c->m.L + (with_heads ? (2 + norms) * c->m.nck : 0) + 1 + norms;
   }
   return EE_OK;
 }

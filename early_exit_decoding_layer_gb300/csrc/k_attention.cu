@@ -11,12 +11,15 @@
 // are issued before the grid dependency wait and overlap the QKV projection
 // still running; the block holding the current position is copied after it.
 //
-// Compute: lanes own 8 head dims (one 16-byte shared load per row); hd/8
-// lanes form a token group; scores are reduced across the group with xor
-// shuffles and the softmax is online (running max m, sum l, weighted values
-// acc).  Token groups, then warps, are merged; the CTA writes one partial
-// (acc, m, l) per head, and the last CTA of each (sequence, kv head) -- found
-// with an atomic counter, nothing waits -- merges the partials:
+// Compute, in three phases over the CTA's tokens (at most BPC * 16): (1)
+// scores s = q_h . k_t / sqrt(hd) for every query head of the group into
+// shared memory -- lanes own 8 head dims (one 16-byte shared load per row),
+// hd/8 lanes form a token group and reduce with xor shuffles; (2) per head
+// the CTA-wide max m and p_t = exp(s_t - m), l = sum p_t; (3) acc = sum p_t
+// v_t with independent accumulators per lane, reduced over token groups and
+// warps.  The CTA writes one partial (acc, m, l) per head, and the last CTA
+// of each (sequence, kv head) -- found with an atomic counter, nothing waits
+// -- merges the partials:
 // o = sum_i acc_i exp(m_i - M) / sum_i l_i exp(m_i - M), M = max_i m_i.
 //
 // Cache layout (one layer): [block][kv head][16 slots][head_dim] fp16.
@@ -29,7 +32,7 @@ namespace ee {
 
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kWarps = 8;
 constexpr int kThreadsA = kWarps * 32;
 constexpr int kKvSmem = 64 * 1024;  // K + V tiles of one CTA
 constexpr int kMaxSplit = 128;
@@ -44,29 +47,11 @@ EE_DEV void to_float8(const uint4& v, float* f) {
   }
 }
 
-// Merge (m2, l2, a2) into (m1, l1, a1).
-template <int N>
-EE_DEV void merge_state(float& m1, float& l1, float* a1, float m2, float l2, const float* a2) {
-  if (l2 == 0.0f) return;
-  if (l1 == 0.0f) {
-    m1 = m2;
-    l1 = l2;
-#pragma unroll
-    for (int i = 0; i < N; ++i) a1[i] = a2[i];
-    return;
-  }
-  const float m = fmaxf(m1, m2);
-  const float c1 = expf(m1 - m), c2 = expf(m2 - m);
-  l1 = l1 * c1 + l2 * c2;
-#pragma unroll
-  for (int i = 0; i < N; ++i) a1[i] = a1[i] * c1 + a2[i] * c2;
-  m1 = m;
-}
-
 template <int HD>
 constexpr int blocks_per_cta() {
   return kKvSmem / (2 * 16 * HD * 2);
 }
+static_assert(blocks_per_cta<64>() <= 32 && blocks_per_cta<128>() <= 32, "one lane per block");
 
 template <int HD, int G>
 __global__ void __launch_bounds__(kThreadsA) k_attention(const AttnParams p) {
@@ -107,13 +92,15 @@ __global__ void __launch_bounds__(kThreadsA) k_attention(const AttnParams p) {
   }
   __syncthreads();
   const uint64_t pol = l2_evict_first_policy();
-  if (tid == 0 && have) {
-    mbar_arrive_expect_tx(&bar, (uint32_t)(b1 - b0) * 2 * TILE * 2);
-    for (int b = b0; b < b1; ++b) {
-      if (b == last) continue;
+  if (warp == 0 && have) {
+    // one lane per block: the block-table reads and the copies go out in parallel
+    if (lane == 0) mbar_arrive_expect_tx(&bar, (uint32_t)(b1 - b0) * 2 * TILE * 2);
+    __syncwarp();
+    const int b = b0 + lane;
+    if (b < b1 && b != last) {
       const size_t off = ((size_t)ld_volatile_i32(bt + b) * hkv + g) * TILE;
-      bulk_g2s(Ks + (b - b0) * TILE, p.kc + off, TILE * 2, &bar, pol);
-      bulk_g2s(Vs + (b - b0) * TILE, p.vc + off, TILE * 2, &bar, pol);
+      bulk_g2s(Ks + lane * TILE, p.kc + off, TILE * 2, &bar, pol);
+      bulk_g2s(Vs + lane * TILE, p.vc + off, TILE * 2, &bar, pol);
     }
   }
   grid_dep_wait();
@@ -125,108 +112,126 @@ __global__ void __launch_bounds__(kThreadsA) k_attention(const AttnParams p) {
   }
   if (!active) return;
 
-  const float scale = rsqrtf((float)HD);
-  float q[G][8];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const float4* qp =
-        reinterpret_cast<const float4*>(p.q + (size_t)seq * p.q_stride + (g * G + h) * HD + dl * 8);
-    const float4 a = qp[0], b = qp[1];
-    q[h][0] = a.x * scale;
-    q[h][1] = a.y * scale;
-    q[h][2] = a.z * scale;
-    q[h][3] = a.w * scale;
-    q[h][4] = b.x * scale;
-    q[h][5] = b.y * scale;
-    q[h][6] = b.z * scale;
-    q[h][7] = b.w * scale;
-  }
-  float mrun[G], lrun[G], acc[G][8];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    mrun[h] = -INFINITY;
-    lrun[h] = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[h][i] = 0.0f;
-  }
+  constexpr int TOK = BPC * 16;  // tokens per CTA at most
+  __shared__ float S[G][TOK];    // scores, then exp(s - m)
+  __shared__ float hm[G], hl[G];
+  float* wpart = reinterpret_cast<float*>(smem);  // [warp][PSZ], after the tiles are consumed
 
   bool ok = true;
   if (have) ok = mbar_wait_bounded(&bar, 0, p.err, DERR_FULL_WAIT);
   if (have && !ok) mbar_wait_bounded(&bar, 0, p.err, DERR_DRAIN_WAIT);  // copies land before reuse
-  if (have && ok) {
-    const int t0 = b0 * 16, t1 = min(ctx, b1 * 16);
-    for (int base = t0 + warp * TPW; base < t1; base += kWarps * TPW) {
-      const int t = base + sub;
-      const bool valid = t < t1;
-      const int row = valid ? t - t0 : 0;
-      float kf[8], vf[8];
-      to_float8(*reinterpret_cast<const uint4*>(Ks + row * HD + dl * 8), kf);
-      to_float8(*reinterpret_cast<const uint4*>(Vs + row * HD + dl * 8), vf);
+  const bool run = have && ok;
+  const int t0 = b0 * 16, n = run ? min(ctx, b1 * 16) - t0 : 0;  // tokens of this CTA
+
+  // (1) scores
+  if (n > 0) {
+    const float scale = rsqrtf((float)HD);
+    float q[G][8];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float4* qp =
+          reinterpret_cast<const float4*>(p.q + (size_t)seq * p.q_stride + (g * G + h) * HD + dl * 8);
+      const float4 a = qp[0], b = qp[1];
+      q[h][0] = a.x * scale;
+      q[h][1] = a.y * scale;
+      q[h][2] = a.z * scale;
+      q[h][3] = a.w * scale;
+      q[h][4] = b.x * scale;
+      q[h][5] = b.y * scale;
+      q[h][6] = b.z * scale;
+      q[h][7] = b.w * scale;
+    }
+    for (int base = warp * TPW; base < n; base += kWarps * TPW) {
+      const int r = base + sub;
+      float kf[8];
+      to_float8(*reinterpret_cast<const uint4*>(Ks + min(r, n - 1) * HD + dl * 8), kf);
+      float sc[G];
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        float s = 0.0f;
+        float d = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) s = fmaf(q[h][i], kf[i], s);
-#pragma unroll
-        for (int o = LPT / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (valid) {
-          const float mn = fmaxf(mrun[h], s);
-          const float c = expf(mrun[h] - mn);
-          const float e = expf(s - mn);
-          lrun[h] = lrun[h] * c + e;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) acc[h][i] = fmaf(acc[h][i], c, e * vf[i]);
-          mrun[h] = mn;
-        }
+        for (int i = 0; i < 8; ++i) d = fmaf(q[h][i], kf[i], d);
+        sc[h] = d;
       }
-    }
-  }
-
-  // merge the token groups of this warp (lanes with the same dims)
 #pragma unroll
-  for (int o = LPT; o < 32; o <<= 1) {
+      for (int o = LPT / 2; o > 0; o >>= 1) {
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, mrun[h], o);
-      const float l2 = __shfl_xor_sync(0xffffffffu, lrun[h], o);
-      float a2[8];
+        for (int h = 0; h < G; ++h) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], o);
+      }
+      if (dl == 0 && r < n) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) a2[i] = __shfl_xor_sync(0xffffffffu, acc[h][i], o);
-      merge_state<8>(mrun[h], lrun[h], acc[h], m2, l2, a2);
-    }
-  }
-  __syncthreads();  // the K/V tiles are no longer read: reuse the space
-  float* wpart = reinterpret_cast<float*>(smem);  // [warp][PSZ]
-  if (sub == 0) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float* dst = wpart + warp * PSZ;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) dst[h * HD + dl * 8 + i] = acc[h][i];
-      if (dl == 0) {
-        dst[G * HD + h] = mrun[h];
-        dst[G * HD + G + h] = lrun[h];
+        for (int h = 0; h < G; ++h) S[h][r] = sc[h];
       }
     }
   }
   __syncthreads();
+  // (2) per head: m = max s, p = exp(s - m), l = sum p
+  if (warp < G) {
+    const int h = warp;
+    float m = -INFINITY;
+    for (int r = lane; r < n; r += 32) m = fmaxf(m, S[h][r]);
+    m = warp_max(m);
+    float l = 0.0f;
+    for (int r = lane; r < n; r += 32) {
+      const float e = expf(S[h][r] - m);
+      S[h][r] = e;
+      l += e;
+    }
+    l = warp_sum(l);
+    if (lane == 0) {
+      hm[h] = n > 0 ? m : -INFINITY;
+      hl[h] = l;
+    }
+  }
+  __syncthreads();
+  // (3) acc = sum_t p_t v_t
+  float acc[G][8];
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[h][i] = 0.0f;
+  for (int base = warp * TPW; base < n; base += kWarps * TPW) {
+    const int r = base + sub;
+    if (r < n) {
+      float vf[8];
+      to_float8(*reinterpret_cast<const uint4*>(Vs + r * HD + dl * 8), vf);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float pr = S[h][r];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[h][i] = fmaf(pr, vf[i], acc[h][i]);
+      }
+    }
+  }
+  // sum the token groups of this warp (lanes with the same dims)
+#pragma unroll
+  for (int o = LPT; o < 32; o <<= 1) {
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[h][i] += __shfl_xor_sync(0xffffffffu, acc[h][i], o);
+  }
+  __syncthreads();  // the K/V tiles are no longer read: reuse the space
+  if (sub == 0) {
+    float* dst = wpart + warp * PSZ;
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dst[h * HD + dl * 8 + i] = acc[h][i];
+  }
+  __syncthreads();
 
-  // CTA partial: merge the warps
+  // CTA partial: sum the warps (one m per head for the whole CTA)
   float* part = p.part + (((size_t)z * hkv + g) * p.nsplit + split) * PSZ;
   for (int idx = tid; idx < G * HD; idx += kThreadsA) {
-    const int h = idx / HD;
-    float m = -INFINITY, l = 0.0f, a = 0.0f;
+    float a = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float* src = wpart + w * PSZ;
-      float a2 = src[idx];
-      merge_state<1>(m, l, &a, src[G * HD + h], src[G * HD + G + h], &a2);
-    }
+    for (int w = 0; w < kWarps; ++w) a += wpart[w * PSZ + idx];
     part[idx] = a;
-    if (idx % HD == 0) {
-      part[G * HD + h] = m;
-      part[G * HD + G + h] = l;
-    }
+  }
+  if (tid < G) {
+    part[G * HD + tid] = hm[tid];
+    part[G * HD + G + tid] = hl[tid];
   }
   __syncthreads();
   if (tid == 0) {

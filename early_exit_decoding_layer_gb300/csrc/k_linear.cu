@@ -51,6 +51,8 @@ constexpr size_t kHeaderBytes = 3072;
 constexpr size_t kXsMaxBytes = 64 * 1024;
 constexpr size_t kSmemMax = 227 * 1024 - 1024;
 static_assert(2 * kListLen * 4 + 16 + kWarps * kMM * 3 * 4 <= kHeaderBytes, "header overflow");
+// the staging RMSNorm keeps its per-warp sums [kMM][kWarps] in the head-statistics area
+static_assert(kMM * kWarps <= kWarps * kMM * 3, "norm scratch");
 
 EE_DEV __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
@@ -193,7 +195,15 @@ EE_DEV bool check_ok(int32_t* err, bool ok, int site, long long v1, long long v2
 
 // One warp's share of a phase: its rows r0 + warp + kWarps * i (i < nrw) of
 // the bf16 matrix (PH 0) or of the packed int4 matrix (PH 1), nv 16-byte
-// vectors each.
+// vectors each.  When nv % 32 == 0 the rows are walked as one stream of
+// steps of 32 vectors (one per lane: a warp reads 512 contiguous bytes per
+// step), in batches of kU<PH> steps.  A batch that lies inside one row takes
+// the unrolled path; one that crosses a row boundary steps vector by vector.
+// Several sequences per pass need more registers per vector: smaller batches.
+template <int PH, int MMAX>
+constexpr int kU = (PH == 0 ? 8 : 4) / (MMAX == 1 ? 1 : 2);
+static_assert(kU<0, 1> <= kBatch && kU<1, 1> <= kBatch, "batch storage");
+
 struct Stream {
   const uint8_t* base;
   size_t rstride;  // bytes per row
@@ -212,14 +222,8 @@ EE_DEV Stream make_stream(const LinearParams& p, const Plan& pl, int warp) {
   return s;
 }
 
-// Streams are walked 32 vectors at a time (nv % 32 == 0), so the 32 lanes of
-// one step always lie in one row and a warp reads 512 contiguous bytes.
-// Position in a warp's stream: its ri-th row, vector v0 + lane.
-struct Cursor {
-  int ri, v0;
-};
-
-// Load-side position: the cursor plus this lane's weight (and scale) address.
+// Load-side position: row ri of the warp's rows, vector v0 + lane, and this
+// lane's weight (and scale) addresses.
 struct LoadCursor {
   int ri, v0;
   const uint8_t* wp;
@@ -236,56 +240,78 @@ EE_DEV LoadCursor load_start(const LinearParams& p, const Stream& st, int lane) 
   return c;
 }
 
-// kBatch vectors per lane (and, for int4, their scales, two per word).
-template <int PH>
+// Vectors of one batch per lane (and, for int4, their scales, two per word).
 struct Batch {
   uint4 w[kBatch];
-  uint32_t s[PH == 1 ? kBatch / 2 : 1];
+  uint32_t s[kBatch / 2];
 };
 
 template <int PH>
-EE_DEV void load_batch(const LinearParams& p, const Stream& st, LoadCursor& c, Batch<PH>& b) {
+EE_DEV void next_row(const LinearParams& p, const Stream& st, LoadCursor& c) {
+  c.v0 = 0;
+  ++c.ri;
+  c.wp += (size_t)kWarps * st.rstride - (size_t)st.nv * 16;
+  if constexpr (PH == 1) c.sp += (size_t)kWarps * p.sstride - st.nv / 4;
+}
+
+template <int PH>
+EE_DEV void put_scale(Batch& b, int j, uint32_t sv) {
+  b.s[j >> 1] = (j & 1) ? (b.s[j >> 1] | (sv << 16)) : sv;
+}
+
+template <int PH, int MMAX>
+EE_DEV void load_batch(const LinearParams& p, const Stream& st, LoadCursor& c, Batch& b) {
+  constexpr int U = kU<PH, MMAX>;
+  if (c.ri >= st.nrw) return;
+  if (c.v0 + 32 * U <= st.nv) {
 #pragma unroll
-  for (int j = 0; j < kBatch; ++j) {
-    if (c.ri < st.nrw) {
-      b.w[j] = ldg_stream_v4(c.wp);
-      if constexpr (PH == 1) {
-        const uint32_t sv = ldg_u16(c.sp);
-        b.s[j >> 1] = (j & 1) ? (b.s[j >> 1] | (sv << 16)) : sv;
-      }
+    for (int j = 0; j < U; ++j) {
+      b.w[j] = ldg_stream_v4(c.wp + j * 512);
+      if constexpr (PH == 1) put_scale<PH>(b, j, ldg_u16(c.sp + j * 8));
     }
-    c.v0 += 32;
-    c.wp += 512;
-    if constexpr (PH == 1) c.sp += 8;
-    if (c.v0 >= st.nv) {
-      c.v0 = 0;
-      ++c.ri;
-      c.wp += (size_t)kWarps * st.rstride - (size_t)st.nv * 16;
-      if constexpr (PH == 1) c.sp += (size_t)kWarps * p.sstride - st.nv / 4;
+    c.v0 += 32 * U;
+    c.wp += 512 * U;
+    if constexpr (PH == 1) c.sp += 8 * U;
+    if (c.v0 == st.nv) next_row<PH>(p, st, c);
+  } else {
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      if (c.ri < st.nrw) {
+        b.w[j] = ldg_stream_v4(c.wp);
+        if constexpr (PH == 1) put_scale<PH>(b, j, ldg_u16(c.sp));
+      }
+      c.v0 += 32;
+      c.wp += 512;
+      if constexpr (PH == 1) c.sp += 8;
+      if (c.v0 == st.nv) next_row<PH>(p, st, c);
     }
   }
 }
 
-// Activations of the pass's sequences: row m starts at xb + xoff[m] (fp16, pair order).
-template <int PH, int MMAX>
-EE_DEV void dot_vec(const uint4& wv, uint32_t sbits, const uint16_t* xb, const int32_t* xoff, int k, int mc,
-                    float* acc) {
+// Activations of the pass's sequences: row m starts at xb + xoff[m] (fp16,
+// pair order).  int4 rows staged in shared memory (PL) are stored as four
+// planes so that the four 16-byte chunks of one vector sit in four planes at
+// the lane's index (conflict-free): chunk c at (c % 4) * (K / 32) + c / 4.
+template <int PH, bool PL, int MMAX>
+EE_DEV void dot_vec(const uint4& wv, uint32_t sbits, const uint16_t* xb, const int32_t* xoff, int v, int nv,
+                    int mc, float* acc) {
   if constexpr (PH == 0) {
 #pragma unroll
     for (int m = 0; m < MMAX; ++m) {
-      if (m < mc) acc[m] = dot8_bf16(wv, *reinterpret_cast<const uint4*>(xb + xoff[m] + k), acc[m]);
+      if (m < mc) acc[m] = dot8_bf16(wv, *reinterpret_cast<const uint4*>(xb + xoff[m] + v * 8), acc[m]);
     }
   } else {
     const float sc = __uint_as_float(sbits << 16);
 #pragma unroll
     for (int m = 0; m < MMAX; ++m) {
       if (m < mc) {
-        const uint4* xp = reinterpret_cast<const uint4*>(xb + xoff[m] + k);
+        const uint4* xp = reinterpret_cast<const uint4*>(xb + xoff[m]);
+        const int i0 = PL ? v : 4 * v, di = PL ? nv : 1;
         __half2 h = __float2half2_rn(0.0f);
-        h = dot8_int4(wv.x, xp[0], h);
-        h = dot8_int4(wv.y, xp[1], h);
-        h = dot8_int4(wv.z, xp[2], h);
-        h = dot8_int4(wv.w, xp[3], h);
+        h = dot8_int4(wv.x, xp[i0], h);
+        h = dot8_int4(wv.y, xp[i0 + di], h);
+        h = dot8_int4(wv.z, xp[i0 + 2 * di], h);
+        h = dot8_int4(wv.w, xp[i0 + 3 * di], h);
         const float2 f = __half22float2(h);
         acc[m] = fmaf(sc, f.x + f.y, acc[m]);
       }
@@ -305,24 +331,38 @@ EE_DEV void flush_row(float* rowsum, int mcap, int row_local, int mc, float* acc
   }
 }
 
-template <int PH, int MMAX>
-EE_DEV void compute_batch(const Stream& st, Cursor& c, const Batch<PH>& b, int& cur, const uint16_t* xb,
+template <int PH>
+EE_DEV uint32_t scale_of(const Batch& b, int j) {
+  return PH == 1 ? (b.s[j >> 1] >> (16 * (j & 1))) & 0xFFFFu : 0u;
+}
+
+// Consumes one batch; the compute-side cursor (ri, v0) mirrors the load
+// side, and each completed row is flushed.
+template <int PH, bool PL, int MMAX>
+EE_DEV void compute_batch(const Stream& st, int& ri, int& v0, const Batch& b, const uint16_t* xb,
                           const int32_t* xoff, int mc, int mcap, float* acc, float* rowsum, int warp, int lane) {
-  const int epv = PH == 0 ? 8 : 32;  // elements per vector
+  constexpr int U = kU<PH, MMAX>;
+  if (ri >= st.nrw) return;
+  if (v0 + 32 * U <= st.nv) {
 #pragma unroll
-  for (int j = 0; j < kBatch; ++j) {
-    if (c.ri < st.nrw) {
-      if (c.ri != cur) {
-        flush_row<MMAX>(rowsum, mcap, warp + kWarps * cur, mc, acc, lane);
-        cur = c.ri;
-      }
-      const uint32_t sbits = PH == 1 ? (b.s[j >> 1] >> (16 * (j & 1))) & 0xFFFFu : 0u;
-      dot_vec<PH, MMAX>(b.w[j], sbits, xb, xoff, (c.v0 + lane) * epv, mc, acc);
+    for (int j = 0; j < U; ++j)
+      dot_vec<PH, PL, MMAX>(b.w[j], scale_of<PH>(b, j), xb, xoff, v0 + 32 * j + lane, st.nv, mc, acc);
+    v0 += 32 * U;
+    if (v0 == st.nv) {
+      flush_row<MMAX>(rowsum, mcap, warp + kWarps * ri, mc, acc, lane);
+      v0 = 0;
+      ++ri;
     }
-    c.v0 += 32;
-    if (c.v0 >= st.nv) {
-      c.v0 = 0;
-      ++c.ri;
+  } else {
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      if (ri < st.nrw) dot_vec<PH, PL, MMAX>(b.w[j], scale_of<PH>(b, j), xb, xoff, v0 + lane, st.nv, mc, acc);
+      v0 += 32;
+      if (v0 == st.nv) {
+        if (ri < st.nrw) flush_row<MMAX>(rowsum, mcap, warp + kWarps * ri, mc, acc, lane);
+        v0 = 0;
+        ++ri;
+      }
     }
   }
 }
@@ -331,29 +371,28 @@ EE_DEV void compute_batch(const Stream& st, Cursor& c, const Batch<PH>& b, int& 
 // writes each row's sums into rowsum.  Two register batches alternate: the
 // next batch's loads are issued before the current one is consumed.  `pre`:
 // batch 0 was loaded into `a` (load cursor `lc`) before the dependency wait.
-template <int PH, int MMAX>
+template <int PH, bool PL, int MMAX>
 EE_DEV void stream_rows(const LinearParams& p, const Plan& pl, int warp, int lane, int mc, const uint16_t* xb,
-                        const int32_t* xoff, float* rowsum, Batch<PH>& a, LoadCursor& lc, bool pre) {
+                        const int32_t* xoff, float* rowsum, Batch& a, LoadCursor& lc, bool pre) {
   const Stream st = make_stream<PH>(p, pl, warp);
   float acc[MMAX];
 #pragma unroll
   for (int m = 0; m < MMAX; ++m) acc[m] = 0.0f;
   if (st.nv % 32 == 0) {
-    const int nb = (st.nrw * st.nv + 32 * kBatch - 1) / (32 * kBatch);
+    constexpr int U = kU<PH, MMAX>;
+    const int nb = (st.nrw * (st.nv / 32) + U - 1) / U;
     if (!pre) {
       lc = load_start<PH>(p, st, lane);
-      load_batch<PH>(p, st, lc, a);
+      load_batch<PH, MMAX>(p, st, lc, a);
     }
-    Cursor cc = {0, 0};
-    int cur = 0;
-    Batch<PH> b;
+    int ri = 0, v0 = 0;
+    Batch b;
     for (int i = 0; i < nb; i += 2) {
-      if (i + 1 < nb) load_batch<PH>(p, st, lc, b);
-      compute_batch<PH, MMAX>(st, cc, a, cur, xb, xoff, mc, pl.mcap, acc, rowsum, warp, lane);
-      if (i + 2 < nb) load_batch<PH>(p, st, lc, a);
-      if (i + 1 < nb) compute_batch<PH, MMAX>(st, cc, b, cur, xb, xoff, mc, pl.mcap, acc, rowsum, warp, lane);
+      if (i + 1 < nb) load_batch<PH, MMAX>(p, st, lc, b);
+      compute_batch<PH, PL, MMAX>(st, ri, v0, a, xb, xoff, mc, pl.mcap, acc, rowsum, warp, lane);
+      if (i + 2 < nb) load_batch<PH, MMAX>(p, st, lc, a);
+      if (i + 1 < nb) compute_batch<PH, PL, MMAX>(st, ri, v0, b, xb, xoff, mc, pl.mcap, acc, rowsum, warp, lane);
     }
-    if (st.nrw > 0) flush_row<MMAX>(rowsum, pl.mcap, warp + kWarps * cur, mc, acc, lane);
   } else {
     // short or odd rows: one row at a time, lanes stride over its vectors
     for (int ri = 0; ri < st.nrw; ++ri) {
@@ -361,7 +400,7 @@ EE_DEV void stream_rows(const LinearParams& p, const Plan& pl, int warp, int lan
       for (int v = lane; v < st.nv; v += 32) {
         const uint4 wv = ldg_stream_v4(st.base + (size_t)row * st.rstride + (size_t)v * 16);
         const uint32_t sbits = PH == 1 ? ldg_u16(p.ws + (size_t)row * p.sstride + (v >> 2)) : 0u;
-        dot_vec<PH, MMAX>(wv, sbits, xb, xoff, v * (PH == 0 ? 8 : 32), mc, acc);
+        dot_vec<PH, PL, MMAX>(wv, sbits, xb, xoff, v, st.nv, mc, acc);
       }
       flush_row<MMAX>(rowsum, pl.mcap, warp + kWarps * ri, mc, acc, lane);
     }
@@ -430,14 +469,62 @@ EE_DEV void pass_epilogue(const LinearParams& p, const Plan& pl, const int32_t* 
   }
 }
 
+// Staged position of 16-byte chunk c of an exit (int4) row: four planes.
+EE_DEV int x_plane_index(int c, int K) { return (c & 3) * (K / 32) + (c >> 2); }
+
 // Everything up to the first pass: the dependency wait, then the step's
 // activations copied into shared memory (XS mode).
 template <bool XS>
 EE_DEV void wait_and_stage(const LinearParams& p, const int32_t* lf, const int32_t* le, int nf, int nx,
-                           uint8_t* xs, int tid) {
+                           uint8_t* xs, float* red, int tid, int warp, int lane) {
   grid_dep_wait();
   grid_dep_launch();
-  if (XS && nx > 0) {
+  if (XS && nx > 0 && p.norm_h) {
+    // RMSNorm of the step's rows of the residual stream (written by the
+    // previous kernel): per-row sum of squares, then the scaled fp16 rows
+    const int v8 = p.K / 8;  // runs of 8 columns per row
+    for (int m = 0; m < nx; ++m) {
+      const int seq = m < nf ? lf[1 + m] : le[1 + m - nf];
+      const float4* h = reinterpret_cast<const float4*>(p.norm_h + (size_t)seq * p.norm_stride);
+      float ss = 0.0f;
+      for (int i = tid; i < v8; i += kThreads) {
+        const float4 a = h[2 * i], b = h[2 * i + 1];
+        ss = fmaf(a.x, a.x, ss);
+        ss = fmaf(a.y, a.y, ss);
+        ss = fmaf(a.z, a.z, ss);
+        ss = fmaf(a.w, a.w, ss);
+        ss = fmaf(b.x, b.x, ss);
+        ss = fmaf(b.y, b.y, ss);
+        ss = fmaf(b.z, b.z, ss);
+        ss = fmaf(b.w, b.w, ss);
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) red[m * kWarps + warp] = ss;
+    }
+    __syncthreads();
+    for (int i = tid; i < nx * v8; i += kThreads) {
+      const int m = i / v8, c = i - m * v8;
+      const int seq = m < nf ? lf[1 + m] : le[1 + m - nf];
+      const int dst = m * v8 + (m < nf ? c : x_plane_index(c, p.K));
+      float tot = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) tot += red[m * kWarps + w];
+      const float r = rsqrtf(tot / (float)p.K + p.norm_eps);
+      const float4* h = reinterpret_cast<const float4*>(p.norm_h + (size_t)seq * p.norm_stride) + 2 * c;
+      const float4 a = h[0], b = h[1];
+      const uint4 gw = *reinterpret_cast<const uint4*>(p.norm_g + (size_t)c * 8);
+      uint4 o;  // pair order: (x0,x4) (x1,x5) (x2,x6) (x3,x7)
+      o.x = uint32_t(float_to_half_bits(a.x * r * bf16_lo(gw.x))) |
+            (uint32_t(float_to_half_bits(b.x * r * bf16_lo(gw.z))) << 16);
+      o.y = uint32_t(float_to_half_bits(a.y * r * bf16_hi(gw.x))) |
+            (uint32_t(float_to_half_bits(b.y * r * bf16_hi(gw.z))) << 16);
+      o.z = uint32_t(float_to_half_bits(a.z * r * bf16_lo(gw.y))) |
+            (uint32_t(float_to_half_bits(b.z * r * bf16_lo(gw.w))) << 16);
+      o.w = uint32_t(float_to_half_bits(a.w * r * bf16_hi(gw.y))) |
+            (uint32_t(float_to_half_bits(b.w * r * bf16_hi(gw.w))) << 16);
+      reinterpret_cast<uint4*>(xs)[dst] = o;
+    }
+  } else if (XS && nx > 0) {
     // the activations of the step's rows, written by the previous kernel
     const int v16 = p.K / 8;  // 16-byte vectors per row
     for (int i = tid; i < nx * v16; i += kThreads) {
@@ -448,7 +535,8 @@ EE_DEV void wait_and_stage(const LinearParams& p, const int32_t* lf, const int32
                     i, seq))
         continue;
 #endif
-      reinterpret_cast<uint4*>(xs)[i] = *reinterpret_cast<const uint4*>(p.xh + (size_t)seq * p.x_stride + c * 8);
+      const int dst = m * v16 + (m < nf ? c : x_plane_index(c, p.K));
+      reinterpret_cast<uint4*>(xs)[dst] = *reinterpret_cast<const uint4*>(p.xh + (size_t)seq * p.x_stride + c * 8);
     }
   }
   __syncthreads();
@@ -459,7 +547,7 @@ EE_DEV void wait_and_stage(const LinearParams& p, const int32_t* lf, const int32
 template <int EPI, bool XS, int MMAX, int PH>
 EE_DEV void run_phase(const LinearParams& p, const Plan& pl, const int32_t* lst, int nlist, int xbase,
                       const uint8_t* xs, float* rowsum, float* hst, int nrows, int tid, int warp, int lane,
-                      Batch<PH>& a, LoadCursor& lc, bool pre) {
+                      Batch& a, LoadCursor& lc, bool pre) {
   for (int pass = 0; pass < pl.passes[PH]; ++pass) {
     const int m0 = pass * pl.mcap;
     const int mc = min(pl.mcap, nlist - m0);
@@ -470,7 +558,7 @@ EE_DEV void run_phase(const LinearParams& p, const Plan& pl, const int32_t* lst,
       const int mm = min(m, mc - 1);
       xoff[m] = XS ? (xbase + m0 + mm) * p.K : lst[1 + m0 + mm] * p.x_stride;
     }
-    stream_rows<PH, MMAX>(p, pl, warp, lane, mc, xb, xoff, rowsum, a, lc, pre && pass == 0);
+    stream_rows<PH, XS && PH == 1, MMAX>(p, pl, warp, lane, mc, xb, xoff, rowsum, a, lc, pre && pass == 0);
     __syncthreads();  // every row sum of this pass is complete
     pass_epilogue<EPI, MMAX>(p, pl, lst, m0, mc, rowsum, hst, nrows, tid, warp, lane);
     __syncthreads();  // row sums are reused by the next pass
@@ -488,8 +576,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
   __shared__ int s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Lists were written at least two launches back (see grid_dep_wait), so
-  // they may be read before this grid's dependency wait.
+  // Lists written at least two launches back (see grid_dep_wait) may be read
+  // before this grid's dependency wait; otherwise wait first.
+  if (p.lists_after_wait) grid_dep_wait();
   if (tid < kListLen) {
     lf[tid] = p.list_full ? ld_volatile_i32(p.list_full + tid) : (tid == 0 ? p.m_direct_full : tid - 1);
     le[tid] = p.list_exit ? ld_volatile_i32(p.list_exit + tid) : (tid == 0 ? p.m_direct_exit : tid - 1);
@@ -511,35 +600,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
   const int nrows = pl.r1 - pl.r0;
 
   // Weights do not depend on the previous kernel: the first batch of this
-  // warp's stream is requested before the dependency wait.
-  if (pl.passes[0] > 0) {
-    Batch<0> a;
-    LoadCursor lc;
-    const Stream st = make_stream<0>(p, pl, warp);
-    const bool pre = st.nv % 32 == 0;
-    if (pre) {
-      lc = load_start<0>(p, st, lane);
-      load_batch<0>(p, st, lc, a);
+  // warp's first phase is requested before the dependency wait.
+  Batch a;
+  LoadCursor lc;
+  int pre_phase = -1;
+  if (!p.lists_after_wait) {
+    if (pl.passes[0] > 0) {
+      const Stream st = make_stream<0>(p, pl, warp);
+      if (st.nv % 32 == 0) {
+        lc = load_start<0>(p, st, lane);
+        load_batch<0, MMAX>(p, st, lc, a);
+        pre_phase = 0;
+      }
+    } else if (pl.passes[1] > 0) {
+      const Stream st = make_stream<1>(p, pl, warp);
+      if (st.nv % 32 == 0) {
+        lc = load_start<1>(p, st, lane);
+        load_batch<1, MMAX>(p, st, lc, a);
+        pre_phase = 1;
+      }
     }
-    wait_and_stage<XS>(p, lf, le, nf, nx, xs, tid);
-    run_phase<EPI, XS, MMAX, 0>(p, pl, lf, nf, 0, xs, rowsum, hst, nrows, tid, warp, lane, a, lc, pre);
-    if (pl.passes[1] > 0) {
-      Batch<1> a1;
-      LoadCursor lc1;
-      run_phase<EPI, XS, MMAX, 1>(p, pl, le, ne, nf, xs, rowsum, hst, nrows, tid, warp, lane, a1, lc1, false);
-    }
-  } else {
-    Batch<1> a;
-    LoadCursor lc;
-    const Stream st = make_stream<1>(p, pl, warp);
-    const bool pre = pl.passes[1] > 0 && st.nv % 32 == 0;
-    if (pre) {
-      lc = load_start<1>(p, st, lane);
-      load_batch<1>(p, st, lc, a);
-    }
-    wait_and_stage<XS>(p, lf, le, nf, nx, xs, tid);
-    run_phase<EPI, XS, MMAX, 1>(p, pl, le, ne, nf, xs, rowsum, hst, nrows, tid, warp, lane, a, lc, pre);
   }
+  wait_and_stage<XS>(p, lf, le, nf, nx, xs, hst, tid, warp, lane);
+  // each phase's code exists once (the kernel stays small in the instruction cache)
+#pragma unroll 1
+  for (int phase = 0; phase < 2; ++phase) {
+    if (phase == 0)
+      run_phase<EPI, XS, MMAX, 0>(p, pl, lf, nf, 0, xs, rowsum, hst, nrows, tid, warp, lane, a, lc, pre_phase == 0);
+    else
+      run_phase<EPI, XS, MMAX, 1>(p, pl, le, ne, nf, xs, rowsum, hst, nrows, tid, warp, lane, a, lc, pre_phase == 1);
+  }
+
   if constexpr (EPI == EPI_HEAD) {
     // Last CTA to finish merges the per-CTA partials (no spin wait: a counter).
     __syncthreads();
@@ -660,9 +751,7 @@ void plan_smem(LinearParams& p, int grid) {
   p.mcap = max_rows < kMM ? max_rows : kMM;
   const int npairs = p.N / 2;
   p.rows_cap = 2 * ((npairs + grid - 1) / grid);
-  const size_t xb = (size_t)max_rows * p.K * 2;
-  const bool xs = max_rows <= kMM && xb <= kXsMaxBytes;
-  p.xs_rows = xs ? max_rows : 0;
+  p.xs_rows = linear_stages_x(max_rows, p.K) ? max_rows : 0;
 }
 
 }  // namespace
@@ -680,6 +769,11 @@ cudaError_t linear_prepare() {
 }
 
 bool linear_shape_ok(int K) { return K >= 32 && K % 32 == 0; }
+
+bool linear_stages_x(int max_rows, int K) {
+  const int rows = max_rows < 1 ? 1 : max_rows;
+  return rows <= kMM && (size_t)rows * K * 2 <= kXsMaxBytes;
+}
 
 int linear_grid(int N, int num_sms) {
   const int pairs = N / 2;
