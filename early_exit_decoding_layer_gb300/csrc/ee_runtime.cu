@@ -7,9 +7,11 @@
 #include <stdarg.h>
 #include <stddef.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <map>
 #include <string>
 #include <vector>
@@ -24,7 +26,7 @@ namespace {
 constexpr size_t kAlign = 256;
 
 size_t step_d2h_bytes(int B) { return offsetof(StepOut, conf) + (size_t)B * EE_MAX_CHECKPOINTS * sizeof(float); }
-constexpr int kHeadGridMax = 256;       // CTAs of a vocabulary-head launch (<= SMs)
+constexpr int kHeadGridMax = 512;       // CTAs of a vocabulary-head launch (>= the GEMV grid)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -87,6 +89,7 @@ struct ee_ctx {
   std::vector<int32_t> ckpts;
   Dims m;
   int dev = 0, num_sms = 0;
+  bool pdl = true;  // programmatic dependent launch between the step's kernels
   cudaStream_t user_stream = nullptr;
   cudaStream_t st = nullptr;   // the caller's stream, or our own if the caller gave NULL
   bool own_stream = false;
@@ -416,7 +419,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
       np.list = c->lists->part;
       np.g = w.g_attn;
       np.xh = c->xh;
-      EE_LAUNCH(log, EE_K_NORM, j, launch_rmsnorm(np, B, true, st));
+      EE_LAUNCH(log, EE_K_NORM, j, launch_rmsnorm(np, B, c->pdl, st));
     }
     // QKV projection + RoPE + K/V write into the shared paged cache
     LinearParams p = base;
@@ -439,7 +442,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.kc = c->kcache + (size_t)j * m.kv_layer_elems;
     p.vc = c->vcache + (size_t)j * m.kv_layer_elems;
     p.max_rows = B;
-    EE_LAUNCH(log, EE_K_QKV, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
+    EE_LAUNCH(log, EE_K_QKV, j, launch_linear(p, linear_grid(p.N, c->num_sms), c->pdl, st));
     lists_just_written = false;
     // decode attention
     AttnParams ap = {};
@@ -461,7 +464,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     ap.oh = c->ah;
     ap.o_stride = m.dq;
     ap.err = err;
-    EE_LAUNCH(log, EE_K_ATTN, j, launch_attention(ap, B, true, st));
+    EE_LAUNCH(log, EE_K_ATTN, j, launch_attention(ap, B, c->pdl, st));
     // O projection + residual
     p = base;
     p.N = m.d;
@@ -476,11 +479,11 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.x_stride = m.dq;
     p.epi = EPI_RESID;
     p.max_rows = B;
-    EE_LAUNCH(log, EE_K_O, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
+    EE_LAUNCH(log, EE_K_O, j, launch_linear(p, linear_grid(p.N, c->num_sms), c->pdl, st));
     // FFN RMSNorm
     if (!fuse_norm) {
       np.g = w.g_ffn;
-      EE_LAUNCH(log, EE_K_NORM, j, launch_rmsnorm(np, B, true, st));
+      EE_LAUNCH(log, EE_K_NORM, j, launch_rmsnorm(np, B, c->pdl, st));
     }
     // gate/up + SwiGLU
     p = base;
@@ -499,7 +502,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.xh_out = c->acth;
     p.xo_stride = m.F;
     p.max_rows = B;
-    EE_LAUNCH(log, EE_K_GATEUP, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
+    EE_LAUNCH(log, EE_K_GATEUP, j, launch_linear(p, linear_grid(p.N, c->num_sms), c->pdl, st));
     // down projection + residual (+ per-layer copy in debug mode)
     p = base;
     p.N = m.d;
@@ -515,7 +518,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.epi = EPI_RESID;
     p.hdbg = c->hdbg + (size_t)j * EE_MAX_BATCH * m.d;
     p.max_rows = B;
-    EE_LAUNCH(log, EE_K_DOWN, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
+    EE_LAUNCH(log, EE_K_DOWN, j, launch_linear(p, linear_grid(p.N, c->num_sms), c->pdl, st));
 
     const auto ck = std::find(c->ckpts.begin(), c->ckpts.end(), j);
     if (heads && ck != c->ckpts.end()) {
@@ -525,7 +528,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
         NormParams fp = np;
         fp.list = c->lists->full;
         fp.g = c->g_final;
-        EE_LAUNCH(log, EE_K_HEAD_NORM, j, launch_rmsnorm(fp, B, true, st));
+        EE_LAUNCH(log, EE_K_HEAD_NORM, j, launch_rmsnorm(fp, B, c->pdl, st));
       }
       p = base;
       p.N = m.d;
@@ -540,7 +543,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
       p.xh_out = c->uh;
       p.xo_stride = m.d;
       p.max_rows = B;
-      EE_LAUNCH(log, EE_K_HEAD_T, j, launch_linear(p, linear_grid(p.N, c->num_sms), true, st));
+      EE_LAUNCH(log, EE_K_HEAD_T, j, launch_linear(p, linear_grid(p.N, c->num_sms), c->pdl, st));
       // z = u E^T, conf = max softmax, exit if conf > gamma_c, compact the lists
       p = base;
       p.N = m.V;
@@ -560,7 +563,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
       p.ckpt_layer = j;
       p.max_rows = B;
       EE_LAUNCH(log, EE_K_HEAD_E, j,
-                launch_linear(p, std::min(linear_grid(p.N, c->num_sms), kHeadGridMax), true, st));
+                launch_linear(p, std::min(linear_grid(p.N, c->num_sms), kHeadGridMax), c->pdl, st));
       lists_just_written = true;  // compacted by the exit head
     }
   }
@@ -569,7 +572,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     NormParams fp = np;
     fp.list = c->lists->fin;
     fp.g = c->g_final;
-    EE_LAUNCH(log, EE_K_FINAL_NORM, -1, launch_rmsnorm(fp, B, true, st));
+    EE_LAUNCH(log, EE_K_FINAL_NORM, -1, launch_rmsnorm(fp, B, c->pdl, st));
   }
   LinearParams p = base;
   p.N = m.V;
@@ -586,7 +589,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
   p.argmax_out = c->out_dev->next_token;
   p.max_rows = B;
   EE_LAUNCH(log, EE_K_FINAL_HEAD, -1,
-            launch_linear(p, std::min(linear_grid(p.N, c->num_sms), kHeadGridMax), true, st));
+            launch_linear(p, std::min(linear_grid(p.N, c->num_sms), kHeadGridMax), c->pdl, st));
   EE_CUDA(c, cudaMemcpyAsync(c->out_host, c->out_dev, step_d2h_bytes(B), cudaMemcpyDeviceToHost, st));
   c->launches[heads ? 1 : 0] = log.n;
   return EE_OK;
@@ -771,7 +774,13 @@ ee_status ee_create(const ee_config* cfg, void* dev_arena, size_t arena_bytes, v
   if (cudaGetDevice(&c->dev) != cudaSuccess) return bail(EE_ERR_CUDA);
   if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->dev) != cudaSuccess)
     return bail(EE_ERR_CUDA);
-  if (c->num_sms > kHeadGridMax) c->num_sms = kHeadGridMax;
+  if (2 * c->num_sms > kHeadGridMax) c->num_sms = kHeadGridMax / 2;
+  {
+    // EE_PDL=0 launches the step's kernels without programmatic dependent
+    // launch (each waits for the previous one to finish), for comparison.
+    const char* e = getenv("EE_PDL");
+    c->pdl = !(e && e[0] == '0');
+  }
   if (linear_prepare() != cudaSuccess || attention_prepare() != cudaSuccess) return bail(EE_ERR_CUDA);
   if (c->user_stream) {
     c->st = c->user_stream;
@@ -1182,12 +1191,21 @@ ee_status ee_debug_int4(ee_ctx* c, int32_t layer, int32_t mat, uint8_t* packed, 
 }
 
 // ------------------------------------------------------------------ single kernels
+// Kernel attributes set and SM count read once per device (the op entry
+// points are called per launch, so they skip the per-call attribute calls).
+constexpr int kMaxOpDevices = 64;
+static std::atomic<int> g_op_sms[kMaxOpDevices];
+
 static int device_sms() {
   int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (linear_prepare() != cudaSuccess) return 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxOpDevices) return 0;
+  const int cached = g_op_sms[dev].load(std::memory_order_acquire);
+  if (cached > 0) return cached;
+  if (linear_prepare() != cudaSuccess || attention_prepare() != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  return n > kHeadGridMax ? kHeadGridMax : n;
+  n = 2 * n > kHeadGridMax ? kHeadGridMax / 2 : n;
+  g_op_sms[dev].store(n, std::memory_order_release);
+  return n;
 }
 
 ee_status ee_op_quantize_int4(const uint16_t* w, int32_t rows, int32_t cols, uint8_t* packed,
@@ -1277,7 +1295,6 @@ ee_status ee_op_attention(int32_t B, int32_t n_heads, int32_t n_kv_heads, int32_
   p.block_table = block_table;
   p.bt_stride = bt_stride;
   p.pos = pos;
-  if (attention_prepare() != cudaSuccess) return EE_ERR_CUDA;
   p.nsplit = attention_nsplit(max_ctx, head_dim);
   p.bpc = attention_blocks_per_cta(head_dim);
   const size_t pbytes = align_up(attention_part_floats(B, n_heads, n_kv_heads, head_dim, p.nsplit) * 4, kAlign);
