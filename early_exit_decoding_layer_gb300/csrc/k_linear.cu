@@ -8,19 +8,21 @@
 // group of 128 input columns, dequantised in registers and never written
 // back).  An empty list reads no byte of its matrix.
 //
-// Data flow: one CTA of 16 warps per SM owns a balanced, pair-aligned range
-// of output rows; warp w owns the CTA's rows w, w+16, ... and walks them as
-// one stream of 16-byte vectors, 32 at a time (a warp reads 512 contiguous
-// bytes per load instruction), straight into registers.  Two batches of 8
-// vectors per lane alternate: the loads of the next batch are issued before
-// the current one is consumed, so up to 64 KB per SM are in flight -- what
-// HBM3e needs to stream near its peak.  The first batch is requested before
-// the grid dependency wait (weights never change), so the stream starts
-// while the previous kernel drains; the activations of the step's rows (fp16,
-// a few KB per sequence), written by that kernel, are copied into shared
-// memory after the wait.  A warp finishes each of its rows alone (one warp
-// reduction), so results do not depend on timing.  The epilogue (RoPE + KV
-// write, SwiGLU, residual add, head statistics) runs once over the CTA's rows.
+// Data flow: two CTAs of 8 warps per SM each own a balanced, pair-aligned
+// range of output rows; warp w owns its CTA's rows w, w+8, ... and walks them
+// as one stream of 16-byte vectors, 32 at a time (a warp reads 512 contiguous
+// bytes per load instruction), straight into registers.  Two batches per
+// lane alternate (8 vectors each for bf16, 4 for int4): the loads of the next
+// batch are issued before the current one is consumed, so up to 64 KB per SM
+// are in flight -- what HBM3e needs to stream near its peak.  The first batch
+// is requested before the grid dependency wait (weights never change), and
+// with two CTA slots per SM the next launch's CTAs start that stream in the
+// slots this launch's finished CTAs free, while its last CTAs drain.  The
+// activations of the step's rows (fp16, a few KB per sequence), written by
+// the previous kernel, are copied into shared memory after the wait.  A warp
+// finishes each of its rows alone (one warp reduction), so results do not
+// depend on timing.  The epilogue (RoPE + KV write, SwiGLU, residual add,
+// head statistics) runs once over the CTA's rows.
 //
 // Activations are stored in "pair order" (within each run of 8 columns:
 // 0,4,1,5,2,6,3,7, see xh_slot) so that one 16-byte load yields the half2
@@ -40,7 +42,8 @@ namespace ee {
 
 namespace {
 
-constexpr int kWarps = 16;
+constexpr int kWarps = 8;
+constexpr int kCtasPerSm = 2;  // two CTAs per SM: one kernel's tail overlaps the next one's start
 constexpr int kThreads = kWarps * 32;
 constexpr int kBatch = 8;  // 16-byte vectors per lane per batch
 constexpr int kMM = 8;     // sequences per pass over the weights
@@ -409,10 +412,10 @@ EE_DEV void stream_rows(const LinearParams& p, const Plan& pl, int warp, int lan
 
 // Epilogue of one pass: the CTA's row sums for sequences m0 .. m0 + mc - 1
 // of list `lst` are complete in rowsum.
-template <int EPI, int MMAX>
+template <int MMAX>
 EE_DEV void pass_epilogue(const LinearParams& p, const Plan& pl, const int32_t* lst, int m0, int mc,
                           const float* rowsum, float* hst, int nrows, int tid, int warp, int lane) {
-  if constexpr (EPI == EPI_HEAD) {
+  if (p.epi == EPI_HEAD) {
     Stat stat[MMAX];
 #pragma unroll
     for (int m = 0; m < MMAX; ++m) stat[m] = Stat{-INFINITY, 0.0f, 0x7fffffff};
@@ -463,8 +466,15 @@ EE_DEV void pass_epilogue(const LinearParams& p, const Plan& pl, const int32_t* 
 #pragma unroll
       for (int mm = 1; mm < MMAX; ++mm)
         if (mm == m) seq = seqs_m[mm];
-      epi_pair<EPI>(p, seq, pl.r0 + 2 * pr, rowsum[(2 * pr) * pl.mcap + m],
-                    rowsum[(2 * pr + 1) * pl.mcap + m]);
+      const int ra = pl.r0 + 2 * pr;
+      const float ya = rowsum[(2 * pr) * pl.mcap + m], yb = rowsum[(2 * pr + 1) * pl.mcap + m];
+      switch (p.epi) {
+        case EPI_F32: epi_pair<EPI_F32>(p, seq, ra, ya, yb); break;
+        case EPI_QKV: epi_pair<EPI_QKV>(p, seq, ra, ya, yb); break;
+        case EPI_RESID: epi_pair<EPI_RESID>(p, seq, ra, ya, yb); break;
+        case EPI_SWIGLU: epi_pair<EPI_SWIGLU>(p, seq, ra, ya, yb); break;
+        default: epi_pair<EPI_X>(p, seq, ra, ya, yb); break;
+      }
     }
   }
 }
@@ -544,7 +554,7 @@ EE_DEV void wait_and_stage(const LinearParams& p, const int32_t* lf, const int32
 
 // All passes of one phase (PH 0: the full list on bf16 weights, PH 1: the
 // exit list on int4 weights).
-template <int EPI, bool XS, int MMAX, int PH>
+template <bool XS, int MMAX, int PH>
 EE_DEV void run_phase(const LinearParams& p, const Plan& pl, const int32_t* lst, int nlist, int xbase,
                       const uint8_t* xs, float* rowsum, float* hst, int nrows, int tid, int warp, int lane,
                       Batch& a, LoadCursor& lc, bool pre) {
@@ -560,13 +570,16 @@ EE_DEV void run_phase(const LinearParams& p, const Plan& pl, const int32_t* lst,
     }
     stream_rows<PH, XS && PH == 1, MMAX>(p, pl, warp, lane, mc, xb, xoff, rowsum, a, lc, pre && pass == 0);
     __syncthreads();  // every row sum of this pass is complete
-    pass_epilogue<EPI, MMAX>(p, pl, lst, m0, mc, rowsum, hst, nrows, tid, warp, lane);
+    pass_epilogue<MMAX>(p, pl, lst, m0, mc, rowsum, hst, nrows, tid, warp, lane);
     __syncthreads();  // row sums are reused by the next pass
   }
 }
 
-template <int EPI, bool XS, int MMAX>
-__global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
+// One kernel binary per (staging, sequences per pass) for every projection and
+// head: the epilogue is chosen at run time, so consecutive launches of a step
+// run the same code and find it warm in the instruction caches.
+template <bool XS, int MMAX>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) k_linear(const LinearParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   int32_t* lf = reinterpret_cast<int32_t*>(smem);
   int32_t* le = lf + kListLen;
@@ -626,12 +639,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
 #pragma unroll 1
   for (int phase = 0; phase < 2; ++phase) {
     if (phase == 0)
-      run_phase<EPI, XS, MMAX, 0>(p, pl, lf, nf, 0, xs, rowsum, hst, nrows, tid, warp, lane, a, lc, pre_phase == 0);
+      run_phase<XS, MMAX, 0>(p, pl, lf, nf, 0, xs, rowsum, hst, nrows, tid, warp, lane, a, lc, pre_phase == 0);
     else
-      run_phase<EPI, XS, MMAX, 1>(p, pl, le, ne, nf, xs, rowsum, hst, nrows, tid, warp, lane, a, lc, pre_phase == 1);
+      run_phase<XS, MMAX, 1>(p, pl, le, ne, nf, xs, rowsum, hst, nrows, tid, warp, lane, a, lc, pre_phase == 1);
   }
 
-  if constexpr (EPI == EPI_HEAD) {
+  if (p.epi == EPI_HEAD) {
     // Last CTA to finish merges the per-CTA partials (no spin wait: a counter).
     __syncthreads();
     if (tid == 0) {
@@ -704,27 +717,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_linear(const LinearParams p) {
   }
 }
 
-template <int EPI>
 cudaError_t set_smem_attr() {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(k_linear<EPI, false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kSmemMax)) != cudaSuccess)
+  if ((e = cudaFuncSetAttribute(k_linear<false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax)) !=
+      cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(k_linear<EPI, true, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kSmemMax)) != cudaSuccess)
+  if ((e = cudaFuncSetAttribute(k_linear<true, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax)) !=
+      cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(k_linear<EPI, false, kMM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kSmemMax)) != cudaSuccess)
+  if ((e = cudaFuncSetAttribute(k_linear<false, kMM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax)) !=
+      cudaSuccess)
     return e;
-  return cudaFuncSetAttribute(k_linear<EPI, true, kMM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)kSmemMax);
+  return cudaFuncSetAttribute(k_linear<true, kMM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax);
 }
 
 size_t smem_of(const LinearParams& p) {
   return kHeaderBytes + (p.xs_rows > 0 ? (size_t)p.xs_rows * p.K * 2 : 0) + (size_t)p.rows_cap * p.mcap * 4;
 }
 
-template <int EPI>
 cudaError_t launch_one(const LinearParams& p, int grid, bool pdl, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -737,11 +747,11 @@ cudaError_t launch_one(const LinearParams& p, int grid, bool pdl, cudaStream_t s
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   if (p.mcap == 1) {
-    if (p.xs_rows > 0) return cudaLaunchKernelEx(&cfg, k_linear<EPI, true, 1>, p);
-    return cudaLaunchKernelEx(&cfg, k_linear<EPI, false, 1>, p);
+    if (p.xs_rows > 0) return cudaLaunchKernelEx(&cfg, k_linear<true, 1>, p);
+    return cudaLaunchKernelEx(&cfg, k_linear<false, 1>, p);
   }
-  if (p.xs_rows > 0) return cudaLaunchKernelEx(&cfg, k_linear<EPI, true, kMM>, p);
-  return cudaLaunchKernelEx(&cfg, k_linear<EPI, false, kMM>, p);
+  if (p.xs_rows > 0) return cudaLaunchKernelEx(&cfg, k_linear<true, kMM>, p);
+  return cudaLaunchKernelEx(&cfg, k_linear<false, kMM>, p);
 }
 
 // Shared-memory plan of one launch: per-row sums for the CTA's rows and the
@@ -759,13 +769,7 @@ void plan_smem(LinearParams& p, int grid) {
 size_t linear_smem_bytes() { return kSmemMax; }
 
 cudaError_t linear_prepare() {
-  cudaError_t e;
-  if ((e = set_smem_attr<EPI_F32>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<EPI_QKV>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<EPI_RESID>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<EPI_SWIGLU>()) != cudaSuccess) return e;
-  if ((e = set_smem_attr<EPI_X>()) != cudaSuccess) return e;
-  return set_smem_attr<EPI_HEAD>();
+  return set_smem_attr();
 }
 
 bool linear_shape_ok(int K) { return K >= 32 && K % 32 == 0; }
@@ -776,23 +780,16 @@ bool linear_stages_x(int max_rows, int K) {
 }
 
 int linear_grid(int N, int num_sms) {
-  const int pairs = N / 2;
-  return pairs < num_sms ? (pairs > 0 ? pairs : 1) : num_sms;
+  const int pairs = N / 2, ctas = kCtasPerSm * num_sms;
+  return pairs < ctas ? (pairs > 0 ? pairs : 1) : ctas;
 }
 
 cudaError_t launch_linear(const LinearParams& p_in, int grid, bool pdl, cudaStream_t st) {
   LinearParams p = p_in;
   plan_smem(p, grid);
   if (smem_of(p) > kSmemMax) return cudaErrorInvalidConfiguration;
-  switch (p.epi) {
-    case EPI_F32: return launch_one<EPI_F32>(p, grid, pdl, st);
-    case EPI_QKV: return launch_one<EPI_QKV>(p, grid, pdl, st);
-    case EPI_RESID: return launch_one<EPI_RESID>(p, grid, pdl, st);
-    case EPI_SWIGLU: return launch_one<EPI_SWIGLU>(p, grid, pdl, st);
-    case EPI_X: return launch_one<EPI_X>(p, grid, pdl, st);
-    case EPI_HEAD: return launch_one<EPI_HEAD>(p, grid, pdl, st);
-  }
-  return cudaErrorInvalidValue;
+  if (p.epi < EPI_F32 || p.epi > EPI_HEAD) return cudaErrorInvalidValue;
+  return launch_one(p, grid, pdl, st);
 }
 
 }  // namespace ee
