@@ -1,6 +1,7 @@
 // Launch parameters and host-side launchers of the decode-step kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -116,6 +117,29 @@ struct LinearParams {
   int32_t ckpt_index, ckpt_layer;
   int32_t* err;
 };
+
+// ------------------------------------------------------------------ tensor-core GEMM
+// For steps whose batch is above the GEMV's staging limit: one launch serves
+// one sub-batch list (MODE 0: the full list on the bf16 weights through
+// `amap`; MODE 1: the exit list on the int4 copy), 128 weight rows per tile,
+// the K range split `ksplit` ways.
+struct TcParams {
+  CUtensorMap amap;     // bf16 weights [N, K]: box 64 (K) x 128 (rows), 128-byte swizzle
+  LinearParams lp;      // shapes, lists, activations, epilogue (as for the GEMV)
+  int32_t ntiles, ksplit, nks, nk;  // tiles, K splits, 64-wide K steps per split, K steps
+  float* part;          // [tile][split][64 columns][128 rows] fp32 partial sums
+  int32_t* tile_cnt;    // [ntiles] split counters, zero between launches
+};
+struct TcPlan {
+  int ntiles, ksplit, nks, nk;
+};
+TcPlan gemm_tc_plan(int N, int K, int num_sms);
+bool gemm_tc_shape_ok(int K);
+size_t gemm_tc_part_floats(int units);
+cudaError_t gemm_tc_prepare();
+cudaError_t launch_gemm_tc(const TcParams& tp, int mode, bool pdl, cudaStream_t st);
+// Tensor map of a bf16 weight matrix [N, K] (row stride K) for MODE 0.
+bool encode_weight_map(CUtensorMap* map, const uint16_t* w, int N, int K);
 
 // Bytes of dynamic shared memory the GEMV kernel uses.
 size_t linear_smem_bytes();

@@ -26,7 +26,10 @@ namespace {
 constexpr size_t kAlign = 256;
 
 size_t step_d2h_bytes(int B) { return offsetof(StepOut, conf) + (size_t)B * EE_MAX_CHECKPOINTS * sizeof(float); }
-constexpr int kHeadGridMax = 512;       // CTAs of a vocabulary-head launch (>= the GEMV grid)
+constexpr int kHeadGridMax = 1024;      // partials of a vocabulary-head launch (GEMV CTAs or GEMM tiles)
+constexpr int kTcMinBatch = 9;          // steps with more sequences use the tensor-core GEMM
+constexpr int kTcMaxUnits = 1024;       // (tile, K split) work units of one tensor-core launch
+constexpr int kTcMaxTiles = 1024;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -114,6 +117,14 @@ struct ee_ctx {
   int32_t* attn_cnt = nullptr;
   float* head_part = nullptr;
   int32_t* head_cnt = nullptr;
+  // tensor-core GEMM (contexts whose max_batch exceeds the GEMV's staging
+  // limit): weight tensor maps, split-K partials, per-tile counters
+  bool tc = false;
+  std::vector<CUtensorMap> tm_layer;  // [layer][qkv, o, gate/up, down]
+  std::vector<CUtensorMap> tm_T;
+  CUtensorMap tm_E;
+  float* tc_part = nullptr;
+  int32_t* tc_cnt = nullptr;
   float* hdbg = nullptr;
   StepLists* lists = nullptr;
   StepDesc* desc_dev = nullptr;
@@ -243,6 +254,8 @@ size_t carve(ee_ctx* c, const ee_config& cfg, uint8_t* base) {
       attention_part_floats(m.maxb, m.hq, m.hkv, m.hd, attention_nsplit(m.maxs, m.hd)));
   float* hpart = cv.take<float>((size_t)kHeadGridMax * EE_MAX_BATCH * 4);
   float* hdbg = cv.take<float>((size_t)m.L * EE_MAX_BATCH * m.d);
+  const bool tc = m.maxb >= kTcMinBatch;
+  float* tcpart = tc ? cv.take<float>(gemm_tc_part_floats(kTcMaxUnits)) : nullptr;
   StepDesc* desc = cv.take<StepDesc>(1);
   StepOut* out = cv.take<StepOut>(1);
   float* gam = cv.take<float>(EE_MAX_CHECKPOINTS);
@@ -251,6 +264,7 @@ size_t carve(ee_ctx* c, const ee_config& cfg, uint8_t* base) {
   int32_t* acnt = cv.take<int32_t>((size_t)EE_MAX_BATCH * m.hkv);
   int32_t* hcnt = cv.take<int32_t>(64);
   int32_t* dflag = cv.take<int32_t>(1);
+  int32_t* tccnt = tc ? cv.take<int32_t>(kTcMaxTiles) : nullptr;
   const size_t ze = align_up(cv.off, kAlign);
   const size_t stg = 2 * (size_t)std::max({(size_t)m.F * m.d, (size_t)m.dq * m.d, (size_t)m.d * m.d,
                                           (size_t)m.dk * m.d});
@@ -281,6 +295,9 @@ size_t carve(ee_ctx* c, const ee_config& cfg, uint8_t* base) {
     c->lists = lists;
     c->attn_cnt = acnt;
     c->head_cnt = hcnt;
+    c->tc = tc;
+    c->tc_part = tcpart;
+    c->tc_cnt = tccnt;
     c->dbg_flag = dflag;
     c->staging = staging;
     c->staging_bytes = stg;
@@ -411,6 +428,36 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     lp.norm_eps = c->cfg.rms_eps;
   };
   bool lists_just_written = true;  // by the step-begin kernel
+  // A projection or head: the GEMV, or for larger batches the tensor-core
+  // GEMM (one launch per non-empty-capable sub-batch list).
+  const bool use_tc = c->tc && B >= kTcMinBatch;
+  auto project = [&](int kind, int layer, const LinearParams& lp, const CUtensorMap* map, int grid) -> ee_status {
+    if (use_tc && map && gemm_tc_shape_ok(lp.K)) {
+      const TcPlan pl = gemm_tc_plan(lp.N, lp.K, c->num_sms);
+      if (pl.ntiles * pl.ksplit <= kTcMaxUnits && pl.ntiles <= kTcMaxTiles) {
+        TcParams tp;
+        memset(&tp, 0, sizeof(tp));
+        tp.amap = *map;
+        tp.lp = lp;
+        tp.ntiles = pl.ntiles;
+        tp.ksplit = pl.ksplit;
+        tp.nks = pl.nks;
+        tp.nk = pl.nk;
+        tp.part = c->tc_part;
+        tp.tile_cnt = c->tc_cnt;
+        if (lp.w) EE_LAUNCH(log, kind, layer, launch_gemm_tc(tp, 0, c->pdl, st));
+        if (lp.wq) EE_LAUNCH(log, kind, layer, launch_gemm_tc(tp, 1, c->pdl, st));
+        return EE_OK;
+      }
+    }
+    EE_LAUNCH(log, kind, layer, launch_linear(lp, grid, c->pdl, st));
+    return EE_OK;
+  };
+#define EE_PROJECT(kind, layer, lp, map, grid)                  \
+  do {                                                          \
+    const ee_status ps_ = project((kind), (layer), (lp), (map), (grid)); \
+    if (ps_ != EE_OK) return ps_;                               \
+  } while (0)
 
   for (int j = 0; j < m.L; ++j) {
     const LayerBufs& w = c->layers[j];
@@ -442,7 +489,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.kc = c->kcache + (size_t)j * m.kv_layer_elems;
     p.vc = c->vcache + (size_t)j * m.kv_layer_elems;
     p.max_rows = B;
-    EE_LAUNCH(log, EE_K_QKV, j, launch_linear(p, linear_grid(p.N, c->num_sms), c->pdl, st));
+    EE_PROJECT(EE_K_QKV, j, p, c->tc ? &c->tm_layer[4 * j + 0] : nullptr, linear_grid(p.N, c->num_sms));
     lists_just_written = false;
     // decode attention
     AttnParams ap = {};
@@ -479,7 +526,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.x_stride = m.dq;
     p.epi = EPI_RESID;
     p.max_rows = B;
-    EE_LAUNCH(log, EE_K_O, j, launch_linear(p, linear_grid(p.N, c->num_sms), c->pdl, st));
+    EE_PROJECT(EE_K_O, j, p, c->tc ? &c->tm_layer[4 * j + 1] : nullptr, linear_grid(p.N, c->num_sms));
     // FFN RMSNorm
     if (!fuse_norm) {
       np.g = w.g_ffn;
@@ -502,7 +549,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.xh_out = c->acth;
     p.xo_stride = m.F;
     p.max_rows = B;
-    EE_LAUNCH(log, EE_K_GATEUP, j, launch_linear(p, linear_grid(p.N, c->num_sms), c->pdl, st));
+    EE_PROJECT(EE_K_GATEUP, j, p, c->tc ? &c->tm_layer[4 * j + 2] : nullptr, linear_grid(p.N, c->num_sms));
     // down projection + residual (+ per-layer copy in debug mode)
     p = base;
     p.N = m.d;
@@ -518,7 +565,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     p.epi = EPI_RESID;
     p.hdbg = c->hdbg + (size_t)j * EE_MAX_BATCH * m.d;
     p.max_rows = B;
-    EE_LAUNCH(log, EE_K_DOWN, j, launch_linear(p, linear_grid(p.N, c->num_sms), c->pdl, st));
+    EE_PROJECT(EE_K_DOWN, j, p, c->tc ? &c->tm_layer[4 * j + 3] : nullptr, linear_grid(p.N, c->num_sms));
 
     const auto ck = std::find(c->ckpts.begin(), c->ckpts.end(), j);
     if (heads && ck != c->ckpts.end()) {
@@ -543,7 +590,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
       p.xh_out = c->uh;
       p.xo_stride = m.d;
       p.max_rows = B;
-      EE_LAUNCH(log, EE_K_HEAD_T, j, launch_linear(p, linear_grid(p.N, c->num_sms), c->pdl, st));
+      EE_PROJECT(EE_K_HEAD_T, j, p, c->tc ? &c->tm_T[ci] : nullptr, linear_grid(p.N, c->num_sms));
       // z = u E^T, conf = max softmax, exit if conf > gamma_c, compact the lists
       p = base;
       p.N = m.V;
@@ -562,8 +609,8 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
       p.ckpt_index = ci;
       p.ckpt_layer = j;
       p.max_rows = B;
-      EE_LAUNCH(log, EE_K_HEAD_E, j,
-                launch_linear(p, std::min(linear_grid(p.N, c->num_sms), kHeadGridMax), c->pdl, st));
+      EE_PROJECT(EE_K_HEAD_E, j, p, c->tc ? &c->tm_E : nullptr,
+                 std::min(linear_grid(p.N, c->num_sms), kHeadGridMax));
       lists_just_written = true;  // compacted by the exit head
     }
   }
@@ -588,8 +635,9 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
   p.head_counter = c->head_cnt;
   p.argmax_out = c->out_dev->next_token;
   p.max_rows = B;
-  EE_LAUNCH(log, EE_K_FINAL_HEAD, -1,
-            launch_linear(p, std::min(linear_grid(p.N, c->num_sms), kHeadGridMax), c->pdl, st));
+  EE_PROJECT(EE_K_FINAL_HEAD, -1, p, c->tc ? &c->tm_E : nullptr,
+             std::min(linear_grid(p.N, c->num_sms), kHeadGridMax));
+#undef EE_PROJECT
   EE_CUDA(c, cudaMemcpyAsync(c->out_host, c->out_dev, step_d2h_bytes(B), cudaMemcpyDeviceToHost, st));
   c->launches[heads ? 1 : 0] = log.n;
   return EE_OK;
@@ -782,6 +830,27 @@ ee_status ee_create(const ee_config* cfg, void* dev_arena, size_t arena_bytes, v
     c->pdl = !(e && e[0] == '0');
   }
   if (linear_prepare() != cudaSuccess || attention_prepare() != cudaSuccess) return bail(EE_ERR_CUDA);
+  if (c->tc) {
+    // tensor maps of every bf16 matrix the tensor-core GEMM streams (the
+    // arena addresses are fixed; the contents are loaded later)
+    if (gemm_tc_prepare() != cudaSuccess) return bail(EE_ERR_CUDA);
+    const Dims& m = c->m;
+    c->tm_layer.resize((size_t)m.L * 4);
+    c->tm_T.resize(m.nck);
+    bool ok = encode_weight_map(&c->tm_E, c->E, m.V, m.d);
+    for (int j = 0; j < m.L && ok; ++j) {
+      const LayerBufs& b = c->layers[j];
+      ok = encode_weight_map(&c->tm_layer[4 * j + 0], b.wqkv, m.nqkv, m.d) &&
+           encode_weight_map(&c->tm_layer[4 * j + 1], b.wo, m.d, m.dq) &&
+           encode_weight_map(&c->tm_layer[4 * j + 2], b.wgu, 2 * m.F, m.d) &&
+           encode_weight_map(&c->tm_layer[4 * j + 3], b.wd, m.d, m.F);
+    }
+    for (int i = 0; i < m.nck && ok; ++i) ok = encode_weight_map(&c->tm_T[i], c->Tt[i], m.d, m.d);
+    if (!ok) {
+      c->err = "encoding the weight tensor maps failed";
+      return bail(EE_ERR_CUDA);
+    }
+  }
   if (c->user_stream) {
     c->st = c->user_stream;
   } else {
@@ -977,7 +1046,9 @@ ee_status ee_step_io(const ee_ctx* c, int32_t batch, int32_t heads, size_t* h2d,
     // O, gate/up, down) + heads (norm, T, E) + final norm and head
     const int with_heads = heads && c->m.nck > 0;
     const int norms = linear_stages_x(batch, c->m.d) ? 0 : 1;
-    *launches = 1 + (5 + 2 * norms) * c->m.L + (with_heads ? (2 + norms) * c->m.nck : 0) + 1 + norms;
+    // the tensor-core GEMM launches once per sub-batch list (full, exit)
+    const int per = c->tc && batch >= kTcMinBatch ? 2 : 1;
+    *launches = 1 + (1 + 4 * per + 2 * norms) * c->m.L + (with_heads ? (2 + norms) * c->m.nck : 0) + 1 + norms;
   }
   return EE_OK;
 }

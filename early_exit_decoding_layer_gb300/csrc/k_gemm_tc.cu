@@ -1,0 +1,461 @@
+// Tensor-core GEMM for steps whose batch is too large for the GEMV to stage:
+// Y[m, n] = sum_k X[m, k] W[n, k] for the sequences m of one sub-batch list,
+// on the 5th-generation tensor cores (tcgen05.mma, fp32 accumulators in
+// tensor memory).
+//
+// The weights are the MMA's A operand (M = 128 rows of W per tile) and the
+// listed sequences' activations its B operand (N columns), both K-major:
+//  * full sub-batch (bf16 weights, MODE 0): A tiles come from HBM by TMA with
+//    the 128-byte swizzle.  The fp16 activations are split into a bf16 high
+//    part and a bf16 remainder (x = hi + lo, 16 significant bits), so the
+//    bf16 x bf16 products keep the activations' precision: B has 64 hi rows
+//    and 64 lo rows (N = 128) and the epilogue adds the two halves of D.
+//  * exit sub-batch (int4 weights, MODE 1): producer warps read the packed
+//    nibbles and bf16 scales, dequantise them in registers to fp16 q * s
+//    (exact: an 8-bit scale times a 4-bit integer fits fp16's 11 bits) and
+//    store them into the swizzled A tile; B holds the fp16 activations
+//    (N = 64).  The int4 weights are never written back to HBM.
+// Producer warps also gather the listed sequences' activations (fp16, pair
+// order) into the B tiles.  One thread issues the MMAs; a stage is released
+// by tcgen05.commit when its MMAs have consumed it.
+//
+// Work unit = (128-row tile, K split).  With several splits per tile each
+// CTA writes its fp32 partial tile; the last CTA of the tile (an atomic
+// counter, nothing waits) adds them in split order, so results do not depend
+// on timing, and runs the epilogue shared with the GEMV (RoPE + K/V write,
+// residual, SwiGLU, fp16 output) or the vocabulary-head statistics.
+#include <cuda.h>
+#include <math.h>
+
+#include "ee_common.cuh"
+#include "ee_epilogue.cuh"
+#include "ee_head.cuh"
+#include "ee_kernels.cuh"
+
+namespace ee {
+
+namespace {
+
+constexpr int kBM = 128;  // weight rows per tile (MMA M)
+constexpr int kBK = 64;   // K elements per stage (one 128-byte swizzle row)
+constexpr int kStages = 4;
+constexpr int kCols = 64;  // sequences per launch at most (EE_MAX_BATCH)
+constexpr int kTcThreads = 192;  // warps 0-3 producers + epilogue, 4 TMA, 5 MMA
+constexpr uint32_t kABytes = kBM * kBK * 2;
+static_assert(kCols == EE_MAX_BATCH, "one launch covers the whole list");
+
+template <int MODE>
+constexpr int kN = MODE == 0 ? 2 * kCols : kCols;  // MMA N
+template <int MODE>
+constexpr uint32_t kBBytes = (uint32_t)kN<MODE> * kBK * 2;
+template <int MODE>
+constexpr uint32_t kStageBytes = kABytes + kBBytes<MODE>;
+template <int MODE>
+constexpr size_t kTcSmem = (size_t)kStages * kStageBytes<MODE> + 1024;
+
+// Shared memory descriptor of a K-major tile with 128-byte rows and the
+// 128-byte swizzle: start address, stride between 8-row groups (1024 B),
+// descriptor version 1, swizzle mode 2 (leading offset unused: 1).
+EE_DEV uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulators, A and B of type
+// `ab` (0 = f16, 1 = bf16), both K-major, N and M given.
+constexpr uint32_t instr_desc(uint32_t ab, int n, int m) {
+  return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+// Byte offset of 16-byte chunk j (8 elements) of row r in a 128B-swizzled tile.
+EE_DEV uint32_t sw128(int r, int j) { return (uint32_t)(r * 128 + ((j ^ (r & 7)) << 4)); }
+
+EE_DEV void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+EE_DEV void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+EE_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+EE_DEV uint32_t pack_h2(float a, float b) {
+  return uint32_t(float_to_half_bits(a)) | (uint32_t(float_to_half_bits(b)) << 16);
+}
+EE_DEV uint32_t pack_bf2(float a, float b) {
+  return uint32_t(float_to_bf16_bits(a)) | (uint32_t(float_to_bf16_bits(b)) << 16);
+}
+
+// 8 fp16 activations stored in pair order (0,4,1,5,2,6,3,7) -> natural order.
+EE_DEV void unpair8(const uint4& v, float* x) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    x[i] = f.x;
+    x[i + 4] = f.y;
+  }
+}
+
+struct TcShared {
+  uint64_t full[kStages], empty[kStages], done;
+  uint32_t tmem;
+  int32_t lf[kListLen], le[kListLen];
+  int last;
+  float red[4 * 3 * 16];   // head statistics: [warp][3][column chunk]
+  float res[2 * EE_MAX_BATCH];
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant__ TcParams tp) {
+  constexpr int N = kN<MODE>;
+  constexpr uint32_t kStage = kStageBytes<MODE>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ TcShared sh;
+  uint8_t* tiles = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const LinearParams& p = tp.lp;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int unit = blockIdx.x, tile = unit / tp.ksplit, split = unit - tile * tp.ksplit;
+  const int row0 = tile * kBM;
+  const int ks0 = split * tp.nks, ks1 = min(tp.nk, ks0 + tp.nks);  // K steps of this unit
+  const int nks = ks1 - ks0;
+
+  if (p.lists_after_wait) grid_dep_wait();
+  if (tid < kListLen) {
+    sh.lf[tid] = p.list_full ? ld_volatile_i32(p.list_full + tid) : (tid == 0 ? p.m_direct_full : tid - 1);
+    sh.le[tid] = p.list_exit ? ld_volatile_i32(p.list_exit + tid) : (tid == 0 ? p.m_direct_exit : tid - 1);
+  }
+  __syncthreads();
+  const int32_t* lst = MODE == 0 ? sh.lf : sh.le;
+  const int ncol = min(lst[0], kCols);
+  if (ncol == 0 || nks <= 0) {  // uniform over the grid: no unit has work
+    grid_dep_wait();
+    grid_dep_launch();
+    return;
+  }
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sh.full[s], MODE == 0 ? 129 : 128);
+      mbar_init(&sh.empty[s], 1);
+    }
+    mbar_init(&sh.done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&sh.tmem)),
+                 "r"(N)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = sh.tmem;
+  const uint32_t tiles_s = smem_addr(tiles);
+
+  if (warp == 4) {
+    // TMA of the bf16 weight tiles; the first stages go out before the
+    // dependency wait (weights never change).
+    if (MODE == 0 && lane == 0) {
+      const CUtensorMap* map = &tp.amap;
+      for (int i = 0; i < nks; ++i) {
+        const int s = i % kStages, n = i / kStages;
+        if (i == kStages) grid_dep_wait();
+        if (n > 0 && !mbar_wait_bounded(&sh.empty[s], (n - 1) & 1, p.err, DERR_EMPTY_WAIT)) break;
+        mbar_arrive_expect_tx(&sh.full[s], kABytes);
+        tma_load_2d(tiles_s + s * kStage, map, (ks0 + i) * kBK, row0, &sh.full[s]);
+      }
+      if (nks <= kStages) grid_dep_wait();
+    } else {
+      grid_dep_wait();
+    }
+    grid_dep_launch();
+  } else if (warp == 5) {
+    grid_dep_wait();
+    grid_dep_launch();
+    if (lane == 0) {
+      constexpr uint32_t idesc = instr_desc(MODE == 0 ? 1u : 0u, N, kBM);
+      for (int i = 0; i < nks; ++i) {
+        const int s = i % kStages;
+        if (!mbar_wait_bounded(&sh.full[s], (i / kStages) & 1, p.err, DERR_FULL_WAIT)) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t a_s = tiles_s + s * kStage, b_s = a_s + kABytes;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          const uint64_t ad = smem_desc_sw128(a_s + kk * 32), bd = smem_desc_sw128(b_s + kk * 32);
+          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+          asm volatile(
+              "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(tmem),
+              "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
+              : "memory");
+        }
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                         smem_addr(&sh.empty[s]))
+                     : "memory");
+      }
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                       smem_addr(&sh.done))
+                   : "memory");
+    }
+  } else {
+    // producers: the B tile (activations of the listed sequences) and, for
+    // int4, the dequantised A tile of every stage
+    grid_dep_wait();
+    grid_dep_launch();
+    const int e = tid & 63, h = tid >> 6;  // list entry, half of the 64-column stage
+    const bool have = e < ncol;
+    const uint16_t* xrow = p.xh + (size_t)(have ? lst[1 + e] : 0) * p.x_stride;
+    const int r = row0 + tid;  // int4: weight row of this thread
+    const bool have_row = MODE == 1 && r < p.N;
+    for (int i = 0; i < nks; ++i) {
+      const int s = i % kStages, n = i / kStages;
+      if (n > 0 && !mbar_wait_bounded(&sh.empty[s], (n - 1) & 1, p.err, DERR_EMPTY_WAIT)) break;
+      const int k0 = (ks0 + i) * kBK;
+      const uint32_t a_s = tiles_s + s * kStage, b_s = a_s + kABytes;
+      // B: 32 activations (4 chunks) of entry e
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float x[8];
+        if (have) {
+          unpair8(*reinterpret_cast<const uint4*>(xrow + k0 + 32 * h + 8 * c), x);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) x[t] = 0.0f;
+        }
+        const int j = 4 * h + c;
+        if (MODE == 0) {
+          float lo[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) lo[t] = x[t] - bf16_bits_to_float(float_to_bf16_bits(x[t]));
+          st_shared_v4(b_s + sw128(e, j), make_uint4(pack_bf2(x[0], x[1]), pack_bf2(x[2], x[3]),
+                                                     pack_bf2(x[4], x[5]), pack_bf2(x[6], x[7])));
+          st_shared_v4(b_s + sw128(kCols + e, j), make_uint4(pack_bf2(lo[0], lo[1]), pack_bf2(lo[2], lo[3]),
+                                                             pack_bf2(lo[4], lo[5]), pack_bf2(lo[6], lo[7])));
+        } else {
+          st_shared_v4(b_s + sw128(e, j), make_uint4(pack_h2(x[0], x[1]), pack_h2(x[2], x[3]), pack_h2(x[4], x[5]),
+                                                     pack_h2(x[6], x[7])));
+        }
+      }
+      if (MODE == 1) {
+        // A: row r, columns k0 .. k0 + 63 (32 packed bytes, one scale)
+        uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0;
+        float sc = 0.0f;
+        if (have_row) {
+          const uint8_t* qp = p.wq + (size_t)r * (p.K / 2) + k0 / 2;
+          q0 = ldg_stream_v4(qp);
+          q1 = ldg_stream_v4(qp + 16);
+          sc = bf16_bits_to_float(p.ws[(size_t)r * p.sstride + k0 / EE_QUANT_GROUP]);
+        }
+        const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          // word j holds columns 8j .. 8j + 7 (low nibble first, two's complement)
+          uint32_t o[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int b = (int)((words[j] >> (8 * t)) & 0xFFu);
+            const int q_lo = ((b & 0xF) ^ 8) - 8, q_hi = ((b >> 4) ^ 8) - 8;
+            o[t] = pack_h2((float)q_lo * sc, (float)q_hi * sc);
+          }
+          st_shared_v4(a_s + sw128(tid, j), make_uint4(o[0], o[1], o[2], o[3]));
+        }
+      }
+      fence_proxy_async();
+      mbar_arrive(&sh.full[s]);
+    }
+  }
+
+  // ---------------------------------------------------------------- epilogue
+  if (warp < 4) {
+    const bool ok = mbar_wait_bounded(&sh.done, 0, p.err, DERR_FULL_WAIT);
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const int rl = warp * 32 + lane;  // tile row = TMEM lane
+    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+    float* part = tp.part + (size_t)unit * kCols * kBM;
+    for (int c0 = 0; c0 < ncol; c0 += 16) {
+      uint32_t v[16], w[16];
+      asm volatile(
+          "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+          : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+            "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+          : "r"(tl + c0));
+      if (MODE == 0) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+            : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]),
+              "=r"(w[8]), "=r"(w[9]), "=r"(w[10]), "=r"(w[11]), "=r"(w[12]), "=r"(w[13]), "=r"(w[14]), "=r"(w[15])
+            : "r"(tl + kCols + c0));
+      }
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float y = __uint_as_float(v[j]) + (MODE == 0 ? __uint_as_float(w[j]) : 0.0f);
+        if (c0 + j < ncol) part[(size_t)(c0 + j) * kBM + rl] = ok ? y : 0.0f;
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 5) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(N) : "memory");
+  }
+  // the last CTA of this tile adds the splits in order and runs the epilogue
+  if (tid == 0) {
+    __threadfence();
+    const int old = tp.ksplit > 1 ? atomicAdd(tp.tile_cnt + tile, 1) : 0;
+    sh.last = (old == tp.ksplit - 1);
+  }
+  __syncthreads();
+  if (!sh.last) return;
+  __threadfence();
+  if (warp >= 4) return;
+  const int rl = warp * 32 + lane;
+  const int r = row0 + rl;
+  const float* parts = tp.part + (size_t)tile * tp.ksplit * kCols * kBM;
+  for (int c0 = 0; c0 < ncol; c0 += 16) {
+    float y[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float acc = 0.0f;
+      if (c0 + j < ncol)
+        for (int sp = 0; sp < tp.ksplit; ++sp) acc += __ldcg(parts + ((size_t)sp * kCols + c0 + j) * kBM + rl);
+      y[j] = acc;
+    }
+    if (p.epi == EPI_HEAD) {
+      // per column (sequence): statistics over this tile's rows
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        Stat st = {-INFINITY, 0.0f, 0x7fffffff};
+        if (r < p.N) stat_push(st, y[j], r);
+        st = stat_warp_merge(st);
+        if (lane == 0) {
+          sh.red[(warp * 3 + 0) * 16 + j] = st.mx;
+          sh.red[(warp * 3 + 1) * 16 + j] = st.sum;
+          sh.red[(warp * 3 + 2) * 16 + j] = __int_as_float(st.arg);
+        }
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (tid < 16 && c0 + tid < ncol) {
+        Stat st = {-INFINITY, 0.0f, 0x7fffffff};
+        for (int w = 0; w < 4; ++w)
+          st = stat_merge(st, Stat{sh.red[(w * 3 + 0) * 16 + tid], sh.red[(w * 3 + 1) * 16 + tid],
+                                   __float_as_int(sh.red[(w * 3 + 2) * 16 + tid])});
+        float* dst = p.head_part + ((size_t)tile * EE_MAX_BATCH + c0 + tid) * 4;
+        dst[0] = st.mx;
+        dst[1] = st.sum;
+        dst[2] = __int_as_float(st.arg);
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float yb = __shfl_down_sync(0xffffffffu, y[j], 1);
+        if ((rl & 1) == 0 && r < p.N && c0 + j < ncol) {
+          const int seq = lst[1 + c0 + j];
+          switch (p.epi) {
+            case EPI_F32: epi_pair<EPI_F32>(p, seq, r, y[j], yb); break;
+            case EPI_QKV: epi_pair<EPI_QKV>(p, seq, r, y[j], yb); break;
+            case EPI_RESID: epi_pair<EPI_RESID>(p, seq, r, y[j], yb); break;
+            case EPI_SWIGLU: epi_pair<EPI_SWIGLU>(p, seq, r, y[j], yb); break;
+            default: epi_pair<EPI_X>(p, seq, r, y[j], yb); break;
+          }
+        }
+      }
+    }
+  }
+  if (tid == 0 && tp.ksplit > 1) tp.tile_cnt[tile] = 0;
+  if (p.epi == EPI_HEAD) {
+    // the last tile to finish merges the vocabulary partials
+    if (tid == 0) {
+      __threadfence();
+      const int old = atomicAdd(p.head_counter, 1);
+      sh.last = (old == tp.ntiles - 1);
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (!sh.last) return;
+    head_finalize_group(p, tp.ntiles, sh.lf, sh.le, ncol, sh.res, 128);
+  }
+}
+
+}  // namespace
+
+TcPlan gemm_tc_plan(int N, int K, int num_sms) {
+  TcPlan pl;
+  pl.ntiles = (N + kBM - 1) / kBM;
+  pl.nk = K / kBK;
+  // the fewest K splits that fill the SMs' waves to 90 %
+  int best = 1;
+  for (int s = 1; s <= 16 && s <= pl.nk; ++s) {
+    const int units = pl.ntiles * s, waves = (units + num_sms - 1) / num_sms;
+    best = s;
+    if ((double)units / ((double)waves * num_sms) >= 0.9) break;
+  }
+  pl.nks = (pl.nk + best - 1) / best;
+  pl.ksplit = (pl.nk + pl.nks - 1) / pl.nks;
+  return pl;
+}
+
+bool gemm_tc_shape_ok(int K) { return K >= kBK && K % kBK == 0; }
+
+size_t gemm_tc_part_floats(int units) { return (size_t)units * kCols * kBM; }
+
+cudaError_t gemm_tc_prepare() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(k_gemm_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem<0>)) !=
+      cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(k_gemm_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem<1>);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+bool encode_weight_map(CUtensorMap* map, const uint16_t* w, int N, int K) {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !f)
+      return false;
+    fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  if (!w || (uintptr_t)w % 16 || K % kBK || N < 1) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)N};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBM};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(w), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_gemm_tc(const TcParams& tp, int mode, bool pdl, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tp.ntiles * tp.ksplit);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = mode == 0 ? kTcSmem<0> : kTcSmem<1>;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (mode == 0) return cudaLaunchKernelEx(&cfg, k_gemm_tc<0>, tp);
+  return cudaLaunchKernelEx(&cfg, k_gemm_tc<1>, tp);
+}
+
+}  // namespace ee

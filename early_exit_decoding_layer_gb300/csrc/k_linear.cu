@@ -36,6 +36,8 @@
 #include <math.h>
 
 #include "ee_common.cuh"
+#include "ee_epilogue.cuh"
+#include "ee_head.cuh"
 #include "ee_kernels.cuh"
 
 namespace ee {
@@ -84,90 +86,6 @@ EE_DEV __half2 dot8_int4(uint32_t word, const uint4& x, __half2 acc) {
   acc = __hfma2(__hsub2(u32_as_h2(((t >> 8) & 0x000F000Fu) | 0x64006400u), bias), u32_as_h2(x.z), acc);
   acc = __hfma2(__hsub2(u32_as_h2(((t >> 12) & 0x000F000Fu) | 0x64006400u), bias), u32_as_h2(x.w), acc);
   return acc;
-}
-
-EE_DEV uint16_t* kv_slot(uint16_t* cache, const LinearParams& p, int seq, int pos, int head) {
-  const int block = p.block_table[(size_t)seq * p.bt_stride + (pos >> 4)];
-  return cache + ((((size_t)block * p.n_kv_heads + head) * 16) + (pos & 15)) * p.head_dim;
-}
-
-// Epilogue of one row pair (ra, ra+1) for one sequence.
-template <int EPI>
-EE_DEV void epi_pair(const LinearParams& p, int seq, int ra, float ya, float yb) {
-  if constexpr (EPI == EPI_F32) {
-    float* o = p.out_f32 + (size_t)seq * p.out_stride + ra;
-    o[0] = ya;
-    o[1] = yb;
-  } else if constexpr (EPI == EPI_QKV) {
-    const int hd = p.head_dim;
-    const int dq = p.n_heads * hd, dk = p.n_kv_heads * hd;
-    const int pos = p.pos[seq];
-    if (ra < dq + dk) {
-      // rows (ra, ra+1) hold head dims (i, i + hd/2): rotate-half RoPE
-      const bool isq = ra < dq;
-      const int rr = isq ? ra : ra - dq;
-      const int head = rr / hd, i = (rr % hd) >> 1;
-      const float2 cs = p.rope[(size_t)pos * (hd >> 1) + i];
-      const float o1 = ya * cs.x - yb * cs.y;
-      const float o2 = yb * cs.x + ya * cs.y;
-      if (isq) {
-        float* q = p.q_out + (size_t)seq * dq + head * hd;
-        q[i] = o1;
-        q[i + (hd >> 1)] = o2;
-      } else {
-        uint16_t* k = kv_slot(p.kc, p, seq, pos, head);
-        k[i] = float_to_half_bits(o1);
-        k[i + (hd >> 1)] = float_to_half_bits(o2);
-      }
-    } else {
-      const int rr = ra - dq - dk;
-      const int head = rr / hd, i = rr % hd;
-      uint16_t* v = kv_slot(p.vc, p, seq, pos, head);
-      const uint32_t packed =
-          uint32_t(float_to_half_bits(ya)) | (uint32_t(float_to_half_bits(yb)) << 16);
-      *reinterpret_cast<uint32_t*>(v + i) = packed;
-    }
-  } else if constexpr (EPI == EPI_RESID) {
-    float* hp = p.h + (size_t)seq * p.h_stride + ra;
-    const float2 old = *reinterpret_cast<float2*>(hp);
-    const float2 nw = make_float2(old.x + ya, old.y + yb);
-    *reinterpret_cast<float2*>(hp) = nw;
-    if (p.hdbg != nullptr && *p.dbg_flag)
-      *reinterpret_cast<float2*>(p.hdbg + (size_t)seq * p.h_stride + ra) = nw;
-  } else if constexpr (EPI == EPI_SWIGLU) {
-    const int i = ra >> 1;
-    const float a = ya / (1.0f + expf(-ya)) * yb;
-    p.xh_out[(size_t)seq * p.xo_stride + xh_slot(i)] = float_to_half_bits(a);
-  } else if constexpr (EPI == EPI_X) {
-    uint16_t* ho = p.xh_out + (size_t)seq * p.xo_stride;
-    ho[xh_slot(ra)] = float_to_half_bits(ya);
-    ho[xh_slot(ra + 1)] = float_to_half_bits(yb);
-  }
-}
-
-// Online (max, sum of exp(z - max), argmax) statistics.
-struct Stat {
-  float mx, sum;
-  int arg;
-};
-EE_DEV void stat_push(Stat& s, float z, int idx) {
-  if (z > s.mx) {
-    s.sum = s.sum * expf(s.mx - z) + 1.0f;
-    s.mx = z;
-    s.arg = idx;
-  } else {
-    s.sum += expf(z - s.mx);
-    if (z == s.mx && idx < s.arg) s.arg = idx;
-  }
-}
-EE_DEV Stat stat_merge(Stat a, Stat b) {
-  if (b.sum == 0.0f) return a;
-  if (a.sum == 0.0f) return b;
-  Stat r;
-  r.mx = fmaxf(a.mx, b.mx);
-  r.sum = a.sum * expf(a.mx - r.mx) + b.sum * expf(b.mx - r.mx);
-  r.arg = a.mx > b.mx ? a.arg : (b.mx > a.mx ? b.arg : min(a.arg, b.arg));
-  return r;
 }
 
 EE_DEV uint16_t ldg_u16(const uint16_t* p) {
@@ -654,66 +572,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_linear(const LinearPar
     }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
-    float* res = hst;  // reuse: [m] (conf, argmax)
-    const int nrows = nf;
-    for (int m = warp; m < nrows; m += kWarps) {
-      Stat s = {-INFINITY, 0.0f, 0x7fffffff};
-      for (int c = lane; c < (int)gridDim.x; c += 32) {
-        const float* src = p.head_part + ((size_t)c * EE_MAX_BATCH + m) * 4;
-        s = stat_merge(s, Stat{__ldcg(src), __ldcg(src + 1), __float_as_int(__ldcg(src + 2))});
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        Stat t;
-        t.mx = __shfl_xor_sync(0xffffffffu, s.mx, o);
-        t.sum = __shfl_xor_sync(0xffffffffu, s.sum, o);
-        t.arg = __shfl_xor_sync(0xffffffffu, s.arg, o);
-        s = stat_merge(s, t);
-      }
-      if (lane == 0) {
-        res[2 * m] = 1.0f / s.sum;  // max softmax = exp(zmax - lse) = 1 / sum exp(z - zmax)
-        res[2 * m + 1] = __int_as_float(s.arg);
-      }
-    }
-    __syncthreads();
-    if (tid == 0) {
-      if (p.head_mode == HEAD_CONF_ARGMAX) {
-        for (int m = 0; m < nrows; ++m) {
-          p.conf_out[m] = res[2 * m];
-          p.argmax_out[m] = __float_as_int(res[2 * m + 1]);
-        }
-      } else if (p.head_mode == HEAD_FINAL) {
-        for (int m = 0; m < nrows; ++m) p.argmax_out[lf[1 + m]] = __float_as_int(res[2 * m + 1]);
-      } else {  // HEAD_CHECKPOINT: decide, then rebuild the two sub-batch lists
-        const float gamma = p.gamma[p.ckpt_index];
-        int32_t nfull = 0, nexit = 0;
-        int32_t newly[EE_MAX_BATCH];
-        int nnew = 0;
-        for (int m = 0; m < nrows; ++m) {
-          const int seq = lf[1 + m];
-          const float conf = res[2 * m];
-          p.conf_out[seq * EE_MAX_CHECKPOINTS + p.ckpt_index] = conf;
-          if (conf > gamma) {
-            newly[nnew++] = seq;
-            p.exit_layer[seq] = p.ckpt_layer;
-          } else {
-            p.lists->full[1 + nfull++] = seq;
-          }
-        }
-        // exit list = merge of the previous exit list and the newly exited, by id
-        const int nold = min(le[0], EE_MAX_BATCH);
-        int a = 0, b = 0;
-        while (a < nold || b < nnew) {
-          const bool take_old = b >= nnew || (a < nold && le[1 + a] < newly[b]);
-          p.lists->exitl[1 + nexit++] = take_old ? le[1 + a++] : newly[b++];
-        }
-        p.lists->full[0] = nfull;
-        p.lists->exitl[0] = nexit;
-      }
-      __threadfence();
-      *p.head_counter = 0;
-    }
+    head_finalize(p, (int)gridDim.x, lf, le, nf, hst);
   }
 }
 

@@ -1,0 +1,90 @@
+"""Parity of the decode step at batch sizes above the GEMV's staging limit,
+where the projections and heads run on the tensor-core GEMM (tcgen05, fp32
+accumulators in tensor memory): the tiny model at batch 12 with mixed exit
+depths every step, and the Llama-3.2-1B shape (128256-row vocabulary head)
+at batch 10 on a short workload."""
+import numpy as np
+import pytest
+
+import synth
+from tests import parity
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import early_exit_decoding_layer_gb300 as ee  # noqa: E402
+
+TINY = synth.WORKLOADS["tiny-b1"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from early_exit_decoding_layer_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def test_launches_per_step_count_both_sub_batches():
+    eng = parity.load_engine(TINY, max_batch=16, max_seq_len=48)
+    L, nck = TINY.shape.n_layers, len(TINY.checkpoints)
+    _, _, n1 = eng.step_io(1, True)
+    _, _, n12 = eng.step_io(12, True)
+    assert n1 == 1 + 5 * L + 2 * nck + 1          # GEMV path: norms applied while staging
+    assert n12 == 1 + (1 + 8 + 2) * L + 3 * nck + 2  # two launches per projection, norm kernels
+    eng.close()
+
+
+def test_tiny_batch12_mixed_exits():
+    """12 ragged sequences; per-step thresholds of -inf/+inf per checkpoint so
+    that the full and exit sub-batches change every step (both GEMM modes,
+    list compaction by the tensor-core head)."""
+    B = 12
+    eng = parity.load_engine(TINY, max_batch=16, max_seq_len=64)
+    orc = parity.build_oracle(TINY, max_batch=16, max_seq_len=64)
+    lens = [5, 16, 17, 31, 9, 12, 20, 3, 33, 15, 8, 26]
+    pr = synth.prompts(TINY.shape, 41, lens)
+    rng = np.random.default_rng(3)
+    gps = [[rng.choice([-np.inf, np.inf], p=[0.3, 0.7]) for _ in TINY.checkpoints] for _ in range(10)]
+    st = parity.drive(eng, orc, pr, gps[0], 10, gamma_per_step=gps)
+    seen = set(int(x) for e in st.gpu_exits for x in e)
+    assert len(st.gpu_exits[0]) == B
+    assert seen >= {1, 3}
+    print("tiny b=12 parity:", st)
+    parity.check_kv(eng, orc)
+    eng.close()
+
+
+def test_tiny_batch12_calibrated_thresholds():
+    """Thresholds between the confidences, so some sequences of a step exit
+    and others do not (decisions inside the window are excused)."""
+    eng = parity.load_engine(TINY, max_batch=16, max_seq_len=64)
+    orc = parity.build_oracle(TINY, max_batch=16, max_seq_len=64)
+    pr = synth.prompts(TINY.shape, 43, [10 + 2 * i for i in range(12)])
+    # confidences of the oracle at gamma = +inf over 2 steps: thresholds at their median
+    o2 = parity.build_oracle(TINY, max_batch=16, max_seq_len=64)
+    o2.set_thresholds(np.full(len(TINY.checkpoints), np.inf))
+    tok = o2.prefill(pr)
+    confs = []
+    for _ in range(2):
+        r = o2.decode_step(tok)
+        confs.append(r.conf)
+        tok = r.next_tokens
+    gamma = np.median(np.concatenate(confs, axis=0), axis=0)
+    st = parity.drive(eng, orc, pr, gamma, 8)
+    print("tiny b=12 calibrated:", st)
+    eng.close()
+
+
+def test_llama1b_shape_batch10():
+    """Llama-3.2-1B shape at batch 10: 24- to 60-token prompts, 3 steps, exits
+    forced at the first checkpoint for half of the steps."""
+    w = synth.WORKLOADS["llama3.2-1b-b1"]
+    eng = parity.load_engine(w, max_batch=10, max_seq_len=72)
+    orc = parity.build_oracle(w, max_batch=10, max_seq_len=72, cache_bytes=16 << 30)
+    pr = synth.prompts(w.shape, w.seed + 5, [24 + 4 * i for i in range(10)])
+    inf = np.inf
+    gps = [[-inf, inf, inf], [inf, inf, inf], [inf, -inf, inf]]
+    st = parity.drive(eng, orc, pr, gps[0], 3, gamma_per_step=gps)
+    assert [sorted(set(int(x) for x in e)) for e in st.gpu_exits] == [[4], [15], [8]]
+    print("1B b=10 parity:", st)
+    eng.close()
