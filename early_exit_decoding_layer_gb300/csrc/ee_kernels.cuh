@@ -133,7 +133,8 @@ struct TcParams {
 struct TcPlan {
   int ntiles, ksplit, nks, nk;
 };
-TcPlan gemm_tc_plan(int N, int K, int num_sms);
+// K splits: the fewest that fill the waves, within max_units work units.
+TcPlan gemm_tc_plan(int N, int K, int num_sms, int max_units);
 bool gemm_tc_shape_ok(int K);
 size_t gemm_tc_part_floats(int units);
 cudaError_t gemm_tc_prepare();

@@ -433,7 +433,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
   const bool use_tc = c->tc && B >= kTcMinBatch;
   auto project = [&](int kind, int layer, const LinearParams& lp, const CUtensorMap* map, int grid) -> ee_status {
     if (use_tc && map && gemm_tc_shape_ok(lp.K)) {
-      const TcPlan pl = gemm_tc_plan(lp.N, lp.K, c->num_sms);
+      const TcPlan pl = gemm_tc_plan(lp.N, lp.K, c->num_sms, kTcMaxUnits);
       if (pl.ntiles * pl.ksplit <= kTcMaxUnits && pl.ntiles <= kTcMaxTiles) {
         TcParams tp;
         memset(&tp, 0, sizeof(tp));
@@ -445,8 +445,10 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
         tp.nk = pl.nk;
         tp.part = c->tc_part;
         tp.tile_cnt = c->tc_cnt;
+        // the exit list is empty until a head has run (no launch for it then)
+        const bool exit_rows = heads && m.nck > 0 && layer > c->ckpts[0];
         if (lp.w) EE_LAUNCH(log, kind, layer, launch_gemm_tc(tp, 0, c->pdl, st));
-        if (lp.wq) EE_LAUNCH(log, kind, layer, launch_gemm_tc(tp, 1, c->pdl, st));
+        if (lp.wq && exit_rows) EE_LAUNCH(log, kind, layer, launch_gemm_tc(tp, 1, c->pdl, st));
         return EE_OK;
       }
     }
@@ -1046,9 +1048,12 @@ ee_status ee_step_io(const ee_ctx* c, int32_t batch, int32_t heads, size_t* h2d,
     // O, gate/up, down) + heads (norm, T, E) + final norm and head
     const int with_heads = heads && c->m.nck > 0;
     const int norms = linear_stages_x(batch, c->m.d) ? 0 : 1;
-    // the tensor-core GEMM launches once per sub-batch list (full, exit)
-    const int per = c->tc && batch >= kTcMinBatch ? 2 : 1;
-    *launches = 1 + (1 + 4 * per + 2 * norms) * c->m.L + (with_heads ? (2 + norms) * c->m.nck : 0) + 1 + norms;
+    // the tensor-core GEMM launches once per sub-batch list (full, and exit
+    // for the layers after the first checkpoint when heads run)
+    const bool tc = c->tc && batch >= kTcMinBatch;
+    const int exit_layers = with_heads ? c->m.L - 1 - c->ckpts[0] : 0;
+    *launches = 1 + (5 + 2 * norms) * c->m.L + (tc ? 4 * exit_layers : 0) +
+                (with_heads ? (2 + norms) * c->m.nck : 0) + 1 + norms;
   }
   return EE_OK;
 }

@@ -38,7 +38,8 @@ namespace {
 
 constexpr int kBM = 128;  // weight rows per tile (MMA M)
 constexpr int kBK = 64;   // K elements per stage (one 128-byte swizzle row)
-constexpr int kStages = 4;
+template <int MODE>
+constexpr int kStages = MODE == 0 ? 3 : 4;  // two CTAs per SM fit in shared memory
 constexpr int kCols = 64;  // sequences per launch at most (EE_MAX_BATCH)
 constexpr int kTcThreads = 192;  // warps 0-3 producers + epilogue, 4 TMA, 5 MMA
 constexpr uint32_t kABytes = kBM * kBK * 2;
@@ -51,7 +52,7 @@ constexpr uint32_t kBBytes = (uint32_t)kN<MODE> * kBK * 2;
 template <int MODE>
 constexpr uint32_t kStageBytes = kABytes + kBBytes<MODE>;
 template <int MODE>
-constexpr size_t kTcSmem = (size_t)kStages * kStageBytes<MODE> + 1024;
+constexpr size_t kTcSmem = (size_t)kStages<MODE> * kStageBytes<MODE> + 1024;
 
 // Shared memory descriptor of a K-major tile with 128-byte rows and the
 // 128-byte swizzle: start address, stride between 8-row groups (1024 B),
@@ -107,17 +108,19 @@ EE_DEV void unpair8(const uint4& v, float* x) {
 }
 
 struct TcShared {
-  uint64_t full[kStages], empty[kStages], done;
+  uint64_t full[4], empty[4], done;
   uint32_t tmem;
   int32_t lf[kListLen], le[kListLen];
   int last;
   float red[4 * 3 * 16];   // head statistics: [warp][3][column chunk]
   float res[2 * EE_MAX_BATCH];
+  EpiSeq col[kCols];       // per-column (sequence) epilogue values
 };
 
 template <int MODE>
-__global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant__ TcParams tp) {
+__global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant__ TcParams tp) {
   constexpr int N = kN<MODE>;
+  constexpr int kStages = ee::kStages<MODE>;
   constexpr uint32_t kStage = kStageBytes<MODE>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ TcShared sh;
@@ -209,69 +212,93 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
     }
   } else {
     // producers: the B tile (activations of the listed sequences) and, for
-    // int4, the dequantised A tile of every stage
+    // int4, the dequantised A tile of every stage.  Global reads run ahead
+    // of the stores in registers (PD stages: activations from L2, and for
+    // int4 the packed weights from HBM), so a stage costs no round trip.
     grid_dep_wait();
     grid_dep_launch();
+    constexpr int PD = MODE == 0 ? 3 : 4;  // stages of reads in flight per thread
     const int e = tid & 63, h = tid >> 6;  // list entry, half of the 64-column stage
     const bool have = e < ncol;
-    const uint16_t* xrow = p.xh + (size_t)(have ? lst[1 + e] : 0) * p.x_stride;
+    const uint16_t* xrow = p.xh + (size_t)(have ? lst[1 + e] : 0) * p.x_stride + 32 * h;
     const int r = row0 + tid;  // int4: weight row of this thread
     const bool have_row = MODE == 1 && r < p.N;
-    for (int i = 0; i < nks; ++i) {
-      const int s = i % kStages, n = i / kStages;
-      if (n > 0 && !mbar_wait_bounded(&sh.empty[s], (n - 1) & 1, p.err, DERR_EMPTY_WAIT)) break;
+    const uint8_t* qrow = MODE == 1 ? p.wq + (size_t)(have_row ? r : 0) * (p.K / 2) : nullptr;
+    const uint16_t* srow = MODE == 1 ? p.ws + (size_t)(have_row ? r : 0) * p.sstride : nullptr;
+    uint4 xr[PD][4];
+    uint4 qr[MODE == 1 ? PD : 1][2];
+    uint16_t sr[MODE == 1 ? PD : 1];
+    auto fetch = [&](int slot, int i) {
+      if (i >= nks) return;
       const int k0 = (ks0 + i) * kBK;
-      const uint32_t a_s = tiles_s + s * kStage, b_s = a_s + kABytes;
-      // B: 32 activations (4 chunks) of entry e
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float x[8];
-        if (have) {
-          unpair8(*reinterpret_cast<const uint4*>(xrow + k0 + 32 * h + 8 * c), x);
-        } else {
-#pragma unroll
-          for (int t = 0; t < 8; ++t) x[t] = 0.0f;
-        }
-        const int j = 4 * h + c;
-        if (MODE == 0) {
-          float lo[8];
-#pragma unroll
-          for (int t = 0; t < 8; ++t) lo[t] = x[t] - bf16_bits_to_float(float_to_bf16_bits(x[t]));
-          st_shared_v4(b_s + sw128(e, j), make_uint4(pack_bf2(x[0], x[1]), pack_bf2(x[2], x[3]),
-                                                     pack_bf2(x[4], x[5]), pack_bf2(x[6], x[7])));
-          st_shared_v4(b_s + sw128(kCols + e, j), make_uint4(pack_bf2(lo[0], lo[1]), pack_bf2(lo[2], lo[3]),
-                                                             pack_bf2(lo[4], lo[5]), pack_bf2(lo[6], lo[7])));
-        } else {
-          st_shared_v4(b_s + sw128(e, j), make_uint4(pack_h2(x[0], x[1]), pack_h2(x[2], x[3]), pack_h2(x[4], x[5]),
-                                                     pack_h2(x[6], x[7])));
-        }
-      }
-      if (MODE == 1) {
-        // A: row r, columns k0 .. k0 + 63 (32 packed bytes, one scale)
-        uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0;
-        float sc = 0.0f;
+      for (int c = 0; c < 4; ++c)
+        xr[slot][c] = have ? *reinterpret_cast<const uint4*>(xrow + k0 + 8 * c) : make_uint4(0, 0, 0, 0);
+      if constexpr (MODE == 1) {
         if (have_row) {
-          const uint8_t* qp = p.wq + (size_t)r * (p.K / 2) + k0 / 2;
-          q0 = ldg_stream_v4(qp);
-          q1 = ldg_stream_v4(qp + 16);
-          sc = bf16_bits_to_float(p.ws[(size_t)r * p.sstride + k0 / EE_QUANT_GROUP]);
-        }
-        const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          // word j holds columns 8j .. 8j + 7 (low nibble first, two's complement)
-          uint32_t o[4];
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int b = (int)((words[j] >> (8 * t)) & 0xFFu);
-            const int q_lo = ((b & 0xF) ^ 8) - 8, q_hi = ((b >> 4) ^ 8) - 8;
-            o[t] = pack_h2((float)q_lo * sc, (float)q_hi * sc);
-          }
-          st_shared_v4(a_s + sw128(tid, j), make_uint4(o[0], o[1], o[2], o[3]));
+          qr[slot][0] = ldg_stream_v4(qrow + k0 / 2);
+          qr[slot][1] = ldg_stream_v4(qrow + k0 / 2 + 16);
+          sr[slot] = srow[k0 / EE_QUANT_GROUP];
+        } else {
+          qr[slot][0] = qr[slot][1] = make_uint4(0, 0, 0, 0);
+          sr[slot] = 0;
         }
       }
-      fence_proxy_async();
-      mbar_arrive(&sh.full[s]);
+    };
+#pragma unroll
+    for (int d = 0; d < PD; ++d) fetch(d, d);
+    for (int i0 = 0; i0 < nks; i0 += PD) {
+#pragma unroll
+      for (int u = 0; u < PD; ++u) {
+        const int i = i0 + u;
+        if (i >= nks) break;
+        const int s = i % kStages, n = i / kStages;
+        if (n > 0 && !mbar_wait_bounded(&sh.empty[s], (n - 1) & 1, p.err, DERR_EMPTY_WAIT)) {
+          i0 = nks;  // give up: the MMA side times out on the stages it misses
+          break;
+        }
+        const uint32_t a_s = tiles_s + s * kStage, b_s = a_s + kABytes;
+        // B: 32 activations (4 chunks) of entry e
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float x[8];
+          unpair8(xr[u][c], x);
+          const int j = 4 * h + c;
+          if (MODE == 0) {
+            float lo[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) lo[t] = x[t] - bf16_bits_to_float(float_to_bf16_bits(x[t]));
+            st_shared_v4(b_s + sw128(e, j), make_uint4(pack_bf2(x[0], x[1]), pack_bf2(x[2], x[3]),
+                                                       pack_bf2(x[4], x[5]), pack_bf2(x[6], x[7])));
+            st_shared_v4(b_s + sw128(kCols + e, j), make_uint4(pack_bf2(lo[0], lo[1]), pack_bf2(lo[2], lo[3]),
+                                                               pack_bf2(lo[4], lo[5]), pack_bf2(lo[6], lo[7])));
+          } else {
+            st_shared_v4(b_s + sw128(e, j), make_uint4(pack_h2(x[0], x[1]), pack_h2(x[2], x[3]),
+                                                       pack_h2(x[4], x[5]), pack_h2(x[6], x[7])));
+          }
+        }
+        if constexpr (MODE == 1) {
+          // A: row r, the stage's 64 columns (32 packed bytes, one scale)
+          const float sc = bf16_bits_to_float(sr[u]);
+          const uint32_t words[8] = {qr[u][0].x, qr[u][0].y, qr[u][0].z, qr[u][0].w,
+                                     qr[u][1].x, qr[u][1].y, qr[u][1].z, qr[u][1].w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            // word j holds columns 8j .. 8j + 7 (low nibble first, two's complement)
+            uint32_t o[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int b = (int)((words[j] >> (8 * t)) & 0xFFu);
+              const int q_lo = ((b & 0xF) ^ 8) - 8, q_hi = ((b >> 4) ^ 8) - 8;
+              o[t] = pack_h2((float)q_lo * sc, (float)q_hi * sc);
+            }
+            st_shared_v4(a_s + sw128(tid, j), make_uint4(o[0], o[1], o[2], o[3]));
+          }
+        }
+        fence_proxy_async();
+        mbar_arrive(&sh.full[s]);
+        fetch(u, i + PD);  // this slot's next stage
+      }
     }
   }
 
@@ -323,14 +350,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
   const int rl = warp * 32 + lane;
   const int r = row0 + rl;
   const float* parts = tp.part + (size_t)tile * tp.ksplit * kCols * kBM;
+  // per-column values once (one round trip), not per row pair
+  if (tid < ncol && p.epi != EPI_HEAD) sh.col[tid] = epi_seq(p, lst[1 + tid]);
+  asm volatile("bar.sync 1, 128;" ::: "memory");
   for (int c0 = 0; c0 < ncol; c0 += 16) {
     float y[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      float acc = 0.0f;
-      if (c0 + j < ncol)
-        for (int sp = 0; sp < tp.ksplit; ++sp) acc += __ldcg(parts + ((size_t)sp * kCols + c0 + j) * kBM + rl);
-      y[j] = acc;
+    for (int j = 0; j < 16; ++j) y[j] = 0.0f;
+    // splits in order; the 16 columns' loads of a split are independent
+    for (int sp = 0; sp < tp.ksplit; ++sp) {
+      const float* src = parts + ((size_t)sp * kCols + c0) * kBM + rl;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (c0 + j < ncol) y[j] += __ldcg(src + (size_t)j * kBM);
     }
     if (p.epi == EPI_HEAD) {
       // per column (sequence): statistics over this tile's rows
@@ -358,18 +390,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       }
       asm volatile("bar.sync 1, 128;" ::: "memory");
     } else {
+      float yb[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float yb = __shfl_down_sync(0xffffffffu, y[j], 1);
-        if ((rl & 1) == 0 && r < p.N && c0 + j < ncol) {
-          const int seq = lst[1 + c0 + j];
-          switch (p.epi) {
-            case EPI_F32: epi_pair<EPI_F32>(p, seq, r, y[j], yb); break;
-            case EPI_QKV: epi_pair<EPI_QKV>(p, seq, r, y[j], yb); break;
-            case EPI_RESID: epi_pair<EPI_RESID>(p, seq, r, y[j], yb); break;
-            case EPI_SWIGLU: epi_pair<EPI_SWIGLU>(p, seq, r, y[j], yb); break;
-            default: epi_pair<EPI_X>(p, seq, r, y[j], yb); break;
-          }
+      for (int j = 0; j < 16; ++j) yb[j] = __shfl_down_sync(0xffffffffu, y[j], 1);
+      if ((rl & 1) == 0 && r < p.N) {
+        switch (p.epi) {
+#define EE_TC_EPI(E)                                                                       \
+  case E:                                                                                  \
+    _Pragma("unroll") for (int j = 0; j < 16; ++j) if (c0 + j < ncol)                      \
+        epi_pair_at<E>(p, sh.col[c0 + j], r, y[j], yb[j]);                                 \
+    break;
+          EE_TC_EPI(EPI_F32)
+          EE_TC_EPI(EPI_QKV)
+          EE_TC_EPI(EPI_RESID)
+          EE_TC_EPI(EPI_SWIGLU)
+          EE_TC_EPI(EPI_X)
+#undef EE_TC_EPI
+          default: break;
         }
       }
     }
@@ -390,16 +427,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
 
 }  // namespace
 
-TcPlan gemm_tc_plan(int N, int K, int num_sms) {
+TcPlan gemm_tc_plan(int N, int K, int num_sms, int max_units) {
   TcPlan pl;
   pl.ntiles = (N + kBM - 1) / kBM;
   pl.nk = K / kBK;
-  // the fewest K splits that fill the SMs' waves to 90 %
+  // the fewest K splits that fill the waves (two CTAs per SM) to 90 %
+  const int slots = 2 * num_sms;
   int best = 1;
-  for (int s = 1; s <= 16 && s <= pl.nk; ++s) {
-    const int units = pl.ntiles * s, waves = (units + num_sms - 1) / num_sms;
+  for (int s = 1; s <= 16 && s <= pl.nk && (s == 1 || pl.ntiles * s <= max_units); ++s) {
+    const int units = pl.ntiles * s, waves = (units + slots - 1) / slots;
     best = s;
-    if ((double)units / ((double)waves * num_sms) >= 0.9) break;
+    if ((double)units / ((double)waves * slots) >= 0.9) break;
   }
   pl.nks = (pl.nk + best - 1) / best;
   pl.ksplit = (pl.nk + pl.nks - 1) / pl.nks;

@@ -30,7 +30,10 @@ def test_launches_per_step_count_both_sub_batches():
     _, _, n1 = eng.step_io(1, True)
     _, _, n12 = eng.step_io(12, True)
     assert n1 == 1 + 5 * L + 2 * nck + 1          # GEMV path: norms applied while staging
-    assert n12 == 1 + (1 + 8 + 2) * L + 3 * nck + 2  # two launches per projection, norm kernels
+    # norm kernels; the exit sub-batch has its own launches after the first checkpoint
+    assert n12 == 1 + (1 + 4 + 2) * L + 4 * (L - 1 - TINY.checkpoints[0]) + 3 * nck + 2
+    _, _, n12_off = eng.step_io(12, False)
+    assert n12_off == 1 + (1 + 4 + 2) * L + 2
     eng.close()
 
 
