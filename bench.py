@@ -36,6 +36,7 @@ if ROOT not in sys.path:
 import synth  # noqa: E402
 
 DEFAULT_WORKLOAD = "llama3.1-8b-b1"
+B32_WORKLOAD = "llama3.1-8b-b32"
 METRIC = "decoded tokens/s"
 L2_BYTES = 129 * 1024 * 1024
 
@@ -365,6 +366,58 @@ def kernel_roofline(sh, ckpts, prof, peak):
     return out
 
 
+def run_workload(ee, w, args, st, rank, world, peak, steps, profile_steps):
+    """Loads the workload's model, calibrates the thresholds, and times the exit
+    runs (one per threshold percentile) and the forced no-exit run."""
+    sh = w.shape
+    B = w.batch
+    max_seq = w.max_prompt() + args.warmup + steps + w.calib_steps + 16
+    lens, prompts = synth.workload_inputs(w)
+    if rank:  # replicas decode different sequences
+        prompts = synth.prompts(sh, w.seed + 1000 * rank, lens)
+    t_load = time.perf_counter()
+    eng = load_engine(ee, w, B, max_seq, st)
+    t_load = time.perf_counter() - t_load
+    gammas, calib = calibrate(eng, w, prompts, w.calib_steps, w.gamma_percentiles)
+
+    runs = {}
+    for pct in w.gamma_percentiles:
+        eng.set_thresholds(gammas[pct])
+        runs[pct] = timed_run(eng, w, prompts, steps, args.warmup, True, world,
+                              profile_steps=profile_steps, ncu_region=args.ncu_region)
+    base = timed_run(eng, w, prompts, steps, args.warmup, False, world,
+                     profile_steps=profile_steps, ncu_region=args.ncu_region)
+
+    def summarize(r, heads):
+        dev_s = sum(r["dev_ms"]) / 1e3
+        max_dev = reduce_max(dev_s, world, True)
+        max_wall = reduce_max(r["wall_s"], world, True)
+        tokens = B * steps * world
+        bytes_total = 0
+        for k, ex in enumerate(r["exits"]):
+            ctx = r["ctx0"] + k + 1
+            bytes_total += step_bytes(sh, w.checkpoints, ex, ctx, heads)
+        hist = {}
+        for ex in r["exits"]:
+            for e in ex:
+                hist[int(e)] = hist.get(int(e), 0) + 1
+        return {"value": tokens / max_dev, "e2e": tokens / max_wall, "ms_per_step": 1e3 * max_dev / steps,
+                "bytes_per_step": bytes_total / steps,
+                "step_roofline_frac_8tbs": bytes_total / dev_s / 8e12,
+                "step_roofline_frac_measured": bytes_total / dev_s / (peak * 1e9),
+                "exit_hist": dict(sorted(hist.items())), "clocks": r["clocks"]}
+
+    main = summarize(runs[w.gamma_percentiles[0]], True)
+    nox = summarize(base, False)
+    prof_main = runs[w.gamma_percentiles[0]]["profile"]
+    kr = kernel_roofline(sh, w.checkpoints, prof_main, peak) if prof_main else None
+    kr_base = kernel_roofline(sh, w.checkpoints, base["profile"], peak) if base["profile"] else None
+    others = {str(pct): dict(summarize(runs[pct], True), gamma=[float(x) for x in gammas[pct]])
+              for pct in w.gamma_percentiles[1:]}
+    return {"eng": eng, "gammas": gammas, "main": main, "nox": nox, "runs": runs, "kr": kr, "kr_base": kr_base,
+            "t_load": t_load, "others": others}
+
+
 def run_ours(args):
     import torch
 
@@ -378,48 +431,10 @@ def run_ours(args):
     sh = w.shape
     peak, peak_kind = peaks()
     B = w.batch
-    max_seq = w.max_prompt() + args.warmup + args.steps + w.calib_steps + 16
-    lens, prompts = synth.workload_inputs(w)
-    if rank:  # replicas decode different sequences
-        prompts = synth.prompts(sh, w.seed + 1000 * rank, lens)
     st = torch.cuda.Stream()
-    t_load = time.perf_counter()
-    eng = load_engine(ee, w, B, max_seq, st)
-    t_load = time.perf_counter() - t_load
-    gammas, calib = calibrate(eng, w, prompts, w.calib_steps, w.gamma_percentiles)
-
-    runs = {}
-    for pct in w.gamma_percentiles:
-        eng.set_thresholds(gammas[pct])
-        runs[pct] = timed_run(eng, w, prompts, args.steps, args.warmup, True, world,
-                              profile_steps=args.profile_steps, ncu_region=args.ncu_region)
-    base = timed_run(eng, w, prompts, args.steps, args.warmup, False, world,
-                     profile_steps=args.profile_steps, ncu_region=args.ncu_region)
-
-    def summarize(r, heads):
-        dev_s = sum(r["dev_ms"]) / 1e3
-        max_dev = reduce_max(dev_s, world, True)
-        max_wall = reduce_max(r["wall_s"], world, True)
-        tokens = B * args.steps * world
-        bytes_total = 0
-        for k, ex in enumerate(r["exits"]):
-            ctx = r["ctx0"] + k + 1
-            bytes_total += step_bytes(sh, w.checkpoints, ex, ctx, heads)
-        hist = {}
-        for ex in r["exits"]:
-            for e in ex:
-                hist[int(e)] = hist.get(int(e), 0) + 1
-        return {"value": tokens / max_dev, "e2e": tokens / max_wall, "ms_per_step": 1e3 * max_dev / args.steps,
-                "bytes_per_step": bytes_total / args.steps,
-                "step_roofline_frac_8tbs": bytes_total / dev_s / 8e12,
-                "step_roofline_frac_measured": bytes_total / dev_s / (peak * 1e9),
-                "exit_hist": dict(sorted(hist.items())), "clocks": r["clocks"]}
-
-    main = summarize(runs[w.gamma_percentiles[0]], True)
-    nox = summarize(base, False)
-    prof_main = runs[w.gamma_percentiles[0]]["profile"]
-    kr = kernel_roofline(sh, w.checkpoints, prof_main, peak) if prof_main else None
-    kr_base = kernel_roofline(sh, w.checkpoints, base["profile"], peak) if base["profile"] else None
+    res = run_workload(ee, w, args, st, rank, world, peak, args.steps, args.profile_steps)
+    eng, gammas, main, nox, runs, kr, kr_base, t_load = (res[k] for k in (
+        "eng", "gammas", "main", "nox", "runs", "kr", "kr_base", "t_load"))
     h2d, d2h, launches = eng.step_io(B, True)
 
     cpu = None
@@ -469,13 +484,38 @@ def run_ours(args):
                                 "traffic": None, "bytes_per_launch": k["bytes_per_launch"],
                                 "ms_per_launch": k["ms_per_launch"]}
             line["kernels"] = kr
-        for pct in w.gamma_percentiles[1:]:
-            extra = summarize(runs[pct], True)
-            line.setdefault("other_gammas", {})[str(pct)] = {
+        for pct, extra in res["others"].items():
+            line.setdefault("other_gammas", {})[pct] = {
                 "value": extra["value"], "ms_per_step": extra["ms_per_step"],
-                "exit_hist": extra["exit_hist"], "gamma": [float(x) for x in gammas[pct]]}
-        print(json.dumps(line), flush=True)
+                "exit_hist": extra["exit_hist"], "gamma": extra["gamma"]}
     eng.close()
+    if rank == 0 and world == 1 and args.b32_steps > 0 and w.name == DEFAULT_WORKLOAD:
+        # the metric's second configuration: the same shape at batch 32
+        # (ragged prompts, thresholds at the 40th and 70th percentiles)
+        import gc
+        del eng, res
+        gc.collect()
+        torch.cuda.empty_cache()
+        w32 = synth.WORKLOADS[B32_WORKLOAD]
+        r32 = run_workload(ee, w32, args, st, rank, world, peak, args.b32_steps, 1)
+        m32, n32 = r32["main"], r32["nox"]
+        line["b32"] = {
+            "workload": w32.name, "steps": args.b32_steps, "warmup": args.warmup,
+            "value": m32["value"], "unit": "tokens/s", "ms_per_step": m32["ms_per_step"],
+            "e2e": m32["e2e"], "step_roofline_frac_measured": m32["step_roofline_frac_measured"],
+            "bytes_per_step": m32["bytes_per_step"], "exit_hist": m32["exit_hist"],
+            "gamma_percentile": w32.gamma_percentiles[0], "clocks": m32["clocks"],
+            "other_gammas": {k: {"value": v["value"], "ms_per_step": v["ms_per_step"],
+                                 "step_roofline_frac_measured": v["step_roofline_frac_measured"]}
+                             for k, v in r32["others"].items()},
+            "no_exit": {"value": n32["value"], "ms_per_step": n32["ms_per_step"],
+                        "step_roofline_frac_measured": n32["step_roofline_frac_measured"],
+                        "bytes_per_step": n32["bytes_per_step"]},
+            "kernels": r32["kr"], "kernels_no_exit": r32["kr_base"],
+        }
+        r32["eng"].close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -508,6 +548,8 @@ def main():
     ap.add_argument("--profile-steps", type=int, default=3)
     ap.add_argument("--cpu-layers", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--b32-steps", type=int, default=32,
+                    help="timed steps of the batch-32 run added to the default workload's line (0: skip)")
     ap.add_argument("--ncu-region", action="store_true",
                     help="bracket the timed steps with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
     ap.add_argument("--dry-dist", action="store_true", help=argparse.SUPPRESS)
