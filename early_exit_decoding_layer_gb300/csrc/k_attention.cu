@@ -21,6 +21,9 @@
 // of each (sequence, kv head) -- found with an atomic counter, nothing waits
 // -- merges the partials:
 // o = sum_i acc_i exp(m_i - M) / sum_i l_i exp(m_i - M), M = max_i m_i.
+// The grid covers the longest context; a CTA whose split lies beyond its own
+// sequence's context returns at once, and the merge counts only the splits
+// that context needs.
 //
 // Cache layout (one layer): [block][kv head][16 slots][head_dim] fp16.
 #include <math.h>
@@ -75,16 +78,19 @@ __global__ void __launch_bounds__(kThreadsA) k_attention(const AttnParams p) {
   // were written at least two launches back: safe before the dependency wait.
   const int count = p.list ? ld_volatile_i32(p.list) : p.m_direct;
   const bool active = z < count;
-  int seq = 0, ctx = 0, b0 = 0, b1 = 0, last = -1;
+  int seq = 0, ctx = 0, b0 = 0, b1 = 0, last = -1, nact = 0;
   if (active) {
     seq = p.list ? ld_volatile_i32(p.list + 1 + z) : z;
     ctx = ld_volatile_i32(p.pos + seq) + 1;
     const int nb = (ctx + 15) >> 4;
+    nact = (nb + p.bpc - 1) / p.bpc;  // splits this sequence's context needs
     b0 = split * p.bpc;
     b1 = min(nb, b0 + p.bpc);
     last = nb - 1;
   }
-  const bool have = active && b0 < b1;
+  // a split beyond the context has nothing to read, write or merge
+  if (!active || split >= nact) return;
+  const bool have = b0 < b1;
   const int32_t* bt = p.block_table + (size_t)seq * p.bt_stride;
   if (tid == 0) {
     mbar_init(&bar, 1);
@@ -110,8 +116,6 @@ __global__ void __launch_bounds__(kThreadsA) k_attention(const AttnParams p) {
     bulk_g2s(Ks + (last - b0) * TILE, p.kc + off, TILE * 2, &bar, pol);
     bulk_g2s(Vs + (last - b0) * TILE, p.vc + off, TILE * 2, &bar, pol);
   }
-  if (!active) return;
-
   constexpr int TOK = BPC * 16;  // tokens per CTA at most
   __shared__ float S[G][TOK];    // scores, then exp(s - m)
   __shared__ float hm[G], hl[G];
@@ -237,7 +241,7 @@ __global__ void __launch_bounds__(kThreadsA) k_attention(const AttnParams p) {
   if (tid == 0) {
     __threadfence();
     const int old = atomicAdd(p.counters + (size_t)z * hkv + g, 1);
-    s_last = (old == p.nsplit - 1);
+    s_last = (old == nact - 1);
   }
   __syncthreads();
   if (!s_last) return;
@@ -250,13 +254,13 @@ __global__ void __launch_bounds__(kThreadsA) k_attention(const AttnParams p) {
   float* inv_l = wts + kMaxSplit * G;           // [G]
   for (int h = warp; h < G; h += kWarps) {
     float mloc = -INFINITY;
-    for (int s = lane; s < p.nsplit; s += 32) {
+    for (int s = lane; s < nact; s += 32) {
       const float l = __ldcg(parts + (size_t)s * PSZ + G * HD + G + h);
       if (l > 0.0f) mloc = fmaxf(mloc, __ldcg(parts + (size_t)s * PSZ + G * HD + h));
     }
     const float M = warp_max(mloc);
     float lsum = 0.0f;
-    for (int s = lane; s < p.nsplit; s += 32) {
+    for (int s = lane; s < nact; s += 32) {
       const float l = __ldcg(parts + (size_t)s * PSZ + G * HD + G + h);
       const float w = l > 0.0f ? expf(__ldcg(parts + (size_t)s * PSZ + G * HD + h) - M) : 0.0f;
       wts[s * G + h] = w;
@@ -270,7 +274,7 @@ __global__ void __launch_bounds__(kThreadsA) k_attention(const AttnParams p) {
     const int h = (i4 * 4) / HD;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
     int s = 0;
-    for (; s + 8 <= p.nsplit; s += 8) {
+    for (; s + 8 <= nact; s += 8) {
       float4 v[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) v[u] = __ldcg(reinterpret_cast<const float4*>(parts + (size_t)(s + u) * PSZ) + i4);
@@ -283,7 +287,7 @@ __global__ void __launch_bounds__(kThreadsA) k_attention(const AttnParams p) {
         o.w = fmaf(w, v[u].w, o.w);
       }
     }
-    for (; s < p.nsplit; ++s) {
+    for (; s < nact; ++s) {
       const float4 v = __ldcg(reinterpret_cast<const float4*>(parts + (size_t)s * PSZ) + i4);
       const float w = wts[s * G + h];
       o.x = fmaf(w, v.x, o.x);

@@ -278,19 +278,31 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
           }
         }
         if constexpr (MODE == 1) {
-          // A: row r, the stage's 64 columns (32 packed bytes, one scale)
-          const float sc = bf16_bits_to_float(sr[u]);
+          // A: row r, the stage's 64 columns (32 packed bytes, one scale).
+          // Byte t of a word holds columns 2t (low nibble) and 2t + 1, two's
+          // complement; XOR 8 makes each nibble n = q + 8.  prmt copies byte t
+          // into both halves, the mask keeps n_lo in the low half and
+          // 16 n_hi in the high one under the fp16 exponent of 1024, and one
+          // HFMA2 leaves (q_lo, q_hi) exactly; one HMUL2 applies the scale.
+          const __half2 s2 = __float2half2_rn(bf16_bits_to_float(sr[u]));
+          const __half2 mul = __halves2half2(__ushort_as_half((unsigned short)0x3C00),   // 1
+                                             __ushort_as_half((unsigned short)0x2C00));  // 1/16
+          const __half2 add = __halves2half2(__ushort_as_half((unsigned short)0xE408),   // -1032
+                                             __ushort_as_half((unsigned short)0xD480));  // -72
           const uint32_t words[8] = {qr[u][0].x, qr[u][0].y, qr[u][0].z, qr[u][0].w,
                                      qr[u][1].x, qr[u][1].y, qr[u][1].z, qr[u][1].w};
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            // word j holds columns 8j .. 8j + 7 (low nibble first, two's complement)
+            const uint32_t t = words[j] ^ 0x88888888u;
             uint32_t o[4];
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const int b = (int)((words[j] >> (8 * t)) & 0xFFu);
-              const int q_lo = ((b & 0xF) ^ 8) - 8, q_hi = ((b >> 4) ^ 8) - 8;
-              o[t] = pack_h2((float)q_lo * sc, (float)q_hi * sc);
+            for (int b = 0; b < 4; ++b) {
+              uint32_t x;
+              asm("prmt.b32 %0, %1, 0, %2;" : "=r"(x) : "r"(t), "r"(0x4040u | (uint32_t)b | ((uint32_t)b << 8)));
+              const uint32_t m = (x & 0x00F0000Fu) | 0x64006400u;
+              __half2 q = __hfma2(*reinterpret_cast<const __half2*>(&m), mul, add);
+              q = __hmul2(q, s2);
+              o[b] = *reinterpret_cast<const uint32_t*>(&q);
             }
             st_shared_v4(a_s + sw128(tid, j), make_uint4(o[0], o[1], o[2], o[3]));
           }
@@ -357,8 +369,23 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
     float y[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) y[j] = 0.0f;
-    // splits in order; the 16 columns' loads of a split are independent
-    for (int sp = 0; sp < tp.ksplit; ++sp) {
+    // splits added in order; the loads of 4 splits x 16 columns are issued
+    // together (independent), the sums keep the split order
+    int sp = 0;
+    for (; sp + 4 <= tp.ksplit; sp += 4) {
+      float v[4][16];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float* src = parts + ((size_t)(sp + u) * kCols + c0) * kBM + rl;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[u][j] = c0 + j < ncol ? __ldcg(src + (size_t)j * kBM) : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) y[j] += v[u][j];
+    }
+    for (; sp < tp.ksplit; ++sp) {
       const float* src = parts + ((size_t)sp * kCols + c0) * kBM + rl;
 #pragma unroll
       for (int j = 0; j < 16; ++j)
@@ -434,7 +461,11 @@ TcPlan gemm_tc_plan(int N, int K, int num_sms, int max_units) {
   // the fewest K splits that fill the waves (two CTAs per SM) to 90 %
   const int slots = 2 * num_sms;
   int best = 1;
-  for (int s = 1; s <= 16 && s <= pl.nk && (s == 1 || pl.ntiles * s <= max_units); ++s) {
+  // each split keeps at least kMinSteps K steps: a unit's fixed costs (set-up,
+  // pipeline fill, partial write, its share of the tile's reduction) need
+  // that much streaming to hide behind
+  constexpr int kMinSteps = 8;
+  for (int s = 1; s <= 16 && s * kMinSteps <= pl.nk && (s == 1 || pl.ntiles * s <= max_units); ++s) {
     const int units = pl.ntiles * s, waves = (units + slots - 1) / slots;
     best = s;
     if ((double)units / ((double)waves * slots) >= 0.9) break;
