@@ -230,4 +230,5 @@ cudaError_t launch_copy_rows(void* dst, int64_t dst_stride_bytes, int64_t dst_ro
 cudaError_t launch_transpose_bf16(uint16_t* dst, const uint16_t* src, int n, cudaStream_t st);
 cudaError_t launch_fill_u16(uint16_t* p, uint16_t v, int64_t n, cudaStream_t st);
 
+
 }  // namespace ee

@@ -471,28 +471,26 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
       EE_LAUNCH(log, EE_K_NORM, j, launch_rmsnorm(np, B, c->pdl, st));
     }
     // QKV projection + RoPE + K/V write into the shared paged cache
-    LinearParams p = base;
-    p.N = m.nqkv;
-    p.K = m.d;
-    p.w = w.wqkv;
-    p.wq = w.qkv.q;
-    p.ws = w.qkv.s;
-    p.sstride = sstride_of(m.d);
-    p.list_full = c->lists->full;
-    p.list_exit = c->lists->exitl;
-    p.xh = c->xh;
-    p.x_stride = m.d;
+    LinearParams pq = base;
+    pq.N = m.nqkv;
+    pq.K = m.d;
+    pq.w = w.wqkv;
+    pq.wq = w.qkv.q;
+    pq.ws = w.qkv.s;
+    pq.sstride = sstride_of(m.d);
+    pq.list_full = c->lists->full;
+    pq.list_exit = c->lists->exitl;
+    pq.xh = c->xh;
+    pq.x_stride = m.d;
     if (fuse_norm) {
-      norm_on_stage(p, w.g_attn);
-      p.lists_after_wait = lists_just_written ? 1 : 0;
+      norm_on_stage(pq, w.g_attn);
+      pq.lists_after_wait = lists_just_written ? 1 : 0;
     }
-    p.epi = EPI_QKV;
-    p.q_out = c->q;
-    p.kc = c->kcache + (size_t)j * m.kv_layer_elems;
-    p.vc = c->vcache + (size_t)j * m.kv_layer_elems;
-    p.max_rows = B;
-    EE_PROJECT(EE_K_QKV, j, p, c->tc ? &c->tm_layer[4 * j + 0] : nullptr, linear_grid(p.N, c->num_sms));
-    lists_just_written = false;
+    pq.epi = EPI_QKV;
+    pq.q_out = c->q;
+    pq.kc = c->kcache + (size_t)j * m.kv_layer_elems;
+    pq.vc = c->vcache + (size_t)j * m.kv_layer_elems;
+    pq.max_rows = B;
     // decode attention
     AttnParams ap = {};
     ap.list = c->lists->part;
@@ -501,8 +499,8 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     ap.head_dim = m.hd;
     ap.q = c->q;
     ap.q_stride = m.dq;
-    ap.kc = p.kc;
-    ap.vc = p.vc;
+    ap.kc = pq.kc;
+    ap.vc = pq.vc;
     ap.block_table = c->block_table;
     ap.bt_stride = m.bps;
     ap.pos = c->pos;
@@ -513,61 +511,65 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     ap.oh = c->ah;
     ap.o_stride = m.dq;
     ap.err = err;
-    EE_LAUNCH(log, EE_K_ATTN, j, launch_attention(ap, B, c->pdl, st));
     // O projection + residual
-    p = base;
-    p.N = m.d;
-    p.K = m.dq;
-    p.w = w.wo;
-    p.wq = w.o.q;
-    p.ws = w.o.s;
-    p.sstride = sstride_of(m.dq);
-    p.list_full = c->lists->full;
-    p.list_exit = c->lists->exitl;
-    p.xh = c->ah;
-    p.x_stride = m.dq;
-    p.epi = EPI_RESID;
-    p.max_rows = B;
-    EE_PROJECT(EE_K_O, j, p, c->tc ? &c->tm_layer[4 * j + 1] : nullptr, linear_grid(p.N, c->num_sms));
+    LinearParams po = base;
+    po.N = m.d;
+    po.K = m.dq;
+    po.w = w.wo;
+    po.wq = w.o.q;
+    po.ws = w.o.s;
+    po.sstride = sstride_of(m.dq);
+    po.list_full = c->lists->full;
+    po.list_exit = c->lists->exitl;
+    po.xh = c->ah;
+    po.x_stride = m.dq;
+    po.epi = EPI_RESID;
+    po.max_rows = B;
+    // gate/up + SwiGLU
+    LinearParams pg = base;
+    pg.N = 2 * m.F;
+    pg.K = m.d;
+    pg.w = w.wgu;
+    pg.wq = w.gu.q;
+    pg.ws = w.gu.s;
+    pg.sstride = sstride_of(m.d);
+    pg.list_full = c->lists->full;
+    pg.list_exit = c->lists->exitl;
+    pg.xh = c->xh;
+    pg.x_stride = m.d;
+    if (fuse_norm) norm_on_stage(pg, w.g_ffn);
+    pg.epi = EPI_SWIGLU;
+    pg.xh_out = c->acth;
+    pg.xo_stride = m.F;
+    pg.max_rows = B;
+    // down projection + residual (+ per-layer copy in debug mode)
+    LinearParams pd = base;
+    pd.N = m.d;
+    pd.K = m.F;
+    pd.w = w.wd;
+    pd.wq = w.d.q;
+    pd.ws = w.d.s;
+    pd.sstride = sstride_of(m.F);
+    pd.list_full = c->lists->full;
+    pd.list_exit = c->lists->exitl;
+    pd.xh = c->acth;
+    pd.x_stride = m.F;
+    pd.epi = EPI_RESID;
+    pd.hdbg = c->hdbg + (size_t)j * EE_MAX_BATCH * m.d;
+    pd.max_rows = B;
+
+    EE_PROJECT(EE_K_QKV, j, pq, c->tc ? &c->tm_layer[4 * j + 0] : nullptr, linear_grid(pq.N, c->num_sms));
+    lists_just_written = false;
+    EE_LAUNCH(log, EE_K_ATTN, j, launch_attention(ap, B, c->pdl, st));
+    EE_PROJECT(EE_K_O, j, po, c->tc ? &c->tm_layer[4 * j + 1] : nullptr, linear_grid(po.N, c->num_sms));
     // FFN RMSNorm
     if (!fuse_norm) {
       np.g = w.g_ffn;
       EE_LAUNCH(log, EE_K_NORM, j, launch_rmsnorm(np, B, c->pdl, st));
     }
-    // gate/up + SwiGLU
-    p = base;
-    p.N = 2 * m.F;
-    p.K = m.d;
-    p.w = w.wgu;
-    p.wq = w.gu.q;
-    p.ws = w.gu.s;
-    p.sstride = sstride_of(m.d);
-    p.list_full = c->lists->full;
-    p.list_exit = c->lists->exitl;
-    p.xh = c->xh;
-    p.x_stride = m.d;
-    if (fuse_norm) norm_on_stage(p, w.g_ffn);
-    p.epi = EPI_SWIGLU;
-    p.xh_out = c->acth;
-    p.xo_stride = m.F;
-    p.max_rows = B;
-    EE_PROJECT(EE_K_GATEUP, j, p, c->tc ? &c->tm_layer[4 * j + 2] : nullptr, linear_grid(p.N, c->num_sms));
-    // down projection + residual (+ per-layer copy in debug mode)
-    p = base;
-    p.N = m.d;
-    p.K = m.F;
-    p.w = w.wd;
-    p.wq = w.d.q;
-    p.ws = w.d.s;
-    p.sstride = sstride_of(m.F);
-    p.list_full = c->lists->full;
-    p.list_exit = c->lists->exitl;
-    p.xh = c->acth;
-    p.x_stride = m.F;
-    p.epi = EPI_RESID;
-    p.hdbg = c->hdbg + (size_t)j * EE_MAX_BATCH * m.d;
-    p.max_rows = B;
-    EE_PROJECT(EE_K_DOWN, j, p, c->tc ? &c->tm_layer[4 * j + 3] : nullptr, linear_grid(p.N, c->num_sms));
+    EE_PROJECT(EE_K_GATEUP, j, pg, c->tc ? &c->tm_layer[4 * j + 2] : nullptr, linear_grid(pg.N, c->num_sms));
+    EE_PROJECT(EE_K_DOWN, j, pd, c->tc ? &c->tm_layer[4 * j + 3] : nullptr, linear_grid(pd.N, c->num_sms));
+    LinearParams p;
 
     const auto ck = std::find(c->ckpts.begin(), c->ckpts.end(), j);
     if (heads && ck != c->ckpts.end()) {
@@ -1052,7 +1054,8 @@ ee_status ee_step_io(const ee_ctx* c, int32_t batch, int32_t heads, size_t* h2d,
     // for the layers after the first checkpoint when heads run)
     const bool tc = c->tc && batch >= kTcMinBatch;
     const int exit_layers = with_heads ? c->m.L - 1 - c->ckpts[0] : 0;
-    *launches = 1 + (5 + 2 * norms) * c->m.L + (tc ? 4 * exit_layers : 0) +
+    const int per_layer = 5 + 2 * norms;
+    *launches = 1 + per_layer * c->m.L + (tc ? 4 * exit_layers : 0) +
                 (with_heads ? (2 + norms) * c->m.nck : 0) + 1 + norms;
   }
   return EE_OK;
