@@ -15,8 +15,8 @@ namespace {
 
 constexpr int kAttnWarps = 8;
 constexpr int kThreadsA = kAttnWarps * 32;
-constexpr int kKvSmem = 64 * 1024;  // K + V tiles of one CTA
-constexpr int kMaxSplit = 128;
+constexpr int kKvSmem = 40 * 1024;  // K + V tiles of one CTA
+constexpr int kMaxSplit = 256;
 
 EE_DEV void to_float8(const uint4& v, float* f) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};

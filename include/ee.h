@@ -318,7 +318,7 @@ ee_status ee_op_vocab_head(int32_t M, int32_t V, int32_t d, const uint16_t *u_f1
  * allocating library call).  A shape whose ee_attention_scratch_bytes(...)
  * exceeds that size returns EE_ERR_CAPACITY without touching the device (for
  * Llama-3.1-8B heads, Hq 32, Hkv 8, hd 128, it fits B = 1 at every max_ctx up
- * to 16384, and B <= 15 at max_ctx 2048).  Invalid shapes return
+ * to 16384, and B <= 9 at max_ctx 2048).  Invalid shapes return
  * EE_ERR_INVALID_ARG.
  *
  *  - The first call on each device looks up the array's device address
