@@ -49,13 +49,23 @@ EE_DEV float dot8_bf16(const uint4& w, const uint4& x, float acc) {
 }
 
 // 8 int4 weights (one packed word) times 8 fp16 activations in pair order.
-EE_DEV __half2 dot8_int4(uint32_t word, const uint4& x, __half2 acc) {
-  const uint32_t t = word ^ 0x88888888u;
-  const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6408));  // 1032
-  acc = __hfma2(__hsub2(u32_as_h2((t & 0x000F000Fu) | 0x64006400u), bias), u32_as_h2(x.x), acc);
-  acc = __hfma2(__hsub2(u32_as_h2(((t >> 4) & 0x000F000Fu) | 0x64006400u), bias), u32_as_h2(x.y), acc);
-  acc = __hfma2(__hsub2(u32_as_h2(((t >> 8) & 0x000F000Fu) | 0x64006400u), bias), u32_as_h2(x.z), acc);
-  acc = __hfma2(__hsub2(u32_as_h2(((t >> 12) & 0x000F000Fu) | 0x64006400u), bias), u32_as_h2(x.w), acc);
+// Nibble j holds column j (two's complement).  Masking nibbles (j, j+4) under
+// the fp16 exponent of 1024 and flipping their sign bit in the same LOP3
+// ((t & m) ^ magic) gives 1024 + q + 8 in the low position or 1024 + 16 (q + 8)
+// in the high one; one HADD2 (-1032) or HFMA2 (x 1/16, -72) leaves q exactly.
+EE_DEV __half2 dot8_int4(uint32_t t, const uint4& x, __half2 acc) {
+  const __half2 m1032 = __half2half2(__ushort_as_half((unsigned short)0xE408));  // -1032
+  const __half2 r16 = __half2half2(__ushort_as_half((unsigned short)0x2C00));    // 1/16
+  const __half2 m72 = __half2half2(__ushort_as_half((unsigned short)0xD480));    // -72
+  const uint32_t t8 = t >> 8;
+  const __half2 q04 = __hadd2(u32_as_h2((t & 0x000F000Fu) ^ 0x64086408u), m1032);
+  const __half2 q15 = __hfma2(u32_as_h2((t & 0x00F000F0u) ^ 0x64806480u), r16, m72);
+  const __half2 q26 = __hadd2(u32_as_h2((t8 & 0x000F000Fu) ^ 0x64086408u), m1032);
+  const __half2 q37 = __hfma2(u32_as_h2((t8 & 0x00F000F0u) ^ 0x64806480u), r16, m72);
+  acc = __hfma2(q04, u32_as_h2(x.x), acc);
+  acc = __hfma2(q15, u32_as_h2(x.y), acc);
+  acc = __hfma2(q26, u32_as_h2(x.z), acc);
+  acc = __hfma2(q37, u32_as_h2(x.w), acc);
   return acc;
 }
 

@@ -280,10 +280,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
         if constexpr (MODE == 1) {
           // A: row r, the stage's 64 columns (32 packed bytes, one scale).
           // Byte t of a word holds columns 2t (low nibble) and 2t + 1, two's
-          // complement; XOR 8 makes each nibble n = q + 8.  prmt copies byte t
-          // into both halves, the mask keeps n_lo in the low half and
-          // 16 n_hi in the high one under the fp16 exponent of 1024, and one
-          // HFMA2 leaves (q_lo, q_hi) exactly; one HMUL2 applies the scale.
+          // complement.  prmt copies byte t into both halves; the mask keeps
+          // the low nibble in the low half and 16 x the high nibble in the
+          // high one under the fp16 exponent of 1024, flipping each nibble's
+          // sign bit (n ^ 8 = q + 8) in the same LOP3; one HFMA2 leaves
+          // (q_lo, q_hi) exactly and one HMUL2 applies the scale.
           const __half2 s2 = __float2half2_rn(bf16_bits_to_float(sr[u]));
           const __half2 mul = __halves2half2(__ushort_as_half((unsigned short)0x3C00),   // 1
                                              __ushort_as_half((unsigned short)0x2C00));  // 1/16
@@ -293,13 +294,13 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
                                      qr[u][1].x, qr[u][1].y, qr[u][1].z, qr[u][1].w};
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const uint32_t t = words[j] ^ 0x88888888u;
+            const uint32_t t = words[j];
             uint32_t o[4];
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
               uint32_t x;
               asm("prmt.b32 %0, %1, 0, %2;" : "=r"(x) : "r"(t), "r"(0x4040u | (uint32_t)b | ((uint32_t)b << 8)));
-              const uint32_t m = (x & 0x00F0000Fu) | 0x64006400u;
+              const uint32_t m = (x & 0x00F0000Fu) ^ 0x64806408u;  // also flips each nibble's sign bit
               __half2 q = __hfma2(*reinterpret_cast<const __half2*>(&m), mul, add);
               q = __hmul2(q, s2);
               o[b] = *reinterpret_cast<const uint32_t*>(&q);
