@@ -106,6 +106,22 @@ EE_DEV void attention_item(const AttnParams& p, int split, int g, int z, uint8_t
   auto& hl = sh.hl;
   float* wpart = reinterpret_cast<float*>(smem);  // [warp][PSZ], after the tiles are consumed
 
+  // the queries (written by the previous kernel) load while the K/V copies land
+  const float scale = rsqrtf((float)HD);
+  float q[G][8];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const float4* qp = reinterpret_cast<const float4*>(p.q + (size_t)seq * p.q_stride + (g * G + h) * HD + dl * 8);
+    const float4 a = qp[0], b = qp[1];
+    q[h][0] = a.x * scale;
+    q[h][1] = a.y * scale;
+    q[h][2] = a.z * scale;
+    q[h][3] = a.w * scale;
+    q[h][4] = b.x * scale;
+    q[h][5] = b.y * scale;
+    q[h][6] = b.z * scale;
+    q[h][7] = b.w * scale;
+  }
   bool ok = true;
   if (have) ok = mbar_wait_bounded(&sh.bar, 0, p.err, DERR_FULL_WAIT);
   if (have && !ok) mbar_wait_bounded(&sh.bar, 0, p.err, DERR_DRAIN_WAIT);  // copies land before reuse
@@ -114,22 +130,6 @@ EE_DEV void attention_item(const AttnParams& p, int split, int g, int z, uint8_t
 
   // (1) scores
   if (n > 0) {
-    const float scale = rsqrtf((float)HD);
-    float q[G][8];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float4* qp =
-          reinterpret_cast<const float4*>(p.q + (size_t)seq * p.q_stride + (g * G + h) * HD + dl * 8);
-      const float4 a = qp[0], b = qp[1];
-      q[h][0] = a.x * scale;
-      q[h][1] = a.y * scale;
-      q[h][2] = a.z * scale;
-      q[h][3] = a.w * scale;
-      q[h][4] = b.x * scale;
-      q[h][5] = b.y * scale;
-      q[h][6] = b.z * scale;
-      q[h][7] = b.w * scale;
-    }
     for (int base = warp * TPW; base < n; base += kAttnWarps * TPW) {
       const int r = base + sub;
       float kf[8];
