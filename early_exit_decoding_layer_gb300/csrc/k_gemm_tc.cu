@@ -459,17 +459,24 @@ TcPlan gemm_tc_plan(int N, int K, int num_sms, int max_units) {
   TcPlan pl;
   pl.ntiles = (N + kBM - 1) / kBM;
   pl.nk = K / kBK;
-  // the fewest K splits that fill the waves (two CTAs per SM) to 90 %
+  // Choose the K split that minimises the estimated time: waves of work units
+  // (two CTAs per SM), each paying a fixed cost (set-up, pipeline fill,
+  // epilogue, its share of the tile's reduction; about 7 us measured) plus
+  // its K steps (about 0.75 us each with every SM streaming).
+  constexpr double kFixedUs = 7.0, kStepUs = 0.75;
   const int slots = 2 * num_sms;
   int best = 1;
-  // each split keeps at least kMinSteps K steps: a unit's fixed costs (set-up,
-  // pipeline fill, partial write, its share of the tile's reduction) need
-  // that much streaming to hide behind
-  constexpr int kMinSteps = 8;
-  for (int s = 1; s <= 16 && s * kMinSteps <= pl.nk && (s == 1 || pl.ntiles * s <= max_units); ++s) {
-    const int units = pl.ntiles * s, waves = (units + slots - 1) / slots;
-    best = s;
-    if ((double)units / ((double)waves * slots) >= 0.9) break;
+  double best_t = 1e30;
+  for (int s = 1; s <= 32 && s <= pl.nk; ++s) {
+    const int nks = (pl.nk + s - 1) / s, splits = (pl.nk + nks - 1) / nks;
+    const int units = pl.ntiles * splits;
+    if (s > 1 && units > max_units) break;
+    const int waves = (units + slots - 1) / slots;
+    const double t = waves * (kFixedUs + nks * kStepUs);
+    if (t < best_t - 1e-9) {
+      best_t = t;
+      best = s;
+    }
   }
   pl.nks = (pl.nk + best - 1) / best;
   pl.ksplit = (pl.nk + pl.nks - 1) / pl.nks;
