@@ -99,9 +99,10 @@ EE_DEV bool check_ok(int32_t* err, bool ok, int site, long long v1, long long v2
 // the bf16 matrix (PH 0) or of the packed int4 matrix (PH 1), nv 16-byte
 // vectors each.  When nv % 32 == 0 the rows are walked as one stream of
 // steps of 32 vectors (one per lane: a warp reads 512 contiguous bytes per
-// step), in batches of kU<PH> steps.  A batch that lies inside one row takes
-// the unrolled path; one that crosses a row boundary steps vector by vector.
-// Several sequences per pass need more registers per vector: smaller batches.
+// step), in batches of kU<PH> steps.  A batch never crosses a row: where kU
+// does not divide a row's steps, the row's last batch holds the remainder.
+// One code path for both keeps the streaming loop small.  Several sequences
+// per pass need more registers per vector: smaller batches.
 template <int PH, int MMAX>
 constexpr int kU = (PH == 0 ? 8 : 4) / (MMAX == 1 ? 1 : 2);
 static_assert(kU<0, 1> <= kBatch && kU<1, 1> <= kBatch, "batch storage");
@@ -165,29 +166,18 @@ template <int PH, int MMAX>
 EE_DEV void load_batch(const LinearParams& p, const Stream& st, LoadCursor& c, Batch& b) {
   constexpr int U = kU<PH, MMAX>;
   if (c.ri >= st.nrw) return;
-  if (c.v0 + 32 * U <= st.nv) {
+  const int cnt = min(U, (st.nv - c.v0) >> 5);  // steps left in the row
 #pragma unroll
-    for (int j = 0; j < U; ++j) {
+  for (int j = 0; j < U; ++j) {
+    if (j < cnt) {
       b.w[j] = ldg_stream_v4(c.wp + j * 512);
       if constexpr (PH == 1) put_scale<PH>(b, j, ldg_u16(c.sp + j * 8));
     }
-    c.v0 += 32 * U;
-    c.wp += 512 * U;
-    if constexpr (PH == 1) c.sp += 8 * U;
-    if (c.v0 == st.nv) next_row<PH>(p, st, c);
-  } else {
-#pragma unroll
-    for (int j = 0; j < U; ++j) {
-      if (c.ri < st.nrw) {
-        b.w[j] = ldg_stream_v4(c.wp);
-        if constexpr (PH == 1) put_scale<PH>(b, j, ldg_u16(c.sp));
-      }
-      c.v0 += 32;
-      c.wp += 512;
-      if constexpr (PH == 1) c.sp += 8;
-      if (c.v0 == st.nv) next_row<PH>(p, st, c);
-    }
   }
+  c.v0 += 32 * cnt;
+  c.wp += 512 * cnt;
+  if constexpr (PH == 1) c.sp += 8 * cnt;
+  if (c.v0 == st.nv) next_row<PH>(p, st, c);
 }
 
 // Activations of the pass's sequences: row m starts at xb + xoff[m] (fp16,
@@ -245,27 +235,15 @@ EE_DEV void compute_batch(const Stream& st, int& ri, int& v0, const Batch& b, co
                           const int32_t* xoff, int mc, int mcap, float* acc, float* rowsum, int warp, int lane) {
   constexpr int U = kU<PH, MMAX>;
   if (ri >= st.nrw) return;
-  if (v0 + 32 * U <= st.nv) {
+  const int cnt = min(U, (st.nv - v0) >> 5);
 #pragma unroll
-    for (int j = 0; j < U; ++j)
-      dot_vec<PH, PL, MMAX>(b.w[j], scale_of<PH>(b, j), xb, xoff, v0 + 32 * j + lane, st.nv, mc, acc);
-    v0 += 32 * U;
-    if (v0 == st.nv) {
-      flush_row<MMAX>(rowsum, mcap, warp + kWarps * ri, mc, acc, lane);
-      v0 = 0;
-      ++ri;
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < U; ++j) {
-      if (ri < st.nrw) dot_vec<PH, PL, MMAX>(b.w[j], scale_of<PH>(b, j), xb, xoff, v0 + lane, st.nv, mc, acc);
-      v0 += 32;
-      if (v0 == st.nv) {
-        if (ri < st.nrw) flush_row<MMAX>(rowsum, mcap, warp + kWarps * ri, mc, acc, lane);
-        v0 = 0;
-        ++ri;
-      }
-    }
+  for (int j = 0; j < U; ++j)
+    if (j < cnt) dot_vec<PH, PL, MMAX>(b.w[j], scale_of<PH>(b, j), xb, xoff, v0 + 32 * j + lane, st.nv, mc, acc);
+  v0 += 32 * cnt;
+  if (v0 == st.nv) {
+    flush_row<MMAX>(rowsum, mcap, warp + kWarps * ri, mc, acc, lane);
+    v0 = 0;
+    ++ri;
   }
 }
 
@@ -282,7 +260,7 @@ EE_DEV void stream_rows(const LinearParams& p, const Plan& pl, int warp, int lan
   for (int m = 0; m < MMAX; ++m) acc[m] = 0.0f;
   if (st.nv % 32 == 0) {
     constexpr int U = kU<PH, MMAX>;
-    const int nb = (st.nrw * (st.nv / 32) + U - 1) / U;
+    const int nb = st.nrw * ((st.nv / 32 + U - 1) / U);  // batches end at row ends
     if (!pre) {
       lc = load_start<PH>(p, st, lane);
       load_batch<PH, MMAX>(p, st, lc, a);
