@@ -8,8 +8,10 @@
 //  * full sub-batch (bf16 weights, MODE 0): A tiles come from HBM by TMA with
 //    the 128-byte swizzle.  The fp16 activations are split into a bf16 high
 //    part and a bf16 remainder (x = hi + lo, 16 significant bits), so the
-//    bf16 x bf16 products keep the activations' precision: B has 64 hi rows
-//    and 64 lo rows (N = 128) and the epilogue adds the two halves of D.
+//    bf16 x bf16 products keep the activations' precision: B has nc hi rows
+//    and nc lo rows (N = 2 nc, nc = 32 for lists of up to 32 sequences, else
+//    64) and the epilogue adds the two halves of D.  Building B each stage
+//    is the producers' work, so the smaller tile halves it.
 //  * exit sub-batch (int4 weights, MODE 1): producer warps read the packed
 //    nibbles and bf16 scales, dequantise them in registers to fp16 q * s
 //    (exact: an 8-bit scale times a 4-bit integer fits fp16's 11 bits) and
@@ -38,21 +40,21 @@ namespace {
 
 constexpr int kBM = 128;  // weight rows per tile (MMA M)
 constexpr int kBK = 64;   // K elements per stage (one 128-byte swizzle row)
-template <int MODE>
-constexpr int kStages = MODE == 0 ? 3 : 4;  // two CTAs per SM fit in shared memory
+constexpr int kMaxStages = 4;
 constexpr int kCols = 64;  // sequences per launch at most (EE_MAX_BATCH)
 constexpr int kTcThreads = 192;  // warps 0-3 producers + epilogue, 4 TMA, 5 MMA
 constexpr uint32_t kABytes = kBM * kBK * 2;
 static_assert(kCols == EE_MAX_BATCH, "one launch covers the whole list");
 
+// Stage ring: the A tile and the B tile (N rows) of one K step per stage.
+// Two CTAs per SM fit in shared memory with three bf16 stages (N up to 128)
+// or four int4 ones (N = 64).  A fourth bf16 stage for N = 64 measured no
+// faster: the per-stage B build, not the bytes in flight, sets the pace.
+constexpr uint32_t stage_bytes(int n) { return kABytes + (uint32_t)n * kBK * 2; }
+constexpr int stage_count(int mode) { return mode == 0 ? 3 : kMaxStages; }
 template <int MODE>
-constexpr int kN = MODE == 0 ? 2 * kCols : kCols;  // MMA N
-template <int MODE>
-constexpr uint32_t kBBytes = (uint32_t)kN<MODE> * kBK * 2;
-template <int MODE>
-constexpr uint32_t kStageBytes = kABytes + kBBytes<MODE>;
-template <int MODE>
-constexpr size_t kTcSmem = (size_t)kStages<MODE> * kStageBytes<MODE> + 1024;
+constexpr size_t kTcSmem = (size_t)stage_count(MODE) * stage_bytes(MODE == 0 ? 2 * kCols : kCols) + 1024;
+static_assert(kTcSmem<0> == kTcSmem<1>, "both modes use the same shared memory");
 
 // Shared memory descriptor of a K-major tile with 128-byte rows and the
 // 128-byte swizzle: start address, stride between 8-row groups (1024 B),
@@ -89,11 +91,13 @@ EE_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint
       : "memory");
 }
 
-EE_DEV uint32_t pack_h2(float a, float b) {
-  return uint32_t(float_to_half_bits(a)) | (uint32_t(float_to_half_bits(b)) << 16);
-}
-EE_DEV uint32_t pack_bf2(float a, float b) {
-  return uint32_t(float_to_bf16_bits(a)) | (uint32_t(float_to_bf16_bits(b)) << 16);
+// x = hi + lo for two values: hi their bf16 roundings (one paired
+// conversion), lo the remainders, exact in bf16 for fp16 inputs.
+EE_DEV void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xFFFF0000u));
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 // 8 fp16 activations stored in pair order (0,4,1,5,2,6,3,7) -> natural order.
@@ -108,7 +112,7 @@ EE_DEV void unpair8(const uint4& v, float* x) {
 }
 
 struct TcShared {
-  uint64_t full[4], empty[4], done;
+  uint64_t full[kMaxStages], empty[kMaxStages], done;
   uint32_t tmem;
   int32_t lf[kListLen], le[kListLen];
   int last;
@@ -119,9 +123,6 @@ struct TcShared {
 
 template <int MODE>
 __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant__ TcParams tp) {
-  constexpr int N = kN<MODE>;
-  constexpr int kStages = ee::kStages<MODE>;
-  constexpr uint32_t kStage = kStageBytes<MODE>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ TcShared sh;
   uint8_t* tiles = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -145,9 +146,14 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
     grid_dep_launch();
     return;
   }
+  // B rows: bf16 keeps nc hi rows then nc lo rows; int4 keeps 64 fp16 rows
+  const int nc = MODE == 0 && ncol <= kCols / 2 ? kCols / 2 : kCols;
+  const int N = MODE == 0 ? 2 * nc : kCols;
+  const int nst = stage_count(MODE);
+  const uint32_t stage_b = stage_bytes(N);
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < nst; ++s) {
       mbar_init(&sh.full[s], MODE == 0 ? 129 : 128);
       mbar_init(&sh.empty[s], 1);
     }
@@ -171,14 +177,14 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
     // dependency wait (weights never change).
     if (MODE == 0 && lane == 0) {
       const CUtensorMap* map = &tp.amap;
-      for (int i = 0; i < nks; ++i) {
-        const int s = i % kStages, n = i / kStages;
-        if (i == kStages) grid_dep_wait();
+      for (int i = 0, s = 0, n = 0; i < nks; ++i) {  // stage s of ring pass n
+        if (i == nst) grid_dep_wait();
         if (n > 0 && !mbar_wait_bounded(&sh.empty[s], (n - 1) & 1, p.err, DERR_EMPTY_WAIT)) break;
         mbar_arrive_expect_tx(&sh.full[s], kABytes);
-        tma_load_2d(tiles_s + s * kStage, map, (ks0 + i) * kBK, row0, &sh.full[s]);
+        tma_load_2d(tiles_s + s * stage_b, map, (ks0 + i) * kBK, row0, &sh.full[s]);
+        if (++s == nst) s = 0, ++n;
       }
-      if (nks <= kStages) grid_dep_wait();
+      if (nks <= nst) grid_dep_wait();
     } else {
       grid_dep_wait();
     }
@@ -187,12 +193,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
     grid_dep_wait();
     grid_dep_launch();
     if (lane == 0) {
-      constexpr uint32_t idesc = instr_desc(MODE == 0 ? 1u : 0u, N, kBM);
-      for (int i = 0; i < nks; ++i) {
-        const int s = i % kStages;
-        if (!mbar_wait_bounded(&sh.full[s], (i / kStages) & 1, p.err, DERR_FULL_WAIT)) break;
+      const uint32_t idesc = instr_desc(MODE == 0 ? 1u : 0u, N, kBM);
+      for (int i = 0, s = 0, n = 0; i < nks; ++i) {
+        if (!mbar_wait_bounded(&sh.full[s], n & 1, p.err, DERR_FULL_WAIT)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t a_s = tiles_s + s * kStage, b_s = a_s + kABytes;
+        const uint32_t a_s = tiles_s + s * stage_b, b_s = a_s + kABytes;
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
           const uint64_t ad = smem_desc_sw128(a_s + kk * 32), bd = smem_desc_sw128(b_s + kk * 32);
@@ -205,6 +210,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                          smem_addr(&sh.empty[s]))
                      : "memory");
+        if (++s == nst) s = 0, ++n;
       }
       asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                        smem_addr(&sh.done))
@@ -218,9 +224,12 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
     grid_dep_wait();
     grid_dep_launch();
     constexpr int PD = MODE == 0 ? 3 : 4;  // stages of reads in flight per thread
-    const int e = tid & 63, h = tid >> 6;  // list entry, half of the 64-column stage
+    // B entry e (of nb = 32 or 64) and part of the stage's 8 column chunks:
+    // the 128 threads share the nb entries, nch chunks each
+    const int nb = MODE == 0 ? nc : kCols, nch = nb / 16;
+    const int e = tid & (nb - 1), part = tid / nb;
     const bool have = e < ncol;
-    const uint16_t* xrow = p.xh + (size_t)(have ? lst[1 + e] : 0) * p.x_stride + 32 * h;
+    const uint16_t* xrow = p.xh + (size_t)(have ? lst[1 + e] : 0) * p.x_stride + 8 * nch * part;
     const int r = row0 + tid;  // int4: weight row of this thread
     const bool have_row = MODE == 1 && r < p.N;
     const uint8_t* qrow = MODE == 1 ? p.wq + (size_t)(have_row ? r : 0) * (p.K / 2) : nullptr;
@@ -233,7 +242,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
       const int k0 = (ks0 + i) * kBK;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
-        xr[slot][c] = have ? *reinterpret_cast<const uint4*>(xrow + k0 + 8 * c) : make_uint4(0, 0, 0, 0);
+        if (c < nch)
+          xr[slot][c] = have ? *reinterpret_cast<const uint4*>(xrow + k0 + 8 * c) : make_uint4(0, 0, 0, 0);
       if constexpr (MODE == 1) {
         if (have_row) {
           qr[slot][0] = ldg_stream_v4(qrow + k0 / 2);
@@ -247,34 +257,35 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
     };
 #pragma unroll
     for (int d = 0; d < PD; ++d) fetch(d, d);
+    int s = 0, n = 0;  // stage of ring pass n
     for (int i0 = 0; i0 < nks; i0 += PD) {
 #pragma unroll
       for (int u = 0; u < PD; ++u) {
         const int i = i0 + u;
         if (i >= nks) break;
-        const int s = i % kStages, n = i / kStages;
         if (n > 0 && !mbar_wait_bounded(&sh.empty[s], (n - 1) & 1, p.err, DERR_EMPTY_WAIT)) {
           i0 = nks;  // give up: the MMA side times out on the stages it misses
           break;
         }
-        const uint32_t a_s = tiles_s + s * kStage, b_s = a_s + kABytes;
-        // B: 32 activations (4 chunks) of entry e
+        const uint32_t a_s = tiles_s + s * stage_b, b_s = a_s + kABytes;
+        // B: nch chunks of 8 activations of entry e (bf16: rows e and nc + e)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          float x[8];
-          unpair8(xr[u][c], x);
-          const int j = 4 * h + c;
+          if (c >= nch) break;
+          const uint4 v = xr[u][c];
+          const int j = nch * part + c;
           if (MODE == 0) {
-            float lo[8];
+            float x[8];
+            unpair8(v, x);
+            uint32_t hi[4], lo[4];
 #pragma unroll
-            for (int t = 0; t < 8; ++t) lo[t] = x[t] - bf16_bits_to_float(float_to_bf16_bits(x[t]));
-            st_shared_v4(b_s + sw128(e, j), make_uint4(pack_bf2(x[0], x[1]), pack_bf2(x[2], x[3]),
-                                                       pack_bf2(x[4], x[5]), pack_bf2(x[6], x[7])));
-            st_shared_v4(b_s + sw128(kCols + e, j), make_uint4(pack_bf2(lo[0], lo[1]), pack_bf2(lo[2], lo[3]),
-                                                               pack_bf2(lo[4], lo[5]), pack_bf2(lo[6], lo[7])));
+            for (int t = 0; t < 4; ++t) split_bf16x2(x[2 * t], x[2 * t + 1], hi[t], lo[t]);
+            st_shared_v4(b_s + sw128(e, j), make_uint4(hi[0], hi[1], hi[2], hi[3]));
+            st_shared_v4(b_s + sw128(nc + e, j), make_uint4(lo[0], lo[1], lo[2], lo[3]));
           } else {
-            st_shared_v4(b_s + sw128(e, j), make_uint4(pack_h2(x[0], x[1]), pack_h2(x[2], x[3]),
-                                                       pack_h2(x[4], x[5]), pack_h2(x[6], x[7])));
+            // pair order (x0,x4) (x1,x5) (x2,x6) (x3,x7) -> natural order
+            st_shared_v4(b_s + sw128(e, j), make_uint4(__byte_perm(v.x, v.y, 0x5410), __byte_perm(v.z, v.w, 0x5410),
+                                                       __byte_perm(v.x, v.y, 0x7632), __byte_perm(v.z, v.w, 0x7632)));
           }
         }
         if constexpr (MODE == 1) {
@@ -311,6 +322,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
         fence_proxy_async();
         mbar_arrive(&sh.full[s]);
         fetch(u, i + PD);  // this slot's next stage
+        if (++s == nst) s = 0, ++n;
       }
     }
   }
@@ -334,7 +346,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
             "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
             : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]),
               "=r"(w[8]), "=r"(w[9]), "=r"(w[10]), "=r"(w[11]), "=r"(w[12]), "=r"(w[13]), "=r"(w[14]), "=r"(w[15])
-            : "r"(tl + kCols + c0));
+            : "r"(tl + nc + c0));
       }
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll

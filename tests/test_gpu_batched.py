@@ -91,3 +91,24 @@ def test_llama1b_shape_batch10():
     assert [sorted(set(int(x) for x in e)) for e in st.gpu_exits] == [[4], [15], [8]]
     print("1B b=10 parity:", st)
     eng.close()
+
+
+def test_tiny_batch40_wide_b_tile():
+    """40 ragged sequences: lists of more than 32 sequences take the wide B
+    tile of the tensor-core GEMM (64 hi + 64 lo rows, three stages) for the
+    full sub-batch, and 40 exit rows on the int4 path when all exit early."""
+    B = 40
+    eng = parity.load_engine(TINY, max_batch=64, max_seq_len=48)
+    orc = parity.build_oracle(TINY, max_batch=64, max_seq_len=48)
+    lens = [3 + (7 * i) % 29 for i in range(B)]
+    pr = synth.prompts(TINY.shape, 47, lens)
+    inf = np.inf
+    ck = len(TINY.checkpoints)
+    gps = [[inf] * ck, [-inf] + [inf] * (ck - 1), [inf] * ck, [inf] + [-inf] * (ck - 1)]
+    st = parity.drive(eng, orc, pr, gps[0], len(gps), gamma_per_step=gps)
+    assert len(st.gpu_exits[0]) == B
+    assert [sorted(set(int(x) for x in e)) for e in st.gpu_exits] == [
+        [TINY.shape.n_layers - 1], [TINY.checkpoints[0]], [TINY.shape.n_layers - 1], [TINY.checkpoints[1]]]
+    print("tiny b=40 parity:", st)
+    parity.check_kv(eng, orc)
+    eng.close()
