@@ -20,6 +20,7 @@ collective on the data path); rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -42,6 +43,41 @@ L2_BYTES = 129 * 1024 * 1024
 
 
 # ----------------------------------------------------------------------------- helpers
+
+# ncu summary with the DRAM bytes per GEMV launch of the default workload
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "k_linear_dram_llama3.1-8b_b1.md")
+GEMV_SOURCES = ("k_linear.cu", "ee_gemv.cuh", "ee_epilogue.cuh", "ee_head.cuh", "ee_common.cuh", "ee_kernels.cuh")
+
+
+def gemv_source_digest():
+    """sha256 (16 hex digits) of the GEMV kernel's sources, in a fixed order."""
+    h = hashlib.sha256()
+    for f in GEMV_SOURCES:
+        with open(os.path.join(ROOT, "early_exit_decoding_layer_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload, path=TRAFFIC_SUMMARY):
+    """DRAM bytes (read + write) per GEMV launch from the committed ncu summary:
+    its `key: value` lines give the workload, the sources' digest and the bytes.
+    None unless the summary was taken on this workload with the GEMV sources
+    unchanged since."""
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and not line.startswith(("|", "#", " ")):
+                k, v = line.split(":", 1)
+                kv[k.strip().strip("`")] = v.strip().strip("`")
+    try:
+        if kv.get("workload") != workload or kv.get("gemv_sources_sha256") != gemv_source_digest():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError, OSError):
+        return None
+
 
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -481,7 +517,7 @@ def run_ours(args):
             line["roofline"] = {"bound": "hbm", "kernel": "k_linear (GEMV, all launches of a step)",
                                 "achieved": k["achieved_gbs"], "peak": peak,
                                 "peak_kind": peak_kind, "unit": "GB/s", "frac": k["frac"],
-                                "traffic": None, "bytes_per_launch": k["bytes_per_launch"],
+                                "traffic": measured_traffic(w.name), "bytes_per_launch": k["bytes_per_launch"],
                                 "ms_per_launch": k["ms_per_launch"]}
             line["kernels"] = kr
         for pct, extra in res["others"].items():

@@ -75,3 +75,18 @@ def test_replicas_world_size_2_gloo():
     assert out["n_gpus"] == 2
     assert out["max_time_s"] == 1.5          # the slower rank sets the time
     assert out["value"] == pytest.approx(2 * 4 * 10 / 1.5)
+
+
+def test_measured_traffic_only_for_unchanged_sources(tmp_path):
+    """The ncu traffic figure is used only for its workload and while the GEMV
+    sources hash to the digest recorded beside it."""
+    digest = bench.gemv_source_digest()
+    p = tmp_path / "summary.md"
+    body = "# title\n\n| a | b |\n|---|---|\nworkload: `llama3.1-8b-b1`\ngemv_sources_sha256: `%s`\n" \
+           "dram_bytes_per_launch: `123456789.5`\n"
+    p.write_text(body % digest)
+    assert bench.measured_traffic("llama3.1-8b-b1", str(p)) == 123456789.5
+    assert bench.measured_traffic("llama3.1-8b-b32", str(p)) is None
+    p.write_text(body % ("0" * 16))
+    assert bench.measured_traffic("llama3.1-8b-b1", str(p)) is None
+    assert bench.measured_traffic("llama3.1-8b-b1", str(tmp_path / "missing.md")) is None

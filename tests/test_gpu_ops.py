@@ -130,6 +130,9 @@ def paged(rng, B, ctxs, hkv, hd, nblocks_extra=5):
     (1, 4, 2, 64, [1]), (1, 4, 2, 64, [15]), (1, 4, 2, 64, [16]), (1, 4, 2, 64, [17]),
     (3, 32, 8, 64, [300, 1, 47]), (1, 32, 8, 128, [2304]), (2, 64, 8, 128, [4100, 33]),
     (4, 8, 8, 128, [5, 64, 129, 1000]), (2, 16, 16, 64, [700, 16]), (1, 64, 8, 128, [1]),
+    # grids of several waves of CTAs, ragged contexts
+    (8, 32, 8, 128, [3000, 17, 1500, 800, 2047, 64, 1201, 2500]),
+    (6, 32, 8, 64, [2000, 900, 31, 1777, 1200, 640]),
 ])
 def test_attention(B, hq, hkv, hd, ctxs):
     rng = np.random.default_rng(B * 7 + hq + hd + sum(ctxs))
