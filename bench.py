@@ -58,11 +58,11 @@ def gemv_source_digest():
     return h.hexdigest()[:16]
 
 
-def measured_traffic(workload, path=TRAFFIC_SUMMARY):
-    """DRAM bytes (read + write) per GEMV launch from the committed ncu summary:
-    its `key: value` lines give the workload, the sources' digest and the bytes.
-    None unless the summary was taken on this workload with the GEMV sources
-    unchanged since."""
+def measured_traffic_ratio(workload, path=TRAFFIC_SUMMARY):
+    """DRAM bytes (read + write) over algorithmic bytes of the GEMV launches in
+    the committed ncu summary: its `key: value` lines give the workload, the
+    sources' digest and the two per-launch figures.  None unless the summary
+    was taken on this workload with the GEMV sources unchanged since."""
     if not os.path.exists(path):
         return None
     kv = {}
@@ -74,8 +74,8 @@ def measured_traffic(workload, path=TRAFFIC_SUMMARY):
     try:
         if kv.get("workload") != workload or kv.get("gemv_sources_sha256") != gemv_source_digest():
             return None
-        return float(kv["dram_bytes_per_launch"])
-    except (KeyError, ValueError, OSError):
+        return float(kv["dram_bytes_per_launch"]) / float(kv["algorithmic_bytes_per_launch"])
+    except (KeyError, ValueError, ZeroDivisionError, OSError):
         return None
 
 
@@ -110,9 +110,14 @@ def launch_bytes(sh, ckpts, kind, layer, exits, ctxs):
         ex = any(e < layer for e in exits)
         return full * w_bytes(N, K, False) + ex * w_bytes(N, K, True)
     d, V = sh.d_model, sh.vocab
-    if kind == "head_t":
-        return d * d * 2
-    if kind in ("head_e", "final_head"):
+    if kind in ("head_t", "head_e"):
+        # a checkpoint's head reads T and E only for sequences still on the
+        # backbone there (e >= layer); after every sequence exited its lists
+        # are empty and it reads nothing
+        if not any(e >= layer for e in exits):
+            return 0
+        return d * d * 2 if kind == "head_t" else V * d * 2
+    if kind == "final_head":
         return V * d * 2
     if kind == "attn":
         return sum(int(c) * 2 * sh.n_kv_heads * sh.head_dim * 2 for c in ctxs)
@@ -517,8 +522,15 @@ def run_ours(args):
             line["roofline"] = {"bound": "hbm", "kernel": "k_linear (GEMV, all launches of a step)",
                                 "achieved": k["achieved_gbs"], "peak": peak,
                                 "peak_kind": peak_kind, "unit": "GB/s", "frac": k["frac"],
-                                "traffic": measured_traffic(w.name), "bytes_per_launch": k["bytes_per_launch"],
+                                "traffic": None, "bytes_per_launch": k["bytes_per_launch"],
                                 "ms_per_launch": k["ms_per_launch"]}
+            ratio = measured_traffic_ratio(w.name)
+            if ratio is not None:
+                line["roofline"]["traffic"] = ratio * k["bytes_per_launch"]
+                line["roofline"]["traffic_note"] = (
+                    "ncu dram__bytes_read.sum + dram__bytes_write.sum over the GEMV launches of two exit-run "
+                    "steps (profiles/k_linear_dram_llama3.1-8b_b1.md) = %.4f x their algorithmic bytes; "
+                    "scaled to this run's algorithmic bytes per launch" % ratio)
             line["kernels"] = kr
         for pct, extra in res["others"].items():
             line.setdefault("other_gammas", {})[pct] = {

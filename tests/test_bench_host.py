@@ -39,6 +39,20 @@ def test_step_bytes_exit_at_first_checkpoint():
     assert 7.5e9 < b < 7.8e9         # the workload's 7.64 GB bound
 
 
+def test_launch_bytes_heads_after_every_exit_read_nothing():
+    """A checkpoint head after all sequences exited runs on empty lists: no
+    algorithmic bytes; before (or at) the exit layer it reads T and E."""
+    w = synth.WORKLOADS["llama3.1-8b-b1"]
+    sh = w.shape
+    E, T = 128256 * 4096 * 2, 4096 * 4096 * 2
+    assert bench.launch_bytes(sh, w.checkpoints, "head_t", 4, [4], [100]) == T
+    assert bench.launch_bytes(sh, w.checkpoints, "head_e", 4, [4], [100]) == E
+    assert bench.launch_bytes(sh, w.checkpoints, "head_t", 8, [4], [100]) == 0
+    assert bench.launch_bytes(sh, w.checkpoints, "head_e", 8, [4], [100]) == 0
+    assert bench.launch_bytes(sh, w.checkpoints, "head_e", 8, [4, 31], [100, 100]) == E
+    assert bench.launch_bytes(sh, w.checkpoints, "final_head", -1, [4], [100]) == E
+
+
 def test_step_bytes_mixed_batch_reads_each_matrix_once():
     w = synth.WORKLOADS["llama3.1-8b-b32"]
     sh = w.shape
@@ -78,15 +92,15 @@ def test_replicas_world_size_2_gloo():
 
 
 def test_measured_traffic_only_for_unchanged_sources(tmp_path):
-    """The ncu traffic figure is used only for its workload and while the GEMV
+    """The ncu traffic ratio is used only for its workload and while the GEMV
     sources hash to the digest recorded beside it."""
     digest = bench.gemv_source_digest()
     p = tmp_path / "summary.md"
     body = "# title\n\n| a | b |\n|---|---|\nworkload: `llama3.1-8b-b1`\ngemv_sources_sha256: `%s`\n" \
-           "dram_bytes_per_launch: `123456789.5`\n"
+           "dram_bytes_per_launch: `1002`\nalgorithmic_bytes_per_launch: `1000`\n"
     p.write_text(body % digest)
-    assert bench.measured_traffic("llama3.1-8b-b1", str(p)) == 123456789.5
-    assert bench.measured_traffic("llama3.1-8b-b32", str(p)) is None
+    assert bench.measured_traffic_ratio("llama3.1-8b-b1", str(p)) == 1.002
+    assert bench.measured_traffic_ratio("llama3.1-8b-b32", str(p)) is None
     p.write_text(body % ("0" * 16))
-    assert bench.measured_traffic("llama3.1-8b-b1", str(p)) is None
-    assert bench.measured_traffic("llama3.1-8b-b1", str(tmp_path / "missing.md")) is None
+    assert bench.measured_traffic_ratio("llama3.1-8b-b1", str(p)) is None
+    assert bench.measured_traffic_ratio("llama3.1-8b-b1", str(tmp_path / "missing.md")) is None
