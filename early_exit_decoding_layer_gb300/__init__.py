@@ -69,7 +69,7 @@ class EESharedWeights(ctypes.Structure):
 
 
 class EELaunchRecord(ctypes.Structure):
-    _fields_ = [("kind", c_i32), ("layer", c_i32), ("ms", c_f32)]
+    _fields_ = [("kind", c_i32), ("layer", c_i32), ("ms", c_f32), ("kernel_ms", c_f32)]
 
 
 class EEWeights(ctypes.Structure):
@@ -305,12 +305,13 @@ class DecodeEngine:
         self._check(self.lib.ee_set_profile(self.ctx, 1 if profile else 0))
 
     def profile_read(self):
-        """[(kind name, layer, ms)] of the last profiled step's launches."""
+        """[(kind name, layer, ms, kernel_ms)] of the last profiled step's
+        launches (kernel_ms: the GEMV's own time, else 0)."""
         n = c_i32()
         self._check(self.lib.ee_profile_read(self.ctx, None, 0, ctypes.byref(n)))
         recs = (EELaunchRecord * max(1, n.value))()
         self._check(self.lib.ee_profile_read(self.ctx, recs, n.value, ctypes.byref(n)))
-        return [(KINDS[r.kind], r.layer, r.ms) for r in recs[: n.value]]
+        return [(KINDS[r.kind], r.layer, r.ms, r.kernel_ms) for r in recs[: n.value]]
 
     # -- inspection ----------------------------------------------------------
     def debug_hidden(self, layer: int) -> np.ndarray:

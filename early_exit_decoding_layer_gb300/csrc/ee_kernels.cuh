@@ -56,6 +56,10 @@ enum Epi : int32_t {
 enum HeadMode : int32_t { HEAD_CONF_ARGMAX = 0, HEAD_CHECKPOINT = 1, HEAD_FINAL = 2 };
 
 struct LinearParams {
+  // profile mode: globaltimer (ns) of the first CTA's start (atomic min) and
+  // the last CTA's end (atomic max) of this launch; null: not recorded
+  unsigned long long* stamp_start;
+  unsigned long long* stamp_end;
   int32_t N, K;
   int32_t max_rows;          // upper bound of the list counts (sequences of the step)
   // filled by launch_linear: staged activation rows (0: read from global),

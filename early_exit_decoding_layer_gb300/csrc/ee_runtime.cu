@@ -149,11 +149,13 @@ struct ee_ctx {
   int exit_enabled = 1, use_graph = 1, debug = 0;
   bool cuda_broken = false;
   std::map<std::pair<int, int>, cudaGraphExec_t> graphs;
-  // profiling: events around each launch of a step
+  // profiling: events around each launch of a step, and the GEMV launches'
+  // own start/end stamps ([0, kProfMax) starts, [kProfMax, 2 kProfMax) ends)
   int profile = 0;
   std::vector<cudaEvent_t> prof_ev;
   std::vector<std::pair<int, int>> prof_tag;  // (kind, layer) per launch of the last step
-  std::vector<float> prof_ms;
+  std::vector<float> prof_ms, prof_kernel_ms;
+  unsigned long long* prof_stamp = nullptr;
   int launches[2] = {0, 0};                   // kernels per step without / with heads
   std::string err;
 };
@@ -329,6 +331,8 @@ ee_status join_user_stream(ee_ctx* c) {
 
 // Launch bookkeeping of one step: counts launches and, in profile mode,
 // records an event before the first and after every launch.
+constexpr int kProfMax = 4096;  // launches per profiled step with stamps
+
 struct LaunchLog {
   ee_ctx* c;
   bool prof;
@@ -375,6 +379,11 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
   const Dims& m = c->m;
   cudaStream_t st = c->st;
   LaunchLog log(c, prof);
+  if (prof) {
+    if (!c->prof_stamp) EE_CUDA(c, cudaMalloc(&c->prof_stamp, 2 * kProfMax * sizeof(unsigned long long)));
+    EE_CUDA(c, cudaMemsetAsync(c->prof_stamp, 0xFF, kProfMax * sizeof(unsigned long long), st));
+    EE_CUDA(c, cudaMemsetAsync(c->prof_stamp + kProfMax, 0, kProfMax * sizeof(unsigned long long), st));
+  }
   EE_CUDA(c, cudaMemcpyAsync(c->desc_dev, c->desc_host, sizeof(StepDesc), cudaMemcpyHostToDevice, st));
 
   BeginParams bp = {};
@@ -452,7 +461,12 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
         return EE_OK;
       }
     }
-    EE_LAUNCH(log, kind, layer, launch_linear(lp, grid, c->pdl, st));
+    LinearParams lq = lp;
+    if (prof && log.n < kProfMax) {  // this launch's stamps
+      lq.stamp_start = c->prof_stamp + log.n;
+      lq.stamp_end = c->prof_stamp + kProfMax + log.n;
+    }
+    EE_LAUNCH(log, kind, layer, launch_linear(lq, grid, c->pdl, st));
     return EE_OK;
   };
 #define EE_PROJECT(kind, layer, lp, map, grid)                  \
@@ -655,6 +669,16 @@ ee_status run_step_profiled(ee_ctx* c, int B, bool heads) {
   c->prof_ms.assign(c->prof_tag.size(), 0.0f);
   for (size_t i = 0; i < c->prof_tag.size(); ++i)
     EE_CUDA(c, cudaEventElapsedTime(&c->prof_ms[i], c->prof_ev[i], c->prof_ev[i + 1]));
+  // the GEMV launches' own durations: first CTA start to last CTA end
+  const size_t nst = std::min(c->prof_tag.size(), (size_t)kProfMax);
+  std::vector<unsigned long long> t0(nst), t1(nst);
+  if (nst > 0) {
+    EE_CUDA(c, cudaMemcpy(t0.data(), c->prof_stamp, nst * 8, cudaMemcpyDeviceToHost));
+    EE_CUDA(c, cudaMemcpy(t1.data(), c->prof_stamp + kProfMax, nst * 8, cudaMemcpyDeviceToHost));
+  }
+  c->prof_kernel_ms.assign(c->prof_tag.size(), 0.0f);
+  for (size_t i = 0; i < nst; ++i)
+    if (t1[i] > t0[i]) c->prof_kernel_ms[i] = (float)((double)(t1[i] - t0[i]) * 1e-6);
   c->last_step_ms = 0.0f;
   for (float v : c->prof_ms) c->last_step_ms += v;
   return EE_OK;
@@ -903,6 +927,7 @@ void ee_destroy(ee_ctx* c) {
   for (auto& kv : c->graphs) cudaGraphExecDestroy(kv.second);
   for (auto e : c->prof_ev) cudaEventDestroy(e);
   if (c->st) cudaStreamSynchronize(c->st);
+  if (c->prof_stamp) cudaFree(c->prof_stamp);
   if (c->desc_host) cudaFreeHost(c->desc_host);
   if (c->out_host) cudaFreeHost(c->out_host);
   if (c->ev) cudaEventDestroy(c->ev);
@@ -1036,7 +1061,8 @@ ee_status ee_profile_read(ee_ctx* c, ee_launch_record* out, int32_t cap, int32_t
   *n = (int32_t)c->prof_ms.size();
   if (out)
     for (int i = 0; i < *n && i < cap; ++i)
-      out[i] = ee_launch_record{c->prof_tag[i].first, c->prof_tag[i].second, c->prof_ms[i]};
+      out[i] = ee_launch_record{c->prof_tag[i].first, c->prof_tag[i].second, c->prof_ms[i],
+                                i < (int)c->prof_kernel_ms.size() ? c->prof_kernel_ms[i] : 0.0f};
   return EE_OK;
 }
 

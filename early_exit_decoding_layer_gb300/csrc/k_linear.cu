@@ -52,10 +52,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_linear(const LinearPar
   __shared__ int s_last;
   // Lists written at least two launches back (see grid_dep_wait) may be read
   // before this grid's dependency wait; otherwise wait first.
+  if (p.stamp_start && threadIdx.x == 0) atomicMin(p.stamp_start, (unsigned long long)globaltimer());
   if (p.lists_after_wait) grid_dep_wait();
   LinState s;
   linear_prologue<XS, MMAX>(p, blockIdx.x, gridDim.x, smem, s);
   linear_body<XS, MMAX>(p, gridDim.x, smem, s, &s_last);
+  // thread 0 passes every barrier of the CTA, so its end is the CTA's end
+  if (p.stamp_end && threadIdx.x == 0) atomicMax(p.stamp_end, (unsigned long long)globaltimer());
 }
 
 cudaError_t set_smem_attr() {

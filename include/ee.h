@@ -215,9 +215,12 @@ enum {
   EE_K_FINAL_HEAD = 11 /* final LM head, argmax                          */
 };
 typedef struct {
-  int32_t kind;   /* EE_K_* */
-  int32_t layer;  /* decoder layer, or -1 */
-  float ms;       /* device time between events around the launch */
+  int32_t kind;     /* EE_K_* */
+  int32_t layer;    /* decoder layer, or -1 */
+  float ms;         /* device time between events around the launch */
+  float kernel_ms;  /* GEMV launches: the kernel's own time, first CTA start
+                       to last CTA end (%globaltimer), no launch gaps; 0 for
+                       the other kernels */
 } ee_launch_record;
 
 /* profile = 1: the following decode steps run without the CUDA graph and
