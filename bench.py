@@ -387,7 +387,7 @@ def kernel_roofline(sh, ckpts, prof, peak):
     lin = ("qkv", "o", "gateup", "down", "head_t", "head_e", "final_head")
     acc = {"linear": [0, 0.0, 0], "attn": [0, 0.0, 0]}
     per_kind = {}
-    own = [0, 0]  # launches timed by the kernel itself, all launches
+    own = [0, 0]  # GEMV launches timed by the kernel itself, all GEMV launches
     for recs, exits, ctx in prof:
         for kind, layer, ms, kms in recs:
             b = launch_bytes(sh, ckpts, kind, layer, exits, ctx)
@@ -400,8 +400,9 @@ def kernel_roofline(sh, ckpts, prof, peak):
                 acc[key][0] += b
                 acc[key][1] += kms if kms > 0 else ms
                 acc[key][2] += 1
-                own[0] += kms > 0
-                own[1] += 1
+                if key == "linear":
+                    own[0] += kms > 0
+                    own[1] += 1
     out = {}
     for k, (b, ms, n) in acc.items():
         gbs = b / (ms * 1e-3) / 1e9 if ms > 0 else 0.0
