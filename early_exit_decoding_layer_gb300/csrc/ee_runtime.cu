@@ -35,6 +35,8 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int sstride_of(int K) { return (int)ceil_div(K, EE_QUANT_GROUP); }
 
+constexpr int kProfMax = 4096;  // launches per profiled step with stamps
+
 struct Carver {
   uint8_t* base;
   size_t off = 0;
@@ -261,6 +263,7 @@ size_t carve(ee_ctx* c, const ee_config& cfg, uint8_t* base) {
   StepDesc* desc = cv.take<StepDesc>(1);
   StepOut* out = cv.take<StepOut>(1);
   float* gam = cv.take<float>(EE_MAX_CHECKPOINTS);
+  unsigned long long* pstamp = cv.take<unsigned long long>(2 * (size_t)kProfMax);  // reset per profiled step
   const size_t zb = align_up(cv.off, kAlign);
   StepLists* lists = cv.take<StepLists>(1);
   int32_t* acnt = cv.take<int32_t>((size_t)EE_MAX_BATCH * m.hkv);
@@ -294,6 +297,7 @@ size_t carve(ee_ctx* c, const ee_config& cfg, uint8_t* base) {
     c->desc_dev = desc;
     c->out_dev = out;
     c->gamma_dev = gam;
+    c->prof_stamp = pstamp;
     c->lists = lists;
     c->attn_cnt = acnt;
     c->head_cnt = hcnt;
@@ -331,8 +335,6 @@ ee_status join_user_stream(ee_ctx* c) {
 
 // Launch bookkeeping of one step: counts launches and, in profile mode,
 // records an event before the first and after every launch.
-constexpr int kProfMax = 4096;  // launches per profiled step with stamps
-
 struct LaunchLog {
   ee_ctx* c;
   bool prof;
@@ -380,7 +382,6 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
   cudaStream_t st = c->st;
   LaunchLog log(c, prof);
   if (prof) {
-    if (!c->prof_stamp) EE_CUDA(c, cudaMalloc(&c->prof_stamp, 2 * kProfMax * sizeof(unsigned long long)));
     EE_CUDA(c, cudaMemsetAsync(c->prof_stamp, 0xFF, kProfMax * sizeof(unsigned long long), st));
     EE_CUDA(c, cudaMemsetAsync(c->prof_stamp + kProfMax, 0, kProfMax * sizeof(unsigned long long), st));
   }
@@ -927,7 +928,6 @@ void ee_destroy(ee_ctx* c) {
   for (auto& kv : c->graphs) cudaGraphExecDestroy(kv.second);
   for (auto e : c->prof_ev) cudaEventDestroy(e);
   if (c->st) cudaStreamSynchronize(c->st);
-  if (c->prof_stamp) cudaFree(c->prof_stamp);
   if (c->desc_host) cudaFreeHost(c->desc_host);
   if (c->out_host) cudaFreeHost(c->out_host);
   if (c->ev) cudaEventDestroy(c->ev);
