@@ -23,6 +23,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -49,12 +50,20 @@ TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "k_linear_dram_llama3.1-8b_b1.m
 GEMV_SOURCES = ("k_linear.cu", "ee_gemv.cuh", "ee_epilogue.cuh", "ee_head.cuh", "ee_common.cuh", "ee_kernels.cuh")
 
 
+def _code_only(text):
+    """Source text without comments and with whitespace collapsed."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return " ".join(text.split())
+
+
 def gemv_source_digest():
-    """sha256 (16 hex digits) of the GEMV kernel's sources, in a fixed order."""
+    """sha256 (16 hex digits) of the GEMV kernel's sources in a fixed order,
+    comments and whitespace removed: edits to comments keep the digest."""
     h = hashlib.sha256()
     for f in GEMV_SOURCES:
-        with open(os.path.join(ROOT, "early_exit_decoding_layer_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "early_exit_decoding_layer_gb300", "csrc", f)) as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

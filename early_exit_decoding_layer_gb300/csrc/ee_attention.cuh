@@ -1,7 +1,6 @@
 // Device code of the split-K paged decode attention (see k_attention.cu for
 // the design): one work item = one split of one kv head of one sequence, run
-// by a whole CTA.  Included by the attention kernel and the persistent layer
-// kernel.
+// by a whole CTA.
 #pragma once
 
 #include <math.h>
@@ -44,8 +43,7 @@ struct AttnShared {
 };
 
 // One work item: split `split` of kv head `g` of sequence slot `z`, run by a
-// whole CTA of kThreadsA threads (a kernel CTA, or a CTA of a persistent
-// kernel that loops over items).  smem: the K/V tile space (kKvSmem bytes).
+// whole CTA of kThreadsA threads.  smem: the K/V tile space (kKvSmem bytes).
 template <int HD, int G>
 EE_DEV void attention_item(const AttnParams& p, int split, int g, int z, uint8_t* smem, AttnShared<HD, G>& sh) {
   constexpr int LPT = HD / 8;    // lanes per token

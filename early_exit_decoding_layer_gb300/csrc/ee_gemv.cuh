@@ -1,7 +1,6 @@
 // Device code of the skinny GEMV (see k_linear.cu for the design): the
 // per-CTA prologue (lists, row plan, first weight batch) and body (staging,
-// streaming, epilogues).  Included by the GEMV kernel and the persistent
-// layer kernel.
+// streaming, epilogues), included by the GEMV kernel.
 #pragma once
 
 #include <math.h>

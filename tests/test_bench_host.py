@@ -104,3 +104,11 @@ def test_measured_traffic_only_for_unchanged_sources(tmp_path):
     p.write_text(body % ("0" * 16))
     assert bench.measured_traffic_ratio("llama3.1-8b-b1", str(p)) is None
     assert bench.measured_traffic_ratio("llama3.1-8b-b1", str(tmp_path / "missing.md")) is None
+
+
+def test_source_digest_ignores_comments_only():
+    a = "int f(int x) { // the sum\n  return x + 1; /* one */ }\n"
+    b = "int f(int x) {\n  return x + 1;\n}\n// a note\n"
+    c = "int f(int x) { return x + 2; }\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
