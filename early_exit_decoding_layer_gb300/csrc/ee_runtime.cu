@@ -1375,17 +1375,32 @@ size_t ee_attention_scratch_bytes(int32_t B, int32_t n_heads, int32_t n_kv_heads
          (size_t)EE_MAX_BATCH * n_kv_heads * 4;
 }
 
-ee_status ee_op_attention(int32_t B, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, int32_t max_ctx,
-                          const float* q, const uint16_t* kcache, const uint16_t* vcache,
-                          const int32_t* block_table, int32_t bt_stride, const int32_t* pos, float* o,
-                          void* scratch, int32_t* err_flag, void* stream) {
+}  // extern "C"
+
+// Argument checks of the attention entry points (scratch checked by the caller).
+ee_status ee_attention_args_check(int32_t B, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                  int32_t max_ctx, const float* q, const uint16_t* kcache,
+                                  const uint16_t* vcache, const int32_t* block_table, int32_t bt_stride,
+                                  const int32_t* pos, const float* o) {
   if (B < 1 || B > EE_MAX_BATCH || n_kv_heads < 1 || n_heads % n_kv_heads || (head_dim != 64 && head_dim != 128))
     return EE_ERR_INVALID_ARG;
   if (max_ctx < 1 || attention_nsplit(max_ctx, head_dim) > attention_max_split()) return EE_ERR_INVALID_ARG;
   const int G = n_heads / n_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return EE_ERR_INVALID_ARG;
-  if (!q || !kcache || !vcache || !block_table || !pos || !o || !scratch || bt_stride < 1)
-    return EE_ERR_INVALID_ARG;
+  if (!q || !kcache || !vcache || !block_table || !pos || !o || bt_stride < 1) return EE_ERR_INVALID_ARG;
+  return EE_OK;
+}
+
+extern "C" {
+
+ee_status ee_op_attention(int32_t B, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, int32_t max_ctx,
+                          const float* q, const uint16_t* kcache, const uint16_t* vcache,
+                          const int32_t* block_table, int32_t bt_stride, const int32_t* pos, float* o,
+                          void* scratch, int32_t* err_flag, void* stream) {
+  const ee_status chk = ee_attention_args_check(B, n_heads, n_kv_heads, head_dim, max_ctx, q, kcache, vcache,
+                                                block_table, bt_stride, pos, o);
+  if (chk != EE_OK) return chk;
+  if (!scratch) return EE_ERR_INVALID_ARG;
   const int sms = device_sms();
   if (sms <= 0) return EE_ERR_CUDA;
   AttnParams p = {};

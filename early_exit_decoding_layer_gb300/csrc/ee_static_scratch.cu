@@ -43,12 +43,22 @@ ee_status scratch_address(void** out) {
 
 }  // namespace
 
+// The argument checks of ee_op_attention (ee_runtime.cu), run here before the
+// array is touched so that a rejected call leaves the device alone.
+ee_status ee_attention_args_check(int32_t B, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                  int32_t max_ctx, const float* q, const uint16_t* kcache,
+                                  const uint16_t* vcache, const int32_t* block_table, int32_t bt_stride,
+                                  const int32_t* pos, const float* o);
+
 extern "C" ee_status ee_op_attention_noalloc(int32_t B, int32_t n_heads, int32_t n_kv_heads,
                                              int32_t head_dim, int32_t max_ctx, const float* q,
                                              const uint16_t* kcache, const uint16_t* vcache,
                                              const int32_t* block_table, int32_t bt_stride,
                                              const int32_t* pos, float* o, int32_t* err_flag,
                                              void* stream) {
+  const ee_status chk = ee_attention_args_check(B, n_heads, n_kv_heads, head_dim, max_ctx, q, kcache, vcache,
+                                                block_table, bt_stride, pos, o);
+  if (chk != EE_OK) return chk;
   const size_t need = ee_attention_scratch_bytes(B, n_heads, n_kv_heads, head_dim, max_ctx);
   if (need == 0) return EE_ERR_INVALID_ARG;
   if (need > EE_ATTN_STATIC_SCRATCH_BYTES) return EE_ERR_CAPACITY;

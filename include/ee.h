@@ -140,7 +140,15 @@ ee_status ee_create(const ee_config *cfg, void *dev_arena, size_t arena_bytes, v
 void ee_destroy(ee_ctx *ctx);
 const char *ee_last_error(const ee_ctx *ctx);
 
-/* Loads all weights (ee_load_layer for every layer, then ee_load_shared). */
+/* Loads all weights (ee_load_layer for every layer, then ee_load_shared):
+ * the bf16 backbone, its int4 exit copies (each exit layer is a parameter
+ * copy of the original layer quantised to 4 bits, "River-LLM 深度解析" §4.1-4.2
+ * and ExitLayer in §8.1), E and the exit transforms T_l (the low-rank head
+ * softmax(h T E^T) of "大语言模型解码加速：自适应层并行机制解析" §2.1).
+ * Host or device pointers; copied, the caller keeps ownership.  Fails with
+ * EE_ERR_INVALID_ARG on a NULL tensor; layers loaded before the failing one
+ * stay loaded, and decoding is refused (EE_ERR_STATE) until every layer and
+ * the shared tensors are in (a CUDA error makes the context unusable). */
 ee_status ee_load_weights(ee_ctx *ctx, const ee_weights *w);
 /* Loads one layer: re-lays its matrices out for the kernels and builds (or
  * copies) its int4 exit copy.  Layers may be loaded in any order. */
@@ -149,8 +157,11 @@ ee_status ee_load_layer(ee_ctx *ctx, int32_t layer, const ee_layer_weights *lw);
 ee_status ee_load_shared(ee_ctx *ctx, const ee_shared_weights *sw);
 
 /* gamma[c] is the threshold of checkpoint c: a sequence exits there when
- * conf > gamma[c] (strict).  +INF never exits, -INF always exits.  Default:
- * all +INF. */
+ * conf > gamma[c] (strict).  One fixed threshold per exit layer (CALM article
+ * §2.2); the test p(t | h^(l)) > gamma of "大语言模型解码加速：自适应层并行机制解析"
+ * §2.2.  +INF never exits, -INF always exits.  Default: all +INF.  gamma is
+ * a host array of n_checkpoints floats, copied; NaN is refused
+ * (EE_ERR_INVALID_ARG). */
 ee_status ee_set_thresholds(ee_ctx *ctx, const float *gamma);
 
 /* enabled = 0: forced no-exit baseline -- no exit head is evaluated and every
@@ -164,7 +175,9 @@ ee_status ee_set_use_graph(ee_ctx *ctx, int32_t use_graph);
 
 /* ---------------------------------------------------------------- decoding */
 
-/* Starts `batch` new sequences (any previous ones are dropped as by
+/* Prefill phase ("River-LLM 深度解析" §6.1, the first of its two phases; it
+ * is run here without an exit, in full precision).
+ * Starts `batch` new sequences (any previous ones are dropped as by
  * ee_reset) and runs the bf16 stack over every prompt position with no exit,
  * writing every layer's K/V at positions 0..len-1.  tokens_concat holds the
  * prompts back to back (sum(prompt_lens) ids in [0, vocab)); each
@@ -173,15 +186,24 @@ ee_status ee_set_use_graph(ee_ctx *ctx, int32_t use_graph);
 ee_status ee_prefill(ee_ctx *ctx, int32_t batch, const int32_t *prompt_lens,
                      const int32_t *tokens_concat, int32_t *first_tokens_out);
 
-/* One early-exit greedy decode step for every sequence: in_tokens[s] (host,
- * [batch]) is the token at the sequence's next position.  Writes
+/* One early-exit greedy decode step for every sequence (the per-token loop
+ * of the CALM article §3.1: run a layer, write its K/V, score the exit head at
+ * a checkpoint and leave the full-precision path once it clears gamma; the
+ * head and test of "大语言模型解码加速：自适应层并行机制解析" §2.1-2.2; after the
+ * exit the int4 copies of "River-LLM 深度解析" §4.1-4.3 run the remaining
+ * layers and write their K/V into the shared cache).  in_tokens[s] (host,
+ * [batch]) is the token at the sequence's next position; ids outside
+ * [0, vocab) give EE_ERR_INVALID_ARG before any launch.  Writes
  * next_tokens_out[s] and exit_layers_out[s] (host, [batch]): the checkpoint
  * layer at which s exited, or n_layers-1 if it ran the whole bf16 stack.
  * Fails with EE_ERR_CAPACITY if a sequence would pass max_seq_len. */
 ee_status ee_decode_step(ee_ctx *ctx, const int32_t *in_tokens, int32_t *next_tokens_out,
                          int32_t *exit_layers_out);
 
-/* Drops all sequences and frees every KV block; weights and thresholds stay. */
+/* Drops all sequences and frees every KV block; weights and thresholds stay.
+ * The pages' shared cache (SharedKVCache of "River-LLM 深度解析" §8.2) grows
+ * per layer by concatenation; here it is a paged pool, and reset returns
+ * every block to the pool (the slots are refilled with a sentinel). */
 ee_status ee_reset(ee_ctx *ctx);
 
 /* Number of active sequences and the position (tokens in the cache) of
@@ -248,7 +270,10 @@ ee_status ee_debug_kv(ee_ctx *ctx, int32_t seq, int32_t layer, int32_t pos, uint
 ee_status ee_debug_block_table(ee_ctx *ctx, int32_t seq, int32_t *out, int32_t cap,
                                int32_t *n_blocks);
 /* The int4 exit copy of matrix `mat` of `layer` in the input layout above:
- * packed [out, in/2] bytes and scales [out, ceil(in/128)] bf16 bits (host). */
+ * packed [out, in/2] bytes and scales [out, ceil(in/128)] bf16 bits (host),
+ * whatever layout the kernels keep internally (the read-back undoes it), so
+ * that the codes and scales can be compared bit for bit with the host
+ * quantiser of "River-LLM 深度解析" §8.1 (dequantised value = q * s). */
 ee_status ee_debug_int4(ee_ctx *ctx, int32_t layer, int32_t mat, uint8_t *packed,
                         uint16_t *scales);
 

@@ -303,6 +303,28 @@ class Weights:
         key = (j, bool(int4))
         if key in self._cache:
             return self._cache[key]
+        lw = self._convert(j, bool(int4))
+        self._keep(key, lw)
+        return lw
+
+    def _keep(self, key, lw: dict):
+        nbytes = sum(v.nbytes for v in lw.values())
+        if self._cached + nbytes <= self._cache_bytes:
+            self._cache[key] = lw
+            self._cached += nbytes
+
+    def warm(self, keys, workers: int = 8):
+        """Converts the (layer, int4) entries ``keys`` ahead of use on a few
+        host threads (the conversions are independent numpy passes) and keeps
+        them within the cache budget.  No arithmetic differs from ``layer``."""
+        from concurrent.futures import ThreadPoolExecutor
+
+        todo = [(int(j), bool(q)) for j, q in keys if (int(j), bool(q)) not in self._cache]
+        with ThreadPoolExecutor(max(1, workers)) as ex:
+            for key, lw in zip(todo, ex.map(lambda k: self._convert(*k), todo)):
+                self._keep(key, lw)
+
+    def _convert(self, j: int, int4: bool) -> dict:
         src = self._layer_src(j)
         lw = {"g_attn": bf16_to_f64(src["g_attn"]), "g_ffn": bf16_to_f64(src["g_ffn"])}
         if int4:
@@ -314,10 +336,6 @@ class Weights:
         else:
             for m in MATS:
                 lw[m] = bf16_to_f64(src[m])
-        nbytes = sum(v.nbytes for v in lw.values())
-        if self._cached + nbytes <= self._cache_bytes:
-            self._cache[key] = lw
-            self._cached += nbytes
         return lw
 
 
@@ -351,6 +369,38 @@ def layer_decode(cfg: ModelConfig, lw: dict, h: np.ndarray, pos: int,
 # full causal forward over all positions (page 1 §2.2 uncached loop; prefill)
 
 
+def layer_full(cfg: ModelConfig, lws: Sequence[dict], x: np.ndarray, rows_q4: np.ndarray):
+    """One decoder layer over positions 0..P-1 of one sequence, causal.
+    ``lws[0]`` is the bf16 layer; rows where ``rows_q4`` is set use the int4
+    copy ``lws[1]``.  Returns (new residual stream [P, d], K, V [P, Hkv, hd])."""
+    P = x.shape[0]
+    hq, hkv, hd = cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
+    mask = np.triu(np.full((P, P), -np.inf), k=1)
+
+    def proj(name, inp):
+        out = linear(inp, lws[0][name])
+        if rows_q4.any():
+            out[rows_q4] = linear(inp[rows_q4], lws[1][name])
+        return out
+
+    n = rmsnorm(x, lws[0]["g_attn"], cfg.rms_eps)
+    Q = proj("wq", n).reshape(P, hq, hd)
+    K = proj("wk", n).reshape(P, hkv, hd)
+    V = proj("wv", n).reshape(P, hkv, hd)
+    for p in range(P):
+        Q[p] = rope(Q[p], p, cfg.rope_theta)
+        K[p] = rope(K[p], p, cfg.rope_theta)
+    O = np.empty((P, hq, hd))
+    for hh in range(hq):
+        g = (hh * hkv) // hq
+        S = Q[:, hh, :] @ K[:, g, :].T / math.sqrt(hd) + mask
+        O[:, hh, :] = softmax(S, axis=-1) @ V[:, g, :]
+    x = x + proj("wo", O.reshape(P, hq * hd))
+    n2 = rmsnorm(x, lws[0]["g_ffn"], cfg.rms_eps)
+    x = x + proj("wd", swiglu(proj("wg", n2), proj("wu", n2)))
+    return x, K, V
+
+
 def forward_full(cfg: ModelConfig, W: Weights, tokens: Sequence[int],
                  int4_after: Optional[Sequence[Optional[int]]] = None,
                  return_kv: bool = False):
@@ -368,36 +418,14 @@ def forward_full(cfg: ModelConfig, W: Weights, tokens: Sequence[int],
     hs = np.empty((L, P, cfg.d_model))
     Ks = np.empty((L, P, hkv, hd)) if return_kv else None
     Vs = np.empty((L, P, hkv, hd)) if return_kv else None
-    mask = np.triu(np.full((P, P), -np.inf), k=1)
     for j in range(L):
         rows_q4 = np.array([a is not None and j > a for a in int4_after], dtype=bool)
         lws = [W.layer(j, False)]
         if rows_q4.any():
             lws.append(W.layer(j, True))
-
-        def proj(name, inp):
-            out = linear(inp, lws[0][name])
-            if rows_q4.any():
-                out[rows_q4] = linear(inp[rows_q4], lws[1][name])
-            return out
-
-        n = rmsnorm(x, lws[0]["g_attn"], cfg.rms_eps)
-        Q = proj("wq", n).reshape(P, hq, hd)
-        K = proj("wk", n).reshape(P, hkv, hd)
-        V = proj("wv", n).reshape(P, hkv, hd)
-        for p in range(P):
-            Q[p] = rope(Q[p], p, cfg.rope_theta)
-            K[p] = rope(K[p], p, cfg.rope_theta)
+        x, K, V = layer_full(cfg, lws, x, rows_q4)
         if return_kv:
             Ks[j], Vs[j] = K, V
-        O = np.empty((P, hq, hd))
-        for hh in range(hq):
-            g = (hh * hkv) // hq
-            S = Q[:, hh, :] @ K[:, g, :].T / math.sqrt(hd) + mask
-            O[:, hh, :] = softmax(S, axis=-1) @ V[:, g, :]
-        x = x + proj("wo", O.reshape(P, hq * hd))
-        n2 = rmsnorm(x, lws[0]["g_ffn"], cfg.rms_eps)
-        x = x + proj("wd", swiglu(proj("wg", n2), proj("wu", n2)))
         hs[j] = x
     logits = head_logits(x[-1], W.g_final, W.E, cfg.rms_eps)
     if return_kv:
@@ -483,6 +511,7 @@ class Oracle:
         assert 1 <= len(prompts) <= self.max_batch
         self.reset()
         first = np.empty(len(prompts), dtype=np.int32)
+        xs = []
         for s, toks in enumerate(prompts):
             P = len(toks)
             assert 1 <= P < self.max_seq_len
@@ -490,12 +519,19 @@ class Oracle:
                                       int4_after=[None] * P))
             for _ in range((P + self.cfg.kv_block - 1) // self.cfg.kv_block):
                 self._alloc_block(s)
-            Kh = np.full(self._kv_shape, np.nan)
-            Vh = np.full(self._kv_shape, np.nan)
-            _, logits, Ks, Vs = forward_full(self.cfg, self.W, toks, return_kv=True)
-            Kh[:, :P], Vh[:, :P] = Ks, Vs
-            self.K.append(Kh)
-            self.V.append(Vh)
+            self.K.append(np.full(self._kv_shape, np.nan))
+            self.V.append(np.full(self._kv_shape, np.nan))
+            xs.append(self.W.E[np.asarray(toks, dtype=np.int64)].copy())
+        # the sequences are independent: each layer's weights serve all of
+        # them in turn (the same arithmetic as forward_full per sequence)
+        for j in range(self.cfg.n_layers):
+            lws = [self.W.layer(j, False)]
+            for s in range(len(prompts)):
+                P = xs[s].shape[0]
+                xs[s], K, V = layer_full(self.cfg, lws, xs[s], np.zeros(P, dtype=bool))
+                self.K[s][j, :P], self.V[s][j, :P] = K, V
+        for s in range(len(prompts)):
+            logits = head_logits(xs[s][-1], self.W.g_final, self.W.E, self.cfg.rms_eps)
             first[s] = argmax_lowest(logits)
         return first
 
@@ -522,21 +558,28 @@ class Oracle:
         logits_all = np.empty((B, cfg.vocab))
         margins = np.empty(B)
         for s in range(B):
-            st = self.seqs[s]
-            pos = st.pos
-            if pos >= self.max_seq_len:
+            if self.seqs[s].pos >= self.max_seq_len:
                 raise RuntimeError("sequence exceeds max_seq_len")
-            if pos % cfg.kv_block == 0:
+        h = []
+        for s in range(B):
+            if self.seqs[s].pos % cfg.kv_block == 0:
                 self._alloc_block(s)
-            h = self.W.E[int(in_tokens[s])].copy()
-            exited_at: Optional[int] = None
-            for j in range(L):
-                lw = self.W.layer(j, exited_at is not None)
-                h = layer_decode(cfg, lw, h, pos, self.K[s][j], self.V[s][j])
-                hidden[j, s] = h
-                if j in ck and exited_at is None and eval_heads:
+            h.append(self.W.E[int(in_tokens[s])].copy())
+        exited_at: List[Optional[int]] = [None] * B
+        # the sequences are independent: each layer's weights serve all of
+        # them in turn; every sequence runs the per-token loop of page 2 §3.1
+        for j in range(L):
+            lws = {}
+            for s in range(B):
+                q4 = exited_at[s] is not None
+                if q4 not in lws:
+                    lws[q4] = self.W.layer(j, q4)
+                pos = self.seqs[s].pos
+                h[s] = layer_decode(cfg, lws[q4], h[s], pos, self.K[s][j], self.V[s][j])
+                hidden[j, s] = h[s]
+                if j in ck and exited_at[s] is None and eval_heads:
                     c = ck.index(j)
-                    z = head_logits(h, self.W.g_final, self.W.E, cfg.rms_eps, self.W.T[c])
+                    z = head_logits(h[s], self.W.g_final, self.W.E, cfg.rms_eps, self.W.T[c])
                     conf[s, c] = max_softmax(z)
                     f = None if forced_exit is None else forced_exit[s]
                     if f is None:
@@ -544,15 +587,17 @@ class Oracle:
                     else:
                         go = (f == j)
                     if go:
-                        exited_at = j
+                        exited_at[s] = j
                         exit_layers[s] = j
-            z = head_logits(h, self.W.g_final, self.W.E, cfg.rms_eps)
+        for s in range(B):
+            st = self.seqs[s]
+            z = head_logits(h[s], self.W.g_final, self.W.E, cfg.rms_eps)
             logits_all[s] = z
             margins[s] = top2_margin(z)
             next_tokens[s] = argmax_lowest(z)
             st.tokens.append(int(in_tokens[s]))
-            st.int4_after.append(exited_at)
-            st.pos = pos + 1
+            st.int4_after.append(exited_at[s])
+            st.pos = st.pos + 1
         return StepResult(next_tokens, exit_layers, conf, hidden, logits_all, margins)
 
 

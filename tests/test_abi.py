@@ -76,3 +76,16 @@ def test_op_argument_validation(lib):
     assert lib.ee_attention_scratch_bytes(0, 4, 2, 64, 100) == 0
     assert lib.ee_attention_scratch_bytes(1, 4, 2, 64, 100) > 0
     assert lib.ee_head_scratch_bytes(1) > 0
+    # the fixed-scratch attention checks its arguments before it touches the
+    # device: bad shapes and NULL pointers are refused with no CUDA call
+    assert lib.ee_op_attention_noalloc(1, 4, 3, 64, 100, 16, 16, 16, 16, 1, 16, 16, None, None) == 1
+    assert lib.ee_op_attention_noalloc(1, 4, 2, 96, 100, 16, 16, 16, 16, 1, 16, 16, None, None) == 1
+    assert lib.ee_op_attention_noalloc(1, 4, 2, 64, 100, None, 16, 16, 16, 1, 16, 16, None, None) == 1
+    assert lib.ee_op_attention_noalloc(1, 4, 2, 64, 100, 16, 16, 16, 16, 0, 16, 16, None, None) == 1
+
+
+def test_static_scratch_size_matches_header():
+    src = open(os.path.join(ROOT, "include", "ee.h")).read()
+    m = re.search(r"#define\s+EE_ATTN_STATIC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", src)
+    assert m, "EE_ATTN_STATIC_SCRATCH_BYTES not found in ee.h"
+    assert ee.ATTN_STATIC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))

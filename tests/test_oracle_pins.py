@@ -291,6 +291,54 @@ def test_percentile_reading():
     assert np.percentile(s, 70) == pytest.approx(g["p70"][0], rel=1e-15)
 
 
+class _ScriptedOracle:
+    """Stands in for the oracle inside calibrate_gammas: it replays fixed
+    confidences and checks how it is driven (thresholds, token flow, calls)."""
+
+    def __init__(self, conf_steps, checkpoints):
+        self.cfg = type("Cfg", (), {"checkpoints": tuple(checkpoints)})()
+        self.conf_steps = conf_steps
+        self.gamma = None
+        self.calls = []
+        self.expect_tok = None
+
+    def set_thresholds(self, g):
+        self.gamma = np.asarray(g, dtype=np.float64)
+
+    def prefill(self, prompts):
+        self.calls.append("prefill")
+        self.expect_tok = np.arange(len(prompts), dtype=np.int32) + 7
+        return self.expect_tok.copy()
+
+    def decode_step(self, tok, forced_exit=None, eval_heads=True):
+        assert self.calls and self.calls[0] == "prefill"
+        assert np.all(np.isposinf(self.gamma)), "calibration must run with exits disabled"
+        assert forced_exit is None and eval_heads
+        assert np.array_equal(np.asarray(tok), self.expect_tok), "tokens must flow step to step"
+        k = sum(c == "step" for c in self.calls)
+        self.calls.append("step")
+        B = len(tok)
+        self.expect_tok = self.expect_tok + 100
+        return oracle.StepResult(self.expect_tok.copy(), np.zeros(B, np.int32),
+                                 np.asarray(self.conf_steps[k], dtype=np.float64).reshape(B, -1),
+                                 np.zeros((1, B, 1)), np.zeros((B, 2)), np.ones(B))
+
+
+def test_calibrate_gammas_hand_worked():
+    """oracle.calibrate_gammas against a hand-worked case: samples come from
+    decode steps 1..N only, with gamma = +inf, per checkpoint, percentiles by
+    linear interpolation (CALM article §2.2: one threshold per layer)."""
+    g = read_golden("gamma_calibration_example.txt")
+    n = int(g["steps"][0])
+    conf = [g["step%d" % (k + 1)] for k in range(n + 1)]
+    fake = _ScriptedOracle(conf, (4, 8))
+    gam, S = oracle.calibrate_gammas(fake, [[1, 2], [3]], n, (40, 70))
+    assert fake.calls == ["prefill"] + ["step"] * n
+    assert S.shape == (n, 2, 2)
+    assert np.allclose(gam[40], g["p40"], rtol=1e-12, atol=0)
+    assert np.allclose(gam[70], g["p70"], rtol=1e-12, atol=0)
+
+
 # --------------------------------------------------------------- whole model
 
 @pytest.fixture(scope="module")

@@ -1,9 +1,13 @@
 """ee_op_attention_noalloc (attention with the library's fixed scratch array,
 for callers that cannot allocate device memory) against ee_op_attention with a
-caller buffer, on the same seeded inputs.  Collected last so that it also runs
-after every other test in the same process; it passes alone as well."""
+caller buffer and against the CPU oracle's attention, on the same seeded
+inputs; and a check that a call allocates no device memory.  Collected last so
+that it also runs after every other test in the same process; it passes alone
+as well."""
 import numpy as np
 import pytest
+
+import oracle
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -43,18 +47,55 @@ CASES = [
 ]
 
 
+def oracle_attention(q, kc, vc, bt, pos, hq, hkv, hd):
+    """The oracle's decode attention per sequence over its gathered history."""
+    q, kc, vc = q.cpu().numpy(), kc.cpu().numpy().view(np.float16), vc.cpu().numpy().view(np.float16)
+    bt, pos = bt.cpu().numpy(), pos.cpu().numpy()
+    out = np.empty((q.shape[0], hq * hd))
+    for b in range(q.shape[0]):
+        ctx = int(pos[b]) + 1
+        slots = [(bt[b, t // 16], t % 16) for t in range(ctx)]
+        K = np.stack([kc[blk, :, off, :] for blk, off in slots]).astype(np.float64)
+        V = np.stack([vc[blk, :, off, :] for blk, off in slots]).astype(np.float64)
+        out[b] = oracle.attention_decode(q[b].astype(np.float64).reshape(hq, hd), K, V).reshape(-1)
+    return out
+
+
 def test_noalloc_matches_attention_two_calls_in_a_row():
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     for i, (B, hq, hkv, hd, ctxs, max_ctx) in enumerate(CASES):
         assert ee.attention_scratch_bytes(B, hq, hkv, hd, max_ctx) <= ee.ATTN_STATIC_SCRATCH_BYTES
         q, kc, vc, bt, pos = paged_inputs(100 + i, B, ctxs, hq, hkv, hd)
         ref = ee.attention(q, kc, vc, bt, pos, hq, hkv, hd, max_ctx, err=err)
+        want = oracle_attention(q, kc, vc, bt, pos, hq, hkv, hd)
         out = torch.empty_like(ref)
         for rep in range(2):
             out.fill_(float("nan"))
             ee.attention_noalloc(q, kc, vc, bt, pos, hq, hkv, hd, max_ctx, out=out, err=err)
             torch.cuda.synchronize()
             assert torch.allclose(out, ref, rtol=1e-4, atol=1e-5), (i, rep)
+            # the same tolerance as the attention kernel's own oracle parity test
+            assert np.allclose(out.cpu().numpy(), want, rtol=1e-4, atol=1e-5), (i, rep)
+    assert err.item() == 0
+
+
+def test_noalloc_call_allocates_no_device_memory():
+    B, hq, hkv, hd, ctxs, max_ctx = CASES[0]
+    q, kc, vc, bt, pos = paged_inputs(7, B, ctxs, hq, hkv, hd)
+    out = torch.empty(B, hq * hd, dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ee.attention_noalloc(q, kc, vc, bt, pos, hq, hkv, hd, max_ctx, out=out, err=err)  # warm-up
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    stats0 = torch.cuda.memory_stats()
+    for _ in range(3):
+        ee.attention_noalloc(q, kc, vc, bt, pos, hq, hkv, hd, max_ctx, out=out, err=err)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    stats1 = torch.cuda.memory_stats()
+    assert free1 == free0                      # nothing taken from the device (cudaMemGetInfo)
+    for k in ("allocation.all.allocated", "reserved_bytes.all.current", "allocated_bytes.all.current"):
+        assert stats1.get(k, 0) == stats0.get(k, 0), k   # nor from torch's caching allocator
     assert err.item() == 0
 
 
