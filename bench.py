@@ -22,6 +22,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -588,6 +589,114 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_ops(args):
+    """Single-kernel timings at a workload's shapes (batch 1): each op entry
+    point replayed from a CUDA graph of back-to-back launches that cycle over
+    enough weight copies that every launch reads HBM (inputs > L2); prints one
+    JSON line with the device time per launch, GB/s and the fraction of the
+    measured copy bandwidth."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import early_exit_decoding_layer_gb300 as ee
+
+    w = synth.WORKLOADS[args.workload]
+    sh = w.shape
+    peak, peak_kind = peaks()
+    d, F, dq, dk, V = sh.d_model, sh.ffn_dim, sh.n_heads * sh.head_dim, sh.n_kv_heads * sh.head_dim, sh.vocab
+    dev = torch.device("cuda")
+    st = torch.cuda.Stream()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    iters = args.ops_iters
+
+    def bf16_bits(n, k):
+        return (torch.randn((n, k), device=dev, generator=gen) * 0.02).to(torch.bfloat16).view(torch.int16)
+
+    def x16(m, k):
+        return torch.randn((m, k), device=dev, generator=gen).to(torch.float16).view(torch.int16)
+
+    def timed(make_call, nbytes):
+        ncopy = max(2, int(math.ceil(3 * L2_BYTES / max(nbytes, 1))))
+        calls = [make_call(i) for i in range(min(ncopy, iters))]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(st):
+            for c in calls:  # warm-up (first launches, kernel attributes) outside the capture
+                c()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=st):
+            for i in range(iters):
+                calls[i % len(calls)]()
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(st):
+            e0.record()
+            g.replay()
+            e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / iters
+        return {"us": us, "bytes": nbytes, "gbs": nbytes / us * 1e-3, "frac": nbytes / us * 1e-3 / peak,
+                "copies": len(calls)}
+
+    out = {}
+    mats = [("qkv", dq + 2 * dk, d), ("o", d, dq), ("gateup", 2 * F, d), ("down", d, F)]
+    for name, N, K in mats:
+        ws = []
+        x = x16(1, K)
+
+        def mk_bf16(i, N=N, K=K, x=x, ws=ws):
+            if i >= len(ws):
+                ws.append(bf16_bits(N, K))
+            wi = ws[i]
+            return lambda: ee.linear_bf16(x, wi, stream=st)
+        out["bf16_" + name] = timed(mk_bf16, N * K * 2)
+        del ws[:]
+        t4 = []
+
+        def mk_int4(i, N=N, K=K, x=x, t4=t4):
+            if i >= len(t4):
+                t4.append(ee.quantize_int4(bf16_bits(N, K)))
+            qi, si = t4[i]
+            return lambda: ee.linear_int4(x, qi, si, stream=st)
+        ng = (K + 127) // 128
+        out["int4_" + name] = timed(mk_int4, N * K // 2 + N * ng * 2)
+        del t4[:]
+        torch.cuda.empty_cache()
+    # paged attention at the workload's context, one sequence
+    ctx = w.max_prompt() + 64
+    hq, hkv, hd = sh.n_heads, sh.n_kv_heads, sh.head_dim
+    nb = (ctx + 15) // 16
+    kvs = []
+
+    def mk_attn(i):
+        if i >= len(kvs):
+            kc = torch.randn((nb, hkv, 16, hd), device=dev, generator=gen).to(torch.float16).view(torch.int16)
+            vc = torch.randn((nb, hkv, 16, hd), device=dev, generator=gen).to(torch.float16).view(torch.int16)
+            kvs.append((kc, vc))
+        kc, vc = kvs[i]
+        q = torch.randn((1, hq * hd), device=dev, generator=gen)
+        bt = torch.arange(nb, dtype=torch.int32, device=dev).view(1, nb)
+        pos = torch.tensor([ctx - 1], dtype=torch.int32, device=dev)
+        scratch = torch.zeros(ee.attention_scratch_bytes(1, hq, hkv, hd, ctx), dtype=torch.uint8, device=dev)
+        return lambda: ee.attention(q, kc, vc, bt, pos, hq, hkv, hd, ctx, scratch=scratch, stream=st)
+    out["attention_ctx%d" % ctx] = timed(mk_attn, 2 * ctx * hkv * hd * 2)
+    del kvs[:]
+    Es = []
+
+    def mk_head(i):
+        if i >= len(Es):
+            Es.append(bf16_bits(V, d))
+        Ei = Es[i]
+        u = x16(1, d)
+        scratch = torch.zeros(ee.head_scratch_bytes(1), dtype=torch.uint8, device=dev)
+        return lambda: ee.vocab_head(u, Ei, scratch=scratch, stream=st)
+    out["vocab_head"] = timed(mk_head, V * d * 2)
+    print(json.dumps({"ops": out, "workload": w.name, "iters": iters, "peak": peak, "peak_kind": peak_kind,
+                      "timing": "CUDA graph of back-to-back launches, events around one replay, device time "
+                                "per launch (includes the gap between launches)"}), flush=True)
+
+
 def run_dry_dist(args):
     """Multi-rank plumbing without a GPU (gloo): each rank reports made-up
     per-rank times; rank 0 prints the aggregate line."""
@@ -619,6 +728,9 @@ def main():
                     help="timed steps of the batch-32 run added to the default workload's line (0: skip)")
     ap.add_argument("--ncu-region", action="store_true",
                     help="bracket the timed steps with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
+    ap.add_argument("--ops", action="store_true",
+                    help="time each kernel's op entry point at the workload's shapes (batch 1) and exit")
+    ap.add_argument("--ops-iters", type=int, default=200)
     ap.add_argument("--dry-dist", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -627,6 +739,8 @@ def main():
         return run_dry_dist(args)
     if args.impl == "reference":
         return run_reference(args)
+    if args.ops:
+        return run_ops(args)
     return run_ours(args)
 
 
