@@ -134,11 +134,14 @@ def launch_bytes(sh, ckpts, kind, layer, exits, ctxs):
     return 0
 
 
-def step_bytes(sh, ckpts, exits, ctxs, heads):
+def step_bytes(sh, ckpts, exits, ctxs, heads, criterion="maxprob"):
     """Bytes a step must read (the workload's roofline rule): for each layer the
     bf16 weights if any sequence runs it in bf16 and the int4 weights plus
-    scales if any runs it on the exit copy; T and E for every head evaluated;
-    E for the final head; every sequence's K/V history of every layer."""
+    scales if any runs it on the exit copy; T and E for every head evaluated
+    (the similarity criterion reads two d-vectors per sequence instead, which
+    is negligible and not counted); E for the final head; every sequence's
+    K/V history of every layer."""
+    heads = heads and criterion == "maxprob"
     total = 0
     for j in range(sh.n_layers):
         for kind in ("qkv", "o", "gateup", "down"):
@@ -337,6 +340,29 @@ def load_engine(ee, w, max_batch, max_seq_len, stream):
     return eng
 
 
+def oracle_gammas(name):
+    """The workload's thresholds calibrated on the CPU oracle (a stored file,
+    see tests/golden/make_oracle_gammas.py), or None."""
+    path = os.path.join(ROOT, "tests", "golden", "oracle_gammas.json")
+    if not os.path.exists(path):
+        return None
+    return json.load(open(path)).get(name)
+
+
+def calibration_hist(conf, gamma, ckpts, n_layers):
+    """Exit layers that thresholds gamma give on no-exit confidence samples
+    [samples, checkpoints] (first checkpoint whose confidence is above gamma)."""
+    hist = {}
+    for row in np.asarray(conf):
+        e = n_layers - 1
+        for c, l in enumerate(ckpts):
+            if row[c] > gamma[c]:
+                e = l
+                break
+        hist[int(e)] = hist.get(int(e), 0) + 1
+    return dict(sorted(hist.items()))
+
+
 def calibrate(eng, w, prompts, steps, percentiles):
     """gamma_l = p-th percentile of the no-exit confidences at checkpoint l over
     the first `steps` decode steps (one sample per sequence and step)."""
@@ -437,7 +463,13 @@ def run_workload(ee, w, args, st, rank, world, peak, steps, profile_steps):
     t_load = time.perf_counter()
     eng = load_engine(ee, w, B, max_seq, st)
     t_load = time.perf_counter() - t_load
-    gammas, calib = calibrate(eng, w, prompts, w.calib_steps, w.gamma_percentiles)
+    lib_gammas, calib = calibrate(eng, w, prompts, w.calib_steps, w.gamma_percentiles)
+    # the thresholds: the oracle's percentiles where they were computed
+    # (tests/golden/oracle_gammas.json, written from the CPU oracle alone),
+    # else the library's own calibration on this run's prompts
+    og = oracle_gammas(w.name)
+    gammas = {p: np.asarray(og["gamma"]["p%g" % p]) for p in w.gamma_percentiles} if og else lib_gammas
+    gamma_source = "oracle" if og else "library"
 
     runs = {}
     for pct in w.gamma_percentiles:
@@ -446,8 +478,24 @@ def run_workload(ee, w, args, st, rank, world, peak, steps, profile_steps):
                               profile_steps=profile_steps, ncu_region=args.ncu_region)
     base = timed_run(eng, w, prompts, steps, args.warmup, False, world,
                      profile_steps=profile_steps, ncu_region=args.ncu_region)
+    # the state-transition-similarity criterion, thresholds at the library's
+    # percentiles of the no-exit similarity scores
+    # (per sequence; at batch > 1 also the batch-minimum rule, whose
+    # thresholds are percentiles of the per-step batch minimum)
+    sts_runs, taus = {}, {}
+    if args.sts:
+        modes = ("sts",) if B == 1 else ("sts", "sts_batch")
+        for mode in modes:
+            eng.set_exit_criterion(mode)
+            tm, _ = calibrate(eng, w, prompts, w.calib_steps, w.gamma_percentiles)
+            for pct in w.gamma_percentiles:
+                key = "%s_p%g" % (mode, pct)
+                taus[key] = tm[pct]
+                eng.set_thresholds(tm[pct])
+                sts_runs[key] = timed_run(eng, w, prompts, steps, args.warmup, True, world)
+        eng.set_exit_criterion("maxprob")
 
-    def summarize(r, heads):
+    def summarize(r, heads, criterion="maxprob"):
         dev_s = sum(r["dev_ms"]) / 1e3
         max_dev = reduce_max(dev_s, world, True)
         max_wall = reduce_max(r["wall_s"], world, True)
@@ -455,7 +503,7 @@ def run_workload(ee, w, args, st, rank, world, peak, steps, profile_steps):
         bytes_total = 0
         for k, ex in enumerate(r["exits"]):
             ctx = r["ctx0"] + k + 1
-            bytes_total += step_bytes(sh, w.checkpoints, ex, ctx, heads)
+            bytes_total += step_bytes(sh, w.checkpoints, ex, ctx, heads, criterion)
         hist = {}
         for ex in r["exits"]:
             for e in ex:
@@ -473,8 +521,13 @@ def run_workload(ee, w, args, st, rank, world, peak, steps, profile_steps):
     kr_base = kernel_roofline(sh, w.checkpoints, base["profile"], peak) if base["profile"] else None
     others = {str(pct): dict(summarize(runs[pct], True), gamma=[float(x) for x in gammas[pct]])
               for pct in w.gamma_percentiles[1:]}
+    sts = {key: dict(summarize(sts_runs[key], True, "sts"), tau=[float(x) for x in taus[key]])
+           for key in sts_runs}
+    # exit depths the library's own thresholds give on its calibration samples
+    lib_hist = calibration_hist(calib, lib_gammas[w.gamma_percentiles[0]], w.checkpoints, sh.n_layers)
     return {"eng": eng, "gammas": gammas, "main": main, "nox": nox, "runs": runs, "kr": kr, "kr_base": kr_base,
-            "t_load": t_load, "others": others}
+            "t_load": t_load, "others": others, "sts": sts, "gamma_source": gamma_source,
+            "lib_gammas": lib_gammas, "lib_hist": lib_hist}
 
 
 def run_ours(args):
@@ -535,6 +588,15 @@ def run_ours(args):
             "exit_hist": main["exit_hist"],
             "load_s": t_load,
         }
+        line["config"]["gamma_source"] = res["gamma_source"]
+        line["gamma_library"] = {"gamma": [float(x) for x in res["lib_gammas"][w.gamma_percentiles[0]]],
+                                 "exit_hist_on_calibration_samples": res["lib_hist"]}
+        if res["sts"]:
+            line["sts"] = {k: {"value": v["value"], "ms_per_step": v["ms_per_step"], "e2e": v["e2e"],
+                               "speedup_vs_no_exit": v["value"] / nox["value"],
+                               "step_roofline_frac_measured": v["step_roofline_frac_measured"],
+                               "bytes_per_step": v["bytes_per_step"], "exit_hist": v["exit_hist"],
+                               "tau": v["tau"]} for k, v in res["sts"].items()}
         if kr:
             k = kr["linear"]
             line["roofline"] = {"bound": "hbm", "kernel": "k_linear (GEMV, all launches of a step)",
@@ -580,6 +642,11 @@ def run_ours(args):
                         "step_roofline_frac_measured": n32["step_roofline_frac_measured"],
                         "bytes_per_step": n32["bytes_per_step"]},
             "kernels": r32["kr"], "kernels_no_exit": r32["kr_base"],
+            "gamma_source": r32["gamma_source"],
+            "sts": {k: {"value": v["value"], "ms_per_step": v["ms_per_step"],
+                        "speedup_vs_no_exit": v["value"] / n32["value"],
+                        "step_roofline_frac_measured": v["step_roofline_frac_measured"],
+                        "exit_hist": v["exit_hist"], "tau": v["tau"]} for k, v in r32["sts"].items()},
         }
         r32["eng"].close()
     if rank == 0:
@@ -728,6 +795,8 @@ def main():
                     help="timed steps of the batch-32 run added to the default workload's line (0: skip)")
     ap.add_argument("--ncu-region", action="store_true",
                     help="bracket the timed steps with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
+    ap.add_argument("--no-sts", dest="sts", action="store_false",
+                    help="skip the runs with the state-transition-similarity exit criterion")
     ap.add_argument("--ops", action="store_true",
                     help="time each kernel's op entry point at the workload's shapes (batch 1) and exit")
     ap.add_argument("--ops-iters", type=int, default=200)

@@ -34,11 +34,11 @@ EXPORTS = (
     "ee_debug_int4", "ee_op_quantize_int4", "ee_op_linear_bf16", "ee_op_linear_int4",
     "ee_attention_scratch_bytes", "ee_op_attention", "ee_head_scratch_bytes",
     "ee_op_vocab_head", "ee_step_io", "ee_set_profile", "ee_profile_read", "ee_last_step_ms",
-    "ee_op_attention_noalloc",
+    "ee_op_attention_noalloc", "ee_set_exit_criterion",
 )
 
 KINDS = ("begin", "norm", "qkv", "attn", "o", "gateup", "down", "head_norm", "head_t", "head_e",
-         "final_norm", "final_head")
+         "final_norm", "final_head", "exit_sts")
 
 
 class EEError(RuntimeError):
@@ -99,6 +99,7 @@ def load_library(path: str = LIB_PATH):
         "ee_load_shared": (i32, [c_vp, P(EESharedWeights)]),
         "ee_set_thresholds": (i32, [c_vp, P(c_f32)]),
         "ee_set_exit_enabled": (i32, [c_vp, i32]),
+        "ee_set_exit_criterion": (i32, [c_vp, i32]),
         "ee_set_use_graph": (i32, [c_vp, i32]),
         "ee_prefill": (i32, [c_vp, i32, P(i32), P(i32), P(i32)]),
         "ee_decode_step": (i32, [c_vp, P(i32), P(i32), P(i32)]),
@@ -254,6 +255,13 @@ class DecodeEngine:
 
     def set_exit_enabled(self, enabled: bool):
         self._check(self.lib.ee_set_exit_enabled(self.ctx, 1 if enabled else 0))
+
+    CRITERIA = {"maxprob": 0, "sts": 1, "sts_batch": 2}
+
+    def set_exit_criterion(self, criterion: str):
+        """'maxprob' (exit-head confidence, default), 'sts' (state transition
+        similarity, per sequence) or 'sts_batch' (its batch-minimum rule)."""
+        self._check(self.lib.ee_set_exit_criterion(self.ctx, self.CRITERIA[criterion]))
 
     def set_use_graph(self, use_graph: bool):
         self._check(self.lib.ee_set_use_graph(self.ctx, 1 if use_graph else 0))

@@ -78,6 +78,7 @@ EE_DEV void epi_pair_at(const LinearParams& p, const EpiSeq& e, int ra, float ya
     const float2 nw = make_float2(old.x + ya, old.y + yb);
     *reinterpret_cast<float2*>(hp) = nw;
     if (e.dbg) *reinterpret_cast<float2*>(p.hdbg + (size_t)seq * p.h_stride + ra) = nw;
+    if (p.hsave) *reinterpret_cast<float2*>(p.hsave + (size_t)seq * p.h_stride + ra) = nw;
   } else if constexpr (EPI == EPI_SWIGLU) {
     const int i = ra >> 1;
     const float a = ya / (1.0f + expf(-ya)) * yb;

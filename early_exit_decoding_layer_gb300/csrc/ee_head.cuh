@@ -48,6 +48,38 @@ EE_DEV Stat stat_warp_merge(Stat s) {
   return s;
 }
 
+// Exit decision at a checkpoint (one thread): list entry m of the full list lf
+// has score[m * stride]; it exits when the score is above gamma (strict).
+// Rebuilds the full list (the sequences that stay, in order) and the exit
+// list (the previous exit list le merged with the newly exited, by id), and
+// records the scores and exit layers.
+EE_DEV void checkpoint_decide(float gamma, int ckpt_index, int ckpt_layer, const float* score, int stride,
+                              const int32_t* lf, const int32_t* le, int nrows, float* conf_out, int32_t* exit_layer,
+                              StepLists* lists) {
+  int32_t nfull = 0, nexit = 0;
+  int32_t newly[EE_MAX_BATCH];
+  int nnew = 0;
+  for (int m = 0; m < nrows; ++m) {
+    const int seq = lf[1 + m];
+    const float conf = score[m * stride];
+    conf_out[seq * EE_MAX_CHECKPOINTS + ckpt_index] = conf;
+    if (conf > gamma) {
+      newly[nnew++] = seq;
+      exit_layer[seq] = ckpt_layer;
+    } else {
+      lists->full[1 + nfull++] = seq;
+    }
+  }
+  const int nold = min(le[0], EE_MAX_BATCH);
+  int a = 0, b = 0;
+  while (a < nold || b < nnew) {
+    const bool take_old = b >= nnew || (a < nold && le[1 + a] < newly[b]);
+    lists->exitl[1 + nexit++] = take_old ? le[1 + a++] : newly[b++];
+  }
+  lists->full[0] = nfull;
+  lists->exitl[0] = nexit;
+}
+
 // Run by threads 0 .. nthreads-1 (whole warps) of the last CTA to finish a
 // head launch: merges the nparts partials head_part[part][m] (max, sum,
 // argmax) of the nrows sequences of list lf, then writes the head's results
@@ -80,30 +112,8 @@ EE_DEV void head_finalize_group(const LinearParams& p, int nparts, const int32_t
     } else if (p.head_mode == HEAD_FINAL) {
       for (int m = 0; m < nrows; ++m) p.argmax_out[lf[1 + m]] = __float_as_int(res[2 * m + 1]);
     } else {  // HEAD_CHECKPOINT: decide, then rebuild the two sub-batch lists
-      const float gamma = p.gamma[p.ckpt_index];
-      int32_t nfull = 0, nexit = 0;
-      int32_t newly[EE_MAX_BATCH];
-      int nnew = 0;
-      for (int m = 0; m < nrows; ++m) {
-        const int seq = lf[1 + m];
-        const float conf = res[2 * m];
-        p.conf_out[seq * EE_MAX_CHECKPOINTS + p.ckpt_index] = conf;
-        if (conf > gamma) {
-          newly[nnew++] = seq;
-          p.exit_layer[seq] = p.ckpt_layer;
-        } else {
-          p.lists->full[1 + nfull++] = seq;
-        }
-      }
-      // exit list = merge of the previous exit list and the newly exited, by id
-      const int nold = min(le[0], EE_MAX_BATCH);
-      int a = 0, b = 0;
-      while (a < nold || b < nnew) {
-        const bool take_old = b >= nnew || (a < nold && le[1 + a] < newly[b]);
-        p.lists->exitl[1 + nexit++] = take_old ? le[1 + a++] : newly[b++];
-      }
-      p.lists->full[0] = nfull;
-      p.lists->exitl[0] = nexit;
+      checkpoint_decide(p.gamma[p.ckpt_index], p.ckpt_index, p.ckpt_layer, res, 2, lf, le, nrows, p.conf_out,
+                        p.exit_layer, p.lists);
     }
     __threadfence();
     *p.head_counter = 0;

@@ -106,6 +106,7 @@ struct LinearParams {
   int32_t h_stride;
   float* hdbg;               // [seq][h_stride] copy when *dbg_flag != 0
   const int32_t* dbg_flag;
+  float* hsave;              // non-null: [seq][h_stride] copy of the new h (the next layer's input state)
   // EPI_SWIGLU / EPI_X (fp16, pair order)
   uint16_t* xh_out;
   int32_t xo_stride;
@@ -216,8 +217,28 @@ struct BeginParams {
   int32_t n_layers;
   int32_t n_ckpt;
   int32_t* dbg_flag;
+  float* hsave;              // non-null: also store the embedding there (input state of layer 0)
 };
 cudaError_t launch_step_begin(const BeginParams& p, int batch_slots, cudaStream_t st);
+
+// State-transition-similarity exit decision at a checkpoint layer: for each
+// sequence of the full list, cos(h_in, h) of the layer's input and output
+// states; exit when it is above the threshold (strict); the lists are rebuilt
+// as after an exit head.  One CTA per list entry, the last CTA decides.
+struct StsParams {
+  StepLists* lists;
+  const float* h;            // residual stream after the checkpoint layer [seq][h_stride]
+  const float* h_in;         // its input state [seq][h_stride]
+  int32_t d, h_stride;
+  const float* gamma;        // thresholds [n_checkpoints]
+  int32_t ckpt_index, ckpt_layer;
+  float* conf_out;           // StepOut.conf ([seq][EE_MAX_CHECKPOINTS])
+  int32_t* exit_layer;       // StepOut.exit_layer
+  float* score;              // scratch [EE_MAX_BATCH]
+  int32_t* counter;          // zero between launches
+  int32_t batch_min;         // nonzero: the list's minimum score decides for all of it
+};
+cudaError_t launch_sts(const StsParams& p, int batch_slots, bool pdl, cudaStream_t st);
 
 cudaError_t launch_quantize_int4(const uint16_t* w, int rows, int cols, uint8_t* packed,
                                  uint16_t* scales, int sstride, cudaStream_t st);

@@ -149,6 +149,14 @@ struct ee_ctx {
   bool shared_loaded = false;
   std::vector<float> gamma;
   int exit_enabled = 1, use_graph = 1, debug = 0;
+  int criterion = EE_EXIT_MAXPROB;
+  // input states of the checkpoint layers (similarity criterion): checkpoint c
+  // uses buffer c % 2, so that the save for checkpoint c + 1 (by the down
+  // projection of checkpoint layer c when the two are adjacent) does not
+  // overwrite it before its decision
+  float* hin = nullptr;
+  float* sts_score = nullptr;
+  int32_t* sts_cnt = nullptr;
   bool cuda_broken = false;
   std::map<std::pair<int, int>, cudaGraphExec_t> graphs;
   // profiling: events around each launch of a step, and the GEMV launches'
@@ -258,6 +266,8 @@ size_t carve(ee_ctx* c, const ee_config& cfg, uint8_t* base) {
       attention_part_floats(m.maxb, m.hq, m.hkv, m.hd, attention_nsplit(m.maxs, m.hd)));
   float* hpart = cv.take<float>((size_t)kHeadGridMax * EE_MAX_BATCH * 4);
   float* hdbg = cv.take<float>((size_t)m.L * EE_MAX_BATCH * m.d);
+  float* hin = cv.take<float>((size_t)2 * EE_MAX_BATCH * m.d);
+  float* stss = cv.take<float>(EE_MAX_BATCH);
   const bool tc = m.maxb >= kTcMinBatch;
   float* tcpart = tc ? cv.take<float>(gemm_tc_part_floats(kTcMaxUnits)) : nullptr;
   StepDesc* desc = cv.take<StepDesc>(1);
@@ -269,6 +279,7 @@ size_t carve(ee_ctx* c, const ee_config& cfg, uint8_t* base) {
   int32_t* acnt = cv.take<int32_t>((size_t)EE_MAX_BATCH * m.hkv);
   int32_t* hcnt = cv.take<int32_t>(64);
   int32_t* dflag = cv.take<int32_t>(1);
+  int32_t* stsc = cv.take<int32_t>(1);
   int32_t* tccnt = tc ? cv.take<int32_t>(kTcMaxTiles) : nullptr;
   const size_t ze = align_up(cv.off, kAlign);
   const size_t stg = 2 * (size_t)std::max({(size_t)m.F * m.d, (size_t)m.dq * m.d, (size_t)m.d * m.d,
@@ -294,6 +305,9 @@ size_t carve(ee_ctx* c, const ee_config& cfg, uint8_t* base) {
     c->attn_part = apart;
     c->head_part = hpart;
     c->hdbg = hdbg;
+    c->hin = hin;
+    c->sts_score = stss;
+    c->sts_cnt = stsc;
     c->desc_dev = desc;
     c->out_dev = out;
     c->gamma_dev = gam;
@@ -401,6 +415,15 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
   bp.n_layers = m.L;
   bp.n_ckpt = m.nck;
   bp.dbg_flag = c->dbg_flag;
+  // similarity criterion: each checkpoint layer's input state is kept (for
+  // layer 0 by the step start, otherwise by the previous layer's down projection)
+  const bool sts = heads && (c->criterion == EE_EXIT_STS || c->criterion == EE_EXIT_STS_BATCH);
+  auto ckpt_index = [&](int j) {
+    const auto it = std::find(c->ckpts.begin(), c->ckpts.end(), j);
+    return it == c->ckpts.end() ? -1 : (int)(it - c->ckpts.begin());
+  };
+  auto hin_of = [&](int ci) { return c->hin + (size_t)(ci % 2) * EE_MAX_BATCH * m.d; };
+  bp.hsave = sts && ckpt_index(0) >= 0 ? hin_of(0) : nullptr;
   EE_LAUNCH(log, EE_K_BEGIN, -1, launch_step_begin(bp, B, st));
 
   int32_t* err = &c->out_dev->err;
@@ -571,6 +594,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     pd.x_stride = m.F;
     pd.epi = EPI_RESID;
     pd.hdbg = c->hdbg + (size_t)j * EE_MAX_BATCH * m.d;
+    pd.hsave = sts && ckpt_index(j + 1) >= 0 ? hin_of(ckpt_index(j + 1)) : nullptr;
     pd.max_rows = B;
 
     EE_PROJECT(EE_K_QKV, j, pq, c->tc ? &c->tm_layer[4 * j + 0] : nullptr, linear_grid(pq.N, c->num_sms));
@@ -587,7 +611,25 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     LinearParams p;
 
     const auto ck = std::find(c->ckpts.begin(), c->ckpts.end(), j);
-    if (heads && ck != c->ckpts.end()) {
+    if (sts && ck != c->ckpts.end()) {
+      // cos(layer input, layer output) against the threshold, lists compacted
+      StsParams sp = {};
+      sp.lists = c->lists;
+      sp.h = c->h;
+      sp.h_in = hin_of((int)(ck - c->ckpts.begin()));
+      sp.d = m.d;
+      sp.h_stride = m.d;
+      sp.gamma = c->gamma_dev;
+      sp.ckpt_index = (int)(ck - c->ckpts.begin());
+      sp.ckpt_layer = j;
+      sp.conf_out = c->out_dev->conf;
+      sp.exit_layer = c->out_dev->exit_layer;
+      sp.score = c->sts_score;
+      sp.counter = c->sts_cnt;
+      sp.batch_min = c->criterion == EE_EXIT_STS_BATCH;
+      EE_LAUNCH(log, EE_K_EXIT_STS, j, launch_sts(sp, B, c->pdl, st));
+      lists_just_written = true;
+    } else if (heads && ck != c->ckpts.end()) {
       const int ci = (int)(ck - c->ckpts.begin());
       // u = RMSNorm_final(h) T_c for the sequences still on the backbone
       if (!fuse_norm) {
@@ -690,7 +732,7 @@ ee_status run_step_profiled(ee_ctx* c, int B, bool heads) {
 ee_status run_step_timed(ee_ctx* c, int B, bool heads) {
   EE_CUDA(c, cudaEventRecord(c->step_ev[0], c->st));
   if (c->use_graph) {
-    const auto key = std::make_pair(B, heads ? 1 : 0);
+    const auto key = std::make_pair(B, heads ? 1 + c->criterion : 0);
     auto it = c->graphs.find(key);
     if (it == c->graphs.end()) {
       cudaGraph_t g = nullptr;
@@ -1038,6 +1080,14 @@ ee_status ee_set_exit_enabled(ee_ctx* c, int32_t enabled) {
   return EE_OK;
 }
 
+ee_status ee_set_exit_criterion(ee_ctx* c, int32_t criterion) {
+  if (!c) return EE_ERR_INVALID_ARG;
+  if (criterion != EE_EXIT_MAXPROB && criterion != EE_EXIT_STS && criterion != EE_EXIT_STS_BATCH)
+    return fail(c, EE_ERR_INVALID_ARG, "unknown exit criterion %d", criterion);
+  c->criterion = criterion;
+  return EE_OK;
+}
+
 ee_status ee_set_use_graph(ee_ctx* c, int32_t use_graph) {
   if (!c) return EE_ERR_INVALID_ARG;
   c->use_graph = use_graph ? 1 : 0;
@@ -1081,8 +1131,10 @@ ee_status ee_step_io(const ee_ctx* c, int32_t batch, int32_t heads, size_t* h2d,
     const bool tc = c->tc && batch >= kTcMinBatch;
     const int exit_layers = with_heads ? c->m.L - 1 - c->ckpts[0] : 0;
     const int per_layer = 5 + 2 * norms;
+    // the similarity criterion replaces each head's launches by one decision launch
+    const int per_ckpt = c->criterion == EE_EXIT_MAXPROB ? 2 + norms : 1;
     *launches = 1 + per_layer * c->m.L + (tc ? 4 * exit_layers : 0) +
-                (with_heads ? (2 + norms) * c->m.nck : 0) + 1 + norms;
+                (with_heads ? per_ckpt * c->m.nck : 0) + 1 + norms;
   }
   return EE_OK;
 }

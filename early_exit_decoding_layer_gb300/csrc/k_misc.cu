@@ -4,6 +4,7 @@
 #include <math.h>
 
 #include "ee_common.cuh"
+#include "ee_head.cuh"
 #include "ee_kernels.cuh"
 
 namespace ee {
@@ -101,6 +102,79 @@ __global__ void __launch_bounds__(256) k_step_begin(const BeginParams p) {
   for (int i = tid * 2; i < p.d; i += 512) {
     const uint32_t w = *reinterpret_cast<const uint32_t*>(e + i);
     *reinterpret_cast<float2*>(h + i) = make_float2(bf16_lo(w), bf16_hi(w));
+    if (p.hsave) *reinterpret_cast<float2*>(p.hsave + (size_t)seq * p.h_stride + i) = make_float2(bf16_lo(w), bf16_hi(w));
+  }
+}
+
+// ------------------------------------------------------------------ similarity exit
+// CTA z scores entry z of the full list: cos(h_in, h) = (h_in . h) /
+// (max(|h_in|, 1e-12) max(|h|, 1e-12)) in fp32, summed in a fixed order.
+// The last CTA to finish (a counter, no spin) takes the decision and
+// rebuilds the lists.
+__global__ void __launch_bounds__(256) k_sts(const StsParams p) {
+  __shared__ float red[3][8];
+  __shared__ int32_t lf[kListLen], le[kListLen];
+  __shared__ int s_last;
+  const int z = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  grid_dep_wait();
+  grid_dep_launch();
+  const int nf = min(ld_volatile_i32(p.lists->full), EE_MAX_BATCH);
+  if (z < nf) {
+    const int seq = ld_volatile_i32(p.lists->full + 1 + z);
+    const float4* a = reinterpret_cast<const float4*>(p.h_in + (size_t)seq * p.h_stride);
+    const float4* b = reinterpret_cast<const float4*>(p.h + (size_t)seq * p.h_stride);
+    float dot = 0.0f, na = 0.0f, nb = 0.0f;
+    for (int i = tid; i < p.d / 4; i += 256) {
+      const float4 x = a[i], y = b[i];
+      dot = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, dot))));
+      na = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, na))));
+      nb = fmaf(y.x, y.x, fmaf(y.y, y.y, fmaf(y.z, y.z, fmaf(y.w, y.w, nb))));
+    }
+    dot = warp_sum(dot);
+    na = warp_sum(na);
+    nb = warp_sum(nb);
+    if (lane == 0) {
+      red[0][warp] = dot;
+      red[1][warp] = na;
+      red[2][warp] = nb;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      float sd = 0.0f, sa = 0.0f, sb = 0.0f;
+      for (int w = 0; w < 8; ++w) {
+        sd += red[0][w];
+        sa += red[1][w];
+        sb += red[2][w];
+      }
+      p.score[z] = sd / (fmaxf(sqrtf(sa), 1e-12f) * fmaxf(sqrtf(sb), 1e-12f));
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    s_last = atomicAdd(p.counter, 1) == (int)gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (tid < kListLen) {
+    lf[tid] = ld_volatile_i32(p.lists->full + tid);
+    le[tid] = ld_volatile_i32(p.lists->exitl + tid);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float sc[EE_MAX_BATCH];
+    float low = INFINITY;
+    for (int m = 0; m < nf; ++m) {
+      sc[m] = __ldcg(p.score + m);
+      low = fminf(low, sc[m]);
+    }
+    if (p.batch_min)  // the batch rule: the sequences on the full path exit together
+      for (int m = 0; m < nf; ++m) sc[m] = low;
+    checkpoint_decide(p.gamma[p.ckpt_index], p.ckpt_index, p.ckpt_layer, sc, 1, lf, le, nf, p.conf_out,
+                      p.exit_layer, p.lists);
+    __threadfence();
+    *p.counter = 0;
   }
 }
 
@@ -229,6 +303,20 @@ cudaError_t launch_rmsnorm(const NormParams& p, int batch_slots, bool pdl, cudaS
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(batch_slots), dim3(256), st, pdl, attr);
   return cudaLaunchKernelEx(&cfg, k_rmsnorm, p);
+}
+
+cudaError_t launch_sts(const StsParams& p, int batch_slots, bool pdl, cudaStream_t st) {
+  if (p.d % 4 || p.h_stride % 4) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(batch_slots < 1 ? 1 : batch_slots);
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_sts, p);
 }
 
 cudaError_t launch_step_begin(const BeginParams& p, int batch_slots, cudaStream_t st) {

@@ -168,6 +168,23 @@ ee_status ee_set_thresholds(ee_ctx *ctx, const float *gamma);
  * layer runs in bf16 (the same kernels, minus the heads).  Default 1. */
 ee_status ee_set_exit_enabled(ee_ctx *ctx, int32_t enabled);
 
+/* Exit criteria at the checkpoint layers (ee_set_exit_criterion):
+ *  EE_EXIT_MAXPROB (default): conf = max softmax(RMSNorm_f(h_l) T_l E^T)
+ *    (the low-rank exit head and test p > gamma of "大语言模型解码加速：自适应层并行机制解析"
+ *    §2.1-2.2);
+ *  EE_EXIT_STS: the state transition similarity of the checkpoint layer,
+ *    cos(layer input, layer output) with both states scaled to unit L2 norm
+ *    ("River-LLM 深度解析" §5.1-5.2): a sequence's token exits when its score
+ *    is above the layer's threshold tau (each token decides, §6.1).  O(d) per
+ *    token, no vocabulary read (§5.3);
+ *  EE_EXIT_STS_BATCH: the same score with the batch rule of §5.2: the
+ *    sequences still on the full-precision path exit together when the
+ *    minimum of their scores is above tau (and each records that minimum).
+ * Either way the thresholds are those of ee_set_thresholds (strict >) and
+ * ee_debug_conf returns the scores. */
+enum { EE_EXIT_MAXPROB = 0, EE_EXIT_STS = 1, EE_EXIT_STS_BATCH = 2 };
+ee_status ee_set_exit_criterion(ee_ctx *ctx, int32_t criterion);
+
 /* use_graph = 1 (default): a decode step is replayed from a CUDA graph
  * captured on first use for the batch size and exit mode (all per-step
  * state lives on the device).  0: launch kernels one by one. */
@@ -234,7 +251,8 @@ enum {
   EE_K_HEAD_T = 8,     /* checkpoint: u = n T GEMV                      */
   EE_K_HEAD_E = 9,     /* checkpoint: vocabulary head + exit decision   */
   EE_K_FINAL_NORM = 10,
-  EE_K_FINAL_HEAD = 11 /* final LM head, argmax                          */
+  EE_K_FINAL_HEAD = 11, /* final LM head, argmax                         */
+  EE_K_EXIT_STS = 12    /* checkpoint: similarity score + exit decision   */
 };
 typedef struct {
   int32_t kind;     /* EE_K_* */

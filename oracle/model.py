@@ -222,6 +222,18 @@ def max_softmax(z: np.ndarray) -> float:
     return float(1.0 / np.sum(np.exp(z - m)))
 
 
+def state_transition_similarity(h_in: np.ndarray, h_out: np.ndarray, eps: float = 1e-12) -> float:
+    """River-LLM §5.1 (compute_sts): the cosine between a layer's input and
+    output states, each first scaled to unit L2 norm (F.normalize: x divided
+    by max(||x||, eps)), then their dot product.  A high value means the layer
+    barely changed the token's state.  O(d); no vocabulary read (§5.3)."""
+    a = np.asarray(h_in, dtype=np.float64)
+    b = np.asarray(h_out, dtype=np.float64)
+    a = a / max(float(np.linalg.norm(a)), eps)
+    b = b / max(float(np.linalg.norm(b)), eps)
+    return float(np.dot(a, b))
+
+
 def argmax_lowest(z: np.ndarray) -> int:
     """Greedy token: argmax with ties to the lowest index (np.argmax's rule)."""
     return int(np.argmax(z))
@@ -462,11 +474,25 @@ class Oracle:
     paged cache's block table.  A decode step follows page 2 §3.1: embed,
     then per layer run it (bf16 until the sequence exits, the int4 copy
     after), write K/V at the current position, and at checkpoint layers
-    score max softmax(RMSNorm_final(h) T_l E^T) against gamma_l (strict >,
-    page 3 §2.2).  The token is the final head's argmax.
+    score the exit criterion against the layer's threshold (strict >, page 3
+    §2.2).  The token is the final head's argmax.
+
+    Exit criteria (``criterion``):
+    * ``"maxprob"`` -- max softmax(RMSNorm_final(h) T_l E^T) (page 3 §2.1-2.2),
+      per sequence;
+    * ``"sts"`` -- the state transition similarity of the checkpoint layer,
+      cos(layer input, layer output) (River-LLM §5.1), per sequence: each
+      generated token decides its own exit layer (§6.1);
+    * ``"sts_batch"`` -- the same score with the batch rule of River-LLM §5.2
+      (ExitDecision.should_exit): the sequences still on the full-precision
+      path exit together when the minimum of their scores clears tau; the
+      score recorded for each of them is that minimum.
     """
 
-    def __init__(self, cfg: ModelConfig, W: Weights, max_batch: int, max_seq_len: int):
+    CRITERIA = ("maxprob", "sts", "sts_batch")
+
+    def __init__(self, cfg: ModelConfig, W: Weights, max_batch: int, max_seq_len: int,
+                 criterion: str = "maxprob"):
         self.cfg = cfg
         self.W = W
         self.max_batch = max_batch
@@ -474,6 +500,8 @@ class Oracle:
         self.blocks_per_seq = (max_seq_len + cfg.kv_block - 1) // cfg.kv_block
         self.n_blocks = max_batch * self.blocks_per_seq
         self.gamma = np.full(len(cfg.checkpoints), np.inf)
+        assert criterion in self.CRITERIA
+        self.criterion = criterion
         self.reset()
 
     # -- lifecycle ---------------------------------------------------------
@@ -570,22 +598,32 @@ class Oracle:
         # them in turn; every sequence runs the per-token loop of page 2 §3.1
         for j in range(L):
             lws = {}
+            scored = []   # sequences scored at this checkpoint
             for s in range(B):
                 q4 = exited_at[s] is not None
                 if q4 not in lws:
                     lws[q4] = self.W.layer(j, q4)
                 pos = self.seqs[s].pos
+                h_in = h[s]
                 h[s] = layer_decode(cfg, lws[q4], h[s], pos, self.K[s][j], self.V[s][j])
                 hidden[j, s] = h[s]
                 if j in ck and exited_at[s] is None and eval_heads:
                     c = ck.index(j)
-                    z = head_logits(h[s], self.W.g_final, self.W.E, cfg.rms_eps, self.W.T[c])
-                    conf[s, c] = max_softmax(z)
-                    f = None if forced_exit is None else forced_exit[s]
-                    if f is None:
-                        go = conf[s, c] > self.gamma[c]
+                    if self.criterion in ("sts", "sts_batch"):
+                        conf[s, c] = state_transition_similarity(h_in, h[s])
                     else:
-                        go = (f == j)
+                        z = head_logits(h[s], self.W.g_final, self.W.E, cfg.rms_eps, self.W.T[c])
+                        conf[s, c] = max_softmax(z)
+                    scored.append(s)
+            if scored:
+                c = ck.index(j)
+                if self.criterion == "sts_batch":   # the batch's score is its minimum
+                    low = min(conf[s, c] for s in scored)
+                    for s in scored:
+                        conf[s, c] = low
+                for s in scored:
+                    f = None if forced_exit is None else forced_exit[s]
+                    go = conf[s, c] > self.gamma[c] if f is None else (f == j)
                     if go:
                         exited_at[s] = j
                         exit_layers[s] = j
@@ -623,7 +661,7 @@ def calibrate_gammas(orc: Oracle, prompts, steps: int, percentiles: Sequence[flo
 
 
 def build_oracle(workload, cache_bytes: int = 4 << 30, max_batch: Optional[int] = None,
-                 max_seq_len: Optional[int] = None) -> Oracle:
+                 max_seq_len: Optional[int] = None, criterion: str = "maxprob") -> Oracle:
     """Oracle over a workload's seeded synthetic weights (``synth`` module)."""
     import synth
 
@@ -634,4 +672,4 @@ def build_oracle(workload, cache_bytes: int = 4 << 30, max_batch: Optional[int] 
                 synth.final_gain(shape),
                 [synth.exit_transform(shape, seed, c) for c in range(len(workload.checkpoints))],
                 cache_bytes=cache_bytes)
-    return Oracle(cfg, W, max_batch or workload.batch, max_seq_len or workload.max_seq_len())
+    return Oracle(cfg, W, max_batch or workload.batch, max_seq_len or workload.max_seq_len(), criterion)

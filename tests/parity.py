@@ -26,6 +26,7 @@ import synth
 
 HIDDEN_TOL = 1e-2        # per-layer relative L2 of the residual stream
 CONF_REL_TOL = 2e-2      # GPU vs oracle confidence, relative
+STS_ABS_TOL = 5e-3       # GPU vs oracle state transition similarity, absolute (a cosine)
 REL_WINDOW = 1e-2        # decision window, relative to gamma
 ABS_WINDOW = 1e-3        # decision window of the workload definition
 MARGIN_WINDOW = 1e-3     # token window: top-2 logit margin
@@ -51,9 +52,9 @@ def load_engine(w: synth.Workload, max_batch=None, max_seq_len=None, checkpoints
 
 
 def build_oracle(w: synth.Workload, max_batch=None, max_seq_len=None, checkpoints=None,
-                 cache_bytes=4 << 30) -> oracle.Oracle:
+                 cache_bytes=4 << 30, criterion="maxprob") -> oracle.Oracle:
     o = oracle.build_oracle(w, cache_bytes=cache_bytes, max_batch=max_batch or w.batch,
-                            max_seq_len=max_seq_len or w.max_seq_len())
+                            max_seq_len=max_seq_len or w.max_seq_len(), criterion=criterion)
     if checkpoints is not None:
         ck = tuple(checkpoints)
         o.cfg.checkpoints = ck
@@ -84,10 +85,12 @@ class Stats:
 
 def drive(eng: ee.DecodeEngine, orc: oracle.Oracle, prompts, gamma, steps: int,
           check_hidden: bool = True, gamma_per_step=None, exit_enabled: bool = True) -> Stats:
-    """Prefill both sides, then decode `steps` steps, asserting parity."""
+    """Prefill both sides, then decode `steps` steps, asserting parity.  The
+    engine runs the oracle's exit criterion (orc.criterion)."""
     L = orc.cfg.n_layers
     ck = list(orc.cfg.checkpoints)
     st = Stats()
+    eng.set_exit_criterion(orc.criterion)
     eng.set_exit_enabled(exit_enabled)
     eng.set_debug(check_hidden)
     g0 = np.asarray(gamma, dtype=np.float64)
@@ -139,9 +142,14 @@ def drive(eng: ee.DecodeEngine, orc: oracle.Oracle, prompts, gamma, steps: int,
         both = ~np.isnan(r.conf) & ~np.isnan(gconf)
         assert np.array_equal(np.isnan(r.conf), np.isnan(gconf)), (k, r.conf, gconf)
         if both.any():
-            rel = np.abs(gconf[both] - r.conf[both]) / r.conf[both]
+            if orc.criterion == "sts":   # a cosine: compared absolutely
+                rel = np.abs(gconf[both] - r.conf[both])
+                tol = STS_ABS_TOL
+            else:
+                rel = np.abs(gconf[both] - r.conf[both]) / r.conf[both]
+                tol = CONF_REL_TOL
             st.max_conf_rel = max(st.max_conf_rel, float(rel.max()))
-            assert rel.max() < CONF_REL_TOL, (k, gconf, r.conf, herr.max(axis=1))
+            assert rel.max() < tol, (k, gconf, r.conf, herr.max(axis=1))
             gmat = np.broadcast_to(g, r.conf.shape)
             dist = np.abs(r.conf[both] - gmat[both])
             st.decisions += int(both.sum())

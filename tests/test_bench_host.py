@@ -112,3 +112,22 @@ def test_source_digest_ignores_comments_only():
     c = "int f(int x) { return x + 2; }\n"
     assert bench._code_only(a) == bench._code_only(b)
     assert bench._code_only(a) != bench._code_only(c)
+
+
+def test_similarity_criterion_reads_no_head_bytes():
+    sh = synth.SHAPES["llama3.1-8b"]
+    ck = synth.WORKLOADS["llama3.1-8b-b1"].checkpoints
+    ctx = [2100]
+    # a sequence still on the backbone at every checkpoint: the max-prob heads read T and E each time
+    full = bench.step_bytes(sh, ck, [31], ctx, True)
+    sts = bench.step_bytes(sh, ck, [31], ctx, True, "sts")
+    nox = bench.step_bytes(sh, ck, [31], ctx, False)
+    assert sts == nox
+    assert full - sts == len(ck) * (sh.d_model * sh.d_model * 2 + sh.vocab * sh.d_model * 2)
+
+
+def test_calibration_histogram_first_checkpoint_above_threshold():
+    conf = [[0.5, 0.9], [0.1, 0.2], [0.6, 0.1], [0.3, 0.8]]
+    assert bench.calibration_hist(conf, [0.4, 0.7], (4, 8), 32) == {4: 2, 8: 1, 31: 1}
+    # strict: equal to the threshold stays
+    assert bench.calibration_hist([[0.4, 0.7]], [0.4, 0.7], (4, 8), 32) == {31: 1}

@@ -479,3 +479,119 @@ def test_tiny_trace_reproduces(tiny):
         assert r.next_tokens.tolist() == ref["trace"]["tokens"][k]
         assert r.exit_layers.tolist() == ref["trace"]["exit_layers"][k]
         tok = r.next_tokens
+
+
+# ---------------------------------------------------- state transition similarity
+
+def test_sts_hand_worked_examples():
+    """River-LLM §5.1: cosine of the unit-normalised input and output states."""
+    g = read_golden("sts_example.txt")
+    for k in "abcde":
+        got = oracle.state_transition_similarity(np.array(g[k + "_in"], float), np.array(g[k + "_out"], float))
+        assert got == pytest.approx(g[k + "_sts"][0], abs=1e-15), k
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal(64)
+    assert oracle.state_transition_similarity(x, 3.5 * x) == pytest.approx(1.0, abs=1e-14)   # scale invariant
+    y = rng.standard_normal(64)
+    assert oracle.state_transition_similarity(x, y) == pytest.approx(
+        oracle.state_transition_similarity(y, x), abs=1e-15)                                 # symmetric
+    assert -1.0 - 1e-12 <= oracle.state_transition_similarity(x, y) <= 1.0 + 1e-12
+
+
+def _tiny_sts_oracle(gamma=None, T_nan=False):
+    w = synth.WORKLOADS["tiny-b1"]
+    o = oracle.build_oracle(w, criterion="sts")
+    if T_nan:
+        o.W.T = [np.full_like(t, np.nan) for t in o.W.T]
+    o.set_thresholds(np.full(len(w.checkpoints), np.inf) if gamma is None else gamma)
+    lens, prompts = synth.workload_inputs(w)
+    return w, o, [list(prompts[0][:20])]
+
+
+def test_sts_scores_the_checkpoint_layers_input_and_output():
+    """At checkpoint j the score compares the state entering layer j (the
+    output of layer j-1) with the state leaving it, read back from the
+    per-layer residual streams the step returns."""
+    w, o, pr = _tiny_sts_oracle()
+    tok = o.prefill(pr)
+    r = o.decode_step(tok)
+    for c, j in enumerate(w.checkpoints):
+        assert j >= 1
+        want = oracle.state_transition_similarity(r.hidden[j - 1, 0], r.hidden[j, 0])
+        assert r.conf[0, c] == pytest.approx(want, abs=1e-15)
+        # a different pair of states (one layer later) gives a different score
+        other = oracle.state_transition_similarity(r.hidden[j, 0], r.hidden[j + 1, 0])
+        assert abs(other - r.conf[0, c]) > 1e-6
+
+
+def test_sts_reads_no_vocabulary_or_exit_transform():
+    """§5.3: the decision is O(d); with the exit transforms replaced by NaN
+    the similarity-criterion decode is unchanged (they are never read)."""
+    w, o1, pr = _tiny_sts_oracle(gamma=[0.5, 0.5])
+    _, o2, _ = _tiny_sts_oracle(gamma=[0.5, 0.5], T_nan=True)
+    t1, t2 = o1.prefill(pr), o2.prefill(pr)
+    for _ in range(3):
+        r1, r2 = o1.decode_step(t1), o2.decode_step(t2)
+        assert np.array_equal(r1.next_tokens, r2.next_tokens)
+        assert np.array_equal(r1.exit_layers, r2.exit_layers)
+        assert np.allclose(r1.conf, r2.conf, equal_nan=True)
+        t1, t2 = r1.next_tokens, r2.next_tokens
+
+
+def test_sts_threshold_is_strict():
+    """A token exits at the first checkpoint whose score is strictly above tau."""
+    w, o, pr = _tiny_sts_oracle()
+    tok = o.prefill(pr)
+    snap = o.snapshot()
+    r = o.decode_step(tok)
+    s0 = r.conf[0, 0]
+    o.restore(snap)
+    o.set_thresholds([s0, -np.inf])              # equal to the score: no exit at layer 1
+    r = o.decode_step(tok)
+    assert r.exit_layers[0] == w.checkpoints[1]
+    o.restore(snap)
+    o.set_thresholds([np.nextafter(s0, -np.inf), np.inf])   # just below: exits at layer 1
+    r = o.decode_step(tok)
+    assert r.exit_layers[0] == w.checkpoints[0]
+
+
+def test_sts_batch_rule_exits_together_on_the_minimum():
+    """River-LLM §5.2: with the batch rule every sequence still on the
+    full-precision path exits when the minimum of their scores clears tau,
+    and none does otherwise; with one sequence it is the per-token rule."""
+    w = synth.WORKLOADS["tiny-b1"]
+    lens = [7, 12, 19]
+    pr = synth.prompts(w.shape, 5, lens)
+    per = oracle.build_oracle(w, max_batch=3, criterion="sts")
+    bat = oracle.build_oracle(w, max_batch=3, criterion="sts_batch")
+    for o in (per, bat):
+        o.set_thresholds([np.inf, np.inf])
+    tp, tb = per.prefill(pr), bat.prefill(pr)
+    sp, sb = per.snapshot(), bat.snapshot()
+    rp = per.decode_step(tp)
+    s0 = rp.conf[:, 0]                                  # per-sequence scores at layer 1
+    lo, hi = float(s0.min()), float(s0.max())
+    assert hi > lo
+    # tau between the minimum and the maximum: some sequences exit per token, none in the batch rule
+    tau = 0.5 * (lo + hi)
+    per.restore(sp)
+    per.set_thresholds([tau, np.inf])
+    assert 0 < int((per.decode_step(tp).exit_layers == 1).sum()) < 3
+    bat.restore(sb)
+    bat.set_thresholds([tau, np.inf])
+    rb = bat.decode_step(tb)
+    assert np.all(rb.exit_layers == w.shape.n_layers - 1)
+    assert np.allclose(rb.conf[:, 0], lo, rtol=0, atol=1e-15)   # every sequence records the minimum
+    # tau just below the minimum: the whole batch exits at layer 1
+    bat.restore(sb)
+    bat.set_thresholds([np.nextafter(lo, -np.inf), np.inf])
+    assert np.all(bat.decode_step(tb).exit_layers == 1)
+    # batch of one: identical to the per-token rule
+    one_p = oracle.build_oracle(w, max_batch=1, criterion="sts")
+    one_b = oracle.build_oracle(w, max_batch=1, criterion="sts_batch")
+    for o in (one_p, one_b):
+        o.set_thresholds([tau, tau])
+        t = o.prefill(pr[:1])
+        o._r = o.decode_step(t)
+    assert np.array_equal(one_p._r.exit_layers, one_b._r.exit_layers)
+    assert np.allclose(one_p._r.conf, one_b._r.conf, equal_nan=True)
