@@ -40,6 +40,7 @@ import synth  # noqa: E402
 
 DEFAULT_WORKLOAD = "llama3.1-8b-b1"
 B32_WORKLOAD = "llama3.1-8b-b32"
+SMALL_WORKLOAD = "llama3.2-1b-b1"
 METRIC = "decoded tokens/s"
 L2_BYTES = 129 * 1024 * 1024
 
@@ -134,25 +135,37 @@ def launch_bytes(sh, ckpts, kind, layer, exits, ctxs):
     return 0
 
 
-def step_bytes(sh, ckpts, exits, ctxs, heads, criterion="maxprob"):
+def step_bytes(sh, ckpts, exits, ctxs, heads, criterion="maxprob", token_source="final"):
     """Bytes a step must read (the workload's roofline rule): for each layer the
     bf16 weights if any sequence runs it in bf16 and the int4 weights plus
     scales if any runs it on the exit copy; T and E for every head evaluated
     (the similarity criterion reads two d-vectors per sequence instead, which
     is negligible and not counted); E for the final head; every sequence's
     K/V history of every layer."""
+    # With exit-head tokens an exited sequence's last layer reads only its QKV
+    # rows, and the final head serves the sequences that never exited.
+    head_tok = heads and criterion == "maxprob" and token_source == "exit_head"
     heads = heads and criterion == "maxprob"
+    L = sh.n_layers
     total = 0
-    for j in range(sh.n_layers):
+    for j in range(L):
         for kind in ("qkv", "o", "gateup", "down"):
-            total += launch_bytes(sh, ckpts, kind, j, exits, ctxs)
-        total += launch_bytes(sh, ckpts, "attn", j, exits, ctxs)
+            if head_tok and j == L - 1 and kind != "qkv":
+                stay = [e for e in exits if e == L - 1]
+                total += launch_bytes(sh, ckpts, kind, j, stay, ctxs) if stay else 0
+            else:
+                total += launch_bytes(sh, ckpts, kind, j, exits, ctxs)
+        if head_tok and j == L - 1:
+            total += launch_bytes(sh, ckpts, "attn", j, exits, [c for c, e in zip(ctxs, exits) if e == L - 1])
+        else:
+            total += launch_bytes(sh, ckpts, "attn", j, exits, ctxs)
     if heads:
         for l in ckpts:
             if any(e >= l for e in exits):
                 total += launch_bytes(sh, ckpts, "head_t", l, exits, ctxs)
                 total += launch_bytes(sh, ckpts, "head_e", l, exits, ctxs)
-    total += launch_bytes(sh, ckpts, "final_head", -1, exits, ctxs)
+    if not head_tok or any(e == L - 1 for e in exits):
+        total += launch_bytes(sh, ckpts, "final_head", -1, exits, ctxs)
     return total
 
 
@@ -478,6 +491,13 @@ def run_workload(ee, w, args, st, rank, world, peak, steps, profile_steps):
                               profile_steps=profile_steps, ncu_region=args.ncu_region)
     base = timed_run(eng, w, prompts, steps, args.warmup, False, world,
                      profile_steps=profile_steps, ncu_region=args.ncu_region)
+    # exit-head tokens (the exit head's argmax is emitted; the same thresholds)
+    head_tok_run = None
+    if args.exit_head_token:
+        eng.set_token_source("exit_head")
+        eng.set_thresholds(gammas[w.gamma_percentiles[0]])
+        head_tok_run = timed_run(eng, w, prompts, steps, args.warmup, True, world)
+        eng.set_token_source("final")
     # the state-transition-similarity criterion, thresholds at the library's
     # percentiles of the no-exit similarity scores
     # (per sequence; at batch > 1 also the batch-minimum rule, whose
@@ -495,7 +515,7 @@ def run_workload(ee, w, args, st, rank, world, peak, steps, profile_steps):
                 sts_runs[key] = timed_run(eng, w, prompts, steps, args.warmup, True, world)
         eng.set_exit_criterion("maxprob")
 
-    def summarize(r, heads, criterion="maxprob"):
+    def summarize(r, heads, criterion="maxprob", token_source="final"):
         dev_s = sum(r["dev_ms"]) / 1e3
         max_dev = reduce_max(dev_s, world, True)
         max_wall = reduce_max(r["wall_s"], world, True)
@@ -503,7 +523,7 @@ def run_workload(ee, w, args, st, rank, world, peak, steps, profile_steps):
         bytes_total = 0
         for k, ex in enumerate(r["exits"]):
             ctx = r["ctx0"] + k + 1
-            bytes_total += step_bytes(sh, w.checkpoints, ex, ctx, heads, criterion)
+            bytes_total += step_bytes(sh, w.checkpoints, ex, ctx, heads, criterion, token_source)
         hist = {}
         for ex in r["exits"]:
             for e in ex:
@@ -523,10 +543,11 @@ def run_workload(ee, w, args, st, rank, world, peak, steps, profile_steps):
               for pct in w.gamma_percentiles[1:]}
     sts = {key: dict(summarize(sts_runs[key], True, "sts"), tau=[float(x) for x in taus[key]])
            for key in sts_runs}
+    head_tok = dict(summarize(head_tok_run, True, "maxprob", "exit_head")) if head_tok_run else None
     # exit depths the library's own thresholds give on its calibration samples
     lib_hist = calibration_hist(calib, lib_gammas[w.gamma_percentiles[0]], w.checkpoints, sh.n_layers)
     return {"eng": eng, "gammas": gammas, "main": main, "nox": nox, "runs": runs, "kr": kr, "kr_base": kr_base,
-            "t_load": t_load, "others": others, "sts": sts, "gamma_source": gamma_source,
+            "t_load": t_load, "others": others, "sts": sts, "head_tok": head_tok, "gamma_source": gamma_source,
             "lib_gammas": lib_gammas, "lib_hist": lib_hist}
 
 
@@ -591,6 +612,12 @@ def run_ours(args):
         line["config"]["gamma_source"] = res["gamma_source"]
         line["gamma_library"] = {"gamma": [float(x) for x in res["lib_gammas"][w.gamma_percentiles[0]]],
                                  "exit_hist_on_calibration_samples": res["lib_hist"]}
+        if res["head_tok"]:
+            v = res["head_tok"]
+            line["exit_head_token"] = {"value": v["value"], "ms_per_step": v["ms_per_step"], "e2e": v["e2e"],
+                                       "speedup_vs_no_exit": v["value"] / nox["value"],
+                                       "step_roofline_frac_measured": v["step_roofline_frac_measured"],
+                                       "bytes_per_step": v["bytes_per_step"], "exit_hist": v["exit_hist"]}
         if res["sts"]:
             line["sts"] = {k: {"value": v["value"], "ms_per_step": v["ms_per_step"], "e2e": v["e2e"],
                                "speedup_vs_no_exit": v["value"] / nox["value"],
@@ -649,6 +676,31 @@ def run_ours(args):
                         "exit_hist": v["exit_hist"], "tau": v["tau"]} for k, v in r32["sts"].items()},
         }
         r32["eng"].close()
+    if rank == 0 and world == 1 and args.also_1b and w.name == DEFAULT_WORKLOAD:
+        # the Llama-3.2-1B shape at batch 1 (512-token prompt), same runs
+        import gc
+        gc.collect()
+        torch.cuda.empty_cache()
+        w1 = synth.WORKLOADS[SMALL_WORKLOAD]
+        r1 = run_workload(ee, w1, args, st, rank, world, peak, args.steps, 1)
+        m1, n1 = r1["main"], r1["nox"]
+        line["b1_" + w1.shape.name] = {
+            "workload": w1.name, "steps": args.steps, "value": m1["value"], "unit": "tokens/s",
+            "ms_per_step": m1["ms_per_step"], "e2e": m1["e2e"],
+            "step_roofline_frac_measured": m1["step_roofline_frac_measured"],
+            "bytes_per_step": m1["bytes_per_step"], "exit_hist": m1["exit_hist"],
+            "gamma_source": r1["gamma_source"], "clocks": m1["clocks"],
+            "no_exit": {"value": n1["value"], "ms_per_step": n1["ms_per_step"],
+                        "step_roofline_frac_measured": n1["step_roofline_frac_measured"]},
+            "speedup_vs_no_exit": m1["value"] / n1["value"],
+            "exit_head_token": ({"value": r1["head_tok"]["value"],
+                                 "speedup_vs_no_exit": r1["head_tok"]["value"] / n1["value"]}
+                                if r1["head_tok"] else None),
+            "sts": {k: {"value": v["value"], "speedup_vs_no_exit": v["value"] / n1["value"],
+                        "exit_hist": v["exit_hist"]} for k, v in r1["sts"].items()},
+            "kernels": r1["kr"],
+        }
+        r1["eng"].close()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -795,6 +847,10 @@ def main():
                     help="timed steps of the batch-32 run added to the default workload's line (0: skip)")
     ap.add_argument("--ncu-region", action="store_true",
                     help="bracket the timed steps with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
+    ap.add_argument("--no-1b", dest="also_1b", action="store_false",
+                    help="skip the Llama-3.2-1B batch-1 runs added to the default workload's line")
+    ap.add_argument("--no-exit-head-token", dest="exit_head_token", action="store_false",
+                    help="skip the run that emits the exit head's token")
     ap.add_argument("--no-sts", dest="sts", action="store_false",
                     help="skip the runs with the state-transition-similarity exit criterion")
     ap.add_argument("--ops", action="store_true",

@@ -34,7 +34,7 @@ EXPORTS = (
     "ee_debug_int4", "ee_op_quantize_int4", "ee_op_linear_bf16", "ee_op_linear_int4",
     "ee_attention_scratch_bytes", "ee_op_attention", "ee_head_scratch_bytes",
     "ee_op_vocab_head", "ee_step_io", "ee_set_profile", "ee_profile_read", "ee_last_step_ms",
-    "ee_op_attention_noalloc", "ee_set_exit_criterion",
+    "ee_op_attention_noalloc", "ee_set_exit_criterion", "ee_set_token_source",
 )
 
 KINDS = ("begin", "norm", "qkv", "attn", "o", "gateup", "down", "head_norm", "head_t", "head_e",
@@ -100,6 +100,7 @@ def load_library(path: str = LIB_PATH):
         "ee_set_thresholds": (i32, [c_vp, P(c_f32)]),
         "ee_set_exit_enabled": (i32, [c_vp, i32]),
         "ee_set_exit_criterion": (i32, [c_vp, i32]),
+        "ee_set_token_source": (i32, [c_vp, i32]),
         "ee_set_use_graph": (i32, [c_vp, i32]),
         "ee_prefill": (i32, [c_vp, i32, P(i32), P(i32), P(i32)]),
         "ee_decode_step": (i32, [c_vp, P(i32), P(i32), P(i32)]),
@@ -262,6 +263,12 @@ class DecodeEngine:
         """'maxprob' (exit-head confidence, default), 'sts' (state transition
         similarity, per sequence) or 'sts_batch' (its batch-minimum rule)."""
         self._check(self.lib.ee_set_exit_criterion(self.ctx, self.CRITERIA[criterion]))
+
+    TOKEN_SOURCES = {"final": 0, "exit_head": 1}
+
+    def set_token_source(self, source: str):
+        """'final' (final head after the int4 layers, default) or 'exit_head'."""
+        self._check(self.lib.ee_set_token_source(self.ctx, self.TOKEN_SOURCES[source]))
 
     def set_use_graph(self, use_graph: bool):
         self._check(self.lib.ee_set_use_graph(self.ctx, 1 if use_graph else 0))

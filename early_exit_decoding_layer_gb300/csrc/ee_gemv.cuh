@@ -527,6 +527,10 @@ EE_DEV void linear_body(const LinearParams& p, int ncta, uint8_t* smem, LinState
       run_phase<XS, MMAX, 1>(p, s.pl, le, s.ne, s.nf, xs, rowsum, hst, s.nrows, tid, warp, lane, s.a, s.lc,
                              s.pre_phase == 1);
   }
+  // A head over empty lists (every sequence left at an earlier checkpoint)
+  // has nothing to merge or decide: the lists stay as they are.  Every CTA
+  // read the same lists, so all of them return here and the counter stays 0.
+  if (p.epi == EPI_HEAD && s.nf == 0 && s.ne == 0) return;
   if (p.epi == EPI_HEAD) {
     // Last CTA to finish merges the per-CTA partials (no spin wait: a counter).
     __syncthreads();

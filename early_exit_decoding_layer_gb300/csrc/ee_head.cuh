@@ -112,6 +112,11 @@ EE_DEV void head_finalize_group(const LinearParams& p, int nparts, const int32_t
     } else if (p.head_mode == HEAD_FINAL) {
       for (int m = 0; m < nrows; ++m) p.argmax_out[lf[1 + m]] = __float_as_int(res[2 * m + 1]);
     } else {  // HEAD_CHECKPOINT: decide, then rebuild the two sub-batch lists
+      if (p.argmax_out) {  // exit-head tokens: an exiting sequence emits this head's argmax
+        const float gamma = p.gamma[p.ckpt_index];
+        for (int m = 0; m < nrows; ++m)
+          if (res[2 * m] > gamma) p.argmax_out[lf[1 + m]] = __float_as_int(res[2 * m + 1]);
+      }
       checkpoint_decide(p.gamma[p.ckpt_index], p.ckpt_index, p.ckpt_layer, res, 2, lf, le, nrows, p.conf_out,
                         p.exit_layer, p.lists);
     }

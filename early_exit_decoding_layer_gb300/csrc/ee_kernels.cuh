@@ -115,7 +115,8 @@ struct LinearParams {
   float* head_part;          // [grid][EE_MAX_BATCH][4] partial (max, sum, argmax, -)
   int32_t* head_counter;     // zero between launches
   float* conf_out;           // HEAD_CONF_ARGMAX: [m]; HEAD_CHECKPOINT: StepOut.conf
-  int32_t* argmax_out;       // HEAD_CONF_ARGMAX: [m]; HEAD_FINAL: StepOut.next_token
+  int32_t* argmax_out;       // HEAD_CONF_ARGMAX: [m]; HEAD_FINAL: StepOut.next_token;
+                             // HEAD_CHECKPOINT (non-null: exit-head tokens): StepOut.next_token of the exiting
   StepLists* lists;          // HEAD_CHECKPOINT: lists to compact
   int32_t* exit_layer;       // HEAD_CHECKPOINT: StepOut.exit_layer
   const float* gamma;        // thresholds [n_checkpoints]

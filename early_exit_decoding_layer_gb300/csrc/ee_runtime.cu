@@ -150,6 +150,7 @@ struct ee_ctx {
   std::vector<float> gamma;
   int exit_enabled = 1, use_graph = 1, debug = 0;
   int criterion = EE_EXIT_MAXPROB;
+  int token_source = EE_TOKEN_FINAL_HEAD;
   // input states of the checkpoint layers (similarity criterion): checkpoint c
   // uses buffer c % 2, so that the save for checkpoint c + 1 (by the down
   // projection of checkpoint layer c when the two are adjacent) does not
@@ -418,6 +419,10 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
   // similarity criterion: each checkpoint layer's input state is kept (for
   // layer 0 by the step start, otherwise by the previous layer's down projection)
   const bool sts = heads && (c->criterion == EE_EXIT_STS || c->criterion == EE_EXIT_STS_BATCH);
+  // exit-head tokens: an exited sequence's token comes from its exit head; in
+  // the last layer only its QKV (the K/V write) runs, and the final head
+  // serves the sequences that never exited
+  const bool head_tok = heads && !sts && c->token_source == EE_TOKEN_EXIT_HEAD;
   auto ckpt_index = [&](int j) {
     const auto it = std::find(c->ckpts.begin(), c->ckpts.end(), j);
     return it == c->ckpts.end() ? -1 : (int)(it - c->ckpts.begin());
@@ -531,7 +536,8 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     pq.max_rows = B;
     // decode attention
     AttnParams ap = {};
-    ap.list = c->lists->part;
+    const bool dead_exit = head_tok && j == m.L - 1;  // exited rows' attention, O and FFN are not needed
+    ap.list = dead_exit ? c->lists->full : c->lists->part;
     ap.n_heads = m.hq;
     ap.n_kv_heads = m.hkv;
     ap.head_dim = m.hd;
@@ -554,8 +560,8 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     po.N = m.d;
     po.K = m.dq;
     po.w = w.wo;
-    po.wq = w.o.q;
-    po.ws = w.o.s;
+    po.wq = dead_exit ? nullptr : w.o.q;
+    po.ws = dead_exit ? nullptr : w.o.s;
     po.sstride = sstride_of(m.dq);
     po.list_full = c->lists->full;
     po.list_exit = c->lists->exitl;
@@ -568,8 +574,8 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     pg.N = 2 * m.F;
     pg.K = m.d;
     pg.w = w.wgu;
-    pg.wq = w.gu.q;
-    pg.ws = w.gu.s;
+    pg.wq = dead_exit ? nullptr : w.gu.q;
+    pg.ws = dead_exit ? nullptr : w.gu.s;
     pg.sstride = sstride_of(m.d);
     pg.list_full = c->lists->full;
     pg.list_exit = c->lists->exitl;
@@ -585,8 +591,8 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     pd.N = m.d;
     pd.K = m.F;
     pd.w = w.wd;
-    pd.wq = w.d.q;
-    pd.ws = w.d.s;
+    pd.wq = dead_exit ? nullptr : w.d.q;
+    pd.ws = dead_exit ? nullptr : w.d.s;
     pd.sstride = sstride_of(m.F);
     pd.list_full = c->lists->full;
     pd.list_exit = c->lists->exitl;
@@ -667,6 +673,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
       p.conf_out = c->out_dev->conf;
       p.lists = c->lists;
       p.exit_layer = c->out_dev->exit_layer;
+      p.argmax_out = head_tok ? c->out_dev->next_token : nullptr;
       p.ckpt_index = ci;
       p.ckpt_layer = j;
       p.max_rows = B;
@@ -676,9 +683,10 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     }
   }
   // final LM head: argmax of RMSNorm_final(h) E^T
+  int32_t* fin_list = head_tok ? c->lists->full : c->lists->fin;
   if (!fuse_norm) {
     NormParams fp = np;
-    fp.list = c->lists->fin;
+    fp.list = fin_list;
     fp.g = c->g_final;
     EE_LAUNCH(log, EE_K_FINAL_NORM, -1, launch_rmsnorm(fp, B, c->pdl, st));
   }
@@ -686,7 +694,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
   p.N = m.V;
   p.K = m.d;
   p.w = c->E;
-  p.list_full = c->lists->fin;
+  p.list_full = fin_list;
   p.list_exit = nullptr;
   p.xh = c->xh;
   p.x_stride = m.d;
@@ -732,7 +740,7 @@ ee_status run_step_profiled(ee_ctx* c, int B, bool heads) {
 ee_status run_step_timed(ee_ctx* c, int B, bool heads) {
   EE_CUDA(c, cudaEventRecord(c->step_ev[0], c->st));
   if (c->use_graph) {
-    const auto key = std::make_pair(B, heads ? 1 + c->criterion : 0);
+    const auto key = std::make_pair(B, heads ? 1 + c->criterion + 3 * c->token_source : 0);
     auto it = c->graphs.find(key);
     if (it == c->graphs.end()) {
       cudaGraph_t g = nullptr;
@@ -1088,6 +1096,14 @@ ee_status ee_set_exit_criterion(ee_ctx* c, int32_t criterion) {
   return EE_OK;
 }
 
+ee_status ee_set_token_source(ee_ctx* c, int32_t source) {
+  if (!c) return EE_ERR_INVALID_ARG;
+  if (source != EE_TOKEN_FINAL_HEAD && source != EE_TOKEN_EXIT_HEAD)
+    return fail(c, EE_ERR_INVALID_ARG, "unknown token source %d", source);
+  c->token_source = source;
+  return EE_OK;
+}
+
 ee_status ee_set_use_graph(ee_ctx* c, int32_t use_graph) {
   if (!c) return EE_ERR_INVALID_ARG;
   c->use_graph = use_graph ? 1 : 0;
@@ -1133,7 +1149,12 @@ ee_status ee_step_io(const ee_ctx* c, int32_t batch, int32_t heads, size_t* h2d,
     const int per_layer = 5 + 2 * norms;
     // the similarity criterion replaces each head's launches by one decision launch
     const int per_ckpt = c->criterion == EE_EXIT_MAXPROB ? 2 + norms : 1;
-    *launches = 1 + per_layer * c->m.L + (tc ? 4 * exit_layers : 0) +
+    // with exit-head tokens the last layer's exit rows run only their QKV
+    const int dead = tc && with_heads && exit_layers > 0 && c->criterion == EE_EXIT_MAXPROB &&
+                             c->token_source == EE_TOKEN_EXIT_HEAD
+                         ? 3
+                         : 0;
+    *launches = 1 + per_layer * c->m.L + (tc ? 4 * exit_layers - dead : 0) +
                 (with_heads ? per_ckpt * c->m.nck : 0) + 1 + norms;
   }
   return EE_OK;
@@ -1237,6 +1258,8 @@ ee_status ee_decode_step(ee_ctx* c, const int32_t* in_tokens, int32_t* next_toke
     if (c->seq_pos[q] >= m.maxs)
       return fail(c, EE_ERR_CAPACITY, "sequence %d reached max_seq_len %d", q, m.maxs);
   }
+  if (c->token_source == EE_TOKEN_EXIT_HEAD && c->criterion != EE_EXIT_MAXPROB && c->exit_enabled)
+    return fail(c, EE_ERR_STATE, "exit-head tokens need the exit-head criterion (EE_EXIT_MAXPROB)");
   ee_status s = check_ready(c);
   if (s != EE_OK) return s;
   DeviceGuard dg(c->dev);

@@ -185,6 +185,19 @@ ee_status ee_set_exit_enabled(ee_ctx *ctx, int32_t enabled);
 enum { EE_EXIT_MAXPROB = 0, EE_EXIT_STS = 1, EE_EXIT_STS_BATCH = 2 };
 ee_status ee_set_exit_criterion(ee_ctx *ctx, int32_t criterion);
 
+/* Token source of an exited sequence (ee_set_token_source):
+ *  EE_TOKEN_FINAL_HEAD (default): the final LM head's argmax after the
+ *    sequence's remaining layers ran on the int4 copies;
+ *  EE_TOKEN_EXIT_HEAD: the argmax of the exit head that let it leave (the
+ *    CALM article §3.1 loop returns the exit head's prediction; page 3 of
+ *    "大语言模型解码加速：自适应层并行机制解析" §2.2).  Its remaining layers still
+ *    run on the int4 copies to write their K/V, except that in the last layer
+ *    only the QKV projection (the K/V write) runs for it; the final head
+ *    serves the sequences that never exited.  Needs EE_EXIT_MAXPROB
+ *    (ee_decode_step returns EE_ERR_STATE otherwise). */
+enum { EE_TOKEN_FINAL_HEAD = 0, EE_TOKEN_EXIT_HEAD = 1 };
+ee_status ee_set_token_source(ee_ctx *ctx, int32_t source);
+
 /* use_graph = 1 (default): a decode step is replayed from a CUDA graph
  * captured on first use for the batch size and exit mode (all per-step
  * state lives on the device).  0: launch kernels one by one. */

@@ -491,8 +491,10 @@ class Oracle:
 
     CRITERIA = ("maxprob", "sts", "sts_batch")
 
+    TOKEN_SOURCES = ("final", "exit_head")
+
     def __init__(self, cfg: ModelConfig, W: Weights, max_batch: int, max_seq_len: int,
-                 criterion: str = "maxprob"):
+                 criterion: str = "maxprob", token_source: str = "final"):
         self.cfg = cfg
         self.W = W
         self.max_batch = max_batch
@@ -501,7 +503,15 @@ class Oracle:
         self.n_blocks = max_batch * self.blocks_per_seq
         self.gamma = np.full(len(cfg.checkpoints), np.inf)
         assert criterion in self.CRITERIA
+        assert token_source in self.TOKEN_SOURCES
+        assert token_source == "final" or criterion == "maxprob", "an exit-head token needs the exit head"
         self.criterion = criterion
+        # "final": the token is the final head's argmax after the int4 layers;
+        # "exit_head": an exited sequence's token is the argmax of the exit
+        # head that let it leave (the CALM article §3.1 loop returns the exit
+        # head's prediction; page 3 §2.2), and its remaining layers only
+        # write their K/V
+        self.token_source = token_source
         self.reset()
 
     # -- lifecycle ---------------------------------------------------------
@@ -594,6 +604,7 @@ class Oracle:
                 self._alloc_block(s)
             h.append(self.W.E[int(in_tokens[s])].copy())
         exited_at: List[Optional[int]] = [None] * B
+        head_z: List[Optional[np.ndarray]] = [None] * B   # logits of each checkpoint head scored
         # the sequences are independent: each layer's weights serve all of
         # them in turn; every sequence runs the per-token loop of page 2 §3.1
         for j in range(L):
@@ -614,6 +625,7 @@ class Oracle:
                     else:
                         z = head_logits(h[s], self.W.g_final, self.W.E, cfg.rms_eps, self.W.T[c])
                         conf[s, c] = max_softmax(z)
+                        head_z[s] = z
                     scored.append(s)
             if scored:
                 c = ck.index(j)
@@ -629,7 +641,10 @@ class Oracle:
                         exit_layers[s] = j
         for s in range(B):
             st = self.seqs[s]
-            z = head_logits(h[s], self.W.g_final, self.W.E, cfg.rms_eps)
+            if self.token_source == "exit_head" and exited_at[s] is not None:
+                z = head_z[s]   # the exit head's logits at the exit layer
+            else:
+                z = head_logits(h[s], self.W.g_final, self.W.E, cfg.rms_eps)
             logits_all[s] = z
             margins[s] = top2_margin(z)
             next_tokens[s] = argmax_lowest(z)
@@ -661,7 +676,8 @@ def calibrate_gammas(orc: Oracle, prompts, steps: int, percentiles: Sequence[flo
 
 
 def build_oracle(workload, cache_bytes: int = 4 << 30, max_batch: Optional[int] = None,
-                 max_seq_len: Optional[int] = None, criterion: str = "maxprob") -> Oracle:
+                 max_seq_len: Optional[int] = None, criterion: str = "maxprob",
+                 token_source: str = "final") -> Oracle:
     """Oracle over a workload's seeded synthetic weights (``synth`` module)."""
     import synth
 
@@ -672,4 +688,5 @@ def build_oracle(workload, cache_bytes: int = 4 << 30, max_batch: Optional[int] 
                 synth.final_gain(shape),
                 [synth.exit_transform(shape, seed, c) for c in range(len(workload.checkpoints))],
                 cache_bytes=cache_bytes)
-    return Oracle(cfg, W, max_batch or workload.batch, max_seq_len or workload.max_seq_len(), criterion)
+    return Oracle(cfg, W, max_batch or workload.batch, max_seq_len or workload.max_seq_len(), criterion,
+                  token_source)

@@ -5,14 +5,20 @@ Decision rule (exit decisions and greedy tokens must be identical except
 where floating point legitimately decides otherwise):
 * an exit decision may differ only where the oracle's confidence lies within
   a window of gamma_l; two windows are counted: the absolute |conf - gamma| <
-  1e-3 of the workload definition and the relative |conf - gamma| < 1e-2 gamma
-  that the tests enforce (with random N(0, 0.02) weights confidences are
-  ~1e-3, so the absolute window would excuse every decision; the relative one
-  follows from the error budget: hidden states agree to ~1e-3 relative, logits
-  to ~1e-3 absolute, so conf to ~1e-3 relative, and 1e-2 leaves a 10x margin);
+  1e-3 of the workload definition and the relative one the tests enforce,
+  |conf - gamma| < w gamma with w = max(1e-2, CONF_PER_HIDDEN e), e the
+  measured relative L2 difference of the residual stream at the head's layer
+  (with random N(0, 0.02) weights confidences are ~1e-3, so the absolute
+  window would excuse every decision; the relative one follows from the
+  error budget below, 1e-2 when the states agree to ~1e-3);
 * a token may differ only where the oracle's top-2 final-logit margin is
-  below 1e-3.
-In both cases the oracle adopts the GPU's decision / token and continues.
+  below 1e-3, or (counted apart, `token_by_hidden`) where the oracle's final
+  head applied to the GPU's own last-layer residual stream picks the GPU's
+  token: the 1e-3 window is far below the logit error that the 1e-2
+  hidden-state tolerance allows (logits have a std of ~1.3 at d=4096, so a
+  0.5% state difference moves them by ~7e-3), and then the difference is
+  explained entirely by a state difference that passed its own check.
+In all cases the oracle adopts the GPU's decision / token and continues.
 """
 from __future__ import annotations
 
@@ -28,6 +34,13 @@ HIDDEN_TOL = 1e-2        # per-layer relative L2 of the residual stream
 CONF_REL_TOL = 2e-2      # GPU vs oracle confidence, relative
 STS_ABS_TOL = 5e-3       # GPU vs oracle state transition similarity, absolute (a cosine)
 REL_WINDOW = 1e-2        # decision window, relative to gamma
+# Where the residual stream entering a head differs by a relative L2 of e, its
+# logits z_v = n . E_v move by ~e |n| |E_v| / sqrt(d) each (std) and by up to
+# ~4.5 of that over a 128k vocabulary; log max-softmax moves by at most twice
+# the largest logit move: ~9-12 e for the N(0, 0.02) models here.  The
+# confidence tolerance and the decision window of a head are therefore at
+# least CONF_PER_HIDDEN times the measured state difference at its layer.
+CONF_PER_HIDDEN = 12.0
 ABS_WINDOW = 1e-3        # decision window of the workload definition
 MARGIN_WINDOW = 1e-3     # token window: top-2 logit margin
 
@@ -52,9 +65,10 @@ def load_engine(w: synth.Workload, max_batch=None, max_seq_len=None, checkpoints
 
 
 def build_oracle(w: synth.Workload, max_batch=None, max_seq_len=None, checkpoints=None,
-                 cache_bytes=4 << 30, criterion="maxprob") -> oracle.Oracle:
+                 cache_bytes=4 << 30, criterion="maxprob", token_source="final") -> oracle.Oracle:
     o = oracle.build_oracle(w, cache_bytes=cache_bytes, max_batch=max_batch or w.batch,
-                            max_seq_len=max_seq_len or w.max_seq_len(), criterion=criterion)
+                            max_seq_len=max_seq_len or w.max_seq_len(), criterion=criterion,
+                            token_source=token_source)
     if checkpoints is not None:
         ck = tuple(checkpoints)
         o.cfg.checkpoints = ck
@@ -77,6 +91,7 @@ class Stats:
     token_mismatch: int = 0
     in_abs_window: int = 0
     in_rel_window: int = 0
+    token_by_hidden: int = 0
     max_hidden_rel: float = 0.0
     max_conf_rel: float = 0.0
     gpu_exits: list = field(default_factory=list)
@@ -91,6 +106,7 @@ def drive(eng: ee.DecodeEngine, orc: oracle.Oracle, prompts, gamma, steps: int,
     ck = list(orc.cfg.checkpoints)
     st = Stats()
     eng.set_exit_criterion(orc.criterion)
+    eng.set_token_source(orc.token_source)
     eng.set_exit_enabled(exit_enabled)
     eng.set_debug(check_hidden)
     g0 = np.asarray(gamma, dtype=np.float64)
@@ -123,7 +139,11 @@ def drive(eng: ee.DecodeEngine, orc: oracle.Oracle, prompts, gamma, steps: int,
                     c = ck.index(min(x for x in (ge[s], r.exit_layers[s]) if x in ck))
                     co = r.conf[s, c]
                     assert not np.isnan(co)
-                    assert abs(co - g[c]) < REL_WINDOW * abs(g[c]), (
+                    win = REL_WINDOW
+                    if orc.criterion == "maxprob" and check_hidden:   # widened by the state difference
+                        gh = eng.debug_hidden(ck[c])[s]
+                        win = max(win, CONF_PER_HIDDEN * rel_l2(gh, r.hidden[ck[c], s]))
+                    assert abs(co - g[c]) < win * abs(g[c]), (
                         "step %d seq %d: exit %d (GPU) vs %d (oracle), conf %.6g gamma %.6g"
                         % (k, s, ge[s], r.exit_layers[s], co, g[c]))
                     st.exit_mismatch += 1
@@ -135,6 +155,8 @@ def drive(eng: ee.DecodeEngine, orc: oracle.Oracle, prompts, gamma, steps: int,
             for j in range(L):
                 gh = eng.debug_hidden(j)
                 for s in range(len(tok)):
+                    if orc.token_source == "exit_head" and j == L - 1 and ge[s] != L - 1:
+                        continue   # an exited sequence's last layer only writes its K/V
                     herr[j, s] = rel_l2(gh[s], r.hidden[j, s])
             st.max_hidden_rel = max(st.max_hidden_rel, float(herr.max()))
             assert herr.max() < HIDDEN_TOL, (k, herr.max(axis=1))
@@ -147,9 +169,10 @@ def drive(eng: ee.DecodeEngine, orc: oracle.Oracle, prompts, gamma, steps: int,
                 tol = STS_ABS_TOL
             else:
                 rel = np.abs(gconf[both] - r.conf[both]) / r.conf[both]
-                tol = CONF_REL_TOL
+                state = herr[[ck[c] for c in range(len(ck))], :].T      # [seq, checkpoint]
+                tol = np.maximum(CONF_REL_TOL, CONF_PER_HIDDEN * state[both])
             st.max_conf_rel = max(st.max_conf_rel, float(rel.max()))
-            assert rel.max() < tol, (k, gconf, r.conf, herr.max(axis=1))
+            assert np.all(rel < tol), (k, gconf, r.conf, herr.max(axis=1))
             gmat = np.broadcast_to(g, r.conf.shape)
             dist = np.abs(r.conf[both] - gmat[both])
             st.decisions += int(both.sum())
@@ -157,7 +180,17 @@ def drive(eng: ee.DecodeEngine, orc: oracle.Oracle, prompts, gamma, steps: int,
             st.in_rel_window += int((dist < REL_WINDOW * np.abs(gmat[both])).sum())
         for s in range(len(tok)):
             if gn[s] != r.next_tokens[s]:
-                assert r.margins[s] < MARGIN_WINDOW, (k, s, gn[s], r.next_tokens[s], r.margins[s])
+                if r.margins[s] >= MARGIN_WINDOW:
+                    assert check_hidden, (k, s, gn[s], r.next_tokens[s], r.margins[s])
+                    if orc.token_source == "exit_head" and ge[s] != L - 1:   # the exit head's state
+                        c = ck.index(int(ge[s]))
+                        hg = eng.debug_hidden(int(ge[s]))[s].astype(np.float64)
+                        zg = oracle.head_logits(hg, orc.W.g_final, orc.W.E, orc.cfg.rms_eps, orc.W.T[c])
+                    else:
+                        hg = eng.debug_hidden(L - 1)[s].astype(np.float64)
+                        zg = oracle.head_logits(hg, orc.W.g_final, orc.W.E, orc.cfg.rms_eps)
+                    assert oracle.argmax_lowest(zg) == gn[s], (k, s, gn[s], r.next_tokens[s], r.margins[s])
+                    st.token_by_hidden += 1
                 st.token_mismatch += 1
         st.gpu_exits.append(ge.copy())
         st.gpu_tokens.append(gn.copy())

@@ -131,3 +131,17 @@ def test_calibration_histogram_first_checkpoint_above_threshold():
     assert bench.calibration_hist(conf, [0.4, 0.7], (4, 8), 32) == {4: 2, 8: 1, 31: 1}
     # strict: equal to the threshold stays
     assert bench.calibration_hist([[0.4, 0.7]], [0.4, 0.7], (4, 8), 32) == {31: 1}
+
+
+def test_exit_head_token_byte_model():
+    sh = synth.SHAPES["llama3.1-8b"]
+    ck = synth.WORKLOADS["llama3.1-8b-b1"].checkpoints
+    ctx = [2100]
+    final = bench.step_bytes(sh, ck, [4], ctx, True)
+    tok = bench.step_bytes(sh, ck, [4], ctx, True, "maxprob", "exit_head")
+    m = bench.mat_list(sh)
+    dead = sum(bench.w_bytes(*m[k], True) for k in ("o", "gateup", "down"))
+    kv = 2100 * 2 * sh.n_kv_heads * sh.head_dim * 2
+    assert final - tok == dead + kv + sh.vocab * sh.d_model * 2
+    # a sequence that never exits reads the same either way
+    assert bench.step_bytes(sh, ck, [31], ctx, True, "maxprob", "exit_head") == bench.step_bytes(sh, ck, [31], ctx, True)

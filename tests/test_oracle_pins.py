@@ -595,3 +595,39 @@ def test_sts_batch_rule_exits_together_on_the_minimum():
         o._r = o.decode_step(t)
     assert np.array_equal(one_p._r.exit_layers, one_b._r.exit_layers)
     assert np.allclose(one_p._r.conf, one_b._r.conf, equal_nan=True)
+
+
+# ---------------------------------------------------- exit-head token
+
+def test_exit_head_token_is_the_exit_heads_argmax():
+    """With the exit-head token source an exited sequence emits the argmax of
+    the head that let it leave (CALM article §3.1); a sequence that never
+    exits emits the final head's argmax, as with the default source."""
+    w = synth.WORKLOADS["tiny-b1"]
+    lens, prompts = synth.workload_inputs(w)
+    pr = [list(prompts[0][:20])]
+    fin = oracle.build_oracle(w)
+    ex = oracle.build_oracle(w, token_source="exit_head")
+    for o in (fin, ex):
+        o.set_thresholds([-np.inf, np.inf])          # exit at the first checkpoint (layer 1)
+    tf, te = fin.prefill(pr), ex.prefill(pr)
+    assert np.array_equal(tf, te)
+    rf, re_ = fin.decode_step(tf), ex.decode_step(te)
+    assert re_.exit_layers[0] == 1 and rf.exit_layers[0] == 1
+    # the exit head of checkpoint 0 on the state after layer 1
+    z = oracle.head_logits(re_.hidden[1, 0], ex.W.g_final, ex.W.E, w.shape.rms_eps, ex.W.T[0])
+    assert re_.next_tokens[0] == oracle.argmax_lowest(z)
+    assert re_.margins[0] == pytest.approx(oracle.top2_margin(z))
+    # the state after the last layer is the same either way (the int4 layers still run)
+    assert np.allclose(re_.hidden, rf.hidden, rtol=0, atol=0)
+    # no exit: both sources agree exactly
+    for o in (fin, ex):
+        o.set_thresholds([np.inf, np.inf])
+    a, b = fin.decode_step(rf.next_tokens), ex.decode_step(rf.next_tokens)
+    assert np.array_equal(a.next_tokens, b.next_tokens)
+
+
+def test_exit_head_token_needs_the_exit_head():
+    w = synth.WORKLOADS["tiny-b1"]
+    with pytest.raises(AssertionError):
+        oracle.build_oracle(w, criterion="sts", token_source="exit_head")
