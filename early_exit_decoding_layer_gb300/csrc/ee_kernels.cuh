@@ -70,6 +70,7 @@ struct LinearParams {
   const uint8_t* wq;
   const uint16_t* ws;
   int32_t sstride;           // scale row stride (elements); ceil(K/128) keeps rows unpadded
+  const uint8_t* wq4t;       // the same int4 copy in the tensor-core GEMM's blocks (or null)
   // rows: either lists (count + ids) or a direct count with ids 0..m_direct-1
   const int32_t* list_full;  // rows on the bf16 weights (may be null)
   const int32_t* list_exit;  // rows on the int4 weights (may be null)
@@ -132,6 +133,7 @@ struct LinearParams {
 struct TcParams {
   CUtensorMap amap;     // bf16 weights [N, K]: box 64 (K) x 128 (rows), 128-byte swizzle
   LinearParams lp;      // shapes, lists, activations, epilogue (as for the GEMV)
+  const uint8_t* q4t;   // MODE 1: the int4 copy in blocks (int4_tc_layout_bytes)
   int32_t ntiles, ksplit, nks, nk;  // tiles, K splits, 64-wide K steps per split, K steps
   float* part;          // [tile][split][64 columns][128 rows] fp32 partial sums
   int32_t* tile_cnt;    // [ntiles] split counters, zero between launches
@@ -145,6 +147,11 @@ bool gemm_tc_shape_ok(int K);
 size_t gemm_tc_part_floats(int units);
 cudaError_t gemm_tc_prepare();
 cudaError_t launch_gemm_tc(const TcParams& tp, int mode, bool pdl, cudaStream_t st);
+// The int4 copy for MODE 1: per 128-row tile and 64-column K step, one
+// block of 128 rows x 32 bytes of nibbles and 128 bf16 scales.
+size_t int4_tc_layout_bytes(int rows, int cols);
+cudaError_t launch_int4_tc_layout(const uint8_t* packed, const uint16_t* scales, int rows, int cols, int sstride,
+                                  uint8_t* out, cudaStream_t st);
 // Tensor map of a bf16 weight matrix [N, K] (row stride K) for MODE 0.
 bool encode_weight_map(CUtensorMap* map, const uint16_t* w, int N, int K);
 

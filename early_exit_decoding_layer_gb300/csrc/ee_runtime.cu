@@ -51,8 +51,9 @@ struct Carver {
 };
 
 struct Mat4 {  // int4 copy of one fused matrix
-  uint8_t* q;
+  uint8_t* q;     // row layout (GEMV)
   uint16_t* s;
+  uint8_t* qt;    // tensor-core GEMM blocks (contexts with max_batch >= kTcMinBatch), else null
 };
 
 struct LayerBufs {
@@ -247,6 +248,11 @@ size_t carve(ee_ctx* c, const ee_config& cfg, uint8_t* base) {
     b.gu.s = cv.take<uint16_t>((size_t)2 * m.F * sstride_of(m.d));
     b.d.q = cv.take<uint8_t>((size_t)m.d * m.F / 2);
     b.d.s = cv.take<uint16_t>((size_t)m.d * sstride_of(m.F));
+    const bool tcl = m.maxb >= kTcMinBatch;
+    b.qkv.qt = tcl ? cv.take<uint8_t>(int4_tc_layout_bytes(m.nqkv, m.d)) : nullptr;
+    b.o.qt = tcl ? cv.take<uint8_t>(int4_tc_layout_bytes(m.d, m.dq)) : nullptr;
+    b.gu.qt = tcl ? cv.take<uint8_t>(int4_tc_layout_bytes(2 * m.F, m.d)) : nullptr;
+    b.d.qt = tcl ? cv.take<uint8_t>(int4_tc_layout_bytes(m.d, m.F)) : nullptr;
   }
   uint16_t* E = cv.take<uint16_t>((size_t)m.V * m.d);
   uint16_t* gf = cv.take<uint16_t>(m.d);
@@ -482,11 +488,12 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
         tp.nks = pl.nks;
         tp.nk = pl.nk;
         tp.part = c->tc_part;
+        tp.q4t = lp.wq4t;
         tp.tile_cnt = c->tc_cnt;
         // the exit list is empty until a head has run (no launch for it then)
         const bool exit_rows = heads && m.nck > 0 && layer > c->ckpts[0];
         if (lp.w) EE_LAUNCH(log, kind, layer, launch_gemm_tc(tp, 0, c->pdl, st));
-        if (lp.wq && exit_rows) EE_LAUNCH(log, kind, layer, launch_gemm_tc(tp, 1, c->pdl, st));
+        if (lp.wq && lp.wq4t && exit_rows) EE_LAUNCH(log, kind, layer, launch_gemm_tc(tp, 1, c->pdl, st));
         return EE_OK;
       }
     }
@@ -520,6 +527,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     pq.w = w.wqkv;
     pq.wq = w.qkv.q;
     pq.ws = w.qkv.s;
+    pq.wq4t = w.qkv.qt;
     pq.sstride = sstride_of(m.d);
     pq.list_full = c->lists->full;
     pq.list_exit = c->lists->exitl;
@@ -562,6 +570,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     po.w = w.wo;
     po.wq = dead_exit ? nullptr : w.o.q;
     po.ws = dead_exit ? nullptr : w.o.s;
+    po.wq4t = w.o.qt;
     po.sstride = sstride_of(m.dq);
     po.list_full = c->lists->full;
     po.list_exit = c->lists->exitl;
@@ -576,6 +585,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     pg.w = w.wgu;
     pg.wq = dead_exit ? nullptr : w.gu.q;
     pg.ws = dead_exit ? nullptr : w.gu.s;
+    pg.wq4t = w.gu.qt;
     pg.sstride = sstride_of(m.d);
     pg.list_full = c->lists->full;
     pg.list_exit = c->lists->exitl;
@@ -593,6 +603,7 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
     pd.w = w.wd;
     pd.wq = dead_exit ? nullptr : w.d.q;
     pd.ws = dead_exit ? nullptr : w.d.s;
+    pd.wq4t = w.d.qt;
     pd.sstride = sstride_of(m.F);
     pd.list_full = c->lists->full;
     pd.list_exit = c->lists->exitl;
@@ -1027,6 +1038,13 @@ ee_status ee_load_layer(ee_ctx* c, int32_t layer, const ee_layer_weights* lw) {
     for (int k = 0; k < 4; ++k)
       EE_CUDA(c, launch_quantize_int4(blocks_bf[k], rows[k], cols[k], blocks_q[k].q, blocks_q[k].s,
                                       sstride_of(cols[k]), c->st));
+  }
+  if (c->tc) {  // the tensor-core GEMM's blocks of the exit copy
+    const int rows[4] = {m.nqkv, m.d, 2 * m.F, m.d};
+    const int cols[4] = {m.d, m.dq, m.d, m.F};
+    for (int k = 0; k < 4; ++k)
+      EE_CUDA(c, launch_int4_tc_layout(blocks_q[k].q, blocks_q[k].s, rows[k], cols[k], sstride_of(cols[k]),
+                                       blocks_q[k].qt, c->st));
   }
   EE_CUDA(c, cudaMemcpyAsync(b.g_attn, lw->g_attn, (size_t)m.d * 2, cudaMemcpyDefault, c->st));
   EE_CUDA(c, cudaMemcpyAsync(b.g_ffn, lw->g_ffn, (size_t)m.d * 2, cudaMemcpyDefault, c->st));

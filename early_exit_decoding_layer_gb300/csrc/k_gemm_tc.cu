@@ -12,11 +12,15 @@
 //    and nc lo rows (N = 2 nc, nc = 32 for lists of up to 32 sequences, else
 //    64) and the epilogue adds the two halves of D.  Building B each stage
 //    is the producers' work, so the smaller tile halves it.
-//  * exit sub-batch (int4 weights, MODE 1): producer warps read the packed
-//    nibbles and bf16 scales, dequantise them in registers to fp16 q * s
-//    (exact: an 8-bit scale times a 4-bit integer fits fp16's 11 bits) and
-//    store them into the swizzled A tile; B holds the fp16 activations
-//    (N = 64).  The int4 weights are never written back to HBM.
+//  * exit sub-batch (int4 weights, MODE 1): the int4 copy is kept in a
+//    layout of its own (k_int4_tc_layout): per 128-row tile and 64-column K
+//    step one contiguous block of 128 rows x 32 bytes of nibbles and the
+//    rows' 128 bf16 scales (4352 bytes), which one bulk copy brings into a
+//    shared-memory ring.  Producer warps dequantise their row of it to fp16
+//    q * s (exact: an 8-bit scale times a 4-bit integer fits fp16's 11
+//    bits) and store it into the swizzled A tile; B holds the fp16
+//    activations (N = 32 for lists of up to 32 sequences, else 64).  The
+//    int4 weights are never written back to HBM.
 // Producer warps also gather the listed sequences' activations (fp16, pair
 // order) into the B tiles.  One thread issues the MMAs; a stage is released
 // by tcgen05.commit when its MMAs have consumed it.
@@ -41,6 +45,8 @@ namespace {
 constexpr int kBM = 128;  // weight rows per tile (MMA M)
 constexpr int kBK = 64;   // K elements per stage (one 128-byte swizzle row)
 constexpr int kMaxStages = 4;
+constexpr uint32_t kQ4Block = kBM * 32 + kBM * 2;  // int4 tile-step block: nibbles + scales
+constexpr int kRawSlots = 5;  // MODE 1: int4 blocks in flight per CTA (their own ring)
 constexpr int kCols = 64;  // sequences per launch at most (EE_MAX_BATCH)
 constexpr int kTcThreads = 192;  // warps 0-3 producers + epilogue, 4 TMA, 5 MMA
 constexpr uint32_t kABytes = kBM * kBK * 2;
@@ -51,10 +57,13 @@ static_assert(kCols == EE_MAX_BATCH, "one launch covers the whole list");
 // or four int4 ones (N = 64).  A fourth bf16 stage for N = 64 measured no
 // faster: the per-stage B build, not the bytes in flight, sets the pace.
 constexpr uint32_t stage_bytes(int n) { return kABytes + (uint32_t)n * kBK * 2; }
-constexpr int stage_count(int mode) { return mode == 0 ? 3 : kMaxStages; }
+// MODE 1 keeps its raw int4 blocks in a ring of their own, refilled as
+// soon as the producers have read a block.
+constexpr int stage_count(int mode) { return 3; }
 template <int MODE>
-constexpr size_t kTcSmem = (size_t)stage_count(MODE) * stage_bytes(MODE == 0 ? 2 * kCols : kCols) + 1024;
-static_assert(kTcSmem<0> == kTcSmem<1>, "both modes use the same shared memory");
+constexpr size_t kTcSmem = (size_t)stage_count(MODE) * stage_bytes(MODE == 0 ? 2 * kCols : kCols) +
+                           (MODE == 1 ? (size_t)kRawSlots * kQ4Block : 0) + 1024;
+static_assert(kTcSmem<1> <= kTcSmem<0>, "MODE 1 fits in MODE 0's shared memory");
 
 // Shared memory descriptor of a K-major tile with 128-byte rows and the
 // 128-byte swizzle: start address, stride between 8-row groups (1024 B),
@@ -112,7 +121,7 @@ EE_DEV void unpair8(const uint4& v, float* x) {
 }
 
 struct TcShared {
-  uint64_t full[kMaxStages], empty[kMaxStages], done;
+  uint64_t full[kMaxStages], empty[kMaxStages], raw[kRawSlots], raw_free[kRawSlots], done;
   uint32_t tmem;
   int32_t lf[kListLen], le[kListLen];
   int last;
@@ -146,9 +155,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
     grid_dep_launch();
     return;
   }
-  // B rows: bf16 keeps nc hi rows then nc lo rows; int4 keeps 64 fp16 rows
-  const int nc = MODE == 0 && ncol <= kCols / 2 ? kCols / 2 : kCols;
-  const int N = MODE == 0 ? 2 * nc : kCols;
+  // B rows: bf16 keeps nc hi rows then nc lo rows; int4 keeps nc fp16 rows
+  const int nc = ncol <= kCols / 2 ? kCols / 2 : kCols;  // columns built (bf16: x2 for hi, lo)
+  const int N = MODE == 0 ? 2 * nc : nc;
   const int nst = stage_count(MODE);
   const uint32_t stage_b = stage_bytes(N);
 
@@ -156,6 +165,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
     for (int s = 0; s < nst; ++s) {
       mbar_init(&sh.full[s], MODE == 0 ? 129 : 128);
       mbar_init(&sh.empty[s], 1);
+    }
+    for (int s = 0; s < kRawSlots; ++s) {
+      mbar_init(&sh.raw[s], 1);
+      mbar_init(&sh.raw_free[s], 4);  // one arrival per producer warp
     }
     mbar_init(&sh.done, 1);
     fence_mbar_init();
@@ -171,6 +184,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = sh.tmem;
   const uint32_t tiles_s = smem_addr(tiles);
+  uint8_t* raw_ring = tiles + (size_t)nst * stage_b;  // MODE 1: raw int4 blocks
 
   if (warp == 4) {
     // TMA of the bf16 weight tiles; the first stages go out before the
@@ -185,6 +199,19 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
         if (++s == nst) s = 0, ++n;
       }
       if (nks <= nst) grid_dep_wait();
+    } else if (MODE == 1 && lane == 0) {
+      // the int4 blocks of this unit's K steps, one bulk copy each, into the
+      // raw ring; a slot is refilled once every producer warp has read it
+      const uint8_t* src = tp.q4t + ((size_t)tile * tp.nk + ks0) * kQ4Block;
+      for (int i = 0, s = 0, n = 0; i < nks; ++i) {
+        if (i == kRawSlots) grid_dep_wait();
+        if (n > 0 && !mbar_wait_bounded(&sh.raw_free[s], (n - 1) & 1, p.err, DERR_EMPTY_WAIT)) break;
+        mbar_arrive_expect_tx(&sh.raw[s], kQ4Block);
+        bulk_g2s(raw_ring + (size_t)s * kQ4Block, src + (size_t)i * kQ4Block, kQ4Block, &sh.raw[s],
+                 l2_evict_first_policy());
+        if (++s == kRawSlots) s = 0, ++n;
+      }
+      if (nks <= kRawSlots) grid_dep_wait();
     } else {
       grid_dep_wait();
     }
@@ -218,25 +245,19 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
     }
   } else {
     // producers: the B tile (activations of the listed sequences) and, for
-    // int4, the dequantised A tile of every stage.  Global reads run ahead
-    // of the stores in registers (PD stages: activations from L2, and for
-    // int4 the packed weights from HBM), so a stage costs no round trip.
+    // int4, the dequantised A tile of every stage.  The activations are read
+    // ahead of the stores in registers (PD stages, from L2); int4 blocks come
+    // through the raw ring.
     grid_dep_wait();
     grid_dep_launch();
-    constexpr int PD = MODE == 0 ? 3 : 4;  // stages of reads in flight per thread
+    constexpr int PD = 3;  // stages of activation reads in flight per thread
     // B entry e (of nb = 32 or 64) and part of the stage's 8 column chunks:
     // the 128 threads share the nb entries, nch chunks each
-    const int nb = MODE == 0 ? nc : kCols, nch = nb / 16;
+    const int nb = nc, nch = nb / 16;
     const int e = tid & (nb - 1), part = tid / nb;
     const bool have = e < ncol;
     const uint16_t* xrow = p.xh + (size_t)(have ? lst[1 + e] : 0) * p.x_stride + 8 * nch * part;
-    const int r = row0 + tid;  // int4: weight row of this thread
-    const bool have_row = MODE == 1 && r < p.N;
-    const uint8_t* qrow = MODE == 1 ? p.wq + (size_t)(have_row ? r : 0) * (p.K / 2) : nullptr;
-    const uint16_t* srow = MODE == 1 ? p.ws + (size_t)(have_row ? r : 0) * p.sstride : nullptr;
     uint4 xr[PD][4];
-    uint4 qr[MODE == 1 ? PD : 1][2];
-    uint16_t sr[MODE == 1 ? PD : 1];
     auto fetch = [&](int slot, int i) {
       if (i >= nks) return;
       const int k0 = (ks0 + i) * kBK;
@@ -244,16 +265,6 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
       for (int c = 0; c < 4; ++c)
         if (c < nch)
           xr[slot][c] = have ? *reinterpret_cast<const uint4*>(xrow + k0 + 8 * c) : make_uint4(0, 0, 0, 0);
-      if constexpr (MODE == 1) {
-        if (have_row) {
-          qr[slot][0] = ldg_stream_v4(qrow + k0 / 2);
-          qr[slot][1] = ldg_stream_v4(qrow + k0 / 2 + 16);
-          sr[slot] = srow[k0 / EE_QUANT_GROUP];
-        } else {
-          qr[slot][0] = qr[slot][1] = make_uint4(0, 0, 0, 0);
-          sr[slot] = 0;
-        }
-      }
     };
 #pragma unroll
     for (int d = 0; d < PD; ++d) fetch(d, d);
@@ -289,34 +300,41 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
           }
         }
         if constexpr (MODE == 1) {
-          // A: row r, the stage's 64 columns (32 packed bytes, one scale).
-          // Byte t of a word holds columns 2t (low nibble) and 2t + 1, two's
-          // complement.  prmt copies byte t into both halves; the mask keeps
-          // the low nibble in the low half and 16 x the high nibble in the
-          // high one under the fp16 exponent of 1024, flipping each nibble's
-          // sign bit (n ^ 8 = q + 8) in the same LOP3; one HFMA2 leaves
-          // (q_lo, q_hi) exactly and one HMUL2 applies the scale.
-          const __half2 s2 = __float2half2_rn(bf16_bits_to_float(sr[u]));
-          const __half2 mul = __halves2half2(__ushort_as_half((unsigned short)0x3C00),   // 1
-                                             __ushort_as_half((unsigned short)0x2C00));  // 1/16
-          const __half2 add = __halves2half2(__ushort_as_half((unsigned short)0xE408),   // -1032
-                                             __ushort_as_half((unsigned short)0xD480));  // -72
-          const uint32_t words[8] = {qr[u][0].x, qr[u][0].y, qr[u][0].z, qr[u][0].w,
-                                     qr[u][1].x, qr[u][1].y, qr[u][1].z, qr[u][1].w};
+          // A: row tid of the tile, the stage's 64 columns, from the raw
+          // block (row tid's 8 words, then its scale).  Word j holds columns
+          // c = 8j .. c+7 as nibbles (c, c+2, c+4, c+6 | c+1, c+3, c+5, c+7):
+          // one masking LOP3 per pair puts (c, c+1) or (c+4, c+5) under the
+          // fp16 exponent of 1024 with the sign bits flipped (1024 + q + 8),
+          // and (c+2, c+3) or (c+6, c+7) at 16x (1024 + 16 (q + 8)); one
+          // HADD2 or HFMA2 leaves q exactly, one HMUL2 applies the scale.
+          const int rs = i % kRawSlots, rn = i / kRawSlots;
+          if (!mbar_wait_bounded(&sh.raw[rs], rn & 1, p.err, DERR_FULL_WAIT)) {
+            i0 = nks;
+            break;
+          }
+          const uint8_t* blk = raw_ring + (size_t)rs * kQ4Block;
+          const uint4 w0 = *reinterpret_cast<const uint4*>(blk + tid * 32);
+          const uint4 w1 = *reinterpret_cast<const uint4*>(blk + tid * 32 + 16);
+          const uint16_t sb = *reinterpret_cast<const uint16_t*>(blk + kBM * 32 + tid * 2);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.raw_free[rs]);  // this warp is done reading the block
+          const __half2 s2 = __float2half2_rn(bf16_bits_to_float(sb));
+          const __half2 m1032 = __half2half2(__ushort_as_half((unsigned short)0xE408));  // -1032
+          const __half2 r16 = __half2half2(__ushort_as_half((unsigned short)0x2C00));    // 1/16
+          const __half2 m72 = __half2half2(__ushort_as_half((unsigned short)0xD480));    // -72
+          const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const uint32_t t = words[j];
-            uint32_t o[4];
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-              uint32_t x;
-              asm("prmt.b32 %0, %1, 0, %2;" : "=r"(x) : "r"(t), "r"(0x4040u | (uint32_t)b | ((uint32_t)b << 8)));
-              const uint32_t m = (x & 0x00F0000Fu) ^ 0x64806408u;  // also flips each nibble's sign bit
-              __half2 q = __hfma2(*reinterpret_cast<const __half2*>(&m), mul, add);
-              q = __hmul2(q, s2);
-              o[b] = *reinterpret_cast<const uint32_t*>(&q);
-            }
-            st_shared_v4(a_s + sw128(tid, j), make_uint4(o[0], o[1], o[2], o[3]));
+            const uint32_t t = words[j], t8 = t >> 8;
+            const uint32_t m0 = (t & 0x000F000Fu) ^ 0x64086408u, m1 = (t & 0x00F000F0u) ^ 0x64806480u;
+            const uint32_t m2 = (t8 & 0x000F000Fu) ^ 0x64086408u, m3 = (t8 & 0x00F000F0u) ^ 0x64806480u;
+            const __half2 q01 = __hmul2(__hadd2(*reinterpret_cast<const __half2*>(&m0), m1032), s2);
+            const __half2 q23 = __hmul2(__hfma2(*reinterpret_cast<const __half2*>(&m1), r16, m72), s2);
+            const __half2 q45 = __hmul2(__hadd2(*reinterpret_cast<const __half2*>(&m2), m1032), s2);
+            const __half2 q67 = __hmul2(__hfma2(*reinterpret_cast<const __half2*>(&m3), r16, m72), s2);
+            st_shared_v4(a_s + sw128(tid, j),
+                         make_uint4(*reinterpret_cast<const uint32_t*>(&q01), *reinterpret_cast<const uint32_t*>(&q23),
+                                    *reinterpret_cast<const uint32_t*>(&q45), *reinterpret_cast<const uint32_t*>(&q67)));
           }
         }
         fence_proxy_async();
@@ -467,6 +485,42 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
 
 }  // namespace
 
+// Row-layout int4 copy -> the tensor-core GEMM's blocks: thread per word of
+// a (tile, K step) block, then per scale.  Word j of row r holds columns
+// c = 64 ks + 8j .. c+7 of row 128 t + r with nibble i = column c + 2i (i < 4)
+// or c + 2(i - 4) + 1: the row layout's word at the same columns with its
+// even-column nibbles moved to the low half and its odd ones to the high
+// half.  Rows past the matrix are zero.
+__global__ void __launch_bounds__(256) k_int4_tc_layout(const uint8_t* __restrict__ q, const uint16_t* __restrict__ s,
+                                                        int rows, int cols, int sstride, uint8_t* __restrict__ out) {
+  const long long nk = cols / kBK, ntiles = (rows + kBM - 1) / kBM;
+  const long long words = ntiles * nk * kBM * 8, scales = ntiles * nk * kBM;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx < words) {
+    const int j = (int)(idx & 7), r = (int)((idx >> 3) % kBM);
+    const long long blk = (idx >> 3) / kBM, ks = blk % nk, t = blk / nk;
+    const long long row = t * kBM + r;
+    uint32_t w = 0;
+    if (row < rows) {
+      const uint32_t src = *reinterpret_cast<const uint32_t*>(q + (size_t)row * (cols / 2) + (ks * kBK + 8 * j) / 2);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {  // source nibble i = column c + i
+        const uint32_t v = (src >> (4 * i)) & 0xF;
+        const int dst = (i & 1) ? 4 + (i >> 1) : (i >> 1);
+        w |= v << (4 * dst);
+      }
+    }
+    *reinterpret_cast<uint32_t*>(out + (size_t)blk * kQ4Block + (size_t)r * 32 + j * 4) = w;
+  } else if (idx < words + scales) {
+    const long long i = idx - words;
+    const int r = (int)(i % kBM);
+    const long long blk = i / kBM, ks = blk % nk, t = blk / nk;
+    const long long row = t * kBM + r;
+    const uint16_t sv = row < rows ? s[(size_t)row * sstride + (ks * kBK) / EE_QUANT_GROUP] : 0;
+    *reinterpret_cast<uint16_t*>(out + (size_t)blk * kQ4Block + kBM * 32 + (size_t)r * 2) = sv;
+  }
+}
+
 TcPlan gemm_tc_plan(int N, int K, int num_sms, int max_units) {
   TcPlan pl;
   pl.ntiles = (N + kBM - 1) / kBM;
@@ -498,6 +552,19 @@ TcPlan gemm_tc_plan(int N, int K, int num_sms, int max_units) {
 bool gemm_tc_shape_ok(int K) { return K >= kBK && K % kBK == 0; }
 
 size_t gemm_tc_part_floats(int units) { return (size_t)units * kCols * kBM; }
+
+size_t int4_tc_layout_bytes(int rows, int cols) {
+  return (size_t)((rows + kBM - 1) / kBM) * (cols / kBK) * kQ4Block;
+}
+
+cudaError_t launch_int4_tc_layout(const uint8_t* packed, const uint16_t* scales, int rows, int cols, int sstride,
+                                  uint8_t* out, cudaStream_t st) {
+  if (rows < 1 || cols % kBK) return cudaErrorInvalidValue;
+  const long long blocks = (long long)((rows + kBM - 1) / kBM) * (cols / kBK);
+  const long long n = blocks * kBM * 9;
+  k_int4_tc_layout<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(packed, scales, rows, cols, sstride, out);
+  return cudaGetLastError();
+}
 
 cudaError_t gemm_tc_prepare() {
   cudaError_t e;
