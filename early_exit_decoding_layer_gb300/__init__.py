@@ -35,6 +35,7 @@ EXPORTS = (
     "ee_attention_scratch_bytes", "ee_op_attention", "ee_head_scratch_bytes",
     "ee_op_vocab_head", "ee_step_io", "ee_set_profile", "ee_profile_read", "ee_last_step_ms",
     "ee_op_attention_noalloc", "ee_set_exit_criterion", "ee_set_token_source",
+    "ee_set_prefill_exit", "ee_prefill_exit_layers",
 )
 
 KINDS = ("begin", "norm", "qkv", "attn", "o", "gateup", "down", "head_norm", "head_t", "head_e",
@@ -101,6 +102,8 @@ def load_library(path: str = LIB_PATH):
         "ee_set_exit_enabled": (i32, [c_vp, i32]),
         "ee_set_exit_criterion": (i32, [c_vp, i32]),
         "ee_set_token_source": (i32, [c_vp, i32]),
+        "ee_set_prefill_exit": (i32, [c_vp, P(c_f32)]),
+        "ee_prefill_exit_layers": (i32, [c_vp, P(i32)]),
         "ee_set_use_graph": (i32, [c_vp, i32]),
         "ee_prefill": (i32, [c_vp, i32, P(i32), P(i32), P(i32)]),
         "ee_decode_step": (i32, [c_vp, P(i32), P(i32), P(i32)]),
@@ -263,6 +266,19 @@ class DecodeEngine:
         """'maxprob' (exit-head confidence, default), 'sts' (state transition
         similarity, per sequence) or 'sts_batch' (its batch-minimum rule)."""
         self._check(self.lib.ee_set_exit_criterion(self.ctx, self.CRITERIA[criterion]))
+
+    def set_prefill_exit(self, tau):
+        """Sequence-level exit in prefill with thresholds tau (None: off)."""
+        if tau is None:
+            self._check(self.lib.ee_set_prefill_exit(self.ctx, None))
+            return
+        t = np.asarray(tau, dtype=np.float32)
+        self._check(self.lib.ee_set_prefill_exit(self.ctx, t.ctypes.data_as(P(c_f32))))
+
+    def prefill_exit_layers(self) -> np.ndarray:
+        out = np.empty(max(self.batch, 1), dtype=np.int32)
+        self._check(self.lib.ee_prefill_exit_layers(self.ctx, out.ctypes.data_as(P(ctypes.c_int32))))
+        return out[: self.batch]
 
     TOKEN_SOURCES = {"final": 0, "exit_head": 1}
 

@@ -53,6 +53,13 @@ EE_DEV Stat stat_warp_merge(Stat s) {
 // Rebuilds the full list (the sequences that stay, in order) and the exit
 // list (the previous exit list le merged with the newly exited, by id), and
 // records the scores and exit layers.
+// A sequence with a forced exit layer (lists->forced[seq] >= 0) exits at
+// that checkpoint whatever its score.
+EE_DEV bool checkpoint_exits(const StepLists* lists, int seq, float conf, float gamma, int ckpt_layer) {
+  const int f = lists->forced[seq];
+  return f >= 0 ? f == ckpt_layer : conf > gamma;
+}
+
 EE_DEV void checkpoint_decide(float gamma, int ckpt_index, int ckpt_layer, const float* score, int stride,
                               const int32_t* lf, const int32_t* le, int nrows, float* conf_out, int32_t* exit_layer,
                               StepLists* lists) {
@@ -63,7 +70,7 @@ EE_DEV void checkpoint_decide(float gamma, int ckpt_index, int ckpt_layer, const
     const int seq = lf[1 + m];
     const float conf = score[m * stride];
     conf_out[seq * EE_MAX_CHECKPOINTS + ckpt_index] = conf;
-    if (conf > gamma) {
+    if (checkpoint_exits(lists, seq, conf, gamma, ckpt_layer)) {
       newly[nnew++] = seq;
       exit_layer[seq] = ckpt_layer;
     } else {
@@ -115,7 +122,8 @@ EE_DEV void head_finalize_group(const LinearParams& p, int nparts, const int32_t
       if (p.argmax_out) {  // exit-head tokens: an exiting sequence emits this head's argmax
         const float gamma = p.gamma[p.ckpt_index];
         for (int m = 0; m < nrows; ++m)
-          if (res[2 * m] > gamma) p.argmax_out[lf[1 + m]] = __float_as_int(res[2 * m + 1]);
+          if (checkpoint_exits(p.lists, lf[1 + m], res[2 * m], gamma, p.ckpt_layer))
+            p.argmax_out[lf[1 + m]] = __float_as_int(res[2 * m + 1]);
       }
       checkpoint_decide(p.gamma[p.ckpt_index], p.ckpt_index, p.ckpt_layer, res, 2, lf, le, nrows, p.conf_out,
                         p.exit_layer, p.lists);

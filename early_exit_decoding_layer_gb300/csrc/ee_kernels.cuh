@@ -19,6 +19,7 @@ struct StepLists {
   int32_t full[kListLen];   // still on the bf16 backbone (ascending ids)
   int32_t exitl[kListLen];  // exited, running the int4 copies (ascending ids)
   int32_t fin[kListLen];    // rows of the final LM head
+  int32_t forced[EE_MAX_BATCH];  // by sequence id: checkpoint layer where it must exit, or -1
 };
 
 // Host -> device step descriptor (copied each step from pinned staging).
@@ -30,6 +31,7 @@ struct StepDesc {
   int32_t tokens[EE_MAX_BATCH];     // by sequence id
   int32_t pos[EE_MAX_BATCH];        // position of this step's token, by sequence id
   int32_t new_block[EE_MAX_BATCH];  // block to map at pos/16, or -1, by sequence id
+  int32_t forced_exit[EE_MAX_BATCH];  // checkpoint layer where the sequence must exit, or -1
   int32_t debug;                    // keep per-layer hidden states
 };
 

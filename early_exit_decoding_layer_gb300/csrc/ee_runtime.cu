@@ -151,6 +151,8 @@ struct ee_ctx {
   std::vector<float> gamma;
   int exit_enabled = 1, use_graph = 1, debug = 0;
   int criterion = EE_EXIT_MAXPROB;
+  std::vector<float> prefill_tau;        // sequence-level prefill exit thresholds (empty: off)
+  std::vector<int32_t> prefill_exit;     // per sequence: layer its prompt left at (n_layers - 1: none)
   int token_source = EE_TOKEN_FINAL_HEAD;
   // input states of the checkpoint layers (similarity criterion): checkpoint c
   // uses buffer c % 2, so that the save for checkpoint c + 1 (by the down
@@ -954,6 +956,7 @@ ee_status ee_create(const ee_config* cfg, void* dev_arena, size_t arena_bytes, v
       cudaHostAlloc((void**)&c->out_host, sizeof(StepOut), cudaHostAllocDefault) != cudaSuccess)
     return bail(EE_ERR_CUDA);
   memset(c->desc_host, 0, sizeof(StepDesc));
+  for (int q = 0; q < EE_MAX_BATCH; ++q) c->desc_host->forced_exit[q] = -1;
   memset(c->out_host, 0, sizeof(StepOut));
   if (join_user_stream(c) != EE_OK) return bail(EE_ERR_CUDA);
   // counters and lists start at zero
@@ -1240,25 +1243,96 @@ ee_status ee_prefill(ee_ctx* c, int32_t batch, const int32_t* prompt_lens, const
   EE_CUDA(c, cudaMemcpyAsync(c->block_table, bt.data(), bt.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
                              c->st));
   EE_CUDA(c, cudaStreamSynchronize(c->st));
-  StepDesc* d = c->desc_host;
-  for (int t = 0; t < Tmax; ++t) {
-    d->n_part = 0;
-    d->n_fin = 0;
-    for (int q = 0; q < batch; ++q) {
-      d->new_block[q] = -1;
-      if (t < prompt_lens[q]) {
-        d->part[d->n_part++] = q;
-        d->tokens[q] = tokens_concat[offs[q] + t];
-        d->pos[q] = t;
-        if (t == prompt_lens[q] - 1) d->fin[d->n_fin++] = q;
-      }
-    }
-    d->debug = c->debug;
-    s = run_step(c, batch, false);
-    if (s != EE_OK) return s;
-    for (int i = 0; i < d->n_fin; ++i) first_tokens_out[d->fin[i]] = c->out_host->next_token[d->fin[i]];
+  c->prefill_exit.assign(batch, m.L - 1);
+  const bool seq_exit = !c->prefill_tau.empty() && m.nck > 0;
+  // One pass over the prompts, one position per step.  Sequence-level exit
+  // ("River-LLM 深度解析" §6.1) takes two: the first scores every prompt
+  // token with the state transition similarity at each checkpoint (no exit)
+  // and keeps each prompt's minimum; a prompt leaves at the first checkpoint
+  // whose minimum is above its threshold (strict); the second pass reruns the
+  // prompts with those exits forced, so the layers after them run on the
+  // int4 copies and rewrite their K/V (the layers before recompute the same
+  // values).
+  std::vector<float> low((size_t)batch * std::max(m.nck, 1), INFINITY);
+  const int saved_criterion = c->criterion;
+  if (seq_exit) {
+    c->criterion = EE_EXIT_STS;
+    std::vector<float> inf(EE_MAX_CHECKPOINTS, INFINITY);
+    EE_CUDA(c, cudaMemcpyAsync(c->gamma_dev, inf.data(), inf.size() * sizeof(float), cudaMemcpyHostToDevice, c->st));
   }
+  auto restore = [&]() -> ee_status {
+    c->criterion = saved_criterion;
+    if (!seq_exit) return EE_OK;
+    std::vector<float> g(EE_MAX_CHECKPOINTS, INFINITY);
+    for (int i = 0; i < m.nck; ++i) g[i] = c->gamma[i];
+    EE_CUDA(c, cudaMemcpyAsync(c->gamma_dev, g.data(), g.size() * sizeof(float), cudaMemcpyHostToDevice, c->st));
+    EE_CUDA(c, cudaStreamSynchronize(c->st));
+    return EE_OK;
+  };
+  StepDesc* d = c->desc_host;
+  const int passes = seq_exit ? 2 : 1;
+  for (int pass = 0; pass < passes; ++pass) {
+    if (pass == 1) {
+      bool any = false;
+      for (int q = 0; q < batch; ++q)
+        for (int k = 0; k < m.nck; ++k)
+          if (c->prefill_exit[q] == m.L - 1 && low[(size_t)q * m.nck + k] > c->prefill_tau[k]) {
+            c->prefill_exit[q] = c->ckpts[k];
+            any = true;
+          }
+      if (!any) break;  // no prompt leaves: the first pass was the plain prefill
+    }
+    for (int t = 0; t < Tmax; ++t) {
+      d->n_part = 0;
+      d->n_fin = 0;
+      for (int q = 0; q < EE_MAX_BATCH; ++q) d->forced_exit[q] = -1;
+      for (int q = 0; q < batch; ++q) {
+        d->new_block[q] = -1;
+        if (pass == 1 && c->prefill_exit[q] != m.L - 1) d->forced_exit[q] = c->prefill_exit[q];
+        if (t < prompt_lens[q]) {
+          d->part[d->n_part++] = q;
+          d->tokens[q] = tokens_concat[offs[q] + t];
+          d->pos[q] = t;
+          if (t == prompt_lens[q] - 1) d->fin[d->n_fin++] = q;
+        }
+      }
+      d->debug = c->debug;
+      s = run_step(c, batch, seq_exit);
+      if (s != EE_OK) {
+        restore();
+        return s;
+      }
+      if (seq_exit && pass == 0)
+        for (int i = 0; i < d->n_part; ++i) {
+          const int q = d->part[i];
+          for (int k = 0; k < m.nck; ++k)
+            low[(size_t)q * m.nck + k] =
+                std::min(low[(size_t)q * m.nck + k], c->out_host->conf[q * EE_MAX_CHECKPOINTS + k]);
+        }
+      for (int i = 0; i < d->n_fin; ++i) first_tokens_out[d->fin[i]] = c->out_host->next_token[d->fin[i]];
+    }
+  }
+  s = restore();
+  if (s != EE_OK) return s;
   for (int q = 0; q < batch; ++q) c->seq_pos[q] = prompt_lens[q];
+  return EE_OK;
+}
+
+ee_status ee_set_prefill_exit(ee_ctx* c, const float* tau) {
+  if (!c) return EE_ERR_INVALID_ARG;
+  if (!tau) {
+    c->prefill_tau.clear();
+    return EE_OK;
+  }
+  for (int i = 0; i < c->m.nck; ++i)
+    if (isnan(tau[i])) return fail(c, EE_ERR_INVALID_ARG, "tau[%d] is NaN", i);
+  c->prefill_tau.assign(tau, tau + c->m.nck);
+  return EE_OK;
+}
+
+ee_status ee_prefill_exit_layers(const ee_ctx* c, int32_t* out) {
+  if (!c || !out) return EE_ERR_INVALID_ARG;
+  for (int q = 0; q < c->batch; ++q) out[q] = q < (int)c->prefill_exit.size() ? c->prefill_exit[q] : c->m.L - 1;
   return EE_OK;
 }
 
@@ -1285,6 +1359,7 @@ ee_status ee_decode_step(ee_ctx* c, const int32_t* in_tokens, int32_t* next_toke
   StepDesc* d = c->desc_host;
   d->n_part = B;
   d->n_fin = B;
+  for (int q = 0; q < EE_MAX_BATCH; ++q) d->forced_exit[q] = -1;
   for (int q = 0; q < B; ++q) {
     d->part[q] = q;
     d->fin[q] = q;

@@ -76,6 +76,7 @@ __global__ void __launch_bounds__(256) k_step_begin(const BeginParams p) {
       p.lists->full[1 + tid] = v;
       p.lists->exitl[1 + tid] = 0;
       p.lists->fin[1 + tid] = tid < d->n_fin ? d->fin[tid] : 0;
+      p.lists->forced[tid] = d->forced_exit[tid];
     }
     if (tid == 0) {
       p.lists->part[0] = n;

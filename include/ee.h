@@ -216,6 +216,20 @@ ee_status ee_set_use_graph(ee_ctx *ctx, int32_t use_graph);
 ee_status ee_prefill(ee_ctx *ctx, int32_t batch, const int32_t *prompt_lens,
                      const int32_t *tokens_concat, int32_t *first_tokens_out);
 
+/* Sequence-level exit in prefill ("River-LLM 深度解析" §6.1, the prefill half
+ * of its two-phase strategy): with tau set (n_checkpoints floats, host,
+ * copied), ee_prefill scores every prompt token with the state transition
+ * similarity at each checkpoint layer (§5.1) and a prompt leaves the
+ * full-precision path at the first checkpoint where the minimum over its
+ * tokens is above tau[c] (strict; the batch rule of §5.2 over the prompt's
+ * tokens): its later layers run on the int4 copies for all of its tokens
+ * and write their K/V.  The prefill then takes two passes over the prompts
+ * (scoring, then the run with those exits).  tau = NULL (default) turns it
+ * off: plain bf16 prefill.  ee_prefill_exit_layers writes, per sequence of
+ * the last prefill, the layer its prompt left at (n_layers - 1: none). */
+ee_status ee_set_prefill_exit(ee_ctx *ctx, const float *tau);
+ee_status ee_prefill_exit_layers(const ee_ctx *ctx, int32_t *out);
+
 /* One early-exit greedy decode step for every sequence (the per-token loop
  * of the CALM article §3.1: run a layer, write its K/V, score the exit head at
  * a checkpoint and leave the full-precision path once it clears gamma; the

@@ -545,9 +545,21 @@ class Oracle:
         return self.seqs[s].blocks[pos // b], pos % b
 
     # -- prefill: plain bf16 stack over all prompt positions, no exit --------
-    def prefill(self, prompts: Sequence[Sequence[int]]) -> np.ndarray:
+    def prefill(self, prompts: Sequence[Sequence[int]], exit_tau=None) -> np.ndarray:
+        """Prefill phase.  Without ``exit_tau`` the plain bf16 stack runs over
+        every prompt position.  With it, sequence-level exit (River-LLM §6.1,
+        the prefill half of its two-phase strategy): at each checkpoint layer
+        l every token of a prompt is scored by the state transition
+        similarity of layer l (§5.1), and the whole prompt leaves the
+        full-precision path when the minimum over its tokens is above
+        exit_tau[c] (the batch rule of §5.2 over the prompt's tokens); its
+        layers after l run on the int4 copies for all its tokens and write
+        their K/V.  ``self.prefill_exits[s]`` is the layer sequence s left at
+        (n_layers - 1: none).  The first token is the final head's argmax."""
         assert 1 <= len(prompts) <= self.max_batch
         self.reset()
+        cfg = self.cfg
+        L, ck = cfg.n_layers, list(cfg.checkpoints)
         first = np.empty(len(prompts), dtype=np.int32)
         xs = []
         for s, toks in enumerate(prompts):
@@ -555,21 +567,38 @@ class Oracle:
             assert 1 <= P < self.max_seq_len
             self.seqs.append(SeqState(pos=P, tokens=list(int(t) for t in toks),
                                       int4_after=[None] * P))
-            for _ in range((P + self.cfg.kv_block - 1) // self.cfg.kv_block):
+            for _ in range((P + cfg.kv_block - 1) // cfg.kv_block):
                 self._alloc_block(s)
             self.K.append(np.full(self._kv_shape, np.nan))
             self.V.append(np.full(self._kv_shape, np.nan))
             xs.append(self.W.E[np.asarray(toks, dtype=np.int64)].copy())
+        exited: List[Optional[int]] = [None] * len(prompts)
+        self.prefill_scores = np.full((len(prompts), len(ck)), np.nan)   # minimum over tokens
         # the sequences are independent: each layer's weights serve all of
         # them in turn (the same arithmetic as forward_full per sequence)
-        for j in range(self.cfg.n_layers):
-            lws = [self.W.layer(j, False)]
+        for j in range(L):
+            lws = {}
             for s in range(len(prompts)):
                 P = xs[s].shape[0]
-                xs[s], K, V = layer_full(self.cfg, lws, xs[s], np.zeros(P, dtype=bool))
+                q4 = exited[s] is not None
+                if False not in lws:
+                    lws[False] = self.W.layer(j, False)
+                if q4 and True not in lws:
+                    lws[True] = self.W.layer(j, True)
+                x_in = xs[s]
+                layers = [lws[False], lws[True]] if q4 else [lws[False]]
+                xs[s], K, V = layer_full(cfg, layers, xs[s], np.full(P, q4, dtype=bool))
                 self.K[s][j, :P], self.V[s][j, :P] = K, V
+                if exit_tau is not None and j in ck and not q4:
+                    c = ck.index(j)
+                    low = min(state_transition_similarity(x_in[p], xs[s][p]) for p in range(P))
+                    self.prefill_scores[s, c] = low
+                    if low > exit_tau[c]:
+                        exited[s] = j
+        self.prefill_exits = np.array([L - 1 if e is None else e for e in exited], dtype=np.int32)
         for s in range(len(prompts)):
-            logits = head_logits(xs[s][-1], self.W.g_final, self.W.E, self.cfg.rms_eps)
+            self.seqs[s].int4_after = [exited[s]] * len(prompts[s])
+            logits = head_logits(xs[s][-1], self.W.g_final, self.W.E, cfg.rms_eps)
             first[s] = argmax_lowest(logits)
         return first
 

@@ -99,7 +99,8 @@ class Stats:
 
 
 def drive(eng: ee.DecodeEngine, orc: oracle.Oracle, prompts, gamma, steps: int,
-          check_hidden: bool = True, gamma_per_step=None, exit_enabled: bool = True) -> Stats:
+          check_hidden: bool = True, gamma_per_step=None, exit_enabled: bool = True,
+          prefill_tau=None) -> Stats:
     """Prefill both sides, then decode `steps` steps, asserting parity.  The
     engine runs the oracle's exit criterion (orc.criterion)."""
     L = orc.cfg.n_layers
@@ -112,11 +113,17 @@ def drive(eng: ee.DecodeEngine, orc: oracle.Oracle, prompts, gamma, steps: int,
     g0 = np.asarray(gamma, dtype=np.float64)
     eng.set_thresholds(g0)
     orc.set_thresholds(g0)
+    eng.set_prefill_exit(prefill_tau)
     gfirst = eng.prefill(prompts)
-    ofirst = orc.prefill(prompts)
+    ofirst = orc.prefill(prompts, exit_tau=prefill_tau)
+    if prefill_tau is not None:   # the prompts' exit layers agree
+        assert np.array_equal(eng.prefill_exit_layers(), orc.prefill_exits), (
+            eng.prefill_exit_layers(), orc.prefill_exits, orc.prefill_scores)
     for s in range(len(prompts)):
         if gfirst[s] != ofirst[s]:
-            hs, logits = oracle.forward_full(orc.cfg, orc.W, list(prompts[s]))
+            ia = None if prefill_tau is None else [int(orc.prefill_exits[s])] * len(prompts[s])
+            ia = None if ia is not None and ia[0] == orc.cfg.n_layers - 1 else ia
+            hs, logits = oracle.forward_full(orc.cfg, orc.W, list(prompts[s]), int4_after=ia)
             assert oracle.top2_margin(logits) < MARGIN_WINDOW, (s, gfirst[s], ofirst[s])
             st.token_mismatch += 1
     tok = gfirst.copy()

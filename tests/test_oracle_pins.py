@@ -631,3 +631,42 @@ def test_exit_head_token_needs_the_exit_head():
     w = synth.WORKLOADS["tiny-b1"]
     with pytest.raises(AssertionError):
         oracle.build_oracle(w, criterion="sts", token_source="exit_head")
+
+
+# ---------------------------------------------------- sequence-level exit in prefill
+
+def test_prefill_sequence_exit_limits_and_minimum_rule():
+    """River-LLM §6.1: in prefill all tokens of a prompt exit at one layer.
+    tau = +inf is the plain prefill; tau = -inf exits every prompt at the
+    first checkpoint, which equals the plain causal forward with every
+    position on the int4 copies after it (checked through forward_full,
+    the uncached route); the decision uses the minimum over the tokens."""
+    w = synth.WORKLOADS["tiny-b1"]
+    pr = synth.prompts(w.shape, 8, [9, 14])
+    ck = w.checkpoints
+    plain = oracle.build_oracle(w, max_batch=2)
+    t0 = plain.prefill(pr)
+    o = oracle.build_oracle(w, max_batch=2)
+    assert np.array_equal(o.prefill(pr, exit_tau=[np.inf] * len(ck)), t0)
+    assert np.all(o.prefill_exits == w.shape.n_layers - 1)
+    for s in range(2):
+        assert np.allclose(o.K[s][:, :len(pr[s])], plain.K[s][:, :len(pr[s])], rtol=0, atol=0)
+    scores = o.prefill_scores.copy()
+    # every prompt exits at the first checkpoint
+    first = o.prefill(pr, exit_tau=[-np.inf] * len(ck))
+    assert np.all(o.prefill_exits == ck[0])
+    for s in range(2):
+        hs, logits, Ks, Vs = oracle.forward_full(o.cfg, o.W, pr[s], int4_after=[ck[0]] * len(pr[s]),
+                                                 return_kv=True)
+        assert first[s] == oracle.argmax_lowest(logits)
+        assert np.allclose(o.K[s][:, :len(pr[s])], Ks, rtol=1e-12, atol=1e-14)
+        assert np.allclose(o.V[s][:, :len(pr[s])], Vs, rtol=1e-12, atol=1e-14)
+    # the minimum over the tokens decides: tau between the two prompts' minima
+    a, b = scores[0, 0], scores[1, 0]
+    tau = 0.5 * (a + b)
+    o.prefill(pr, exit_tau=[tau, np.inf])
+    want = [ck[0] if sc > tau else w.shape.n_layers - 1 for sc in (a, b)]
+    assert o.prefill_exits.tolist() == want and len(set(want)) == 2
+    # the minimum itself: a prompt whose minimum equals tau does not exit (strict)
+    o.prefill(pr, exit_tau=[a, np.inf])
+    assert o.prefill_exits[0] == w.shape.n_layers - 1
