@@ -48,7 +48,7 @@ L2_BYTES = 129 * 1024 * 1024
 # ----------------------------------------------------------------------------- helpers
 
 # ncu summary with the DRAM bytes per GEMV launch of the default workload
-TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "k_linear_dram_llama3.1-8b_b1.md")
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "k_linear_dram_llama3.2-1b_b1.md")
 GEMV_SOURCES = ("k_linear.cu", "ee_gemv.cuh", "ee_epilogue.cuh", "ee_head.cuh", "ee_common.cuh", "ee_kernels.cuh")
 
 
@@ -71,19 +71,23 @@ def gemv_source_digest():
 
 def measured_traffic_ratio(workload, path=TRAFFIC_SUMMARY):
     """DRAM bytes (read + write) over algorithmic bytes of the GEMV launches in
-    the committed ncu summary: its `key: value` lines give the workload, the
-    sources' digest and the two per-launch figures.  None unless the summary
-    was taken on this workload with the GEMV sources unchanged since."""
+    the committed ncu summary: its `key: value` lines give the workload the
+    capture ran on, the workloads the ratio is applied to (`applies_to`, a
+    comma list; the GEMV streams each weight byte once per launch at any
+    shape, so the ratio carries over from a small capture), the sources'
+    digest and the two per-launch figures.  None unless `workload` is covered
+    and the GEMV sources are unchanged since the capture."""
     if not os.path.exists(path):
         return None
     kv = {}
     with open(path) as f:
         for line in f:
-            if ":" in line and not line.startswith(("|", "#", " ")):
+            if ":" in line and not line.startswith(("|", "#", " ", "-")):
                 k, v = line.split(":", 1)
                 kv[k.strip().strip("`")] = v.strip().strip("`")
     try:
-        if kv.get("workload") != workload or kv.get("gemv_sources_sha256") != gemv_source_digest():
+        covered = {kv["workload"]} | {x.strip() for x in kv.get("applies_to", "").split(",") if x.strip()}
+        if workload not in covered or kv.get("gemv_sources_sha256") != gemv_source_digest():
             return None
         return float(kv["dram_bytes_per_launch"]) / float(kv["algorithmic_bytes_per_launch"])
     except (KeyError, ValueError, ZeroDivisionError, OSError):
@@ -496,7 +500,8 @@ def run_workload(ee, w, args, st, rank, world, peak, steps, profile_steps):
     if args.exit_head_token:
         eng.set_token_source("exit_head")
         eng.set_thresholds(gammas[w.gamma_percentiles[0]])
-        head_tok_run = timed_run(eng, w, prompts, steps, args.warmup, True, world)
+        head_tok_run = timed_run(eng, w, prompts, steps, args.warmup, True, world,
+                                 ncu_region=args.ncu_region)
         eng.set_token_source("final")
     # the state-transition-similarity criterion, thresholds at the library's
     # percentiles of the no-exit similarity scores
@@ -512,7 +517,8 @@ def run_workload(ee, w, args, st, rank, world, peak, steps, profile_steps):
                 key = "%s_p%g" % (mode, pct)
                 taus[key] = tm[pct]
                 eng.set_thresholds(tm[pct])
-                sts_runs[key] = timed_run(eng, w, prompts, steps, args.warmup, True, world)
+                sts_runs[key] = timed_run(eng, w, prompts, steps, args.warmup, True, world,
+                                          ncu_region=args.ncu_region)
         eng.set_exit_criterion("maxprob")
 
     def summarize(r, heads, criterion="maxprob", token_source="final"):
@@ -637,9 +643,10 @@ def run_ours(args):
             if ratio is not None:
                 line["roofline"]["traffic"] = ratio * k["bytes_per_launch"]
                 line["roofline"]["traffic_note"] = (
-                    "ncu dram__bytes_read.sum + dram__bytes_write.sum over the GEMV launches of two exit-run "
-                    "steps (profiles/k_linear_dram_llama3.1-8b_b1.md) = %.4f x their algorithmic bytes; "
-                    "scaled to this run's algorithmic bytes per launch" % ratio)
+                    "ncu dram__bytes_read.sum + dram__bytes_write.sum over the GEMV launches of one exit-run "
+                    "and one no-exit step of the Llama-3.2-1B batch-1 workload (profiles/%s) = %.4f x their "
+                    "algorithmic bytes; scaled to this run's algorithmic bytes per launch"
+                    % (os.path.basename(TRAFFIC_SUMMARY), ratio))
             line["kernels"] = kr
         for pct, extra in res["others"].items():
             line.setdefault("other_gammas", {})[pct] = {

@@ -104,6 +104,12 @@ def test_measured_traffic_only_for_unchanged_sources(tmp_path):
     p.write_text(body % ("0" * 16))
     assert bench.measured_traffic_ratio("llama3.1-8b-b1", str(p)) is None
     assert bench.measured_traffic_ratio("llama3.1-8b-b1", str(tmp_path / "missing.md")) is None
+    # a capture on a small workload applies to the workloads it names
+    p.write_text((body % digest).replace("llama3.1-8b-b1", "llama3.2-1b-b1")
+                 + "applies_to: `llama3.1-8b-b1, llama3.2-1b-b1`\n")
+    assert bench.measured_traffic_ratio("llama3.1-8b-b1", str(p)) == 1.002
+    assert bench.measured_traffic_ratio("llama3.2-1b-b1", str(p)) == 1.002
+    assert bench.measured_traffic_ratio("llama3.1-8b-b32", str(p)) is None
 
 
 def test_source_digest_ignores_comments_only():
