@@ -230,22 +230,33 @@ EE_DEV void attention_item(const AttnParams& p, int split, int g, int z, uint8_t
   if (!sh.s_last) return;
   __threadfence();
 
-  // last CTA of this (sequence, kv head): merge the splits.  Warp w takes
-  // heads w, w+4, ...: M = max m, weights exp(m - M), L = sum weight * l.
+  // last CTA of this (sequence, kv head): merge the splits.  One pass reads
+  // every split's (m, l) from L2 into shared memory (warp w takes heads w,
+  // w+8, ...): M = max m, weights exp(m - M), L = sum weight * l.  Then all
+  // threads accumulate the outputs: thread (item i4, part) sums the splits
+  // s = part, part + parts, ... of its 4 output values, eight loads in
+  // flight, and the parts are added in part order (fixed: results do not
+  // depend on timing).
   const float* parts = p.part + ((size_t)z * hkv + g) * p.nsplit * PSZ;
-  float* wts = reinterpret_cast<float*>(smem);  // [split][G]
-  float* inv_l = wts + kMaxSplit * G;           // [G]
+  float4* comb = reinterpret_cast<float4*>(smem);                  // [kThreadsA] (16-byte aligned)
+  float* wts = reinterpret_cast<float*>(smem + kThreadsA * 16);  // [split][G]
+  float* inv_l = wts + kMaxSplit * G;                            // [G]
+  float* msm = inv_l + G;                                        // [split][G]
+  float* lsm = msm + kMaxSplit * G;                              // [split][G]
   for (int h = warp; h < G; h += kAttnWarps) {
     float mloc = -INFINITY;
     for (int s = lane; s < nact; s += 32) {
+      const float m = __ldcg(parts + (size_t)s * PSZ + G * HD + h);
       const float l = __ldcg(parts + (size_t)s * PSZ + G * HD + G + h);
-      if (l > 0.0f) mloc = fmaxf(mloc, __ldcg(parts + (size_t)s * PSZ + G * HD + h));
+      msm[s * G + h] = m;
+      lsm[s * G + h] = l;
+      if (l > 0.0f) mloc = fmaxf(mloc, m);
     }
     const float M = warp_max(mloc);
     float lsum = 0.0f;
     for (int s = lane; s < nact; s += 32) {
-      const float l = __ldcg(parts + (size_t)s * PSZ + G * HD + G + h);
-      const float w = l > 0.0f ? expf(__ldcg(parts + (size_t)s * PSZ + G * HD + h) - M) : 0.0f;
+      const float l = lsm[s * G + h];
+      const float w = l > 0.0f ? expf(msm[s * G + h] - M) : 0.0f;
       wts[s * G + h] = w;
       lsum += w * l;
     }
@@ -253,38 +264,61 @@ EE_DEV void attention_item(const AttnParams& p, int split, int g, int z, uint8_t
     if (lane == 0) inv_l[h] = 1.0f / lsum;
   }
   __syncthreads();
-  for (int i4 = tid; i4 < G * HD / 4; i4 += kThreadsA) {
+  constexpr int NI = G * HD / 4;                                 // float4 output items
+  constexpr int NPART = NI >= kThreadsA ? 1 : kThreadsA / NI;    // threads per item
+  static_assert(NI % kThreadsA == 0 || kThreadsA % NI == 0, "item split");
+  for (int base = 0; base < NI; base += kThreadsA / NPART) {
+    const int i4 = base + tid % (kThreadsA / NPART), part = tid / (kThreadsA / NPART);
     const int h = (i4 * 4) / HD;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    int s = 0;
-    for (; s + 8 <= nact; s += 8) {
-      float4 v[8];
+    if (i4 < NI) {
+      int s = part;
+      for (; s + 7 * NPART < nact; s += 8 * NPART) {
+        float4 v[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = __ldcg(reinterpret_cast<const float4*>(parts + (size_t)(s + u) * PSZ) + i4);
+        for (int u = 0; u < 8; ++u)
+          v[u] = __ldcg(reinterpret_cast<const float4*>(parts + (size_t)(s + u * NPART) * PSZ) + i4);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float w = wts[(s + u) * G + h];
-        o.x = fmaf(w, v[u].x, o.x);
-        o.y = fmaf(w, v[u].y, o.y);
-        o.z = fmaf(w, v[u].z, o.z);
-        o.w = fmaf(w, v[u].w, o.w);
+        for (int u = 0; u < 8; ++u) {
+          const float w = wts[(s + u * NPART) * G + h];
+          o.x = fmaf(w, v[u].x, o.x);
+          o.y = fmaf(w, v[u].y, o.y);
+          o.z = fmaf(w, v[u].z, o.z);
+          o.w = fmaf(w, v[u].w, o.w);
+        }
+      }
+      for (; s < nact; s += NPART) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(parts + (size_t)s * PSZ) + i4);
+        const float w = wts[s * G + h];
+        o.x = fmaf(w, v.x, o.x);
+        o.y = fmaf(w, v.y, o.y);
+        o.z = fmaf(w, v.z, o.z);
+        o.w = fmaf(w, v.w, o.w);
       }
     }
-    for (; s < nact; ++s) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(parts + (size_t)s * PSZ) + i4);
-      const float w = wts[s * G + h];
-      o.x = fmaf(w, v.x, o.x);
-      o.y = fmaf(w, v.y, o.y);
-      o.z = fmaf(w, v.z, o.z);
-      o.w = fmaf(w, v.w, o.w);
+    if (NPART > 1) {
+      comb[tid] = o;
+      __syncthreads();
+      if (part == 0 && i4 < NI) {
+        for (int q = 1; q < NPART; ++q) {
+          const float4 t = comb[q * (kThreadsA / NPART) + tid];
+          o.x += t.x;
+          o.y += t.y;
+          o.z += t.z;
+          o.w += t.w;
+        }
+      }
+      __syncthreads();
     }
-    const float il = inv_l[h];
-    const float ov[4] = {o.x * il, o.y * il, o.z * il, o.w * il};
-    const int col0 = g * G * HD + i4 * 4;
+    if (part == 0 && i4 < NI) {
+      const float il = inv_l[h];
+      const float ov[4] = {o.x * il, o.y * il, o.z * il, o.w * il};
+      const int col0 = g * G * HD + i4 * 4;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (p.o_f32) p.o_f32[(size_t)seq * p.o_stride + col0 + u] = ov[u];
-      if (p.oh) p.oh[(size_t)seq * p.o_stride + xh_slot(col0 + u)] = float_to_half_bits(ov[u]);
+      for (int u = 0; u < 4; ++u) {
+        if (p.o_f32) p.o_f32[(size_t)seq * p.o_stride + col0 + u] = ov[u];
+        if (p.oh) p.oh[(size_t)seq * p.o_stride + xh_slot(col0 + u)] = float_to_half_bits(ov[u]);
+      }
     }
   }
   if (tid == 0) p.counters[(size_t)z * hkv + g] = 0;

@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(kThreadsA) k_attention(const AttnParams p) {
 
 template <int HD, int G>
 cudaError_t set_attr_t() {
-  static_assert(kMaxSplit * G * 4 + G * 4 <= kKvSmem, "merge scratch");
+  static_assert(kThreadsA * 16 + 3 * kMaxSplit * G * 4 + G * 4 <= kKvSmem, "merge scratch");
   static_assert(kAttnWarps * (G * HD + 8 * G) * 4 <= kKvSmem, "warp partials");
   return cudaFuncSetAttribute(k_attention<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvSmem);
 }

@@ -14,9 +14,9 @@
 //    is the producers' work, so the smaller tile halves it.
 //  * exit sub-batch (int4 weights, MODE 1): the int4 copy is kept in a
 //    layout of its own (k_int4_tc_layout): per 128-row tile and 64-column K
-//    step one contiguous block of 128 rows x 32 bytes of nibbles and the
-//    rows' 128 bf16 scales (4352 bytes), which one bulk copy brings into a
-//    shared-memory ring.  Producer warps dequantise their row of it to fp16
+//    step one contiguous block of two halves (columns 0-31, 32-63), each 128
+//    rows x 16 bytes of nibbles, then the rows' 128 bf16 scales (4352
+//    bytes), which one bulk copy brings into a shared-memory ring.  Producer warps dequantise their row of it to fp16
 //    q * s (exact: an 8-bit scale times a 4-bit integer fits fp16's 11
 //    bits) and store it into the swizzled A tile; B holds the fp16
 //    activations (N = 32 for lists of up to 32 sequences, else 64).  The
@@ -301,7 +301,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
         }
         if constexpr (MODE == 1) {
           // A: row tid of the tile, the stage's 64 columns, from the raw
-          // block (row tid's 8 words, then its scale).  Word j holds columns
+          // block (row tid's 4 words in each half -- a warp reads 512
+          // contiguous bytes per half -- then its scale).  Word j holds columns
           // c = 8j .. c+7 as nibbles (c, c+2, c+4, c+6 | c+1, c+3, c+5, c+7):
           // one masking LOP3 per pair puts (c, c+1) or (c+4, c+5) under the
           // fp16 exponent of 1024 with the sign bits flipped (1024 + q + 8),
@@ -313,8 +314,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
             break;
           }
           const uint8_t* blk = raw_ring + (size_t)rs * kQ4Block;
-          const uint4 w0 = *reinterpret_cast<const uint4*>(blk + tid * 32);
-          const uint4 w1 = *reinterpret_cast<const uint4*>(blk + tid * 32 + 16);
+          const uint4 w0 = *reinterpret_cast<const uint4*>(blk + tid * 16);
+          const uint4 w1 = *reinterpret_cast<const uint4*>(blk + (kBM + tid) * 16);
           const uint16_t sb = *reinterpret_cast<const uint16_t*>(blk + kBM * 32 + tid * 2);
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh.raw_free[rs]);  // this warp is done reading the block
@@ -486,7 +487,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
 }  // namespace
 
 // Row-layout int4 copy -> the tensor-core GEMM's blocks: thread per word of
-// a (tile, K step) block, then per scale.  Word j of row r holds columns
+// a (tile, K step) block, then per scale.  Word j of row r sits in half
+// j / 4 at (j / 4) * 128 * 16 + r * 16 + (j % 4) * 4 and holds columns
 // c = 64 ks + 8j .. c+7 of row 128 t + r with nibble i = column c + 2i (i < 4)
 // or c + 2(i - 4) + 1: the row layout's word at the same columns with its
 // even-column nibbles moved to the low half and its odd ones to the high
@@ -510,7 +512,7 @@ __global__ void __launch_bounds__(256) k_int4_tc_layout(const uint8_t* __restric
         w |= v << (4 * dst);
       }
     }
-    *reinterpret_cast<uint32_t*>(out + (size_t)blk * kQ4Block + (size_t)r * 32 + j * 4) = w;
+    *reinterpret_cast<uint32_t*>(out + (size_t)blk * kQ4Block + (size_t)((j >> 2) * kBM + r) * 16 + (j & 3) * 4) = w;
   } else if (idx < words + scales) {
     const long long i = idx - words;
     const int r = (int)(i % kBM);
