@@ -114,15 +114,16 @@ def w_bytes(N, K, int4):
     return N * K * 2
 
 
-def launch_bytes(sh, ckpts, kind, layer, exits, ctxs):
+def launch_bytes(sh, ckpts, kind, layer, exits, ctxs, lists="both"):
     """Algorithmic bytes one launch must read: the weights of the sub-batches
     it serves (bf16 rows of sequences still on the backbone, int4 rows of
-    exited ones), the head tensors, or the K/V history."""
+    exited ones; a tensor-core launch serves one list, `lists` "full" or
+    "exit", the GEMV both), the head tensors, or the K/V history."""
     mats = mat_list(sh)
     if kind in mats:
         N, K = mats[kind]
-        full = any(e >= layer for e in exits)
-        ex = any(e < layer for e in exits)
+        full = lists in ("both", "full") and any(e >= layer for e in exits)
+        ex = lists in ("both", "exit") and any(e < layer for e in exits)
         return full * w_bytes(N, K, False) + ex * w_bytes(N, K, True)
     d, V = sh.d_model, sh.vocab
     if kind in ("head_t", "head_e"):
@@ -435,15 +436,16 @@ def kernel_roofline(sh, ckpts, prof, peak):
     """Achieved HBM bandwidth of the GEMV kernel (every projection, exit-head and
     LM-head launch) and of the attention kernel from the profiled launches.
     A launch's duration is its own (first CTA start to last CTA end) where the
-    kernel records it, else the event pair around it (which adds the launch
-    gap); the shares use the event times throughout."""
+    kernel records it (the GEMV and the tensor-core GEMM), else the event
+    pair around it (which adds the launch gap); the shares use the event
+    times throughout."""
     lin = ("qkv", "o", "gateup", "down", "head_t", "head_e", "final_head")
     acc = {"linear": [0, 0.0, 0], "attn": [0, 0.0, 0]}
     per_kind = {}
-    own = [0, 0]  # GEMV launches timed by the kernel itself, all GEMV launches
+    own = [0, 0]  # projection and head launches timed by the kernel itself, all of them
     for recs, exits, ctx in prof:
-        for kind, layer, ms, kms in recs:
-            b = launch_bytes(sh, ckpts, kind, layer, exits, ctx)
+        for kind, layer, ms, kms, lists in recs:
+            b = launch_bytes(sh, ckpts, kind, layer, exits, ctx, lists)
             key = "linear" if kind in lin else ("attn" if kind == "attn" else None)
             pk = per_kind.setdefault(kind, [0, 0.0, 0])
             pk[0] += b

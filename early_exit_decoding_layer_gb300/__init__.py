@@ -38,6 +38,7 @@ EXPORTS = (
     "ee_set_prefill_exit", "ee_prefill_exit_layers",
 )
 
+LISTS = ("both", "full", "exit")  # EE_LISTS_*
 KINDS = ("begin", "norm", "qkv", "attn", "o", "gateup", "down", "head_norm", "head_t", "head_e",
          "final_norm", "final_head", "exit_sts")
 
@@ -70,7 +71,7 @@ class EESharedWeights(ctypes.Structure):
 
 
 class EELaunchRecord(ctypes.Structure):
-    _fields_ = [("kind", c_i32), ("layer", c_i32), ("ms", c_f32), ("kernel_ms", c_f32)]
+    _fields_ = [("kind", c_i32), ("layer", c_i32), ("ms", c_f32), ("kernel_ms", c_f32), ("lists", c_i32)]
 
 
 class EEWeights(ctypes.Structure):
@@ -336,13 +337,15 @@ class DecodeEngine:
         self._check(self.lib.ee_set_profile(self.ctx, 1 if profile else 0))
 
     def profile_read(self):
-        """[(kind name, layer, ms, kernel_ms)] of the last profiled step's
-        launches (kernel_ms: the GEMV's own time, else 0)."""
+        """[(kind name, layer, ms, kernel_ms, lists)] of the last profiled
+        step's launches (kernel_ms: the GEMV's or tensor-core GEMM's own time,
+        else 0; lists: "both", "full" or "exit", the sub-batch lists the
+        launch serves)."""
         n = c_i32()
         self._check(self.lib.ee_profile_read(self.ctx, None, 0, ctypes.byref(n)))
         recs = (EELaunchRecord * max(1, n.value))()
         self._check(self.lib.ee_profile_read(self.ctx, recs, n.value, ctypes.byref(n)))
-        return [(KINDS[r.kind], r.layer, r.ms, r.kernel_ms) for r in recs[: n.value]]
+        return [(KINDS[r.kind], r.layer, r.ms, r.kernel_ms, LISTS[r.lists]) for r in recs[: n.value]]
 
     # -- inspection ----------------------------------------------------------
     def debug_hidden(self, layer: int) -> np.ndarray:

@@ -167,7 +167,10 @@ struct ee_ctx {
   // own start/end stamps ([0, kProfMax) starts, [kProfMax, 2 kProfMax) ends)
   int profile = 0;
   std::vector<cudaEvent_t> prof_ev;
-  std::vector<std::pair<int, int>> prof_tag;  // (kind, layer) per launch of the last step
+  struct ProfTag {
+    int kind, layer, lists;
+  };
+  std::vector<ProfTag> prof_tag;  // per launch of the last step
   std::vector<float> prof_ms, prof_kernel_ms;
   unsigned long long* prof_stamp = nullptr;
   int launches[2] = {0, 0};                   // kernels per step without / with heads
@@ -373,13 +376,13 @@ struct LaunchLog {
     }
     return EE_OK;
   }
-  ee_status after(int kind, int layer) {
+  ee_status after(int kind, int layer, int lists = EE_LISTS_BOTH) {
     ++n;
     if (!prof) return EE_OK;
     while ((int)c->prof_ev.size() < n + 1)
       if (add_event() != EE_OK) return EE_ERR_CUDA;
     EE_CUDA(c, cudaEventRecord(c->prof_ev[n], c->st));
-    c->prof_tag.emplace_back(kind, layer);
+    c->prof_tag.push_back(ee_ctx::ProfTag{kind, layer, lists});
     return EE_OK;
   }
   ee_status add_event() {
@@ -390,14 +393,15 @@ struct LaunchLog {
   }
 };
 
-#define EE_LAUNCH(log, kind, layer, call) \
-  do {                                    \
-    ee_status s_ = (log).before();        \
-    if (s_ != EE_OK) return s_;           \
-    EE_CUDA(c, (call));                   \
-    s_ = (log).after((kind), (layer));    \
-    if (s_ != EE_OK) return s_;           \
+#define EE_LAUNCH_L(log, kind, layer, lists, call) \
+  do {                                             \
+    ee_status s_ = (log).before();                 \
+    if (s_ != EE_OK) return s_;                    \
+    EE_CUDA(c, (call));                            \
+    s_ = (log).after((kind), (layer), (lists));    \
+    if (s_ != EE_OK) return s_;                    \
   } while (0)
+#define EE_LAUNCH(log, kind, layer, call) EE_LAUNCH_L(log, kind, layer, EE_LISTS_BOTH, call)
 
 // ---------------------------------------------------------------- step enqueue
 ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
@@ -494,8 +498,19 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
         tp.tile_cnt = c->tc_cnt;
         // the exit list is empty until a head has run (no launch for it then)
         const bool exit_rows = heads && m.nck > 0 && layer > c->ckpts[0];
-        if (lp.w) EE_LAUNCH(log, kind, layer, launch_gemm_tc(tp, 0, c->pdl, st));
-        if (lp.wq && lp.wq4t && exit_rows) EE_LAUNCH(log, kind, layer, launch_gemm_tc(tp, 1, c->pdl, st));
+        auto stamps = [&](TcParams& t) {  // this launch's own start/end stamps (profiled steps)
+          const bool on = prof && log.n < kProfMax;
+          t.lp.stamp_start = on ? c->prof_stamp + log.n : nullptr;
+          t.lp.stamp_end = on ? c->prof_stamp + kProfMax + log.n : nullptr;
+        };
+        if (lp.w) {
+          stamps(tp);
+          EE_LAUNCH_L(log, kind, layer, EE_LISTS_FULL, launch_gemm_tc(tp, 0, c->pdl, st));
+        }
+        if (lp.wq && lp.wq4t && exit_rows) {
+          stamps(tp);
+          EE_LAUNCH_L(log, kind, layer, EE_LISTS_EXIT, launch_gemm_tc(tp, 1, c->pdl, st));
+        }
         return EE_OK;
       }
     }
@@ -1148,8 +1163,9 @@ ee_status ee_profile_read(ee_ctx* c, ee_launch_record* out, int32_t cap, int32_t
   *n = (int32_t)c->prof_ms.size();
   if (out)
     for (int i = 0; i < *n && i < cap; ++i)
-      out[i] = ee_launch_record{c->prof_tag[i].first, c->prof_tag[i].second, c->prof_ms[i],
-                                i < (int)c->prof_kernel_ms.size() ? c->prof_kernel_ms[i] : 0.0f};
+      out[i] = ee_launch_record{c->prof_tag[i].kind, c->prof_tag[i].layer, c->prof_ms[i],
+                                i < (int)c->prof_kernel_ms.size() ? c->prof_kernel_ms[i] : 0.0f,
+                                c->prof_tag[i].lists};
   return EE_OK;
 }
 

@@ -131,7 +131,7 @@ struct TcShared {
 };
 
 template <int MODE>
-__global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant__ TcParams tp) {
+__device__ __forceinline__ void gemm_tc_body(const TcParams& tp) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ TcShared sh;
   uint8_t* tiles = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -482,6 +482,17 @@ __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant
     if (!sh.last) return;
     head_finalize_group(p, tp.ntiles, sh.lf, sh.le, ncol, sh.res, 128);
   }
+}
+
+// Profiled steps pass stamp pointers: thread 0 of every CTA records the
+// kernel's first start (atomic min) and last end (atomic max) of
+// %globaltimer.  Thread 0 passes every barrier of its CTA and returns from
+// the body last, so its end is the CTA's end.
+template <int MODE>
+__global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant__ TcParams tp) {
+  if (tp.lp.stamp_start && threadIdx.x == 0) atomicMin(tp.lp.stamp_start, (unsigned long long)globaltimer());
+  gemm_tc_body<MODE>(tp);
+  if (tp.lp.stamp_end && threadIdx.x == 0) atomicMax(tp.lp.stamp_end, (unsigned long long)globaltimer());
 }
 
 }  // namespace

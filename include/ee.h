@@ -281,13 +281,21 @@ enum {
   EE_K_FINAL_HEAD = 11, /* final LM head, argmax                         */
   EE_K_EXIT_STS = 12    /* checkpoint: similarity score + exit decision   */
 };
+/* Sub-batch lists a projection or head launch serves (ee_launch_record.lists). */
+enum {
+  EE_LISTS_BOTH = 0,  /* the GEMV: the full list on bf16 weights and the exit list on int4 in one launch
+                         (also every launch that is not a projection or head) */
+  EE_LISTS_FULL = 1,  /* tensor-core GEMM launch for the full list (bf16 weights) */
+  EE_LISTS_EXIT = 2   /* tensor-core GEMM launch for the exit list (int4 weights) */
+};
 typedef struct {
   int32_t kind;     /* EE_K_* */
   int32_t layer;    /* decoder layer, or -1 */
   float ms;         /* device time between events around the launch */
-  float kernel_ms;  /* GEMV launches: the kernel's own time, first CTA start
-                       to last CTA end (%globaltimer), no launch gaps; 0 for
-                       the other kernels */
+  float kernel_ms;  /* GEMV and tensor-core GEMM launches: the kernel's own
+                       time, first CTA start to last CTA end (%globaltimer),
+                       no launch gaps; 0 for the other kernels */
+  int32_t lists;    /* EE_LISTS_* */
 } ee_launch_record;
 
 /* profile = 1: the following decode steps run without the CUDA graph and

@@ -51,6 +51,13 @@ def test_launch_bytes_heads_after_every_exit_read_nothing():
     assert bench.launch_bytes(sh, w.checkpoints, "head_e", 8, [4], [100]) == 0
     assert bench.launch_bytes(sh, w.checkpoints, "head_e", 8, [4, 31], [100, 100]) == E
     assert bench.launch_bytes(sh, w.checkpoints, "final_head", -1, [4], [100]) == E
+    # a layer with sequences on both paths: the GEMV reads both copies, each
+    # tensor-core launch only its own list's
+    bf16 = bench.w_bytes(*bench.mat_list(sh)["gateup"], False)
+    q4 = bench.w_bytes(*bench.mat_list(sh)["gateup"], True)
+    assert bench.launch_bytes(sh, w.checkpoints, "gateup", 10, [4, 31], [100, 100]) == bf16 + q4
+    assert bench.launch_bytes(sh, w.checkpoints, "gateup", 10, [4, 31], [100, 100], "full") == bf16
+    assert bench.launch_bytes(sh, w.checkpoints, "gateup", 10, [4, 31], [100, 100], "exit") == q4
 
 
 def test_step_bytes_mixed_batch_reads_each_matrix_once():

@@ -112,3 +112,36 @@ def test_tiny_batch40_wide_b_tile():
     print("tiny b=40 parity:", st)
     parity.check_kv(eng, orc)
     eng.close()
+
+
+def test_profiled_step_records_own_times_and_lists():
+    """A profiled step at batch 12: every projection and head launch carries
+    its own kernel time (globaltimer stamps, no launch gap), the tensor-core
+    GEMM launches name the one list they serve, and the profiled step's
+    tokens and exits equal those of the graph-replayed step."""
+    B = 12
+    lens = [5, 16, 17, 31, 9, 12, 20, 3, 33, 15, 8, 26]
+    pr = synth.prompts(TINY.shape, 41, lens)
+    gamma = [-np.inf, np.inf]   # everyone leaves at the first checkpoint
+    runs = []
+    for profile in (False, True):
+        eng = parity.load_engine(TINY, max_batch=16, max_seq_len=64)
+        eng.set_thresholds(np.asarray(gamma))
+        tok = eng.prefill(pr)
+        tok, ex = eng.decode_step(tok)
+        eng.set_profile(profile)
+        tok2, ex2 = eng.decode_step(tok)
+        runs.append((tok2.copy(), ex2.copy(), eng.profile_read() if profile else None))
+        eng.close()
+    assert np.array_equal(runs[0][0], runs[1][0]) and np.array_equal(runs[0][1], runs[1][1])
+    recs = runs[1][2]
+    proj = [r for r in recs if r[0] in ("qkv", "o", "gateup", "down", "head_t", "head_e", "final_head")]
+    assert proj and all(r[3] > 0 for r in proj), [r for r in proj if r[3] <= 0][:4]
+    assert all(r[3] <= r[2] * 1.5 + 0.05 for r in proj)     # own time within the event pair (loose)
+    ck = TINY.checkpoints[0]
+    # after the exit at the first checkpoint the projections run on the exit list's int4 copy
+    late = [r for r in proj if r[0] in ("qkv", "o", "gateup", "down") and r[1] > ck]
+    assert late and {r[4] for r in late} >= {"exit"}, late[:4]
+    early = [r for r in proj if r[0] in ("qkv", "o", "gateup", "down") and r[1] <= ck]
+    assert early and {r[4] for r in early} == {"full"}, early[:4]
+    assert all(r[4] == "both" for r in recs if r[0] in ("attn", "begin", "norm"))
