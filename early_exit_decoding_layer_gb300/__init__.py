@@ -38,7 +38,7 @@ EXPORTS = (
     "ee_set_prefill_exit", "ee_prefill_exit_layers",
 )
 
-LISTS = ("both", "full", "exit")  # EE_LISTS_*
+LISTS = ("both", "full")  # EE_LISTS_*
 KINDS = ("begin", "norm", "qkv", "attn", "o", "gateup", "down", "head_norm", "head_t", "head_e",
          "final_norm", "final_head", "exit_sts")
 
@@ -339,8 +339,8 @@ class DecodeEngine:
     def profile_read(self):
         """[(kind name, layer, ms, kernel_ms, lists)] of the last profiled
         step's launches (kernel_ms: the GEMV's or tensor-core GEMM's own time,
-        else 0; lists: "both", "full" or "exit", the sub-batch lists the
-        launch serves)."""
+        else 0; lists: "both" or "full", the sub-batch lists the launch
+        serves)."""
         n = c_i32()
         self._check(self.lib.ee_profile_read(self.ctx, None, 0, ctypes.byref(n)))
         recs = (EELaunchRecord * max(1, n.value))()

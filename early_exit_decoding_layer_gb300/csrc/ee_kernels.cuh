@@ -137,8 +137,9 @@ struct TcParams {
   LinearParams lp;      // shapes, lists, activations, epilogue (as for the GEMV)
   const uint8_t* q4t;   // MODE 1: the int4 copy in blocks (int4_tc_layout_bytes)
   int32_t ntiles, ksplit, nks, nk;  // tiles, K splits, 64-wide K steps per split, K steps
-  float* part;          // [tile][split][64 columns][128 rows] fp32 partial sums
-  int32_t* tile_cnt;    // [ntiles] split counters, zero between launches
+  int32_t modes;        // 1: the full list's units (bf16) only; 2: then the exit list's (int4)
+  float* part;          // [mode][tile][split][64 columns][128 rows] fp32 partial sums
+  int32_t* tile_cnt;    // [mode][ntiles] split counters, zero between launches
 };
 struct TcPlan {
   int ntiles, ksplit, nks, nk;
@@ -148,7 +149,7 @@ TcPlan gemm_tc_plan(int N, int K, int num_sms, int max_units);
 bool gemm_tc_shape_ok(int K);
 size_t gemm_tc_part_floats(int units);
 cudaError_t gemm_tc_prepare();
-cudaError_t launch_gemm_tc(const TcParams& tp, int mode, bool pdl, cudaStream_t st);
+cudaError_t launch_gemm_tc(const TcParams& tp, bool pdl, cudaStream_t st);
 // The int4 copy for MODE 1: per 128-row tile and 64-column K step, one
 // block of 128 rows x 32 bytes of nibbles and 128 bf16 scales.
 size_t int4_tc_layout_bytes(int rows, int cols);

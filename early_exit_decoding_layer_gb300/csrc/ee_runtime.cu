@@ -281,7 +281,7 @@ size_t carve(ee_ctx* c, const ee_config& cfg, uint8_t* base) {
   float* hin = cv.take<float>((size_t)2 * EE_MAX_BATCH * m.d);
   float* stss = cv.take<float>(EE_MAX_BATCH);
   const bool tc = m.maxb >= kTcMinBatch;
-  float* tcpart = tc ? cv.take<float>(gemm_tc_part_floats(kTcMaxUnits)) : nullptr;
+  float* tcpart = tc ? cv.take<float>(gemm_tc_part_floats(2 * kTcMaxUnits)) : nullptr;  // per list
   StepDesc* desc = cv.take<StepDesc>(1);
   StepOut* out = cv.take<StepOut>(1);
   float* gam = cv.take<float>(EE_MAX_CHECKPOINTS);
@@ -292,7 +292,7 @@ size_t carve(ee_ctx* c, const ee_config& cfg, uint8_t* base) {
   int32_t* hcnt = cv.take<int32_t>(64);
   int32_t* dflag = cv.take<int32_t>(1);
   int32_t* stsc = cv.take<int32_t>(1);
-  int32_t* tccnt = tc ? cv.take<int32_t>(kTcMaxTiles) : nullptr;
+  int32_t* tccnt = tc ? cv.take<int32_t>(2 * kTcMaxTiles) : nullptr;  // per list
   const size_t ze = align_up(cv.off, kAlign);
   const size_t stg = 2 * (size_t)std::max({(size_t)m.F * m.d, (size_t)m.dq * m.d, (size_t)m.d * m.d,
                                           (size_t)m.dk * m.d});
@@ -496,21 +496,14 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
         tp.part = c->tc_part;
         tp.q4t = lp.wq4t;
         tp.tile_cnt = c->tc_cnt;
-        // the exit list is empty until a head has run (no launch for it then)
+        // the exit list is empty until a head has run (no units for it then)
         const bool exit_rows = heads && m.nck > 0 && layer > c->ckpts[0];
-        auto stamps = [&](TcParams& t) {  // this launch's own start/end stamps (profiled steps)
-          const bool on = prof && log.n < kProfMax;
-          t.lp.stamp_start = on ? c->prof_stamp + log.n : nullptr;
-          t.lp.stamp_end = on ? c->prof_stamp + kProfMax + log.n : nullptr;
-        };
-        if (lp.w) {
-          stamps(tp);
-          EE_LAUNCH_L(log, kind, layer, EE_LISTS_FULL, launch_gemm_tc(tp, 0, c->pdl, st));
-        }
-        if (lp.wq && lp.wq4t && exit_rows) {
-          stamps(tp);
-          EE_LAUNCH_L(log, kind, layer, EE_LISTS_EXIT, launch_gemm_tc(tp, 1, c->pdl, st));
-        }
+        tp.modes = lp.wq && lp.wq4t && exit_rows ? 2 : 1;
+        const bool on = prof && log.n < kProfMax;  // this launch's own start/end stamps (profiled steps)
+        tp.lp.stamp_start = on ? c->prof_stamp + log.n : nullptr;
+        tp.lp.stamp_end = on ? c->prof_stamp + kProfMax + log.n : nullptr;
+        if (lp.w)
+          EE_LAUNCH_L(log, kind, layer, tp.modes == 2 ? EE_LISTS_BOTH : EE_LISTS_FULL, launch_gemm_tc(tp, c->pdl, st));
         return EE_OK;
       }
     }
@@ -1179,20 +1172,12 @@ ee_status ee_step_io(const ee_ctx* c, int32_t batch, int32_t heads, size_t* h2d,
     // O, gate/up, down) + heads (norm, T, E) + final norm and head
     const int with_heads = heads && c->m.nck > 0;
     const int norms = linear_stages_x(batch, c->m.d) ? 0 : 1;
-    // the tensor-core GEMM launches once per sub-batch list (full, and exit
-    // for the layers after the first checkpoint when heads run)
+    // the tensor-core GEMM serves both sub-batch lists in one launch
     const bool tc = c->tc && batch >= kTcMinBatch;
-    const int exit_layers = with_heads ? c->m.L - 1 - c->ckpts[0] : 0;
     const int per_layer = 5 + 2 * norms;
     // the similarity criterion replaces each head's launches by one decision launch
     const int per_ckpt = c->criterion == EE_EXIT_MAXPROB ? 2 + norms : 1;
-    // with exit-head tokens the last layer's exit rows run only their QKV
-    const int dead = tc && with_heads && exit_layers > 0 && c->criterion == EE_EXIT_MAXPROB &&
-                             c->token_source == EE_TOKEN_EXIT_HEAD
-                         ? 3
-                         : 0;
-    *launches = 1 + per_layer * c->m.L + (tc ? 4 * exit_layers - dead : 0) +
-                (with_heads ? per_ckpt * c->m.nck : 0) + 1 + norms;
+    *launches = 1 + per_layer * c->m.L + (with_heads ? per_ckpt * c->m.nck : 0) + 1 + norms;
   }
   return EE_OK;
 }

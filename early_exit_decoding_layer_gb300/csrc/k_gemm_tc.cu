@@ -30,6 +30,10 @@
 // counter, nothing waits) adds them in split order, so results do not depend
 // on timing, and runs the epilogue shared with the GEMV (RoPE + K/V write,
 // residual, SwiGLU, fp16 output) or the vocabulary-head statistics.
+// One launch serves both lists of a projection: the full list's units come
+// first in the grid, then (where sequences may have exited) the exit list's,
+// each with partials and counters of its own.  A list that is empty returns
+// at once, so its CTAs leave room for the other list's in the same launch.
 #include <cuda.h>
 #include <math.h>
 
@@ -131,13 +135,13 @@ struct TcShared {
 };
 
 template <int MODE>
-__device__ __forceinline__ void gemm_tc_body(const TcParams& tp) {
+__device__ __forceinline__ void gemm_tc_body(const TcParams& tp, TcShared& sh, int unit) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ TcShared sh;
   uint8_t* tiles = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const LinearParams& p = tp.lp;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int unit = blockIdx.x, tile = unit / tp.ksplit, split = unit - tile * tp.ksplit;
+  const int tile = unit / tp.ksplit, split = unit - tile * tp.ksplit;
+  const int units = tp.ntiles * tp.ksplit;  // per list
   const int row0 = tile * kBM;
   const int ks0 = split * tp.nks, ks1 = min(tp.nk, ks0 + tp.nks);  // K steps of this unit
   const int nks = ks1 - ks0;
@@ -352,7 +356,7 @@ __device__ __forceinline__ void gemm_tc_body(const TcParams& tp) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const int rl = warp * 32 + lane;  // tile row = TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
-    float* part = tp.part + (size_t)unit * kCols * kBM;
+    float* part = tp.part + ((size_t)MODE * units + unit) * kCols * kBM;
     for (int c0 = 0; c0 < ncol; c0 += 16) {
       uint32_t v[16], w[16];
       asm volatile(
@@ -384,7 +388,7 @@ __device__ __forceinline__ void gemm_tc_body(const TcParams& tp) {
   // the last CTA of this tile adds the splits in order and runs the epilogue
   if (tid == 0) {
     __threadfence();
-    const int old = tp.ksplit > 1 ? atomicAdd(tp.tile_cnt + tile, 1) : 0;
+    const int old = tp.ksplit > 1 ? atomicAdd(tp.tile_cnt + MODE * tp.ntiles + tile, 1) : 0;
     sh.last = (old == tp.ksplit - 1);
   }
   __syncthreads();
@@ -393,7 +397,7 @@ __device__ __forceinline__ void gemm_tc_body(const TcParams& tp) {
   if (warp >= 4) return;
   const int rl = warp * 32 + lane;
   const int r = row0 + rl;
-  const float* parts = tp.part + (size_t)tile * tp.ksplit * kCols * kBM;
+  const float* parts = tp.part + ((size_t)MODE * units + (size_t)tile * tp.ksplit) * kCols * kBM;
   // per-column values once (one round trip), not per row pair
   if (tid < ncol && p.epi != EPI_HEAD) sh.col[tid] = epi_seq(p, lst[1 + tid]);
   asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -470,7 +474,7 @@ __device__ __forceinline__ void gemm_tc_body(const TcParams& tp) {
       }
     }
   }
-  if (tid == 0 && tp.ksplit > 1) tp.tile_cnt[tile] = 0;
+  if (tid == 0 && tp.ksplit > 1) tp.tile_cnt[MODE * tp.ntiles + tile] = 0;
   if (p.epi == EPI_HEAD) {
     // the last tile to finish merges the vocabulary partials
     if (tid == 0) {
@@ -488,10 +492,14 @@ __device__ __forceinline__ void gemm_tc_body(const TcParams& tp) {
 // kernel's first start (atomic min) and last end (atomic max) of
 // %globaltimer.  Thread 0 passes every barrier of its CTA and returns from
 // the body last, so its end is the CTA's end.
-template <int MODE>
 __global__ void __launch_bounds__(kTcThreads, 2) k_gemm_tc(const __grid_constant__ TcParams tp) {
+  __shared__ TcShared sh;
   if (tp.lp.stamp_start && threadIdx.x == 0) atomicMin(tp.lp.stamp_start, (unsigned long long)globaltimer());
-  gemm_tc_body<MODE>(tp);
+  const int units = tp.ntiles * tp.ksplit;
+  if ((int)blockIdx.x < units)
+    gemm_tc_body<0>(tp, sh, blockIdx.x);
+  else
+    gemm_tc_body<1>(tp, sh, blockIdx.x - units);
   if (tp.lp.stamp_end && threadIdx.x == 0) atomicMax(tp.lp.stamp_end, (unsigned long long)globaltimer());
 }
 
@@ -580,11 +588,7 @@ cudaError_t launch_int4_tc_layout(const uint8_t* packed, const uint16_t* scales,
 }
 
 cudaError_t gemm_tc_prepare() {
-  cudaError_t e;
-  if ((e = cudaFuncSetAttribute(k_gemm_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem<0>)) !=
-      cudaSuccess)
-    return e;
-  return cudaFuncSetAttribute(k_gemm_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem<1>);
+  return cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem<0>);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -612,19 +616,19 @@ bool encode_weight_map(CUtensorMap* map, const uint16_t* w, int N, int K) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t launch_gemm_tc(const TcParams& tp, int mode, bool pdl, cudaStream_t st) {
+cudaError_t launch_gemm_tc(const TcParams& tp, bool pdl, cudaStream_t st) {
+  if (tp.modes < 1 || tp.modes > 2 || (tp.modes == 2 && !tp.q4t)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(tp.ntiles * tp.ksplit);
+  cfg.gridDim = dim3(tp.ntiles * tp.ksplit * tp.modes);
   cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = mode == 0 ? kTcSmem<0> : kTcSmem<1>;
+  cfg.dynamicSmemBytes = kTcSmem<0>;  // MODE 1's layout fits in MODE 0's
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (mode == 0) return cudaLaunchKernelEx(&cfg, k_gemm_tc<0>, tp);
-  return cudaLaunchKernelEx(&cfg, k_gemm_tc<1>, tp);
+  return cudaLaunchKernelEx(&cfg, k_gemm_tc, tp);
 }
 
 }  // namespace ee

@@ -283,10 +283,11 @@ enum {
 };
 /* Sub-batch lists a projection or head launch serves (ee_launch_record.lists). */
 enum {
-  EE_LISTS_BOTH = 0,  /* the GEMV: the full list on bf16 weights and the exit list on int4 in one launch
-                         (also every launch that is not a projection or head) */
-  EE_LISTS_FULL = 1,  /* tensor-core GEMM launch for the full list (bf16 weights) */
-  EE_LISTS_EXIT = 2   /* tensor-core GEMM launch for the exit list (int4 weights) */
+  EE_LISTS_BOTH = 0,  /* the full list on bf16 weights and the exit list on int4 in one launch: the
+                         GEMV, and the tensor-core GEMM after the first checkpoint (also every
+                         launch that is not a projection or head) */
+  EE_LISTS_FULL = 1   /* the full list only: tensor-core GEMM launches up to the first checkpoint,
+                         and the heads */
 };
 typedef struct {
   int32_t kind;     /* EE_K_* */

@@ -30,8 +30,8 @@ def test_launches_per_step_count_both_sub_batches():
     _, _, n1 = eng.step_io(1, True)
     _, _, n12 = eng.step_io(12, True)
     assert n1 == 1 + 5 * L + 2 * nck + 1          # GEMV path: norms applied while staging
-    # norm kernels; the exit sub-batch has its own launches after the first checkpoint
-    assert n12 == 1 + (1 + 4 + 2) * L + 4 * (L - 1 - TINY.checkpoints[0]) + 3 * nck + 2
+    # norm kernels; one tensor-core launch serves both sub-batch lists
+    assert n12 == 1 + (1 + 4 + 2) * L + 3 * nck + 2
     _, _, n12_off = eng.step_io(12, False)
     assert n12_off == 1 + (1 + 4 + 2) * L + 2
     eng.close()
@@ -117,8 +117,10 @@ def test_tiny_batch40_wide_b_tile():
 def test_profiled_step_records_own_times_and_lists():
     """A profiled step at batch 12: every projection and head launch carries
     its own kernel time (globaltimer stamps, no launch gap), the tensor-core
-    GEMM launches name the one list they serve, and the profiled step's
-    tokens and exits equal those of the graph-replayed step."""
+    GEMM launches name the lists they serve (the full list alone up to the
+    first checkpoint, both lists after it), the step launches as many
+    kernels as ee_step_io states, and the profiled step's tokens and exits
+    equal those of the graph-replayed step."""
     B = 12
     lens = [5, 16, 17, 31, 9, 12, 20, 3, 33, 15, 8, 26]
     pr = synth.prompts(TINY.shape, 41, lens)
@@ -131,17 +133,18 @@ def test_profiled_step_records_own_times_and_lists():
         tok, ex = eng.decode_step(tok)
         eng.set_profile(profile)
         tok2, ex2 = eng.decode_step(tok)
-        runs.append((tok2.copy(), ex2.copy(), eng.profile_read() if profile else None))
+        runs.append((tok2.copy(), ex2.copy(), eng.profile_read() if profile else None, eng.step_io(B, True)[2]))
         eng.close()
     assert np.array_equal(runs[0][0], runs[1][0]) and np.array_equal(runs[0][1], runs[1][1])
     recs = runs[1][2]
+    assert len(recs) == runs[1][3], (len(recs), runs[1][3])
     proj = [r for r in recs if r[0] in ("qkv", "o", "gateup", "down", "head_t", "head_e", "final_head")]
     assert proj and all(r[3] > 0 for r in proj), [r for r in proj if r[3] <= 0][:4]
     assert all(r[3] <= r[2] * 1.5 + 0.05 for r in proj)     # own time within the event pair (loose)
     ck = TINY.checkpoints[0]
-    # after the exit at the first checkpoint the projections run on the exit list's int4 copy
+    # after the first checkpoint one launch serves both lists (bf16 units, then int4 units)
     late = [r for r in proj if r[0] in ("qkv", "o", "gateup", "down") and r[1] > ck]
-    assert late and {r[4] for r in late} >= {"exit"}, late[:4]
+    assert late and {r[4] for r in late} == {"both"}, late[:4]
     early = [r for r in proj if r[0] in ("qkv", "o", "gateup", "down") and r[1] <= ck]
     assert early and {r[4] for r in early} == {"full"}, early[:4]
     assert all(r[4] == "both" for r in recs if r[0] in ("attn", "begin", "norm"))
