@@ -41,6 +41,7 @@ import synth  # noqa: E402
 DEFAULT_WORKLOAD = "llama3.1-8b-b1"
 B32_WORKLOAD = "llama3.1-8b-b32"
 SMALL_WORKLOAD = "llama3.2-1b-b1"
+LARGE_WORKLOAD = "codellama-34b-b8"
 METRIC = "decoded tokens/s"
 L2_BYTES = 129 * 1024 * 1024
 
@@ -710,6 +711,32 @@ def run_ours(args):
             "kernels": r1["kr"],
         }
         r1["eng"].close()
+    if rank == 0 and world == 1 and args.with_34b and w.name == DEFAULT_WORKLOAD:
+        # the CodeLlama-34B shape at batch 8 (4096-token prompts): the exit run
+        # and the forced no-exit run only (each run re-prefills 8 x 4096 tokens)
+        import copy
+        import gc
+        gc.collect()
+        torch.cuda.empty_cache()
+        w34 = synth.WORKLOADS[LARGE_WORKLOAD]
+        a34 = copy.copy(args)
+        a34.exit_head_token = False
+        a34.sts = False
+        r34 = run_workload(ee, w34, a34, st, rank, world, peak, args.steps_34b, 1)
+        m34, n34 = r34["main"], r34["nox"]
+        line["b8_" + w34.shape.name] = {
+            "workload": w34.name, "steps": args.steps_34b, "value": m34["value"], "unit": "tokens/s",
+            "ms_per_step": m34["ms_per_step"], "e2e": m34["e2e"],
+            "step_roofline_frac_measured": m34["step_roofline_frac_measured"],
+            "bytes_per_step": m34["bytes_per_step"], "exit_hist": m34["exit_hist"],
+            "gamma_source": r34["gamma_source"], "clocks": m34["clocks"],
+            "no_exit": {"value": n34["value"], "ms_per_step": n34["ms_per_step"],
+                        "step_roofline_frac_measured": n34["step_roofline_frac_measured"],
+                        "bytes_per_step": n34["bytes_per_step"]},
+            "speedup_vs_no_exit": m34["value"] / n34["value"],
+            "kernels": r34["kr"],
+        }
+        r34["eng"].close()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -856,6 +883,9 @@ def main():
                     help="timed steps of the batch-32 run added to the default workload's line (0: skip)")
     ap.add_argument("--ncu-region", action="store_true",
                     help="bracket the timed steps with cudaProfilerStart/Stop (for ncu --profile-from-start off)")
+    ap.add_argument("--with-34b", action="store_true",
+                    help="also time the CodeLlama-34B shape at batch 8 (4096-token prompts; several minutes)")
+    ap.add_argument("--34b-steps", dest="steps_34b", type=int, default=32)
     ap.add_argument("--no-1b", dest="also_1b", action="store_false",
                     help="skip the Llama-3.2-1B batch-1 runs added to the default workload's line")
     ap.add_argument("--no-exit-head-token", dest="exit_head_token", action="store_false",

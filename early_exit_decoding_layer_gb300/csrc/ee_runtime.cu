@@ -53,7 +53,7 @@ struct Carver {
 struct Mat4 {  // int4 copy of one fused matrix
   uint8_t* q;     // row layout (GEMV)
   uint16_t* s;
-  uint8_t* qt;    // tensor-core GEMM blocks (contexts with max_batch >= kTcMinBatch), else null
+  uint8_t* qt;    // tensor-core GEMM blocks (contexts that may run a step on it), else null
 };
 
 struct LayerBufs {
@@ -87,6 +87,15 @@ Dims dims_of(const ee_config& c) {
   m.kv_layer_elems = (size_t)m.nblocks * m.hkv * EE_KV_BLOCK * m.hd;
   return m;
 }
+
+// The GEMV stages a step's activations in shared memory only for a few short
+// rows; a step whose activations it cannot stage for every projection (more
+// than kTcMinBatch - 1 sequences, or rows of the widest input too long for
+// the staging area) runs its projections and heads on the tensor-core GEMM.
+int widest_input(const Dims& m) { return std::max({m.d, m.dq, m.F}); }
+bool batch_uses_tc(const Dims& m, int B) { return B >= kTcMinBatch || !linear_stages_x(B, widest_input(m)); }
+// contexts that may run such a step carry the tensor-core GEMM's buffers
+bool ctx_needs_tc(const Dims& m) { return batch_uses_tc(m, m.maxb); }
 
 }  // namespace
 
@@ -253,7 +262,7 @@ size_t carve(ee_ctx* c, const ee_config& cfg, uint8_t* base) {
     b.gu.s = cv.take<uint16_t>((size_t)2 * m.F * sstride_of(m.d));
     b.d.q = cv.take<uint8_t>((size_t)m.d * m.F / 2);
     b.d.s = cv.take<uint16_t>((size_t)m.d * sstride_of(m.F));
-    const bool tcl = m.maxb >= kTcMinBatch;
+    const bool tcl = ctx_needs_tc(m);
     b.qkv.qt = tcl ? cv.take<uint8_t>(int4_tc_layout_bytes(m.nqkv, m.d)) : nullptr;
     b.o.qt = tcl ? cv.take<uint8_t>(int4_tc_layout_bytes(m.d, m.dq)) : nullptr;
     b.gu.qt = tcl ? cv.take<uint8_t>(int4_tc_layout_bytes(2 * m.F, m.d)) : nullptr;
@@ -280,7 +289,7 @@ size_t carve(ee_ctx* c, const ee_config& cfg, uint8_t* base) {
   float* hdbg = cv.take<float>((size_t)m.L * EE_MAX_BATCH * m.d);
   float* hin = cv.take<float>((size_t)2 * EE_MAX_BATCH * m.d);
   float* stss = cv.take<float>(EE_MAX_BATCH);
-  const bool tc = m.maxb >= kTcMinBatch;
+  const bool tc = ctx_needs_tc(m);
   float* tcpart = tc ? cv.take<float>(gemm_tc_part_floats(2 * kTcMaxUnits)) : nullptr;  // per list
   StepDesc* desc = cv.take<StepDesc>(1);
   StepOut* out = cv.take<StepOut>(1);
@@ -470,7 +479,8 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
 
   // With at most a few sequences the GEMV stages its activations in shared
   // memory and applies each RMSNorm itself; otherwise a norm kernel runs first.
-  const bool fuse_norm = linear_stages_x(B, m.d);
+  const bool use_tc = c->tc && batch_uses_tc(m, B);
+  const bool fuse_norm = !use_tc && linear_stages_x(B, m.d);
   auto norm_on_stage = [&](LinearParams& lp, const uint16_t* g) {
     lp.norm_h = c->h;
     lp.norm_stride = m.d;
@@ -480,7 +490,6 @@ ee_status enqueue_step(ee_ctx* c, int B, bool heads, bool prof) {
   bool lists_just_written = true;  // by the step-begin kernel
   // A projection or head: the GEMV, or for larger batches the tensor-core
   // GEMM (one launch per non-empty-capable sub-batch list).
-  const bool use_tc = c->tc && B >= kTcMinBatch;
   auto project = [&](int kind, int layer, const LinearParams& lp, const CUtensorMap* map, int grid) -> ee_status {
     if (use_tc && map && gemm_tc_shape_ok(lp.K)) {
       const TcPlan pl = gemm_tc_plan(lp.N, lp.K, c->num_sms, kTcMaxUnits);
@@ -1171,9 +1180,9 @@ ee_status ee_step_io(const ee_ctx* c, int32_t batch, int32_t heads, size_t* h2d,
     // begin + per layer (2 norms unless the GEMVs apply them, QKV, attention,
     // O, gate/up, down) + heads (norm, T, E) + final norm and head
     const int with_heads = heads && c->m.nck > 0;
-    const int norms = linear_stages_x(batch, c->m.d) ? 0 : 1;
+    const bool tc = c->tc && batch_uses_tc(c->m, batch);
+    const int norms = !tc && linear_stages_x(batch, c->m.d) ? 0 : 1;
     // the tensor-core GEMM serves both sub-batch lists in one launch
-    const bool tc = c->tc && batch >= kTcMinBatch;
     const int per_layer = 5 + 2 * norms;
     // the similarity criterion replaces each head's launches by one decision launch
     const int per_ckpt = c->criterion == EE_EXIT_MAXPROB ? 2 + norms : 1;

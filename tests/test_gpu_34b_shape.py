@@ -1,9 +1,10 @@
 """Parity at the CodeLlama-34B layer shape (d=8192, 64 query / 8 KV heads,
 hd 128, F=22016, V=32016), truncated to two layers so that the fp64 oracle
-stays small: the batch-8 path (activations read from global memory, RMSNorm
-kernels, 8 sequences per pass, grouped-query attention with 8 query heads per
-KV head, int4 rows of K=22016 on the per-row path) and the batch-10 path
-(tensor-core GEMM with K=22016)."""
+stays small: batch 1 on the GEMV (activation rows of up to 22016 values
+staged in shared memory, grouped-query attention with 8 query heads per KV
+head), and batches 8 and 10 on the tensor-core GEMM with K=22016 (eight rows
+of 8192 values no longer fit the GEMV's staging area, so a batch-8 step
+runs there too, with RMSNorm kernels)."""
 import numpy as np
 import pytest
 
@@ -24,11 +25,13 @@ def _lib():
     assert torch.cuda.is_available()
 
 
-@pytest.mark.parametrize("batch", [8, 10])
+@pytest.mark.parametrize("batch", [1, 8, 10])
 def test_codellama34b_layer_shape(batch):
     eng = parity.load_engine(W34, max_batch=batch, max_seq_len=32)
     orc = parity.build_oracle(W34, max_batch=batch, max_seq_len=32, cache_bytes=24 << 30)
     pr = synth.prompts(SHAPE, 77 + batch, [6 + i for i in range(batch)])
+    _, _, n = eng.step_io(batch, True)
+    assert n == 1 + (7 if batch > 1 else 5) * SHAPE.n_layers + (3 if batch > 1 else 2) + (2 if batch > 1 else 1)
     # step 0 exits every sequence at layer 0 (layer 1 on the int4 copy), step 1 none
     gps = [[-np.inf], [np.inf]]
     st = parity.drive(eng, orc, pr, gps[0], 2, gamma_per_step=gps)
