@@ -19,6 +19,7 @@ constexpr int kCtasPerSm = 2;  // two CTAs per SM: one kernel's tail overlaps th
 constexpr int kThreads = kWarps * 32;
 constexpr int kBatch = 8;  // 16-byte vectors per lane per batch
 constexpr int kMM = 8;     // sequences per pass over the weights
+constexpr size_t kL2PrefetchMax = 64 * 1024;  // int4 slice a CTA prefetches into L2 before its wait
 
 // Shared memory: header (lists, head statistics), the staged activations
 // (XS mode), then the per-row sums [rows][mcap].
@@ -488,6 +489,19 @@ EE_DEV void linear_prologue(const LinearParams& p, int cta, int ncta, uint8_t* s
   s.pl.passes[1] = (s.ne + s.pl.mcap - 1) / s.pl.mcap;
   s.nrows = s.pl.r1 - s.pl.r0;
   s.pre_phase = -1;
+  // A small int4 slice (the exit copy's QKV and O rows of a CTA) is asked of
+  // L2 as a whole before the dependency wait: under programmatic dependent
+  // launch the CTA may already be resident while the previous kernel runs.
+  if (threadIdx.x == 0 && s.pl.passes[1] > 0 && p.wq) {
+    const size_t rb = (size_t)p.K / 2, sb = (size_t)p.sstride * 2;
+    const size_t qb = (size_t)s.nrows * rb, qs = (size_t)s.nrows * sb;
+    const uint8_t* qa = p.wq + (size_t)s.pl.r0 * rb;
+    const uint8_t* sa = reinterpret_cast<const uint8_t*>(p.ws) + (size_t)s.pl.r0 * sb;
+    if (qb > 0 && qb <= kL2PrefetchMax && qb % 16 == 0 && ((uintptr_t)qa & 15) == 0)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(qa), "r"((uint32_t)qb) : "memory");
+    if (qs > 0 && qs <= kL2PrefetchMax && qs % 16 == 0 && ((uintptr_t)sa & 15) == 0)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(sa), "r"((uint32_t)qs) : "memory");
+  }
   if (s.pl.passes[0] > 0) {
     const Stream st = make_stream<0>(p, s.pl, warp);
     if (st.nv % 32 == 0) {
