@@ -158,3 +158,27 @@ def test_exit_head_token_byte_model():
     assert final - tok == dead + kv + sh.vocab * sh.d_model * 2
     # a sequence that never exits reads the same either way
     assert bench.step_bytes(sh, ck, [31], ctx, True, "maxprob", "exit_head") == bench.step_bytes(sh, ck, [31], ctx, True)
+
+
+def test_reference_arm_contract():
+    """--impl reference times the oracle on the host and prints the base
+    contract's line with impl, cpu_baseline and e2e (no host-device copies);
+    under a multi-rank launch only rank 0 works and prints."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--workload", "tiny-b1",
+           "--steps", "1", "--warmup", "3"]
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    out = subprocess.run(cmd, capture_output=True, text=True, env=env, cwd=root, timeout=300)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads([l for l in out.stdout.splitlines() if l.startswith("{")][-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["higher_is_better"] is True
+    assert line["metric"] == bench.METRIC and line["config"]["workload"] == "tiny-b1"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    env1 = dict(env, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    out1 = subprocess.run(cmd, capture_output=True, text=True, env=env1, cwd=root, timeout=300)
+    assert out1.returncode == 0 and "{" not in out1.stdout, (out1.stdout, out1.stderr[-2000:])
